@@ -1,0 +1,212 @@
+/*
+ * shortconv.h -- C ABI of libshortconv.so: the LFM2 gated short convolution
+ * ("ShortConv") hot path on GB300 (sm_103a).
+ *
+ * The operation (MAX Pipelines LFM2 article, "MAX Pipelines 的 LFM2 架构支持：
+ * 混合全注意力 + 短卷积解码器实现解析", section "短卷积实现（LFM2ShortConv）"):
+ * the in_proj output of a token is split into B, C and x; u = B * x; a
+ * per-sequence window of the last K values of u slides by one per token
+ * (oldest dropped, u appended); z = sum_k w[h,k] * window[k]; y = C * z.
+ * Tap k = K-1 multiplies the newest value. There is no bias and no
+ * activation (the released LFM2 configurations are bias-free: Liger-Kernel
+ * PR #1317, "Kernel changes / Gated short convolution").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layouts (row-major, contiguous):
+ *   bcx   [T, 3H]         in_proj output, columns B | C | x
+ *   w     [H, K]          depthwise conv weight
+ *   pool  [n_slots, H, K] conv-state pool; slot s, channel h holds the last K
+ *                         values of u (index K-1 newest). The pool stores u
+ *                         after rounding to the pool dtype, exactly as the
+ *                         convolution consumed it.
+ *   y     [T, H]          output
+ * dtype: bcx, w, pool, y (and win, dy, dbcx) all share one dtype, SC_F32 or
+ *   SC_BF16. Products B*x are rounded once to that dtype to form u; the sum
+ *   over taps and C*z are computed in fp32 and y is rounded once to the dtype.
+ * Pointers: every array pointer is a DEVICE pointer (cudaMalloc'd or
+ *   equivalent, e.g. a torch CUDA tensor's data pointer) on the current
+ *   device, 16-byte aligned; int32 index arrays need 4-byte alignment. A
+ *   pointer may be NULL only when the array it describes is empty.
+ * Sizes: H > 0 and a multiple of 8; 1 <= K <= 4.
+ * Ownership: the caller owns every buffer. The library allocates no device
+ *   or host memory and keeps no pointer after a call returns.
+ * Execution: every call only enqueues work on `stream` (a cudaStream_t; NULL
+ *   means the legacy default stream) and returns without synchronizing,
+ *   except shortconv_get_error.
+ * Aliasing: no output may overlap any input of the same call, except the
+ *   pool, which is read and written in place where stated.
+ * Errors: argument errors are found on the host; the call then returns
+ *   SC_EINVAL or SC_EUNSUPPORTED and enqueues nothing. A failed launch
+ *   returns SC_ECUDA. Errors in DEVICE-resident data (slot ids, cu_seqlens,
+ *   accepted lengths) cannot be seen by the host without a synchronization,
+ *   so the kernels record them in a per-device error word (a bit mask of
+ *   SC_DEV_* codes) and skip the offending unit; shortconv_get_error()
+ *   returns and clears that word. No kernel traps or asserts.
+ * Slot ids within one call must be distinct (not checked).
+ */
+#ifndef LFM2_SHORTCONV_H
+#define LFM2_SHORTCONV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SC_OK = 0,
+    SC_EINVAL = 1,        /* bad argument: null/misaligned pointer, bad size, overlap */
+    SC_EUNSUPPORTED = 2,  /* valid request outside what is built (dtype, K, H % 8) */
+    SC_ECUDA = 3,         /* a CUDA runtime call or launch failed */
+    SC_EDEVICE = 4        /* shortconv_get_error found device-side errors */
+} sc_status;
+
+typedef enum { SC_F32 = 0, SC_BF16 = 1 } sc_dtype;
+
+/* Bits of the device error word. */
+#define SC_DEV_BAD_SLOT 0x1u      /* a slot id outside [0, n_slots): that sequence skipped */
+#define SC_DEV_BAD_SEQLENS 0x2u   /* cu_seqlens not 0 = c0 <= c1 <= ... <= cN = T: call skipped */
+#define SC_DEV_BAD_ACCEPTED 0x4u  /* an accepted length outside [0, D]: that sequence skipped */
+
+/*
+ * Packed variable-length prefill (continued prefill from each slot's state).
+ *
+ * Sequence i (0 <= i < N) is rows cu_seqlens[i] .. cu_seqlens[i+1]-1 of bcx
+ * and y. Its history before its first row is the state in pool slot
+ * slot_ids[i]; after the call that slot holds the last K values of u of the
+ * sequence appended to its old state (for a sequence shorter than K the old
+ * values that remain are kept). No history crosses a sequence boundary
+ * ("feat(model): support LFM2-1.2B", section "供审阅者关注的事项"). A fresh
+ * sequence is given a zeroed slot by the caller. Empty sequences leave their
+ * slot unchanged. Slots not named in slot_ids are not touched.
+ *
+ *   dtype       SC_F32 or SC_BF16
+ *   H, K        channels, taps
+ *   bcx         device [T, 3H]           read
+ *   T           total rows, 0 <= T < 2^31
+ *   w           device [H, K]            read
+ *   cu_seqlens  device int32 [N + 1]     read; must be 0, non-decreasing, end at T
+ *   N           number of sequences, >= 0 (N = 0 requires T = 0)
+ *   slot_ids    device int32 [N]         read
+ *   pool        device [n_slots, H, K]   read and written in place
+ *   y           device [T, H]            written
+ * Device errors: SC_DEV_BAD_SEQLENS (nothing is written), SC_DEV_BAD_SLOT
+ * (that sequence's rows of y and its slot are not written).
+ */
+sc_status shortconv_prefill(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
+                            const void *w, const int32_t *cu_seqlens, int N,
+                            const int32_t *slot_ids, void *pool, int n_slots, void *y,
+                            void *stream);
+
+/*
+ * shortconv_prefill with an explicit tile: each thread computes 8 channels
+ * of `rows_per_thread` consecutive rows (one of 4, 8, 16, 32; 0 picks one
+ * from T, H and the device's SM count, which is what shortconv_prefill
+ * does). Results are identical for every tile; only the speed differs.
+ */
+sc_status shortconv_prefill_tiled(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
+                                  const void *w, const int32_t *cu_seqlens, int N,
+                                  const int32_t *slot_ids, void *pool, int n_slots, void *y,
+                                  int rows_per_thread, void *stream);
+
+/*
+ * Decode: one new token per sequence, in place on the pool.
+ *
+ * Row i of bcx is the next token of sequence i, whose state lives in slot
+ * slot_ids[i]. The slot's window slides by one and y[i] is that token's
+ * output: the MAX per-token loop ("短卷积实现（LFM2ShortConv）": gather the
+ * request's state, drop the oldest column, append bx_t, scatter back) for a
+ * single token.
+ *
+ *   bcx [N, 3H] read; w [H, K] read; slot_ids int32 [N] read;
+ *   pool [n_slots, H, K] read and written; y [N, H] written.
+ * Device errors: SC_DEV_BAD_SLOT (that sequence skipped).
+ */
+sc_status shortconv_decode(sc_dtype dtype, int H, int K, const void *bcx, int N,
+                           const void *w, const int32_t *slot_ids, void *pool,
+                           int n_slots, void *y, void *stream);
+
+/*
+ * Speculative verify: D draft tokens per sequence, recording the conv window
+ * after every draft step (SGLang PR #31041, section "实现拆解 2": the target
+ * verify pass writes each step's conv window to a speculative tape so that
+ * the state can be rolled back to the accepted boundary).
+ *
+ * Rows i*D .. i*D+D-1 of bcx are sequence i's drafts, taken in order from
+ * the state in slot slot_ids[i]. After draft j the K-wide window (what the
+ * slot would hold had the sequence accepted j+1 drafts) is written to
+ * win[i, j, :, :] and the draft's output to y[i*D + j]. The pool is only
+ * read; shortconv_rollback commits the accepted prefix.
+ *
+ *   bcx [N*D, 3H] read; w [H, K] read; slot_ids int32 [N] read;
+ *   pool [n_slots, H, K] read; win [N, D, H, K] written; y [N*D, H] written.
+ * Device errors: SC_DEV_BAD_SLOT (that sequence's win and y rows not written).
+ */
+sc_status shortconv_verify(sc_dtype dtype, int H, int K, const void *bcx, int N, int D,
+                           const void *w, const int32_t *slot_ids, const void *pool,
+                           int n_slots, void *win, void *y, void *stream);
+
+/*
+ * Rollback after verify: sequence i accepted accepted[i] of its D drafts
+ * (0 <= accepted[i] <= D). For accepted[i] >= 1, win[i, accepted[i]-1]
+ * becomes the state of slot slot_ids[i]; for 0 the slot keeps the state it
+ * had before verify (verify does not modify the pool).
+ *
+ *   win [N, D, H, K] read (from shortconv_verify); accepted int32 [N] read;
+ *   slot_ids int32 [N] read; pool [n_slots, H, K] written.
+ * Device errors: SC_DEV_BAD_ACCEPTED, SC_DEV_BAD_SLOT (that sequence skipped).
+ */
+sc_status shortconv_rollback(sc_dtype dtype, int H, int K, int N, int D, const void *win,
+                             const int32_t *accepted, const int32_t *slot_ids, void *pool,
+                             int n_slots, void *stream);
+
+/*
+ * Bytes of device workspace shortconv_backward needs for these sizes
+ * (fp32 partial weight gradients). Host-only; no CUDA call; depends only on
+ * the arguments. Returns 0 for invalid sizes.
+ */
+size_t shortconv_backward_workspace_bytes(int H, int K, int64_t T);
+
+/*
+ * Backward of one sequence of T rows that started from a zero state (the
+ * training path: Liger-Kernel PR #1317, "Kernel changes / Gated short
+ * convolution": the B/C gate gradients fused with the depthwise-conv input
+ * gradient, and the weight gradient of all K taps of a channel reduced
+ * together, bias-free). With z_t = sum_k w_k u_{t-K+1+k} (u before row 0 is 0):
+ *   dC_t = dy_t z_t;  dz_t = dy_t C_t;  du_s = sum_k w_k dz_{s+K-1-k}
+ *   (terms past row T-1 are 0);  dB_s = du_s x_s;  dx_s = du_s B_s;
+ *   dW[h,k] = sum_t dz_t u_{t-K+1+k}.
+ * The rounding of u is passed straight through.
+ *
+ *   bcx [T, 3H] read; w [H, K] read; dy [T, H] read;
+ *   dbcx [T, 3H] written (dB | dC | dx, same dtype as bcx);
+ *   dw [H, K] fp32 written (overwritten, not accumulated);
+ *   workspace: device scratch of at least
+ *   shortconv_backward_workspace_bytes(H, K, T) bytes, 16-byte aligned,
+ *   owned by the caller, contents ignored on entry and unspecified after.
+ * The weight gradient is reduced in a fixed order: repeated calls give
+ * identical bits.
+ */
+sc_status shortconv_backward(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
+                             const void *w, const void *dy, void *dbcx, float *dw,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronize `stream`, then read and clear the current device's error word.
+ * *device_code receives the SC_DEV_* bits seen since the last clear (0 if
+ * none). Returns SC_OK if the word was 0, SC_EDEVICE if not, SC_ECUDA if a
+ * CUDA call failed, SC_EINVAL if device_code is NULL. The word is shared by
+ * all streams on the device.
+ */
+sc_status shortconv_get_error(void *stream, int *device_code);
+
+/* Static, never-NULL description of a status code. */
+const char *shortconv_status_string(sc_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LFM2_SHORTCONV_H */

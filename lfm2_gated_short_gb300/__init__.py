@@ -1,1 +1,213 @@
-"""LFM2 gated short convolution (ShortConv) on GB300 (sm_103a)."""
+"""LFM2 gated short convolution (ShortConv) on GB300 (sm_103a).
+
+A thin ctypes binding over ``libshortconv.so`` (see ``include/shortconv.h``).
+Every function here only checks and marshals arguments: torch CUDA tensors
+become device pointers plus sizes, the current torch stream becomes the
+``cudaStream_t``, and all the work runs in the library's CUDA kernels. There
+is no CPU or PyTorch fallback: if the library is not built, or a call fails,
+an exception is raised.
+
+Layouts (row-major, contiguous, one dtype per call: torch.bfloat16 or
+torch.float32): ``bcx [T, 3H]`` (B | C | x), ``w [H, K]``, state pool
+``[n_slots, H, K]`` (tap K-1 newest), ``y [T, H]``; index arrays are int32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libshortconv.so")
+
+SC_OK, SC_EINVAL, SC_EUNSUPPORTED, SC_ECUDA, SC_EDEVICE = 0, 1, 2, 3, 4
+SC_F32, SC_BF16 = 0, 1
+DEV_BAD_SLOT, DEV_BAD_SEQLENS, DEV_BAD_ACCEPTED = 0x1, 0x2, 0x4
+
+_lock = threading.Lock()
+_lib = None
+
+
+class ShortConvError(RuntimeError):
+    """A library call returned a status other than SC_OK."""
+
+    def __init__(self, fn: str, status: int, message: str):
+        super().__init__(f"{fn}: {message} (status {status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (argument types declared). Raises if it is not built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m lfm2_gated_short_gb300.build` (nvcc, sm_103a)")
+            L = ctypes.CDLL(LIB_PATH)
+            p, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+            L.shortconv_prefill.argtypes = [i32, i32, i32, p, i64, p, p, i32, p, p, i32, p, p]
+            L.shortconv_prefill_tiled.argtypes = [i32, i32, i32, p, i64, p, p, i32, p, p, i32,
+                                                  p, i32, p]
+            L.shortconv_decode.argtypes = [i32, i32, i32, p, i32, p, p, p, i32, p, p]
+            L.shortconv_verify.argtypes = [i32, i32, i32, p, i32, i32, p, p, p, i32, p, p, p]
+            L.shortconv_rollback.argtypes = [i32, i32, i32, i32, i32, p, p, p, p, i32, p]
+            L.shortconv_backward_workspace_bytes.argtypes = [i32, i32, i64]
+            L.shortconv_backward_workspace_bytes.restype = ctypes.c_size_t
+            L.shortconv_backward.argtypes = [i32, i32, i32, p, i64, p, p, p, p, p,
+                                             ctypes.c_size_t, p]
+            L.shortconv_get_error.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
+            L.shortconv_status_string.argtypes = [i32]
+            L.shortconv_status_string.restype = ctypes.c_char_p
+            for f in ("prefill", "prefill_tiled", "decode", "verify", "rollback", "backward",
+                      "get_error"):
+                getattr(L, "shortconv_" + f).restype = i32
+            _lib = L
+    return _lib
+
+
+def _raise_on(fn: str, status: int) -> None:
+    if status != SC_OK:
+        msg = lib().shortconv_status_string(status).decode()
+        raise ShortConvError(fn, status, msg)
+
+
+def _dcode(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SC_BF16
+    if t.dtype == torch.float32:
+        return SC_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: use torch.bfloat16 or torch.float32")
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, shape=None) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _stream(stream, device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def prefill(bcx, w, cu_seqlens, slot_ids, pool, y=None, rows_per_thread=0, stream=None):
+    """Packed varlen prefill; updates ``pool`` in place and returns ``y [T, H]``."""
+    dt = bcx.dtype
+    T, H3 = bcx.shape
+    H, K = w.shape
+    if H3 != 3 * H:
+        raise ValueError("bcx must be [T, 3H] for w [H, K]")
+    N = slot_ids.shape[0]
+    if y is None:
+        y = torch.empty((T, H), dtype=dt, device=bcx.device)
+    args = (_dcode(bcx), H, K, _dev(bcx, "bcx", dt), T, _dev(w, "w", dt),
+            _dev(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,)), N,
+            _dev(slot_ids, "slot_ids", torch.int32, (N,)),
+            _dev(pool, "pool", dt, (pool.shape[0], H, K)), pool.shape[0],
+            _dev(y, "y", dt, (T, H)))
+    st = _stream(stream, bcx.device)
+    if rows_per_thread:
+        _raise_on("shortconv_prefill_tiled",
+                  lib().shortconv_prefill_tiled(*args, rows_per_thread, st))
+    else:
+        _raise_on("shortconv_prefill", lib().shortconv_prefill(*args, st))
+    return y
+
+
+def decode(bcx, w, slot_ids, pool, y=None, stream=None):
+    """One token per sequence; updates ``pool`` in place and returns ``y [N, H]``."""
+    dt = bcx.dtype
+    N, H3 = bcx.shape
+    H, K = w.shape
+    if H3 != 3 * H:
+        raise ValueError("bcx must be [N, 3H] for w [H, K]")
+    if y is None:
+        y = torch.empty((N, H), dtype=dt, device=bcx.device)
+    _raise_on("shortconv_decode", lib().shortconv_decode(
+        _dcode(bcx), H, K, _dev(bcx, "bcx", dt), N, _dev(w, "w", dt),
+        _dev(slot_ids, "slot_ids", torch.int32, (N,)),
+        _dev(pool, "pool", dt, (pool.shape[0], H, K)), pool.shape[0],
+        _dev(y, "y", dt, (N, H)), _stream(stream, bcx.device)))
+    return y
+
+
+def verify(bcx, w, slot_ids, pool, D, win=None, y=None, stream=None):
+    """Speculative verify of ``D`` drafts per sequence; returns ``(win, y)``. Pool is read only."""
+    dt = bcx.dtype
+    H, K = w.shape
+    N = slot_ids.shape[0]
+    if tuple(bcx.shape) != (N * D, 3 * H):
+        raise ValueError(f"bcx must be [N*D, 3H] = {(N * D, 3 * H)}")
+    if win is None:
+        win = torch.empty((N, D, H, K), dtype=dt, device=bcx.device)
+    if y is None:
+        y = torch.empty((N * D, H), dtype=dt, device=bcx.device)
+    _raise_on("shortconv_verify", lib().shortconv_verify(
+        _dcode(bcx), H, K, _dev(bcx, "bcx", dt), N, D, _dev(w, "w", dt),
+        _dev(slot_ids, "slot_ids", torch.int32, (N,)),
+        _dev(pool, "pool", dt, (pool.shape[0], H, K)), pool.shape[0],
+        _dev(win, "win", dt, (N, D, H, K)), _dev(y, "y", dt, (N * D, H)),
+        _stream(stream, bcx.device)))
+    return win, y
+
+
+def rollback(win, accepted, slot_ids, pool, stream=None):
+    """Commit each sequence's accepted prefix into its slot (in place on ``pool``)."""
+    dt = win.dtype
+    N, D, H, K = win.shape
+    _raise_on("shortconv_rollback", lib().shortconv_rollback(
+        _dcode(win), H, K, N, D, _dev(win, "win", dt),
+        _dev(accepted, "accepted", torch.int32, (N,)),
+        _dev(slot_ids, "slot_ids", torch.int32, (N,)),
+        _dev(pool, "pool", dt, (pool.shape[0], H, K)), pool.shape[0],
+        _stream(stream, win.device)))
+
+
+def backward_workspace_bytes(H: int, K: int, T: int) -> int:
+    return int(lib().shortconv_backward_workspace_bytes(H, K, T))
+
+
+def backward(bcx, w, dy, dbcx=None, dw=None, workspace=None, stream=None):
+    """Backward from a zero state; returns ``(dbcx [T, 3H], dw [H, K] fp32)``."""
+    dt = bcx.dtype
+    T, H3 = bcx.shape
+    H, K = w.shape
+    if H3 != 3 * H:
+        raise ValueError("bcx must be [T, 3H] for w [H, K]")
+    need = backward_workspace_bytes(H, K, T)
+    if dbcx is None:
+        dbcx = torch.empty_like(bcx)
+    if dw is None:
+        dw = torch.empty((H, K), dtype=torch.float32, device=bcx.device)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=bcx.device)
+    if workspace.dtype != torch.uint8 or workspace.numel() < need:
+        raise ValueError(f"workspace must be a uint8 tensor of at least {need} bytes")
+    _raise_on("shortconv_backward", lib().shortconv_backward(
+        _dcode(bcx), H, K, _dev(bcx, "bcx", dt), T, _dev(w, "w", dt),
+        _dev(dy, "dy", dt, (T, H)), _dev(dbcx, "dbcx", dt, (T, 3 * H)),
+        _dev(dw, "dw", torch.float32, (H, K)), _dev(workspace, "workspace"),
+        workspace.numel(), _stream(stream, bcx.device)))
+    return dbcx, dw
+
+
+def get_error(stream=None, device=None) -> int:
+    """Synchronize the stream, return and clear the device error word (SC_DEV_* bits)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    code = ctypes.c_int(0)
+    st = lib().shortconv_get_error(_stream(stream, dev), ctypes.byref(code))
+    if st not in (SC_OK, SC_EDEVICE):
+        _raise_on("shortconv_get_error", st)
+    return code.value

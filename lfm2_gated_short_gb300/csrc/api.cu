@@ -1,0 +1,226 @@
+// api.cu -- the extern "C" entry points declared in include/shortconv.h.
+//
+// Each entry point validates its arguments on the host (no CUDA call before
+// the arguments are known good), then enqueues the kernel(s) on the caller's
+// stream. Nothing is allocated and nothing is synchronized, except in
+// shortconv_get_error.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "kernels.h"
+#include "shortconv.h"
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// A pointer describing `bytes` bytes: NULL allowed only when empty.
+bool ptr_ok(const void *p, size_t bytes, uintptr_t align) {
+    if (bytes == 0) return p == nullptr || aligned(p, align);
+    return p != nullptr && aligned(p, align);
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    if (na == 0 || nb == 0 || a == nullptr || b == nullptr) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+size_t elem_size(sc_dtype d) { return d == SC_BF16 ? 2 : 4; }
+
+// Common size checks: dtype, H, K.
+sc_status check_shape(sc_dtype dtype, int H, int K) {
+    if (dtype != SC_F32 && dtype != SC_BF16) return SC_EUNSUPPORTED;
+    if (H <= 0 || K <= 0) return SC_EINVAL;
+    if (H % 8 != 0 || K > 4) return SC_EUNSUPPORTED;
+    if ((int64_t)H * 3 > INT32_MAX / 2) return SC_EUNSUPPORTED;
+    return SC_OK;
+}
+
+int sm_count_of_current_device() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+sc_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SC_OK : SC_ECUDA; }
+
+sc_status prefill_impl(sc_dtype dtype, int H, int K, const void *bcx, int64_t T, const void *w,
+                       const int32_t *cu_seqlens, int N, const int32_t *slot_ids, void *pool,
+                       int n_slots, void *y, int rows_per_thread, void *stream) {
+    sc_status st = check_shape(dtype, H, K);
+    if (st != SC_OK) return st;
+    if (T < 0 || T > INT32_MAX || N < 0 || n_slots <= 0) return SC_EINVAL;
+    if (N == 0 && T != 0) return SC_EINVAL;
+    if (rows_per_thread != 0 && rows_per_thread != 4 && rows_per_thread != 8 &&
+        rows_per_thread != 16 && rows_per_thread != 32)
+        return SC_EINVAL;
+    const size_t es = elem_size(dtype);
+    const size_t n_bcx = (size_t)T * 3 * H * es, n_y = (size_t)T * H * es;
+    const size_t n_w = (size_t)H * K * es, n_pool = (size_t)n_slots * H * K * es;
+    if (!ptr_ok(bcx, n_bcx, 16) || !ptr_ok(y, n_y, 16) || !ptr_ok(w, n_w, 16) ||
+        !ptr_ok(pool, n_pool, 16) || !ptr_ok(cu_seqlens, (size_t)(N + 1) * 4, 4) ||
+        !ptr_ok(slot_ids, (size_t)N * 4, 4))
+        return SC_EINVAL;
+    if (overlaps(y, n_y, bcx, n_bcx) || overlaps(y, n_y, pool, n_pool) ||
+        overlaps(y, n_y, w, n_w) || overlaps(pool, n_pool, bcx, n_bcx) ||
+        overlaps(pool, n_pool, w, n_w))
+        return SC_EINVAL;
+    if (N == 0) return SC_OK;
+    int L = rows_per_thread;
+    if (L == 0) {
+        const int sms = sm_count_of_current_device();
+        if (sms <= 0) return SC_ECUDA;
+        L = sc::prefill_rows_per_thread(T, H, sms);
+    }
+    return from_cuda(sc::launch_prefill(dtype, H, K, bcx, T, w, cu_seqlens, N, slot_ids, pool,
+                                        n_slots, y, L, (cudaStream_t)stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+sc_status shortconv_prefill(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
+                            const void *w, const int32_t *cu_seqlens, int N,
+                            const int32_t *slot_ids, void *pool, int n_slots, void *y,
+                            void *stream) {
+    return prefill_impl(dtype, H, K, bcx, T, w, cu_seqlens, N, slot_ids, pool, n_slots, y, 0,
+                        stream);
+}
+
+sc_status shortconv_prefill_tiled(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
+                                  const void *w, const int32_t *cu_seqlens, int N,
+                                  const int32_t *slot_ids, void *pool, int n_slots, void *y,
+                                  int rows_per_thread, void *stream) {
+    return prefill_impl(dtype, H, K, bcx, T, w, cu_seqlens, N, slot_ids, pool, n_slots, y,
+                        rows_per_thread, stream);
+}
+
+sc_status shortconv_decode(sc_dtype dtype, int H, int K, const void *bcx, int N, const void *w,
+                           const int32_t *slot_ids, void *pool, int n_slots, void *y,
+                           void *stream) {
+    sc_status st = check_shape(dtype, H, K);
+    if (st != SC_OK) return st;
+    if (N < 0 || n_slots <= 0) return SC_EINVAL;
+    const size_t es = elem_size(dtype);
+    const size_t n_bcx = (size_t)N * 3 * H * es, n_y = (size_t)N * H * es;
+    const size_t n_w = (size_t)H * K * es, n_pool = (size_t)n_slots * H * K * es;
+    if (!ptr_ok(bcx, n_bcx, 16) || !ptr_ok(y, n_y, 16) || !ptr_ok(w, n_w, 16) ||
+        !ptr_ok(pool, n_pool, 16) || !ptr_ok(slot_ids, (size_t)N * 4, 4))
+        return SC_EINVAL;
+    if (overlaps(y, n_y, bcx, n_bcx) || overlaps(y, n_y, pool, n_pool) ||
+        overlaps(y, n_y, w, n_w) || overlaps(pool, n_pool, bcx, n_bcx) ||
+        overlaps(pool, n_pool, w, n_w))
+        return SC_EINVAL;
+    if (N == 0) return SC_OK;
+    return from_cuda(sc::launch_decode(dtype, H, K, bcx, N, w, slot_ids, pool, n_slots, y,
+                                       (cudaStream_t)stream));
+}
+
+sc_status shortconv_verify(sc_dtype dtype, int H, int K, const void *bcx, int N, int D,
+                           const void *w, const int32_t *slot_ids, const void *pool,
+                           int n_slots, void *win, void *y, void *stream) {
+    sc_status st = check_shape(dtype, H, K);
+    if (st != SC_OK) return st;
+    if (N < 0 || D <= 0 || n_slots <= 0) return SC_EINVAL;
+    if ((int64_t)N * D > INT32_MAX) return SC_EINVAL;
+    const size_t es = elem_size(dtype);
+    const size_t rows = (size_t)N * D;
+    const size_t n_bcx = rows * 3 * H * es, n_y = rows * H * es, n_win = rows * H * K * es;
+    const size_t n_w = (size_t)H * K * es, n_pool = (size_t)n_slots * H * K * es;
+    if (!ptr_ok(bcx, n_bcx, 16) || !ptr_ok(y, n_y, 16) || !ptr_ok(w, n_w, 16) ||
+        !ptr_ok(pool, n_pool, 16) || !ptr_ok(win, n_win, 16) ||
+        !ptr_ok(slot_ids, (size_t)N * 4, 4))
+        return SC_EINVAL;
+    const void *ins[3] = {bcx, w, pool};
+    const size_t nins[3] = {n_bcx, n_w, n_pool};
+    for (int i = 0; i < 3; ++i)
+        if (overlaps(y, n_y, ins[i], nins[i]) || overlaps(win, n_win, ins[i], nins[i]))
+            return SC_EINVAL;
+    if (overlaps(y, n_y, win, n_win)) return SC_EINVAL;
+    if (N == 0) return SC_OK;
+    return from_cuda(sc::launch_verify(dtype, H, K, bcx, N, D, w, slot_ids, pool, n_slots, win,
+                                       y, (cudaStream_t)stream));
+}
+
+sc_status shortconv_rollback(sc_dtype dtype, int H, int K, int N, int D, const void *win,
+                             const int32_t *accepted, const int32_t *slot_ids, void *pool,
+                             int n_slots, void *stream) {
+    sc_status st = check_shape(dtype, H, K);
+    if (st != SC_OK) return st;
+    if (N < 0 || D <= 0 || n_slots <= 0) return SC_EINVAL;
+    const size_t es = elem_size(dtype);
+    const size_t n_win = (size_t)N * D * H * K * es, n_pool = (size_t)n_slots * H * K * es;
+    if (!ptr_ok(win, n_win, 16) || !ptr_ok(pool, n_pool, 16) ||
+        !ptr_ok(accepted, (size_t)N * 4, 4) || !ptr_ok(slot_ids, (size_t)N * 4, 4))
+        return SC_EINVAL;
+    if (overlaps(pool, n_pool, win, n_win)) return SC_EINVAL;
+    if (N == 0) return SC_OK;
+    return from_cuda(sc::launch_rollback(dtype, H, K, N, D, win, accepted, slot_ids, pool,
+                                         n_slots, (cudaStream_t)stream));
+}
+
+size_t shortconv_backward_workspace_bytes(int H, int K, int64_t T) {
+    if (H <= 0 || H % 8 != 0 || K <= 0 || K > 4 || T < 0 || T > INT32_MAX) return 0;
+    return sc::backward_workspace_bytes(H, K, T);
+}
+
+sc_status shortconv_backward(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
+                             const void *w, const void *dy, void *dbcx, float *dw,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+    sc_status st = check_shape(dtype, H, K);
+    if (st != SC_OK) return st;
+    if (T < 0 || T > INT32_MAX) return SC_EINVAL;
+    const size_t es = elem_size(dtype);
+    const size_t n_bcx = (size_t)T * 3 * H * es, n_dy = (size_t)T * H * es;
+    const size_t n_w = (size_t)H * K * es, n_dw = (size_t)H * K * 4;
+    const size_t need = sc::backward_workspace_bytes(H, K, T);
+    if (workspace_bytes < need) return SC_EINVAL;
+    if (!ptr_ok(bcx, n_bcx, 16) || !ptr_ok(dy, n_dy, 16) || !ptr_ok(w, n_w, 16) ||
+        !ptr_ok(dbcx, n_bcx, 16) || !ptr_ok(dw, n_dw, 4) || !ptr_ok(workspace, need, 16))
+        return SC_EINVAL;
+    const void *ins[3] = {bcx, w, dy};
+    const size_t nins[3] = {n_bcx, n_w, n_dy};
+    for (int i = 0; i < 3; ++i)
+        if (overlaps(dbcx, n_bcx, ins[i], nins[i]) || overlaps(dw, n_dw, ins[i], nins[i]) ||
+            overlaps(workspace, need, ins[i], nins[i]))
+            return SC_EINVAL;
+    if (overlaps(dbcx, n_bcx, dw, n_dw) || overlaps(dbcx, n_bcx, workspace, need) ||
+        overlaps(dw, n_dw, workspace, need))
+        return SC_EINVAL;
+    return from_cuda(sc::launch_backward(dtype, H, K, bcx, T, w, dy, dbcx, dw, workspace,
+                                         (cudaStream_t)stream));
+}
+
+sc_status shortconv_get_error(void *stream, int *device_code) {
+    if (device_code == nullptr) return SC_EINVAL;
+    unsigned int code = 0;
+    const cudaError_t e = sc::read_and_clear_error((cudaStream_t)stream, &code);
+    if (e != cudaSuccess) return SC_ECUDA;
+    *device_code = (int)code;
+    return code == 0 ? SC_OK : SC_EDEVICE;
+}
+
+const char *shortconv_status_string(sc_status status) {
+    switch (status) {
+        case SC_OK: return "ok";
+        case SC_EINVAL: return "invalid argument";
+        case SC_EUNSUPPORTED: return "unsupported dtype or size";
+        case SC_ECUDA: return "CUDA runtime error";
+        case SC_EDEVICE: return "device-side data error (see the device error code)";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,436 @@
+// forward.cu -- ShortConv forward kernels: varlen prefill, decode, speculative
+// verify and rollback.
+//
+// The arithmetic is the MAX LFM2ShortConv definition ("MAX Pipelines 的 LFM2
+// 架构支持", section "短卷积实现（LFM2ShortConv）"): u = B*x (rounded to the
+// storage dtype, the value the state keeps), a K-wide window sliding by one
+// per token, z = sum_k w_k window_k in fp32, y = C*z rounded once.
+//
+// Instead of the page's sequential per-token loop, prefill is a parallel FIR:
+// each thread owns 8 channels and a tile of L consecutive rows and rebuilds
+// the K-1 values of u before its tile from the B and x rows just above it.
+#include "common.cuh"
+#include "kernels.h"
+#include "shortconv.h"
+
+namespace sc {
+
+__device__ unsigned int g_error_word;   // bit mask of SC_DEV_* codes
+__device__ unsigned int g_error_taken;  // last value taken by read_and_clear_error
+
+__device__ __forceinline__ void raise_error(unsigned int code) { atomicOr(&g_error_word, code); }
+
+__global__ void k_take_error() { g_error_taken = atomicExch(&g_error_word, 0u); }
+
+constexpr int kThreads = 256;
+constexpr int kMaxStagedSeqs = 2048;  // cu_seqlens entries staged in shared memory
+constexpr int kChunk = 4;             // rows whose loads are issued together
+
+// u of one row (8 channels) from its B and x sections.
+template <typename T>
+__device__ __forceinline__ void row_u(const T *__restrict__ bcx, int64_t row, int H, int h0,
+                                      float (&u)[kCh]) {
+    const T *p = bcx + row * 3 * (int64_t)H + h0;
+    const Row<T> rb = load_row(p), rx = load_row(p + 2 * H);
+    float b[kCh], x[kCh];
+    unpack_row(rb, b);
+    unpack_row(rx, x);
+#pragma unroll
+    for (int c = 0; c < kCh; ++c) u[c] = gate_in<T>(b[c], x[c]);
+}
+
+// Rows [a, e) of one sequence for 8 channels; `win` enters holding the last K
+// values of u before row a and leaves holding the last K up to row e-1.
+template <typename T, int K>
+__device__ __forceinline__ void run_rows(const T *__restrict__ bcx, int H, int h0, int64_t a,
+                                         int64_t e, const float (&wt)[kCh][K],
+                                         float (&win)[kCh][K], T *__restrict__ y) {
+    const int64_t ld = 3 * (int64_t)H;
+    for (int64_t r = a; r < e; r += kChunk) {
+        Row<T> rb[kChunk], rc[kChunk], rx[kChunk];
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+            if (r + j < e) {
+                const T *p = bcx + (r + j) * ld + h0;
+                rb[j] = load_row(p);
+                rc[j] = load_row(p + H);
+                rx[j] = load_row(p + 2 * H);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+            if (r + j < e) {
+                float b[kCh], c[kCh], x[kCh], out[kCh];
+                unpack_row(rb[j], b);
+                unpack_row(rc[j], c);
+                unpack_row(rx[j], x);
+#pragma unroll
+                for (int ch = 0; ch < kCh; ++ch) {
+                    const float u = gate_in<T>(b[ch], x[ch]);
+                    out[ch] = c[ch] * slide_dot<K>(win[ch], wt[ch], u);
+                }
+                store_row(y + (r + j) * (int64_t)H + h0, out);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ prefill
+//
+// Unit = (row tile of L rows, channel group cg of 8 channels). A tile may
+// hold pieces of several sequences; each piece restarts its window.
+//
+// Race-free state update: the piece that holds a sequence's FIRST row (its
+// "owner") is the only reader of the old slot state, and it is extended to
+// cover at least the sequence's first K-1 rows (other tiles start that
+// sequence at row s0+K-1 or later, so their history comes from B and x rows
+// of the same sequence). The owner also writes the final state, after its own
+// read, rebuilding the last K values of u from the sequence's last K rows
+// when the sequence ends in another tile.
+template <typename T, int K, int L>
+__global__ void __launch_bounds__(kThreads)
+    k_prefill(const T *__restrict__ bcx, int64_t T_rows, int H, const T *__restrict__ w,
+              const int32_t *__restrict__ cu, int N, const int32_t *__restrict__ slots,
+              T *__restrict__ pool, int n_slots, T *__restrict__ y) {
+    __shared__ int32_t s_cu[kMaxStagedSeqs + 1];
+    const bool staged = N <= kMaxStagedSeqs;
+
+    // The whole call is skipped unless cu_seqlens is 0 = c0 <= ... <= cN = T.
+    int bad = 0;
+    for (int j = threadIdx.x; j <= N; j += blockDim.x) {
+        const int32_t c = cu[j];
+        if (staged) s_cu[j] = c;
+        if (j == 0 && c != 0) bad = 1;
+        if (j == N && (int64_t)c != T_rows) bad = 1;
+        if (j < N && cu[j + 1] < c) bad = 1;
+    }
+    if (__syncthreads_or(bad)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(SC_DEV_BAD_SEQLENS);
+        return;
+    }
+
+    const int groups = H / kCh;
+    const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t n_tiles = (T_rows + L - 1) / L;
+    if (unit >= n_tiles * groups) return;
+    const int cg = (int)(unit % groups);
+    const int h0 = cg * kCh;
+    const int64_t r0 = (unit / groups) * L;
+    const int64_t r1 = min(r0 + (int64_t)L, T_rows);
+    auto CU = [&](int j) -> int64_t { return staged ? s_cu[j] : cu[j]; };
+
+    // Largest i with cu[i] <= r0: the sequence holding row r0.
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (CU(mid) <= r0) lo = mid; else hi = mid - 1;
+    }
+
+    float wt[kCh][K];
+    load_block<T, K>(w + (int64_t)h0 * K, wt);
+
+    for (int i = lo; i < N; ++i) {
+        const int64_t s0 = CU(i), s1 = CU(i + 1);
+        if (s0 >= r1) break;
+        if (s1 <= s0) continue;  // empty: its slot keeps its state
+        const bool owner = s0 >= r0;
+        int64_t a, e;
+        if (owner) {
+            a = s0;
+            e = min(s1, max(r1, s0 + (K - 1)));
+        } else {
+            a = max(r0, s0 + (K - 1));
+            e = min(s1, r1);
+            if (a >= e) continue;
+        }
+        const int slot = slots[i];
+        if (slot < 0 || slot >= n_slots) {
+            if (owner && cg == 0) raise_error(SC_DEV_BAD_SLOT);
+            continue;
+        }
+        T *st = pool + ((int64_t)slot * H + h0) * K;
+        float win[kCh][K];
+        if (owner) {
+            load_block<T, K>(st, win);
+        } else {
+#pragma unroll
+            for (int ch = 0; ch < kCh; ++ch) win[ch][0] = 0.f;
+#pragma unroll
+            for (int k = 1; k < K; ++k) {
+                float u[kCh];
+                row_u<T>(bcx, a - K + k, H, h0, u);
+#pragma unroll
+                for (int ch = 0; ch < kCh; ++ch) win[ch][k] = u[ch];
+            }
+        }
+        run_rows<T, K>(bcx, H, h0, a, e, wt, win, y);
+        if (owner) {
+            if (e < s1) {  // the sequence ends in a later tile: rebuild its last K values
+#pragma unroll
+                for (int k = 0; k < K; ++k) {
+                    float u[kCh];
+                    row_u<T>(bcx, s1 - K + k, H, h0, u);
+#pragma unroll
+                    for (int ch = 0; ch < kCh; ++ch) win[ch][k] = u[ch];
+                }
+            }
+            store_block<T, K>(st, win);
+        }
+    }
+}
+
+int prefill_rows_per_thread(int64_t T, int H, int sm_count) {
+    // Enough tiles for several resident CTAs per SM; longer tiles amortize the
+    // K-1 halo rows each tile re-reads.
+    const int64_t groups = H / kCh;
+    const int choices[4] = {32, 16, 8, 4};
+    for (int L : choices) {
+        const int64_t ctas = ((T + L - 1) / L * groups + kThreads - 1) / kThreads;
+        if (ctas >= 4LL * sm_count) return L;
+    }
+    return 4;
+}
+
+template <typename T, int K, int L>
+static cudaError_t prefill_inst(const void *bcx, int64_t rows, int H, const void *w,
+                                const int32_t *cu, int N, const int32_t *slots, void *pool,
+                                int n_slots, void *y, cudaStream_t stream) {
+    const int64_t units = (rows + L - 1) / L * (H / kCh);
+    int64_t blocks = (units + kThreads - 1) / kThreads;
+    if (blocks < 1) blocks = 1;  // still validates cu_seqlens
+    k_prefill<T, K, L><<<(unsigned)blocks, kThreads, 0, stream>>>(
+        (const T *)bcx, rows, H, (const T *)w, cu, N, slots, (T *)pool, n_slots, (T *)y);
+    return cudaGetLastError();
+}
+
+template <typename T, int K>
+static cudaError_t prefill_L(int L, const void *bcx, int64_t rows, int H, const void *w,
+                             const int32_t *cu, int N, const int32_t *slots, void *pool,
+                             int n_slots, void *y, cudaStream_t s) {
+    switch (L) {
+        case 4: return prefill_inst<T, K, 4>(bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
+        case 8: return prefill_inst<T, K, 8>(bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
+        case 16: return prefill_inst<T, K, 16>(bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
+        default: return prefill_inst<T, K, 32>(bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
+    }
+}
+
+template <typename T>
+static cudaError_t prefill_K(int K, int L, const void *bcx, int64_t rows, int H, const void *w,
+                             const int32_t *cu, int N, const int32_t *slots, void *pool,
+                             int n_slots, void *y, cudaStream_t s) {
+    switch (K) {
+        case 1: return prefill_L<T, 1>(L, bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
+        case 2: return prefill_L<T, 2>(L, bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
+        case 3: return prefill_L<T, 3>(L, bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
+        default: return prefill_L<T, 4>(L, bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
+    }
+}
+
+cudaError_t launch_prefill(int dtype, int H, int K, const void *bcx, int64_t rows, const void *w,
+                           const int32_t *cu, int N, const int32_t *slots, void *pool,
+                           int n_slots, void *y, int L, cudaStream_t s) {
+    if (dtype == SC_BF16)
+        return prefill_K<__nv_bfloat16>(K, L, bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
+    return prefill_K<float>(K, L, bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
+}
+
+// ------------------------------------------------------------------- decode
+//
+// Unit = (sequence i, channel group). The token's B, C, x loads do not depend
+// on the slot id, so they are issued before the slot-dependent state load.
+template <typename T, int K>
+__global__ void __launch_bounds__(kThreads)
+    k_decode(const T *__restrict__ bcx, int N, int H, const T *__restrict__ w,
+             const int32_t *__restrict__ slots, T *__restrict__ pool, int n_slots,
+             T *__restrict__ y) {
+    const int groups = H / kCh;
+    const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (unit >= (int64_t)N * groups) return;
+    const int i = (int)(unit / groups), cg = (int)(unit % groups), h0 = cg * kCh;
+    const T *p = bcx + (int64_t)i * 3 * H + h0;
+    const Row<T> rb = load_row(p), rc = load_row(p + H), rx = load_row(p + 2 * H);
+    const int slot = slots[i];
+    float wt[kCh][K];
+    load_block<T, K>(w + (int64_t)h0 * K, wt);
+    if (slot < 0 || slot >= n_slots) {
+        if (cg == 0) raise_error(SC_DEV_BAD_SLOT);
+        return;
+    }
+    T *st = pool + ((int64_t)slot * H + h0) * K;
+    float win[kCh][K];
+    load_block<T, K>(st, win);
+    float b[kCh], c[kCh], x[kCh], out[kCh];
+    unpack_row(rb, b);
+    unpack_row(rc, c);
+    unpack_row(rx, x);
+#pragma unroll
+    for (int ch = 0; ch < kCh; ++ch)
+        out[ch] = c[ch] * slide_dot<K>(win[ch], wt[ch], gate_in<T>(b[ch], x[ch]));
+    store_row(y + (int64_t)i * H + h0, out);
+    store_block<T, K>(st, win);
+}
+
+template <typename T, int K>
+static cudaError_t decode_inst(const void *bcx, int N, int H, const void *w,
+                               const int32_t *slots, void *pool, int n_slots, void *y,
+                               cudaStream_t stream) {
+    const int64_t units = (int64_t)N * (H / kCh);
+    const int64_t blocks = (units + kThreads - 1) / kThreads;
+    k_decode<T, K><<<(unsigned)blocks, kThreads, 0, stream>>>(
+        (const T *)bcx, N, H, (const T *)w, slots, (T *)pool, n_slots, (T *)y);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t decode_K(int K, const void *bcx, int N, int H, const void *w,
+                            const int32_t *slots, void *pool, int n_slots, void *y,
+                            cudaStream_t s) {
+    switch (K) {
+        case 1: return decode_inst<T, 1>(bcx, N, H, w, slots, pool, n_slots, y, s);
+        case 2: return decode_inst<T, 2>(bcx, N, H, w, slots, pool, n_slots, y, s);
+        case 3: return decode_inst<T, 3>(bcx, N, H, w, slots, pool, n_slots, y, s);
+        default: return decode_inst<T, 4>(bcx, N, H, w, slots, pool, n_slots, y, s);
+    }
+}
+
+cudaError_t launch_decode(int dtype, int H, int K, const void *bcx, int N, const void *w,
+                          const int32_t *slots, void *pool, int n_slots, void *y,
+                          cudaStream_t s) {
+    if (dtype == SC_BF16) return decode_K<__nv_bfloat16>(K, bcx, N, H, w, slots, pool, n_slots, y, s);
+    return decode_K<float>(K, bcx, N, H, w, slots, pool, n_slots, y, s);
+}
+
+// ------------------------------------------------------------------- verify
+//
+// Unit = (sequence i, channel group); the D draft steps run in order in
+// registers. Small CTAs spread the few units over all SMs.
+constexpr int kVerifyThreads = 64;
+
+template <typename T, int K>
+__global__ void __launch_bounds__(kVerifyThreads)
+    k_verify(const T *__restrict__ bcx, int N, int D, int H, const T *__restrict__ w,
+             const int32_t *__restrict__ slots, const T *__restrict__ pool, int n_slots,
+             T *__restrict__ win_out, T *__restrict__ y) {
+    const int groups = H / kCh;
+    const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (unit >= (int64_t)N * groups) return;
+    const int i = (int)(unit / groups), cg = (int)(unit % groups), h0 = cg * kCh;
+    const int slot = slots[i];
+    if (slot < 0 || slot >= n_slots) {
+        if (cg == 0) raise_error(SC_DEV_BAD_SLOT);
+        return;
+    }
+    float wt[kCh][K], win[kCh][K];
+    load_block<T, K>(w + (int64_t)h0 * K, wt);
+    load_block<T, K>(pool + ((int64_t)slot * H + h0) * K, win);
+    const int64_t ld = 3 * (int64_t)H;
+    for (int j0 = 0; j0 < D; j0 += kChunk) {
+        Row<T> rb[kChunk], rc[kChunk], rx[kChunk];
+#pragma unroll
+        for (int jj = 0; jj < kChunk; ++jj) {
+            if (j0 + jj < D) {
+                const T *p = bcx + ((int64_t)i * D + j0 + jj) * ld + h0;
+                rb[jj] = load_row(p);
+                rc[jj] = load_row(p + H);
+                rx[jj] = load_row(p + 2 * H);
+            }
+        }
+#pragma unroll
+        for (int jj = 0; jj < kChunk; ++jj) {
+            if (j0 + jj < D) {
+                const int64_t t = (int64_t)i * D + j0 + jj;
+                float b[kCh], c[kCh], x[kCh], out[kCh];
+                unpack_row(rb[jj], b);
+                unpack_row(rc[jj], c);
+                unpack_row(rx[jj], x);
+#pragma unroll
+                for (int ch = 0; ch < kCh; ++ch)
+                    out[ch] = c[ch] * slide_dot<K>(win[ch], wt[ch], gate_in<T>(b[ch], x[ch]));
+                store_row(y + t * H + h0, out);
+                store_block<T, K>(win_out + (t * H + h0) * K, win);
+            }
+        }
+    }
+}
+
+template <typename T, int K>
+static cudaError_t verify_inst(const void *bcx, int N, int D, int H, const void *w,
+                               const int32_t *slots, const void *pool, int n_slots, void *win,
+                               void *y, cudaStream_t stream) {
+    const int64_t units = (int64_t)N * (H / kCh);
+    const int64_t blocks = (units + kVerifyThreads - 1) / kVerifyThreads;
+    k_verify<T, K><<<(unsigned)blocks, kVerifyThreads, 0, stream>>>(
+        (const T *)bcx, N, D, H, (const T *)w, slots, (const T *)pool, n_slots, (T *)win,
+        (T *)y);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t verify_K(int K, const void *bcx, int N, int D, int H, const void *w,
+                            const int32_t *slots, const void *pool, int n_slots, void *win,
+                            void *y, cudaStream_t s) {
+    switch (K) {
+        case 1: return verify_inst<T, 1>(bcx, N, D, H, w, slots, pool, n_slots, win, y, s);
+        case 2: return verify_inst<T, 2>(bcx, N, D, H, w, slots, pool, n_slots, win, y, s);
+        case 3: return verify_inst<T, 3>(bcx, N, D, H, w, slots, pool, n_slots, win, y, s);
+        default: return verify_inst<T, 4>(bcx, N, D, H, w, slots, pool, n_slots, win, y, s);
+    }
+}
+
+cudaError_t launch_verify(int dtype, int H, int K, const void *bcx, int N, int D, const void *w,
+                          const int32_t *slots, const void *pool, int n_slots, void *win,
+                          void *y, cudaStream_t s) {
+    if (dtype == SC_BF16)
+        return verify_K<__nv_bfloat16>(K, bcx, N, D, H, w, slots, pool, n_slots, win, y, s);
+    return verify_K<float>(K, bcx, N, D, H, w, slots, pool, n_slots, win, y, s);
+}
+
+// ----------------------------------------------------------------- rollback
+//
+// A plain 16-byte copy of the accepted window record into the slot.
+__global__ void __launch_bounds__(kThreads)
+    k_rollback(int N, int D, int64_t q_per_seq, const uint4 *__restrict__ win,
+               const int32_t *__restrict__ accepted, const int32_t *__restrict__ slots,
+               uint4 *__restrict__ pool, int n_slots) {
+    const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (unit >= (int64_t)N * q_per_seq) return;
+    const int i = (int)(unit / q_per_seq);
+    const int64_t q = unit % q_per_seq;
+    const int a = accepted[i], slot = slots[i];
+    if (a < 0 || a > D) {
+        if (q == 0) raise_error(SC_DEV_BAD_ACCEPTED);
+        return;
+    }
+    if (slot < 0 || slot >= n_slots) {
+        if (q == 0) raise_error(SC_DEV_BAD_SLOT);
+        return;
+    }
+    if (a == 0) return;
+    pool[(int64_t)slot * q_per_seq + q] = win[((int64_t)i * D + (a - 1)) * q_per_seq + q];
+}
+
+cudaError_t launch_rollback(int dtype, int H, int K, int N, int D, const void *win,
+                            const int32_t *accepted, const int32_t *slots, void *pool,
+                            int n_slots, cudaStream_t stream) {
+    const int64_t elem = dtype == SC_BF16 ? 2 : 4;
+    const int64_t q_per_seq = (int64_t)H * K * elem / 16;
+    const int64_t blocks = ((int64_t)N * q_per_seq + kThreads - 1) / kThreads;
+    k_rollback<<<(unsigned)blocks, kThreads, 0, stream>>>(N, D, q_per_seq, (const uint4 *)win,
+                                                         accepted, slots, (uint4 *)pool, n_slots);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ error word
+
+cudaError_t read_and_clear_error(cudaStream_t stream, unsigned int *code) {
+    k_take_error<<<1, 1, 0, stream>>>();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbolAsync(code, g_error_taken, sizeof(unsigned int), 0,
+                                  cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    return cudaStreamSynchronize(stream);
+}
+
+}  // namespace sc

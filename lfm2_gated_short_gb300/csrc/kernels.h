@@ -1,0 +1,42 @@
+// kernels.h -- internal launchers behind the C ABI (api.cu). Arguments are
+// already validated by the caller; these only pick a template instance and
+// enqueue on the stream. All return the cudaError_t of the launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace sc {
+
+// Prefill tile (rows per thread) chosen from the sizes and the SM count.
+int prefill_rows_per_thread(int64_t T, int H, int sm_count);
+
+cudaError_t launch_prefill(int dtype, int H, int K, const void *bcx, int64_t T, const void *w,
+                           const int32_t *cu_seqlens, int N, const int32_t *slot_ids,
+                           void *pool, int n_slots, void *y, int rows_per_thread,
+                           cudaStream_t stream);
+
+cudaError_t launch_decode(int dtype, int H, int K, const void *bcx, int N, const void *w,
+                          const int32_t *slot_ids, void *pool, int n_slots, void *y,
+                          cudaStream_t stream);
+
+cudaError_t launch_verify(int dtype, int H, int K, const void *bcx, int N, int D,
+                          const void *w, const int32_t *slot_ids, const void *pool,
+                          int n_slots, void *win, void *y, cudaStream_t stream);
+
+cudaError_t launch_rollback(int dtype, int H, int K, int N, int D, const void *win,
+                            const int32_t *accepted, const int32_t *slot_ids, void *pool,
+                            int n_slots, cudaStream_t stream);
+
+size_t backward_workspace_bytes(int H, int K, int64_t T);
+
+cudaError_t launch_backward(int dtype, int H, int K, const void *bcx, int64_t T,
+                            const void *w, const void *dy, void *dbcx, float *dw,
+                            void *workspace, cudaStream_t stream);
+
+// Read and clear the device error word of the current device (synchronous
+// with respect to `stream`).
+cudaError_t read_and_clear_error(cudaStream_t stream, unsigned int *code);
+
+}  // namespace sc

@@ -1,0 +1,126 @@
+"""The C ABI without a GPU: the library loads, exports what the header declares,
+and host-side argument validation answers before any CUDA call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from lfm2_gated_short_gb300 import build as sc_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+SC_OK, SC_EINVAL, SC_EUNSUPPORTED = 0, 1, 2
+BF16, F32 = 1, 0
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(HEADER_DIR)):
+        if fn.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(shortconv_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def L():
+    path = sc_build.build()
+    lib = ctypes.CDLL(path)
+    p, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    lib.shortconv_prefill.argtypes = [i32, i32, i32, p, i64, p, p, i32, p, p, i32, p, p]
+    lib.shortconv_prefill_tiled.argtypes = [i32, i32, i32, p, i64, p, p, i32, p, p, i32, p, i32, p]
+    lib.shortconv_decode.argtypes = [i32, i32, i32, p, i32, p, p, p, i32, p, p]
+    lib.shortconv_verify.argtypes = [i32, i32, i32, p, i32, i32, p, p, p, i32, p, p, p]
+    lib.shortconv_rollback.argtypes = [i32, i32, i32, i32, i32, p, p, p, p, i32, p]
+    lib.shortconv_backward_workspace_bytes.argtypes = [i32, i32, i64]
+    lib.shortconv_backward_workspace_bytes.restype = ctypes.c_size_t
+    lib.shortconv_backward.argtypes = [i32, i32, i32, p, i64, p, p, p, p, p, ctypes.c_size_t, p]
+    lib.shortconv_get_error.argtypes = [p, p]
+    lib.shortconv_status_string.argtypes = [i32]
+    lib.shortconv_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+def test_header_declares_the_hot_path_calls():
+    names = declared_functions()
+    for must in ("shortconv_prefill", "shortconv_decode", "shortconv_verify",
+                 "shortconv_rollback", "shortconv_backward",
+                 "shortconv_backward_workspace_bytes", "shortconv_get_error",
+                 "shortconv_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_function(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in include/ but not exported"
+
+
+# Fake, 256-byte aligned, non-overlapping "device" addresses: validation must
+# reject the call before anything touches them.
+BASE = 1 << 40
+A, Bp, Cp, Dp, Ep, Fp, Gp = (BASE + i * (1 << 32) for i in range(7))
+
+
+def prefill(L, dtype=BF16, H=256, K=3, bcx=A, T=64, w=Bp, cu=Cp, N=1, slots=Dp, pool=Ep,
+            n_slots=4, y=Fp):
+    return L.shortconv_prefill(dtype, H, K, bcx, T, w, cu, N, slots, pool, n_slots, y, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=7), SC_EUNSUPPORTED),
+    (dict(H=12), SC_EUNSUPPORTED),
+    (dict(K=5), SC_EUNSUPPORTED),
+    (dict(K=0), SC_EINVAL),
+    (dict(H=0), SC_EINVAL),
+    (dict(T=-1), SC_EINVAL),
+    (dict(T=1 << 31), SC_EINVAL),
+    (dict(N=-1), SC_EINVAL),
+    (dict(N=0), SC_EINVAL),                 # T > 0 with no sequences
+    (dict(n_slots=0), SC_EINVAL),
+    (dict(bcx=A + 8), SC_EINVAL),           # not 16-byte aligned
+    (dict(y=0), SC_EINVAL),                 # NULL output with rows
+    (dict(cu=Cp + 2), SC_EINVAL),           # int32 array not 4-byte aligned
+    (dict(y=A + 64), SC_EINVAL),            # y overlaps bcx
+    (dict(pool=Bp), SC_EINVAL),             # pool overlaps w
+])
+def test_prefill_argument_errors(L, kw, status):
+    assert prefill(L, **kw) == status
+
+
+def test_prefill_empty_call_is_ok_without_a_device(L):
+    assert prefill(L, T=0, N=0, bcx=0, y=0, cu=Cp, slots=0) == SC_OK
+
+
+def test_prefill_tiled_rejects_unbuilt_tiles(L):
+    st = L.shortconv_prefill_tiled(BF16, 256, 3, A, 64, Bp, Cp, 1, Dp, Ep, 4, Fp, 12, None)
+    assert st == SC_EINVAL
+
+
+def test_decode_verify_rollback_argument_errors(L):
+    assert L.shortconv_decode(BF16, 256, 3, A, 4, Bp, Dp, Ep, 4, A + 16, None) == SC_EINVAL
+    assert L.shortconv_decode(BF16, 256, 3, A, 4, Bp, Dp, Ep, 0, Fp, None) == SC_EINVAL
+    assert L.shortconv_decode(BF16, 256, 3, A, 0, Bp, 0, Ep, 4, 0, None) == SC_OK
+    assert L.shortconv_verify(BF16, 256, 3, A, 4, 0, Bp, Dp, Ep, 4, Fp, Gp, None) == SC_EINVAL
+    assert L.shortconv_verify(BF16, 256, 3, A, 4, 2, Bp, Dp, Ep, 4, Fp, Fp, None) == SC_EINVAL
+    assert L.shortconv_rollback(BF16, 256, 3, 4, 2, Fp, Cp, Dp, Fp, 4, None) == SC_EINVAL
+    assert L.shortconv_rollback(F32, 256, 3, 0, 2, 0, 0, 0, Ep, 4, None) == SC_OK
+
+
+def test_backward_workspace_and_errors(L):
+    ws = L.shortconv_backward_workspace_bytes(2048, 3, 65536)
+    assert ws > 0 and ws % 16 == 0
+    assert ws < 64 * 1024 * 1024        # a few MB of fp32 partials, not a T-sized buffer
+    assert L.shortconv_backward_workspace_bytes(12, 3, 100) == 0
+    assert L.shortconv_backward_workspace_bytes(2048, 3, -1) == 0
+    need = L.shortconv_backward_workspace_bytes(256, 3, 64)
+    assert L.shortconv_backward(BF16, 256, 3, A, 64, Bp, Cp, Dp, Ep, Fp, need - 1, None) == SC_EINVAL
+    assert L.shortconv_backward(BF16, 256, 3, A, 64, Bp, Cp, A, Ep, Fp, need, None) == SC_EINVAL
+
+
+def test_status_strings_and_get_error_null(L):
+    for s in range(6):
+        assert L.shortconv_status_string(s)
+    assert L.shortconv_get_error(None, None) == SC_EINVAL
