@@ -1,0 +1,584 @@
+#!/usr/bin/env python3
+"""Benchmark of the ShortConv hot path on GB300.
+
+Headline (one "step"): prefill of one LFM2-1.2B-shaped sequence, T=4096,
+H=2048, K=3, bf16, from slot 0 of a one-slot pool, through the C ABI. The
+value is algorithmic HBM bytes moved per second (GB/s). Inputs are resident
+in HBM; each step uses the next of R buffer sets (R x 67 MB > 4 x L2) so no
+step finds its inputs in L2.
+
+Also reported on the same run (rank 0): decode us/step (bs=256, 10 layers,
+CUDA-graph replay, L2 flushed between steps), speculative verify + rollback
+us/step (64 x 8 drafts, 10 layers), packed varlen prefill GB/s (16 sequences),
+the training path (T=65536 forward + backward) and the T=4096 forward +
+backward, an end-to-end number through host buffers, the roofline of the
+prefill kernel, SM clocks sampled during the run, and the CPU oracle timed
+on this host as a baseline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 launch with torchrun: every rank runs an independent replica of the
+headline (no data exchange), value = all ranks' bytes / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from lfm2_gated_short_gb300 import workloads as wl  # noqa: E402
+from lfm2_gated_short_gb300 import replicas  # noqa: E402
+
+METRIC = "ShortConv HBM GB/s (% peak), T=4096 H=2048 bf16; decode µs/step bs=256"
+WORKLOAD = "ShortConv prefill, 1 sequence, T=4096 H=2048 K=3 bf16, zero state (LFM2-1.2B conv layer)"
+H, K, T = 2048, 3, 4096
+E = 2  # bf16 bytes
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["lfm2_gated_short_gb300/csrc/forward.cu", "lfm2_gated_short_gb300/csrc/common.cuh"]
+PROFILE = "profiles/prefill_T4096_H2048.txt"
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def prefill_bytes(T_, H_, K_, N_, e=E):
+    """Algorithmic bytes of a prefill: read B,C,x and w, read K-1 state taps and
+    write K per sequence, write y."""
+    return T_ * 3 * H_ * e + T_ * H_ * e + H_ * K_ * e + N_ * H_ * (K_ - 1) * e + N_ * H_ * K_ * e
+
+
+def decode_bytes_per_layer(N_, H_, K_, e=E):
+    return N_ * (3 * H_ * e + H_ * e + H_ * (K_ - 1) * e + H_ * K_ * e)
+
+
+def verify_bytes_per_layer(N_, D_, H_, K_, e=E):
+    return N_ * D_ * (3 * H_ * e + H_ * e + H_ * K_ * e) + N_ * H_ * (K_ - 1) * e
+
+
+def rollback_bytes_per_layer(accepted, H_, K_, e=E):
+    return int((np.asarray(accepted) > 0).sum()) * 2 * H_ * K_ * e
+
+
+def backward_bytes(T_, H_, K_, e=E):
+    return T_ * (3 * H_ + H_) * e + T_ * 3 * H_ * e + H_ * K_ * e + H_ * K_ * 4
+
+
+def peak_hbm():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """dram bytes per launch from the committed ncu summary, if it covers this source."""
+    try:
+        fields = {}
+        with open(os.path.join(ROOT, PROFILE)) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("kernel_source_sha256_16") == kernel_source_hash():
+            return int(float(fields["traffic_bytes_per_launch"]))
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = []
+        for line in self.file.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), float(parts[3]),
+                             parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [r for r in rows if r[3] >= 50.0] or rows
+        reasons = sorted({n for r in loaded for n, v in zip(self.NAMES, r[4]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+# ---------------------------------------------------------------- helpers
+
+def to_dev(a, dtype, device):
+    if dtype == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.to(device)
+
+
+def randn_bf16(shape, gen, device, std=1.0):
+    t = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(torch.bfloat16)
+
+
+def run_ahead():
+    """Hold the stream for a few ms so the host can enqueue a whole timed loop
+    ahead of the GPU (launch cost then stays out of the device timings)."""
+    torch.cuda._sleep(20_000_000)
+
+
+def events(n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+# ----------------------------------------------------------------- sections
+
+def headline(sc, device, steps, warmup, dist):
+    p = wl.single_prefill()
+    bcx0 = to_dev(p.bcx, "bf16", device)
+    w = to_dev(p.w, "bf16", device)
+    cu = torch.tensor(p.cu_seqlens, device=device)
+    slots = torch.tensor(p.slot_ids, device=device)
+    nbytes = prefill_bytes(T, H, K, 1)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    R = max(2, math.ceil(4 * l2 / nbytes))
+    sets = [(bcx0.clone(), torch.empty((T, H), dtype=torch.bfloat16, device=device),
+             torch.zeros((1, H, K), dtype=torch.bfloat16, device=device)) for _ in range(R)]
+    for i in range(warmup):
+        b, y, pool = sets[i % R]
+        sc.prefill(b, w, cu, slots, pool, y=y)
+    torch.cuda.synchronize()
+    dist.barrier()
+    t0, t1 = events(2)
+    es, ee = events(steps), events(steps)
+    run_ahead()
+    t0.record()
+    for i in range(steps):
+        b, y, pool = sets[i % R]
+        es[i].record()
+        sc.prefill(b, w, cu, slots, pool, y=y)
+        ee[i].record()
+    t1.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    total_ms = t0.elapsed_time(t1)
+    launch_ms = [es[i].elapsed_time(ee[i]) for i in range(steps)]
+    assert sc.get_error() == 0
+    return dict(total_ms=total_ms, launch_ms=launch_ms, bytes=nbytes, R=R, l2=l2,
+                inputs=(p, w, cu, slots))
+
+
+def e2e(sc, device, inputs, steps):
+    """Same prefill through the public API from pinned host buffers: H2D of the
+    step's inputs, the call, D2H of y, all inside the timed region."""
+    p, w, _, _ = inputs
+    h_bcx = torch.from_numpy(p.bcx.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_cu = torch.from_numpy(p.cu_seqlens).pin_memory()
+    h_slots = torch.from_numpy(p.slot_ids).pin_memory()
+    h_y = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    d_bcx = torch.empty((T, 3 * H), dtype=torch.bfloat16, device=device)
+    d_cu = torch.empty(2, dtype=torch.int32, device=device)
+    d_slots = torch.empty(1, dtype=torch.int32, device=device)
+    d_y = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+    pool = torch.zeros((1, H, K), dtype=torch.bfloat16, device=device)
+
+    def step():
+        d_bcx.copy_(h_bcx, non_blocking=True)
+        d_cu.copy_(h_cu, non_blocking=True)
+        d_slots.copy_(h_slots, non_blocking=True)
+        sc.prefill(d_bcx, w, d_cu, d_slots, pool, y=d_y)
+        h_y.copy_(d_y, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    t0, t1 = events(2)
+    t0.record()
+    for _ in range(steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    h2d = h_bcx.numel() * 2 + h_cu.numel() * 4 + h_slots.numel() * 4
+    d2h = h_y.numel() * 2
+    return dict(ms=ms, value=prefill_bytes(T, H, K, 1) / (ms * 1e-3) / 1e9, h2d=h2d, d2h=d2h)
+
+
+def decode_section(sc, device, flush, layers=10, steps=64, batch=256, n_slots=1024):
+    g = torch.Generator(device=device).manual_seed(4)
+    rng = np.random.default_rng(4)
+    slots = torch.tensor(rng.permutation(n_slots)[:batch].astype(np.int32), device=device)
+    w = randn_bf16((layers, H, K), g, device, wl.WEIGHT_STD)
+    pools = randn_bf16((layers, n_slots, H, K), g, device)
+    bcx = randn_bf16((layers, steps, batch, 3 * H), g, device)
+    y = torch.empty((layers, batch, H), dtype=torch.bfloat16, device=device)
+
+    def one_step(s):
+        for l in range(layers):
+            sc.decode(bcx[l, s], w[l], slots, pools[l], y=y[l])
+
+    one_step(0)  # warm
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(device)
+    graphs = []
+    with torch.cuda.stream(side):
+        for s in range(steps):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=side):
+                one_step(s)
+            graphs.append(gr)
+    torch.cuda.synchronize()
+    es, ee = events(steps), events(steps)
+    for s in range(steps):
+        flush()
+        es[s].record()
+        graphs[s].replay()
+        ee[s].record()
+    torch.cuda.synchronize()
+    step_us = [es[s].elapsed_time(ee[s]) * 1e3 for s in range(steps)]
+    # one layer's kernel alone (cold L2), for the per-layer roofline
+    les, lee = events(steps), events(steps)
+    for s in range(steps):
+        flush()
+        les[s].record()
+        sc.decode(bcx[0, s], w[0], slots, pools[0], y=y[0])
+        lee[s].record()
+    torch.cuda.synchronize()
+    layer_us = [les[s].elapsed_time(lee[s]) * 1e3 for s in range(steps)]
+    assert sc.get_error() == 0
+    nb = decode_bytes_per_layer(batch, H, K)
+    return dict(us_per_step=statistics.median(step_us), us_per_step_mean=statistics.mean(step_us),
+                layer_us=statistics.median(layer_us), bytes_per_layer=nb,
+                layer_gbs=nb / (statistics.median(layer_us) * 1e-6) / 1e9,
+                step_gbs=layers * nb / (statistics.median(step_us) * 1e-6) / 1e9,
+                launches_per_step=layers)
+
+
+def verify_section(sc, device, flush, layers=10, batch=64, D=8, n_slots=1024, steps=32):
+    g = torch.Generator(device=device).manual_seed(5)
+    rng = np.random.default_rng(5)
+    slots = torch.tensor(rng.permutation(n_slots)[:batch].astype(np.int32), device=device)
+    accepted_np = rng.integers(0, D, size=batch, endpoint=True).astype(np.int32)
+    accepted = torch.tensor(accepted_np, device=device)
+    w = randn_bf16((layers, H, K), g, device, wl.WEIGHT_STD)
+    pools = randn_bf16((layers, n_slots, H, K), g, device)
+    bcx = randn_bf16((layers, batch * D, 3 * H), g, device)
+    win = torch.empty((layers, batch, D, H, K), dtype=torch.bfloat16, device=device)
+    y = torch.empty((layers, batch * D, H), dtype=torch.bfloat16, device=device)
+
+    def one_step():
+        for l in range(layers):
+            sc.verify(bcx[l], w[l], slots, pools[l], D, win=win[l], y=y[l])
+            sc.rollback(win[l], accepted, slots, pools[l])
+
+    one_step()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(device)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(gr, stream=side):
+            one_step()
+    torch.cuda.synchronize()
+    es, ee = events(steps), events(steps)
+    for s in range(steps):
+        flush()
+        es[s].record()
+        gr.replay()
+        ee[s].record()
+    torch.cuda.synchronize()
+    step_us = [es[s].elapsed_time(ee[s]) * 1e3 for s in range(steps)]
+    les, lee = events(steps), events(steps)
+    for s in range(steps):
+        flush()
+        les[s].record()
+        sc.verify(bcx[0], w[0], slots, pools[0], D, win=win[0], y=y[0])
+        lee[s].record()
+    torch.cuda.synchronize()
+    verify_us = statistics.median(les[s].elapsed_time(lee[s]) * 1e3 for s in range(steps))
+    assert sc.get_error() == 0
+    vb = verify_bytes_per_layer(batch, D, H, K)
+    rb = rollback_bytes_per_layer(accepted_np, H, K)
+    return dict(us_per_step=statistics.median(step_us), verify_layer_us=verify_us,
+                verify_bytes_per_layer=vb, rollback_bytes_per_layer=rb,
+                verify_layer_gbs=vb / (verify_us * 1e-6) / 1e9,
+                step_gbs=layers * (vb + rb) / (statistics.median(step_us) * 1e-6) / 1e9,
+                launches_per_step=2 * layers)
+
+
+def varlen_section(sc, device, reps=20):
+    p = wl.varlen_prefill()
+    sets = []
+    for _ in range(2):  # 2 x 277 MB > 4 x L2 per pair
+        sets.append((to_dev(p.bcx, "bf16", device), to_dev(p.pool, "bf16", device),
+                     torch.empty((p.T, H), dtype=torch.bfloat16, device=device)))
+    w = to_dev(p.w, "bf16", device)
+    cu = torch.tensor(p.cu_seqlens, device=device)
+    slots = torch.tensor(p.slot_ids, device=device)
+    for i in range(3):
+        b, pool, y = sets[i % 2]
+        sc.prefill(b, w, cu, slots, pool, y=y)
+    torch.cuda.synchronize()
+    es, ee = events(reps), events(reps)
+    run_ahead()
+    for i in range(reps):
+        b, pool, y = sets[i % 2]
+        es[i].record()
+        sc.prefill(b, w, cu, slots, pool, y=y)
+        ee[i].record()
+    torch.cuda.synchronize()
+    us = statistics.median(es[i].elapsed_time(ee[i]) * 1e3 for i in range(reps))
+    assert sc.get_error() == 0
+    nb = prefill_bytes(p.T, H, K, p.N)
+    return dict(T=p.T, n_seqs=p.N, us=us, bytes=nb, gbs=nb / (us * 1e-6) / 1e9)
+
+
+def training_section(sc, device, T_, reps, sets_n):
+    g = torch.Generator(device=device).manual_seed(6)
+    w = randn_bf16((H, K), g, device, wl.WEIGHT_STD)
+    cu = torch.tensor([0, T_], dtype=torch.int32, device=device)
+    slot = torch.zeros(1, dtype=torch.int32, device=device)
+    ws = torch.empty(max(16, sc.backward_workspace_bytes(H, K, T_)), dtype=torch.uint8,
+                     device=device)
+    dw = torch.empty((H, K), dtype=torch.float32, device=device)
+    sets = []
+    for _ in range(sets_n):
+        sets.append(dict(bcx=randn_bf16((T_, 3 * H), g, device), dy=randn_bf16((T_, H), g, device),
+                         y=torch.empty((T_, H), dtype=torch.bfloat16, device=device),
+                         dbcx=torch.empty((T_, 3 * H), dtype=torch.bfloat16, device=device),
+                         pool=torch.zeros((1, H, K), dtype=torch.bfloat16, device=device)))
+
+    def fwd(s):
+        sc.prefill(s["bcx"], w, cu, slot, s["pool"], y=s["y"])
+
+    def bwd(s):
+        sc.backward(s["bcx"], w, s["dy"], dbcx=s["dbcx"], dw=dw, workspace=ws)
+
+    for i in range(3):
+        fwd(sets[i % sets_n])
+        bwd(sets[i % sets_n])
+    torch.cuda.synchronize()
+    e0, e1, e2 = events(reps), events(reps), events(reps)
+    run_ahead()
+    for i in range(reps):
+        s = sets[i % sets_n]
+        e0[i].record()
+        fwd(s)
+        e1[i].record()
+        bwd(s)
+        e2[i].record()
+    torch.cuda.synchronize()
+    f_us = statistics.median(e0[i].elapsed_time(e1[i]) * 1e3 for i in range(reps))
+    b_us = statistics.median(e1[i].elapsed_time(e2[i]) * 1e3 for i in range(reps))
+    fb, bb = prefill_bytes(T_, H, K, 1), backward_bytes(T_, H, K)
+    return dict(T=T_, fwd_us=f_us, bwd_us=b_us, fwd_bwd_ms=(f_us + b_us) / 1e3,
+                fwd_gbs=fb / (f_us * 1e-6) / 1e9, bwd_gbs=bb / (b_us * 1e-6) / 1e9,
+                fwd_bytes=fb, bwd_bytes=bb)
+
+
+def cpu_baseline(seconds=10.0):
+    """The CPU oracle as it stands, single-threaded, on the headline workload."""
+    import oracle
+    p = wl.single_prefill()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        pool = p.pool.copy()
+        st, _ = oracle.prefill("bf16", p.bcx, p.w, p.cu_seqlens, p.slot_ids, pool)
+        assert st == oracle.OK
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    v = reps * prefill_bytes(T, H, K, 1) / el / 1e9
+    return {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} full T=4096 H=2048 prefills through the single-threaded C oracle "
+                      f"({el:.1f} s)"}
+
+
+# ------------------------------------------------------------ reference arm
+
+def reference_arm(args, rank):
+    """The CPU oracle timed as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    p = wl.single_prefill()
+    ch = np.arange(256)  # 256 of the 2048 channels (channels are independent)
+    cols = np.concatenate([ch, H + ch, 2 * H + ch])
+    bcx = np.ascontiguousarray(p.bcx[:, cols])
+    w = np.ascontiguousarray(p.w[ch])
+    nb = prefill_bytes(T, 256, K, 1)
+
+    def step():
+        pool = np.zeros((1, 256, K), np.uint16)
+        st, _ = oracle.prefill("bf16", bcx, w, p.cu_seqlens, p.slot_ids, pool)
+        assert st == oracle.OK
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    v = args.steps * nb / el / 1e9
+    sample = "T=4096 prefill on 256 of the 2048 channels per step, single-threaded C oracle"
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": config_dict(None),
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(h):
+    d = {"workload": WORKLOAD, "H": H, "K": K, "T": T, "n_seqs": 1,
+         "parallelism": "independent replicas, one per GPU"}
+    if h is not None:
+        d["l2"] = (f"rotating {h['R']} input/output buffer sets "
+                   f"({h['R'] * h['bytes'] / 1e6:.0f} MB > 4x the {h['l2'] / 1e6:.0f} MB L2)")
+    else:
+        d["l2"] = "host run"
+    return d
+
+
+# -------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = replicas.env_rank()
+
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        return
+
+    import lfm2_gated_short_gb300 as sc
+    sc.lib()  # fails loudly if the library is not built
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = replicas.Group(world, backend="nccl")
+    clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local)
+    clocks.start()
+    h = headline(sc, device, args.steps, args.warmup, dist)
+    max_ms = dist.max(h["total_ms"])
+    value = replicas.aggregate_gbs(h["bytes"], args.steps, world, max_ms)
+
+    if rank != 0:
+        clocks.stop()
+        dist.close()
+        return
+
+    flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+
+    def flush():
+        flush_buf.zero_()
+
+    extras = {}
+    extras["e2e"] = e2e(sc, device, h["inputs"], min(args.steps, 50))
+    extras["decode"] = decode_section(sc, device, flush)
+    extras["verify"] = verify_section(sc, device, flush)
+    extras["varlen"] = varlen_section(sc, device)
+    extras["train_T4096"] = training_section(sc, device, 4096, 20, 4)
+    extras["train_T65536"] = training_section(sc, device, 65536, 10, 1)
+    clk = clocks.stop()
+    del flush_buf
+    torch.cuda.empty_cache()
+    cpu = cpu_baseline()
+
+    peak, peak_kind = peak_hbm()
+    launch_s = statistics.mean(h["launch_ms"]) * 1e-3
+    achieved = h["bytes"] / launch_s / 1e9
+    ms_per_step = max_ms / args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) inputs, N(0,1/3) weights)",
+        "config": config_dict(h),
+        "pct_of_peak": 100.0 * value / world / peak,
+        "decode_us_per_step": extras["decode"]["us_per_step"],
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(),
+                     "kernel": "k_prefill<bf16,K=3>", "bytes_per_launch": h["bytes"],
+                     "peak_source": f"{peak_kind} hbm_gbs (copy)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": extras["e2e"]["value"], "unit": "GB/s",
+                "h2d_bytes_per_step": extras["e2e"]["h2d"],
+                "d2h_bytes_per_step": extras["e2e"]["d2h"],
+                "ms_per_step": extras["e2e"]["ms"]},
+        "clocks": clk,
+        "gpu_launches": args.steps,
+        "sections": {k: v for k, v in extras.items() if k != "e2e"},
+    }
+    log(json.dumps(line, indent=1))
+    print(json.dumps(line), flush=True)
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()

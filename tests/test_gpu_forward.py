@@ -1,0 +1,228 @@
+"""GPU forward path (prefill, decode, verify, rollback) against the CPU oracle.
+
+Every call goes through the C ABI (via the ctypes binding) on seeded inputs
+shared with the oracle: conv states and verify windows must match bit for
+bit, outputs within the tolerances in gpu_util.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import lfm2_gated_short_gb300 as sc
+from lfm2_gated_short_gb300 import workloads as wl
+from fixtures import tiny_fp32_golden, worked_example
+from gpu_util import assert_bits, assert_close, dev, host
+
+pytestmark = pytest.mark.gpu
+
+TILES = [4, 8, 16, 32]
+
+
+def run_prefill(p, tile=0):
+    pool = dev(p.pool, p.dtype)
+    y = sc.prefill(dev(p.bcx, p.dtype), dev(p.w, p.dtype), dev(p.cu_seqlens, "i32"),
+                   dev(p.slot_ids, "i32"), pool, rows_per_thread=tile)
+    torch.cuda.synchronize()
+    return host(y), host(pool)
+
+
+def oracle_prefill(p):
+    pool = p.pool.copy()
+    st, y = oracle.prefill(p.dtype, p.bcx, p.w, p.cu_seqlens, p.slot_ids, pool)
+    assert st == oracle.OK
+    return y, pool
+
+
+# ------------------------------------------------------------------ prefill
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_worked_example(dtype):
+    ex = worked_example(dtype)
+    pool = dev(ex["state"][None], dtype)
+    y = sc.prefill(dev(ex["bcx"], dtype), dev(ex["w"], dtype), dev(np.array([0, 4]), "i32"),
+                   dev(np.array([0]), "i32"), pool)
+    assert_bits(host(y), ex["y"], "y")
+    assert_bits(host(pool)[0], ex["final_state"], "state")
+
+
+def test_tiny_fp32_config_against_golden_and_oracle():
+    """One fp32 sequence, H=64, K=3, T=16 from zero state, then 4 decode tokens."""
+    g = tiny_fp32_golden()
+    pool = torch.zeros((1, g["H"], g["K"]), dtype=torch.float32, device="cuda")
+    w = dev(g["w"], "f32")
+    y = sc.prefill(dev(g["bcx"], "f32"), w, dev(np.array([0, g["T"]]), "i32"),
+                   dev(np.array([0]), "i32"), pool)
+    assert_close("f32", host(y), g["y_prefill"], "y prefill")
+    assert_bits(host(pool)[0], g["state_after_prefill"], "state after prefill")
+    slot = dev(np.array([0]), "i32")
+    for s in range(g["steps"]):
+        yd = sc.decode(dev(g["decode_bcx"][s], "f32"), w, slot, pool)
+        assert_close("f32", host(yd)[0], g["y_decode"][s], f"y decode {s}")
+    assert_bits(host(pool)[0], g["state_after_decode"], "state after decode")
+    assert sc.get_error() == 0
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
+@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_single_sequence_ragged(dtype, tile, K):
+    p = wl.single_prefill(T=301, H=256, K=K, seed=10 + K, dtype=dtype)
+    p.pool = wl.normal(np.random.default_rng(K), (1, 256, K), 1.0, dtype)  # continued prefill
+    y, pool = run_prefill(p, tile)
+    y_ref, pool_ref = oracle_prefill(p)
+    assert_close(dtype, y, y_ref, "y")
+    assert_bits(pool, pool_ref, "state")
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 5])
+def test_sequences_shorter_than_the_window(T):
+    p = wl.single_prefill(T=T, H=64, K=4, seed=20 + T)
+    p.pool = wl.normal(np.random.default_rng(T), (1, 64, 4), 1.0, "bf16")
+    y, pool = run_prefill(p, 4)
+    y_ref, pool_ref = oracle_prefill(p)
+    assert_close("bf16", y, y_ref, "y")
+    assert_bits(pool, pool_ref, "state")
+
+
+@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("K", [2, 3, 4])
+def test_varlen_with_empty_and_tiny_sequences(tile, K):
+    lengths = [0, 1, 2, 3, 5, 64, 100, 7, 0, 33, 4, 1, 0, 31, 32, 9]
+    p = wl.varlen_prefill(H=128, K=K, n_slots=40, seed=30 + K, lengths=lengths)
+    y, pool = run_prefill(p, tile)
+    y_ref, pool_ref = oracle_prefill(p)
+    assert_close("bf16", y, y_ref, "y")
+    assert_bits(pool, pool_ref, "pool (named and untouched slots)")
+
+
+def test_tiles_give_identical_bits():
+    p = wl.varlen_prefill(n_seqs=9, lo=1, hi=300, H=256, K=3, n_slots=16, seed=40)
+    outs = [run_prefill(p, t) for t in TILES]
+    for y, pool in outs[1:]:
+        assert_bits(y, outs[0][0], "y across tiles")
+        assert_bits(pool, outs[0][1], "pool across tiles")
+
+
+def test_prefill_T4096_H2048_full_size():
+    """LFM2-1.2B-shaped single-sequence prefill (T=4096, H=2048, K=3), automatic tile."""
+    p = wl.single_prefill()
+    y, pool = run_prefill(p, 0)
+    y_ref, pool_ref = oracle_prefill(p)
+    assert_close("bf16", y, y_ref, "y")
+    assert_bits(pool, pool_ref, "state")
+
+
+def test_packed_varlen_16_sequences_full_size():
+    """16 sequences, lengths U{64..2048}, 1024-slot pool, half continued from N(0,1) states."""
+    p = wl.varlen_prefill()
+    y, pool = run_prefill(p, 0)
+    y_ref, pool_ref = oracle_prefill(p)
+    assert_close("bf16", y, y_ref, "y")
+    assert_bits(pool, pool_ref, "pool")
+
+
+def test_chunked_prefill_and_decode_equal_full_prefill_on_gpu():
+    p = wl.single_prefill(T=200, H=256, K=3, seed=50)
+    y_full, pool_full = run_prefill(p, 8)
+    bcx = dev(p.bcx, "bf16")
+    w = dev(p.w, "bf16")
+    pool = dev(p.pool, "bf16")
+    slot = dev(np.array([0]), "i32")
+    ys = []
+    for a, b in [(0, 1), (1, 2), (2, 70), (70, 71), (71, 150)]:
+        ys.append(sc.prefill(bcx[a:b].contiguous(), w, dev(np.array([0, b - a]), "i32"), slot,
+                             pool))
+    for t in range(150, 200):
+        ys.append(sc.decode(bcx[t:t + 1].contiguous(), w, slot, pool))
+    assert_bits(host(torch.cat(ys)), y_full, "y")
+    assert_bits(host(pool), pool_full, "state")
+
+
+# ------------------------------------------------------------------- decode
+
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_decode_small(dtype, K):
+    s = wl.decode_serving(layers=1, steps=3, batch=37, H=64, K=K, n_slots=50, seed=60 + K,
+                          dtype=dtype)
+    pool = dev(s.pools[0], dtype)
+    ref = s.pools[0].copy()
+    w = dev(s.w[0], dtype)
+    slots = dev(s.slot_ids, "i32")
+    for step in range(3):
+        y = sc.decode(dev(s.bcx[0, step], dtype), w, slots, pool)
+        st, y_ref = oracle.decode(dtype, s.bcx[0, step], s.w[0], s.slot_ids, ref)
+        assert st == oracle.OK
+        assert_close(dtype, host(y), y_ref, f"y step {step}")
+    assert_bits(host(pool), ref, "pool")
+
+
+def test_decode_serving_256_sequences_two_layers():
+    """bs=256 decode, H=2048, 1024-slot pools, 2 layers x 8 steps of the serving workload."""
+    s = wl.decode_serving(layers=2, steps=8)
+    for layer in range(2):
+        pool = dev(s.pools[layer], "bf16")
+        ref = s.pools[layer].copy()
+        w = dev(s.w[layer], "bf16")
+        slots = dev(s.slot_ids, "i32")
+        for step in range(8):
+            y = sc.decode(dev(s.bcx[layer, step], "bf16"), w, slots, pool)
+            st, y_ref = oracle.decode("bf16", s.bcx[layer, step], s.w[layer], s.slot_ids, ref)
+            assert st == oracle.OK
+            assert_close("bf16", host(y), y_ref, f"layer {layer} step {step}")
+        assert_bits(host(pool), ref, f"pool layer {layer}")
+
+
+# ----------------------------------------------------------- verify/rollback
+
+@pytest.mark.parametrize("D", [1, 3, 4, 8])
+@pytest.mark.parametrize("K", [1, 3, 4])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_verify_and_rollback_small(dtype, K, D):
+    s = wl.verify_serving(layers=1, batch=9, D=D, H=64, K=K, n_slots=12, seed=70 + D + K,
+                          dtype=dtype)
+    pool = dev(s.pools[0], dtype)
+    win, y = sc.verify(dev(s.bcx[0], dtype), dev(s.w[0], dtype), dev(s.slot_ids, "i32"), pool, D)
+    st, win_ref, y_ref = oracle.verify(dtype, s.bcx[0], s.w[0], s.slot_ids, s.pools[0], D)
+    assert st == oracle.OK
+    assert_close(dtype, host(y), y_ref, "y")
+    assert_bits(host(win), win_ref, "win")
+    assert_bits(host(pool), s.pools[0], "pool untouched by verify")
+    sc.rollback(win, dev(s.accepted, "i32"), dev(s.slot_ids, "i32"), pool)
+    ref = s.pools[0].copy()
+    assert oracle.rollback(dtype, win_ref, s.accepted, s.slot_ids, ref) == oracle.OK
+    assert_bits(host(pool), ref, "pool after rollback")
+    assert sc.get_error() == 0
+
+
+def test_verify_64x8_full_width_then_rollback():
+    """64 sequences x 8 drafts, H=2048, 1024-slot pool, accepted ~ U{0..8}."""
+    s = wl.verify_serving(layers=1)
+    pool = dev(s.pools[0], "bf16")
+    win, y = sc.verify(dev(s.bcx[0], "bf16"), dev(s.w[0], "bf16"), dev(s.slot_ids, "i32"),
+                       pool, s.D)
+    st, win_ref, y_ref = oracle.verify("bf16", s.bcx[0], s.w[0], s.slot_ids, s.pools[0], s.D)
+    assert st == oracle.OK
+    assert_close("bf16", host(y), y_ref, "y")
+    assert_bits(host(win), win_ref, "win")
+    sc.rollback(win, dev(s.accepted, "i32"), dev(s.slot_ids, "i32"), pool)
+    ref = s.pools[0].copy()
+    assert oracle.rollback("bf16", win_ref, s.accepted, s.slot_ids, ref) == oracle.OK
+    assert_bits(host(pool), ref, "pool after rollback")
+
+
+def test_rollback_equals_decoding_the_accepted_prefix_on_gpu():
+    s = wl.verify_serving(layers=1, batch=16, D=5, H=128, K=3, n_slots=20, seed=80)
+    s.accepted = np.arange(16, dtype=np.int32) % 6
+    pool_v = dev(s.pools[0], "bf16")
+    w = dev(s.w[0], "bf16")
+    win, _ = sc.verify(dev(s.bcx[0], "bf16"), w, dev(s.slot_ids, "i32"), pool_v, s.D)
+    sc.rollback(win, dev(s.accepted, "i32"), dev(s.slot_ids, "i32"), pool_v)
+    pool_d = dev(s.pools[0], "bf16")
+    rows = s.bcx[0].reshape(16, s.D, -1)
+    for j in range(s.D):
+        take = np.nonzero(s.accepted > j)[0]
+        if len(take):
+            sc.decode(dev(rows[take, j], "bf16"), w, dev(s.slot_ids[take], "i32"), pool_d)
+    assert_bits(host(pool_v), host(pool_d), "rollback vs decode")
