@@ -69,6 +69,7 @@ typedef enum { SC_F32 = 0, SC_BF16 = 1 } sc_dtype;
 #define SC_DEV_BAD_SLOT 0x1u      /* a slot id outside [0, n_slots): that sequence skipped */
 #define SC_DEV_BAD_SEQLENS 0x2u   /* cu_seqlens not 0 = c0 <= c1 <= ... <= cN = T: call skipped */
 #define SC_DEV_BAD_ACCEPTED 0x4u  /* an accepted length outside [0, D]: that sequence skipped */
+#define SC_DEV_TIMEOUT 0x8u       /* a bounded wait on an asynchronous copy gave up: output incomplete */
 
 /*
  * Packed variable-length prefill (continued prefill from each slot's state).
@@ -93,7 +94,12 @@ typedef enum { SC_F32 = 0, SC_BF16 = 1 } sc_dtype;
  *   pool        device [n_slots, H, K]   read and written in place
  *   y           device [T, H]            written
  * Device errors: SC_DEV_BAD_SEQLENS (nothing is written), SC_DEV_BAD_SLOT
- * (that sequence's rows of y and its slot are not written).
+ * (that sequence's rows of y and its slot are not written), SC_DEV_TIMEOUT
+ * (an asynchronous row copy did not complete within 2 s; output incomplete).
+ *
+ * Implementation: one CTA per SM streams a balanced range of rows through
+ * shared memory with bulk asynchronous copies (see shortconv_prefill_tiled
+ * for the register-tiled alternative; both give identical bits).
  */
 sc_status shortconv_prefill(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
                             const void *w, const int32_t *cu_seqlens, int N,
@@ -101,10 +107,10 @@ sc_status shortconv_prefill(sc_dtype dtype, int H, int K, const void *bcx, int64
                             void *stream);
 
 /*
- * shortconv_prefill with an explicit tile: each thread computes 8 channels
- * of `rows_per_thread` consecutive rows (one of 4, 8, 16, 32; 0 picks one
- * from T, H and the device's SM count, which is what shortconv_prefill
- * does). Results are identical for every tile; only the speed differs.
+ * shortconv_prefill computed by the register-tiled kernel: each thread loads
+ * and computes 8 channels of `rows_per_thread` consecutive rows (one of 4, 8,
+ * 16, 32) straight from global memory; 0 means shortconv_prefill's streamed
+ * kernel. Every choice gives identical bits; only the speed differs.
  */
 sc_status shortconv_prefill_tiled(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
                                   const void *w, const int32_t *cu_seqlens, int N,

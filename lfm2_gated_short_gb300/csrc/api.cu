@@ -77,14 +77,11 @@ sc_status prefill_impl(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
         overlaps(pool, n_pool, w, n_w))
         return SC_EINVAL;
     if (N == 0) return SC_OK;
-    int L = rows_per_thread;
-    if (L == 0) {
-        const int sms = sm_count_of_current_device();
-        if (sms <= 0) return SC_ECUDA;
-        L = sc::prefill_rows_per_thread(T, H, sms);
-    }
+    const int sms = sm_count_of_current_device();
+    if (sms <= 0) return SC_ECUDA;
     return from_cuda(sc::launch_prefill(dtype, H, K, bcx, T, w, cu_seqlens, N, slot_ids, pool,
-                                        n_slots, y, L, (cudaStream_t)stream));
+                                        n_slots, y, rows_per_thread, sms,
+                                        (cudaStream_t)stream));
 }
 
 }  // namespace

@@ -9,6 +9,9 @@
 // Instead of the page's sequential per-token loop, prefill is a parallel FIR:
 // each thread owns 8 channels and a tile of L consecutive rows and rebuilds
 // the K-1 values of u before its tile from the B and x rows just above it.
+#include <algorithm>
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "shortconv.h"
@@ -75,7 +78,9 @@ __device__ __forceinline__ void run_rows(const T *__restrict__ bcx, int H, int h
     }
 }
 
-// ------------------------------------------------------------------ prefill
+#include "prefill_stream.cuh"
+
+// ------------------------------------------------------------ tiled prefill
 //
 // Unit = (row tile of L rows, channel group cg of 8 channels). A tile may
 // hold pieces of several sequences; each piece restarts its window.
@@ -179,18 +184,6 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-int prefill_rows_per_thread(int64_t T, int H, int sm_count) {
-    // Enough tiles for several resident CTAs per SM; longer tiles amortize the
-    // K-1 halo rows each tile re-reads.
-    const int64_t groups = H / kCh;
-    const int choices[4] = {32, 16, 8, 4};
-    for (int L : choices) {
-        const int64_t ctas = ((T + L - 1) / L * groups + kThreads - 1) / kThreads;
-        if (ctas >= 4LL * sm_count) return L;
-    }
-    return 4;
-}
-
 template <typename T, int K, int L>
 static cudaError_t prefill_inst(const void *bcx, int64_t rows, int H, const void *w,
                                 const int32_t *cu, int N, const int32_t *slots, void *pool,
@@ -227,9 +220,69 @@ static cudaError_t prefill_K(int K, int L, const void *bcx, int64_t rows, int H,
     }
 }
 
+template <typename T, int K>
+static cudaError_t prefill_stream_inst(const void *bcx, int64_t rows, int H, const void *w,
+                                       const int32_t *cu, int N, const int32_t *slots,
+                                       void *pool, int n_slots, void *y, int sm_count,
+                                       cudaStream_t stream) {
+    const int CW = std::min(kStreamSlice, H);
+    const int n_slices = (H + kStreamSlice - 1) / kStreamSlice;
+    const int threads = (CW / kCh + 31) / 32 * 32;
+    const size_t smem = stream_smem_bytes<T>(CW);
+    auto kern = k_prefill_stream<T, K>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    // Opt in to the large dynamic shared memory once per device; remember the
+    // occupancy of the last (device, slice width) seen.
+    static std::atomic<unsigned long long> configured{0};
+    static std::atomic<int> last_key{-1}, last_occ{0};
+    if (dev < 64 && !(configured.load() & (1ull << dev))) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)stream_smem_bytes<T>(kStreamSlice));
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(1ull << dev);
+    }
+    const int key = dev * 4096 + CW / kCh;
+    int occ = last_key.load() == key ? last_occ.load() : 0;
+    if (occ <= 0) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+        if (e != cudaSuccess) return e;
+        if (occ <= 0) return cudaErrorInvalidConfiguration;
+        last_occ.store(occ);
+        last_key.store(key);
+    }
+    int64_t n_row = std::min<int64_t>((rows + kStreamMinRows - 1) / kStreamMinRows,
+                                      (int64_t)sm_count * occ / n_slices);
+    if (n_row < 1) n_row = 1;
+    k_prefill_stream<T, K><<<(unsigned)(n_row * n_slices), threads, smem, stream>>>(
+        (const T *)bcx, rows, H, (const T *)w, cu, N, slots, (T *)pool, n_slots, (T *)y,
+        n_slices, (int)n_row);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t prefill_stream_K(int K, const void *bcx, int64_t rows, int H, const void *w,
+                                    const int32_t *cu, int N, const int32_t *slots, void *pool,
+                                    int n_slots, void *y, int sms, cudaStream_t s) {
+    switch (K) {
+        case 1: return prefill_stream_inst<T, 1>(bcx, rows, H, w, cu, N, slots, pool, n_slots, y, sms, s);
+        case 2: return prefill_stream_inst<T, 2>(bcx, rows, H, w, cu, N, slots, pool, n_slots, y, sms, s);
+        case 3: return prefill_stream_inst<T, 3>(bcx, rows, H, w, cu, N, slots, pool, n_slots, y, sms, s);
+        default: return prefill_stream_inst<T, 4>(bcx, rows, H, w, cu, N, slots, pool, n_slots, y, sms, s);
+    }
+}
+
 cudaError_t launch_prefill(int dtype, int H, int K, const void *bcx, int64_t rows, const void *w,
                            const int32_t *cu, int N, const int32_t *slots, void *pool,
-                           int n_slots, void *y, int L, cudaStream_t s) {
+                           int n_slots, void *y, int L, int sm_count, cudaStream_t s) {
+    if (L == 0) {
+        if (dtype == SC_BF16)
+            return prefill_stream_K<__nv_bfloat16>(K, bcx, rows, H, w, cu, N, slots, pool,
+                                                   n_slots, y, sm_count, s);
+        return prefill_stream_K<float>(K, bcx, rows, H, w, cu, N, slots, pool, n_slots, y,
+                                       sm_count, s);
+    }
     if (dtype == SC_BF16)
         return prefill_K<__nv_bfloat16>(K, L, bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
     return prefill_K<float>(K, L, bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);

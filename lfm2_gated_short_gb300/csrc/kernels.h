@@ -9,13 +9,12 @@
 
 namespace sc {
 
-// Prefill tile (rows per thread) chosen from the sizes and the SM count.
-int prefill_rows_per_thread(int64_t T, int H, int sm_count);
-
+// Prefill: rows_per_thread 0 selects the TMA-streamed kernel (one CTA per SM),
+// 4/8/16/32 the register-tiled kernel with that many rows per thread.
 cudaError_t launch_prefill(int dtype, int H, int K, const void *bcx, int64_t T, const void *w,
                            const int32_t *cu_seqlens, int N, const int32_t *slot_ids,
                            void *pool, int n_slots, void *y, int rows_per_thread,
-                           cudaStream_t stream);
+                           int sm_count, cudaStream_t stream);
 
 cudaError_t launch_decode(int dtype, int H, int K, const void *bcx, int N, const void *w,
                           const int32_t *slot_ids, void *pool, int n_slots, void *y,

@@ -16,7 +16,7 @@ from gpu_util import assert_bits, assert_close, dev, host
 
 pytestmark = pytest.mark.gpu
 
-TILES = [4, 8, 16, 32]
+TILES = [0, 4, 8, 16, 32]  # 0: the TMA-streamed kernel; others: register-tiled rows per thread
 
 
 def run_prefill(p, tile=0):
@@ -79,10 +79,11 @@ def test_single_sequence_ragged(dtype, tile, K):
 def test_sequences_shorter_than_the_window(T):
     p = wl.single_prefill(T=T, H=64, K=4, seed=20 + T)
     p.pool = wl.normal(np.random.default_rng(T), (1, 64, 4), 1.0, "bf16")
-    y, pool = run_prefill(p, 4)
     y_ref, pool_ref = oracle_prefill(p)
-    assert_close("bf16", y, y_ref, "y")
-    assert_bits(pool, pool_ref, "state")
+    for tile in (0, 4):
+        y, pool = run_prefill(p, tile)
+        assert_close("bf16", y, y_ref, "y")
+        assert_bits(pool, pool_ref, "state")
 
 
 @pytest.mark.parametrize("tile", TILES)
@@ -102,6 +103,39 @@ def test_tiles_give_identical_bits():
     for y, pool in outs[1:]:
         assert_bits(y, outs[0][0], "y across tiles")
         assert_bits(pool, outs[0][1], "pool across tiles")
+
+
+@pytest.mark.parametrize("H", [2560, 4096])
+def test_channel_slices_wider_than_one_cta(H):
+    p = wl.varlen_prefill(n_seqs=5, lo=1, hi=90, H=H, K=3, n_slots=7, seed=41)
+    outs = [run_prefill(p, t) for t in (0, 8)]
+    y_ref, pool_ref = oracle_prefill(p)
+    for y, pool in outs:
+        assert_close("bf16", y, y_ref, "y")
+        assert_bits(pool, pool_ref, "pool")
+
+
+def test_more_sequences_than_staged_in_shared_memory():
+    rng = np.random.default_rng(42)
+    lengths = rng.integers(0, 4, size=2100)
+    p = wl.varlen_prefill(H=64, K=3, n_slots=2200, seed=42, lengths=lengths)
+    y_ref, pool_ref = oracle_prefill(p)
+    for t in (0, 4):
+        y, pool = run_prefill(p, t)
+        assert_close("bf16", y, y_ref, "y")
+        assert_bits(pool, pool_ref, "pool")
+
+
+@pytest.mark.parametrize("T", [1, 7, 9, 17, 1217])
+def test_stream_kernel_row_split_edges(T):
+    """Few rows per CTA: halo and owner extensions cross many CTA boundaries."""
+    p = wl.varlen_prefill(H=256, K=4, n_slots=T + 2, seed=43 + T,
+                          lengths=np.diff(np.unique(np.r_[0, np.random.default_rng(T).integers(
+                              0, T, size=max(1, T // 3)), T])))
+    y_ref, pool_ref = oracle_prefill(p)
+    y, pool = run_prefill(p, 0)
+    assert_close("bf16", y, y_ref, "y")
+    assert_bits(pool, pool_ref, "pool")
 
 
 def test_prefill_T4096_H2048_full_size():
