@@ -192,7 +192,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 
     // Start sequence i at row max(s0, sr0): its output rows here, its slot, its window.
     auto enter = [&]() {
-        owner = s0 >= cr0;
+        // Sequences starting in the extension rows past cr1 belong to the next CTA.
+        owner = s0 >= cr0 && s0 < cr1;
         if (owner) {
             oa = s0;
             oe = min(s1, max(cr1, s0 + (K - 1)));
