@@ -47,7 +47,9 @@ WORKLOAD = "ShortConv prefill, 1 sequence, T=4096 H=2048 K=3 bf16, zero state (L
 H, K, T = 2048, 3, 4096
 E = 2  # bf16 bytes
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["lfm2_gated_short_gb300/csrc/forward.cu", "lfm2_gated_short_gb300/csrc/common.cuh"]
+KERNEL_SOURCES = ["lfm2_gated_short_gb300/csrc/forward.cu",
+                  "lfm2_gated_short_gb300/csrc/prefill_stream.cuh",
+                  "lfm2_gated_short_gb300/csrc/common.cuh", "lfm2_gated_short_gb300/csrc/launch.h"]
 PROFILE = "profiles/prefill_T4096_H2048.txt"
 
 
@@ -189,6 +191,18 @@ def events(n):
     return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
 
+def time_loop(fn, n):
+    """Average device time (us) of n back-to-back calls of fn(i), events at both ends."""
+    t0, t1 = events(2)
+    run_ahead()
+    t0.record()
+    for i in range(n):
+        fn(i)
+    t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) * 1e3 / n
+
+
 # ----------------------------------------------------------------- sections
 
 def headline(sc, device, steps, warmup, dist):
@@ -208,22 +222,17 @@ def headline(sc, device, steps, warmup, dist):
     torch.cuda.synchronize()
     dist.barrier()
     t0, t1 = events(2)
-    es, ee = events(steps), events(steps)
     run_ahead()
     t0.record()
     for i in range(steps):
         b, y, pool = sets[i % R]
-        es[i].record()
         sc.prefill(b, w, cu, slots, pool, y=y)
-        ee[i].record()
     t1.record()
     torch.cuda.synchronize()
     dist.barrier()
     total_ms = t0.elapsed_time(t1)
-    launch_ms = [es[i].elapsed_time(ee[i]) for i in range(steps)]
     assert sc.get_error() == 0
-    return dict(total_ms=total_ms, launch_ms=launch_ms, bytes=nbytes, R=R, l2=l2,
-                inputs=(p, w, cu, slots))
+    return dict(total_ms=total_ms, bytes=nbytes, R=R, l2=l2, inputs=(p, w, cu, slots))
 
 
 def e2e(sc, device, inputs, steps):
@@ -372,19 +381,14 @@ def varlen_section(sc, device, reps=20):
     w = to_dev(p.w, "bf16", device)
     cu = torch.tensor(p.cu_seqlens, device=device)
     slots = torch.tensor(p.slot_ids, device=device)
+    def call(i):
+        b, pool, y = sets[i % 2]
+        sc.prefill(b, w, cu, slots, pool, y=y)
+
     for i in range(3):
-        b, pool, y = sets[i % 2]
-        sc.prefill(b, w, cu, slots, pool, y=y)
+        call(i)
     torch.cuda.synchronize()
-    es, ee = events(reps), events(reps)
-    run_ahead()
-    for i in range(reps):
-        b, pool, y = sets[i % 2]
-        es[i].record()
-        sc.prefill(b, w, cu, slots, pool, y=y)
-        ee[i].record()
-    torch.cuda.synchronize()
-    us = statistics.median(es[i].elapsed_time(ee[i]) * 1e3 for i in range(reps))
+    us = time_loop(call, reps)
     assert sc.get_error() == 0
     nb = prefill_bytes(p.T, H, K, p.N)
     return dict(T=p.T, n_seqs=p.N, us=us, bytes=nb, gbs=nb / (us * 1e-6) / 1e9)
@@ -415,22 +419,14 @@ def training_section(sc, device, T_, reps, sets_n):
         fwd(sets[i % sets_n])
         bwd(sets[i % sets_n])
     torch.cuda.synchronize()
-    e0, e1, e2 = events(reps), events(reps), events(reps)
-    run_ahead()
-    for i in range(reps):
-        s = sets[i % sets_n]
-        e0[i].record()
-        fwd(s)
-        e1[i].record()
-        bwd(s)
-        e2[i].record()
-    torch.cuda.synchronize()
-    f_us = statistics.median(e0[i].elapsed_time(e1[i]) * 1e3 for i in range(reps))
-    b_us = statistics.median(e1[i].elapsed_time(e2[i]) * 1e3 for i in range(reps))
+    f_us = time_loop(lambda i: fwd(sets[i % sets_n]), reps)
+    b_us = time_loop(lambda i: bwd(sets[i % sets_n]), reps)
+    fb_us = time_loop(lambda i: (fwd(sets[i % sets_n]), bwd(sets[i % sets_n])), reps)
+    assert sc.get_error() == 0
     fb, bb = prefill_bytes(T_, H, K, 1), backward_bytes(T_, H, K)
-    return dict(T=T_, fwd_us=f_us, bwd_us=b_us, fwd_bwd_ms=(f_us + b_us) / 1e3,
+    return dict(T=T_, fwd_us=f_us, bwd_us=b_us, fwd_bwd_ms=fb_us / 1e3,
                 fwd_gbs=fb / (f_us * 1e-6) / 1e9, bwd_gbs=bb / (b_us * 1e-6) / 1e9,
-                fwd_bytes=fb, bwd_bytes=bb)
+                fwd_bwd_gbs=(fb + bb) / (fb_us * 1e-6) / 1e9, fwd_bytes=fb, bwd_bytes=bb)
 
 
 def cpu_baseline(seconds=10.0):
@@ -551,7 +547,7 @@ def main():
     cpu = cpu_baseline()
 
     peak, peak_kind = peak_hbm()
-    launch_s = statistics.mean(h["launch_ms"]) * 1e-3
+    launch_s = h["total_ms"] * 1e-3 / args.steps  # average launch duration, events at both ends
     achieved = h["bytes"] / launch_s / 1e9
     ms_per_step = max_ms / args.steps
     line = {
@@ -564,7 +560,8 @@ def main():
         "decode_us_per_step": extras["decode"]["us_per_step"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(),
-                     "kernel": "k_prefill<bf16,K=3>", "bytes_per_launch": h["bytes"],
+                     "kernel": "k_prefill_stream<bf16,K=3>", "bytes_per_launch": h["bytes"],
+                     "launch_us": launch_s * 1e6,
                      "peak_source": f"{peak_kind} hbm_gbs (copy)"},
         "cpu_baseline": cpu,
         "e2e": {"value": extras["e2e"]["value"], "unit": "GB/s",

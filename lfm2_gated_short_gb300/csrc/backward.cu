@@ -16,6 +16,7 @@
 // kernel adds the partials in a fixed order (deterministic bits).
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.h"
 #include "shortconv.h"
 
 namespace sc {
@@ -48,6 +49,7 @@ __global__ void __launch_bounds__(kBwdGroups *kBwdSegs)
                const T *__restrict__ dy, T *__restrict__ dbcx, float *__restrict__ partial,
                int RB) {
     constexpr int KH = K > 1 ? K - 1 : 1;  // history / look-ahead depth
+    pdl_wait();
     const int groups = H / kCh;
     const int cg = blockIdx.x * kBwdGroups + threadIdx.x;
     const int h0 = cg * kCh;
@@ -194,6 +196,7 @@ __global__ void __launch_bounds__(kBwdGroups *kBwdSegs)
         }
     }
 
+    pdl_launch_dependents();
     // dW: add the 8 segments of this CTA in a fixed order, one partial per CTA row.
     __shared__ float red[kBwdSegs][kBwdGroups * kCh * K];
 #pragma unroll
@@ -215,6 +218,8 @@ __global__ void __launch_bounds__(kBwdGroups *kBwdSegs)
 // dw[e] = sum over CTA rows g = 0 .. G-1 of partial[g][e], in that order.
 __global__ void __launch_bounds__(256)
     k_dw_reduce(const float *__restrict__ partial, int64_t G, int HK, float *__restrict__ dw) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= HK) return;
     float s = 0.f;
@@ -230,14 +235,14 @@ static cudaError_t backward_inst(const void *bcx, int64_t rows, int H, const voi
     const int64_t gy = bwd_row_ctas(H, rows);
     const int gx = (H / kCh + kBwdGroups - 1) / kBwdGroups;
     if (gy > 0) {
-        k_backward<T, K><<<dim3(gx, (unsigned)gy), dim3(kBwdGroups, kBwdSegs), 0, stream>>>(
+        const cudaError_t e = launch_pdl(
+            k_backward<T, K>, dim3(gx, (unsigned)gy), dim3(kBwdGroups, kBwdSegs), 0, stream,
             (const T *)bcx, rows, H, (const T *)w, (const T *)dy, (T *)dbcx, (float *)ws, RB);
-        const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     const int HK = H * K;
-    k_dw_reduce<<<(HK + 255) / 256, 256, 0, stream>>>((const float *)ws, gy, HK, dw);
-    return cudaGetLastError();
+    return launch_pdl(k_dw_reduce, dim3((HK + 255) / 256), dim3(256), 0, stream,
+                      (const float *)ws, gy, HK, dw);
 }
 
 template <typename T>

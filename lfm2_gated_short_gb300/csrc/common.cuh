@@ -13,6 +13,19 @@ namespace sc {
 
 constexpr int kCh = 8;  // channels per thread
 
+// Programmatic dependent launch. The kernels are launched with programmatic
+// stream serialization, so a kernel may be scheduled while the previous one
+// in the stream is still running. pdl_wait() returns once every previous
+// kernel has completed and its writes are visible: it comes before a
+// kernel's first global memory access. pdl_launch_dependents() lets the next
+// kernel be scheduled as soon as this grid's CTAs have all started; that
+// kernel still waits for this one to complete before touching memory.
+// Launched without the attribute, both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------- raw 128-bit I/O
 
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
@@ -186,6 +199,181 @@ __device__ __forceinline__ float slide_dot(float (&win)[K], const float (&wk)[K]
 #pragma unroll
     for (int k = 1; k < K; ++k) z = fmaf(wk[k], win[k], z);
     return z;
+}
+
+// ------------------------------------------------ packed pairs (sm_100 family)
+//
+// Two fp32 lanes in one 64-bit register (f32x2) and two bf16 lanes in one
+// 32-bit register. mul.rn.bf16x2 rounds the exact product once to bf16, the
+// same value as gate_in<bf16>; fma.rn.f32x2 / mul.rn.f32x2 round each lane
+// exactly like the scalar fmaf / multiply. Kernels using these produce the
+// same bits as the scalar helpers above when they keep the operation order.
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 f2_make(float lo, float hi) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(f32x2 v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 bf2_to_f2(uint32_t w) {
+    return f2_make(bf16_lo(w), bf16_hi(w));
+}
+__device__ __forceinline__ uint32_t f2_to_bf2(f32x2 v) {
+    float lo, hi;
+    f2_split(v, lo, hi);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));  // hi -> upper half
+    return r;
+}
+
+// CPT consecutive channels of one row section (CPT = 2, 4 or 8) as raw
+// 32-bit words, loaded from shared memory and stored to global memory with
+// one access of CPT * sizeof(T) bytes (two for 32 bytes).
+template <typename T, int CPT>
+struct Sec {
+    static constexpr int NW = CPT * (int)sizeof(T) / 4;  // 32-bit words
+    static constexpr int NP = CPT / 2;                    // channel pairs
+    uint32_t w[NW];
+};
+
+__device__ __forceinline__ void lds_words(uint32_t addr, uint32_t *w, int nw) {
+    if (nw == 1) {
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[0]) : "r"(addr));
+    } else if (nw == 2) {
+        asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "r"(addr));
+    } else {
+        for (int i = 0; i < nw; i += 4)
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(w[i]), "=r"(w[i + 1]), "=r"(w[i + 2]), "=r"(w[i + 3])
+                         : "r"(addr + 4 * i));
+    }
+}
+
+__device__ __forceinline__ void stg_words(void *p, const uint32_t *w, int nw) {
+    if (nw == 1) {
+        asm volatile("st.global.cs.b32 [%0], %1;" ::"l"(p), "r"(w[0]) : "memory");
+    } else if (nw == 2) {
+        asm volatile("st.global.cs.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(w[0]), "r"(w[1])
+                     : "memory");
+    } else {
+        for (int i = 0; i < nw; i += 4)
+            asm volatile("st.global.cs.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"((char *)p + 4 * i),
+                         "r"(w[i]), "r"(w[i + 1]), "r"(w[i + 2]), "r"(w[i + 3])
+                         : "memory");
+    }
+}
+
+template <typename T, int CPT>
+__device__ __forceinline__ Sec<T, CPT> lds_sec(uint32_t addr) {
+    Sec<T, CPT> r;
+    lds_words(addr, r.w, Sec<T, CPT>::NW);
+    return r;
+}
+
+// u = round(B * x) and widening of C, as CPT/2 f32x2 pairs, and the y store.
+template <typename T, int CPT>
+struct Pairs;
+
+template <int CPT>
+struct Pairs<__nv_bfloat16, CPT> {
+    using S = Sec<__nv_bfloat16, CPT>;
+    static __device__ __forceinline__ void widen(const S &r, f32x2 (&f)[S::NP]) {
+#pragma unroll
+        for (int p = 0; p < S::NP; ++p) f[p] = bf2_to_f2(r.w[p]);
+    }
+    static __device__ __forceinline__ void gate(const S &b, const S &x, f32x2 (&u)[S::NP]) {
+#pragma unroll
+        for (int p = 0; p < S::NP; ++p) u[p] = bf2_to_f2(bf2_mul(b.w[p], x.w[p]));
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16 *dst, const f32x2 (&y)[S::NP]) {
+        uint32_t w[S::NW];
+#pragma unroll
+        for (int p = 0; p < S::NP; ++p) w[p] = f2_to_bf2(y[p]);
+        stg_words(dst, w, S::NW);
+    }
+};
+
+template <int CPT>
+struct Pairs<float, CPT> {
+    using S = Sec<float, CPT>;
+    static __device__ __forceinline__ void widen(const S &r, f32x2 (&f)[S::NP]) {
+#pragma unroll
+        for (int p = 0; p < S::NP; ++p)
+            f[p] = f2_make(__uint_as_float(r.w[2 * p]), __uint_as_float(r.w[2 * p + 1]));
+    }
+    static __device__ __forceinline__ void gate(const S &b, const S &x, f32x2 (&u)[S::NP]) {
+        f32x2 fb[S::NP], fx[S::NP];
+        widen(b, fb);
+        widen(x, fx);
+#pragma unroll
+        for (int p = 0; p < S::NP; ++p) u[p] = f2_mul(fb[p], fx[p]);
+    }
+    static __device__ __forceinline__ void store(float *dst, const f32x2 (&y)[S::NP]) {
+        uint32_t w[S::NW];
+#pragma unroll
+        for (int p = 0; p < S::NP; ++p) {
+            float lo, hi;
+            f2_split(y[p], lo, hi);
+            w[2 * p] = __float_as_uint(lo);
+            w[2 * p + 1] = __float_as_uint(hi);
+        }
+        stg_words(dst, w, S::NW);
+    }
+};
+
+// CPT channels x K taps of a [H, K] array (weights or a state), element by
+// element (these are read once per sequence, so alignment is not assumed).
+template <typename T>
+__device__ __forceinline__ float ld_elem(const T *p) {
+    if constexpr (sizeof(T) == 2)
+        return __uint_as_float((uint32_t)(*reinterpret_cast<const unsigned short *>(p)) << 16);
+    else
+        return *p;
+}
+template <typename T>
+__device__ __forceinline__ void st_elem(T *p, float v) {  // v representable in T
+    if constexpr (sizeof(T) == 2)
+        *reinterpret_cast<unsigned short *>(p) = (unsigned short)(__float_as_uint(v) >> 16);
+    else
+        *p = v;
+}
+template <typename T, int CPT, int K>
+__device__ __forceinline__ void load_taps(const T *p, f32x2 (&f)[K][CPT / 2]) {
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+#pragma unroll
+        for (int q = 0; q < CPT / 2; ++q)
+            f[k][q] = f2_make(ld_elem(p + (2 * q) * K + k), ld_elem(p + (2 * q + 1) * K + k));
+}
+template <typename T, int CPT, int K>
+__device__ __forceinline__ void store_taps(T *p, const f32x2 (&f)[K][CPT / 2]) {
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+#pragma unroll
+        for (int q = 0; q < CPT / 2; ++q) {
+            float lo, hi;
+            f2_split(f[k][q], lo, hi);
+            st_elem(p + (2 * q) * K + k, lo);
+            st_elem(p + (2 * q + 1) * K + k, hi);
+        }
 }
 
 }  // namespace sc

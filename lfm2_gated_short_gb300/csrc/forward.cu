@@ -14,6 +14,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.h"
 #include "shortconv.h"
 
 namespace sc {
@@ -99,6 +100,8 @@ __global__ void __launch_bounds__(kThreads)
               T *__restrict__ pool, int n_slots, T *__restrict__ y) {
     __shared__ int32_t s_cu[kMaxStagedSeqs + 1];
     const bool staged = N <= kMaxStagedSeqs;
+    pdl_wait();
+    pdl_launch_dependents();
 
     // The whole call is skipped unless cu_seqlens is 0 = c0 <= ... <= cN = T.
     int bad = 0;
@@ -191,9 +194,9 @@ static cudaError_t prefill_inst(const void *bcx, int64_t rows, int H, const void
     const int64_t units = (rows + L - 1) / L * (H / kCh);
     int64_t blocks = (units + kThreads - 1) / kThreads;
     if (blocks < 1) blocks = 1;  // still validates cu_seqlens
-    k_prefill<T, K, L><<<(unsigned)blocks, kThreads, 0, stream>>>(
-        (const T *)bcx, rows, H, (const T *)w, cu, N, slots, (T *)pool, n_slots, (T *)y);
-    return cudaGetLastError();
+    return launch_pdl(k_prefill<T, K, L>, dim3((unsigned)blocks), dim3(kThreads), 0, stream,
+                      (const T *)bcx, rows, H, (const T *)w, cu, N, slots, (T *)pool, n_slots,
+                      (T *)y);
 }
 
 template <typename T, int K>
@@ -227,7 +230,7 @@ static cudaError_t prefill_stream_inst(const void *bcx, int64_t rows, int H, con
                                        cudaStream_t stream) {
     const int CW = std::min(kStreamSlice, H);
     const int n_slices = (H + kStreamSlice - 1) / kStreamSlice;
-    const int threads = (CW / kCh + 31) / 32 * 32;
+    const int threads = (CW / kStreamCpt + 31) / 32 * 32 + 32;  // consumers + one producer warp
     const size_t smem = stream_smem_bytes<T>(CW);
     auto kern = k_prefill_stream<T, K>;
     int dev = 0;
@@ -255,10 +258,9 @@ static cudaError_t prefill_stream_inst(const void *bcx, int64_t rows, int H, con
     int64_t n_row = std::min<int64_t>((rows + kStreamMinRows - 1) / kStreamMinRows,
                                       (int64_t)sm_count * occ / n_slices);
     if (n_row < 1) n_row = 1;
-    k_prefill_stream<T, K><<<(unsigned)(n_row * n_slices), threads, smem, stream>>>(
-        (const T *)bcx, rows, H, (const T *)w, cu, N, slots, (T *)pool, n_slots, (T *)y,
-        n_slices, (int)n_row);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)(n_row * n_slices)), dim3(threads), smem, stream,
+                      (const T *)bcx, rows, H, (const T *)w, cu, N, slots, (T *)pool, n_slots,
+                      (T *)y, n_slices, (int)n_row);
 }
 
 template <typename T>
@@ -297,6 +299,8 @@ __global__ void __launch_bounds__(kThreads)
     k_decode(const T *__restrict__ bcx, int N, int H, const T *__restrict__ w,
              const int32_t *__restrict__ slots, T *__restrict__ pool, int n_slots,
              T *__restrict__ y) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int groups = H / kCh;
     const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (unit >= (int64_t)N * groups) return;
@@ -330,9 +334,8 @@ static cudaError_t decode_inst(const void *bcx, int N, int H, const void *w,
                                cudaStream_t stream) {
     const int64_t units = (int64_t)N * (H / kCh);
     const int64_t blocks = (units + kThreads - 1) / kThreads;
-    k_decode<T, K><<<(unsigned)blocks, kThreads, 0, stream>>>(
-        (const T *)bcx, N, H, (const T *)w, slots, (T *)pool, n_slots, (T *)y);
-    return cudaGetLastError();
+    return launch_pdl(k_decode<T, K>, dim3((unsigned)blocks), dim3(kThreads), 0, stream,
+                      (const T *)bcx, N, H, (const T *)w, slots, (T *)pool, n_slots, (T *)y);
 }
 
 template <typename T>
@@ -365,6 +368,8 @@ __global__ void __launch_bounds__(kVerifyThreads)
     k_verify(const T *__restrict__ bcx, int N, int D, int H, const T *__restrict__ w,
              const int32_t *__restrict__ slots, const T *__restrict__ pool, int n_slots,
              T *__restrict__ win_out, T *__restrict__ y) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int groups = H / kCh;
     const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (unit >= (int64_t)N * groups) return;
@@ -413,10 +418,9 @@ static cudaError_t verify_inst(const void *bcx, int N, int D, int H, const void 
                                void *y, cudaStream_t stream) {
     const int64_t units = (int64_t)N * (H / kCh);
     const int64_t blocks = (units + kVerifyThreads - 1) / kVerifyThreads;
-    k_verify<T, K><<<(unsigned)blocks, kVerifyThreads, 0, stream>>>(
-        (const T *)bcx, N, D, H, (const T *)w, slots, (const T *)pool, n_slots, (T *)win,
-        (T *)y);
-    return cudaGetLastError();
+    return launch_pdl(k_verify<T, K>, dim3((unsigned)blocks), dim3(kVerifyThreads), 0, stream,
+                      (const T *)bcx, N, D, H, (const T *)w, slots, (const T *)pool, n_slots,
+                      (T *)win, (T *)y);
 }
 
 template <typename T>
@@ -446,6 +450,8 @@ __global__ void __launch_bounds__(kThreads)
     k_rollback(int N, int D, int64_t q_per_seq, const uint4 *__restrict__ win,
                const int32_t *__restrict__ accepted, const int32_t *__restrict__ slots,
                uint4 *__restrict__ pool, int n_slots) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (unit >= (int64_t)N * q_per_seq) return;
     const int i = (int)(unit / q_per_seq);
@@ -469,9 +475,8 @@ cudaError_t launch_rollback(int dtype, int H, int K, int N, int D, const void *w
     const int64_t elem = dtype == SC_BF16 ? 2 : 4;
     const int64_t q_per_seq = (int64_t)H * K * elem / 16;
     const int64_t blocks = ((int64_t)N * q_per_seq + kThreads - 1) / kThreads;
-    k_rollback<<<(unsigned)blocks, kThreads, 0, stream>>>(N, D, q_per_seq, (const uint4 *)win,
-                                                         accepted, slots, (uint4 *)pool, n_slots);
-    return cudaGetLastError();
+    return launch_pdl(k_rollback, dim3((unsigned)blocks), dim3(kThreads), 0, stream, N, D,
+                      q_per_seq, (const uint4 *)win, accepted, slots, (uint4 *)pool, n_slots);
 }
 
 // ------------------------------------------------------------ error word

@@ -1,0 +1,29 @@
+// launch.h -- host-side kernel launch with programmatic stream serialization.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <utility>
+
+namespace sc {
+
+// Launch `kernel` on `stream` allowing it to be scheduled before the previous
+// kernel in the stream completes (the kernel itself waits with pdl_wait()
+// before touching memory). Returns the launch's cudaError_t.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace sc
