@@ -200,6 +200,34 @@ sc_status shortconv_backward(sc_dtype dtype, int H, int K, const void *bcx, int6
                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * shortconv_backward without a workspace argument, for callers that cannot
+ * allocate device memory when they call: code running inside a host
+ * framework that owns all device memory through its own pool and forbids
+ * direct cudaMalloc, and latency-critical paths where an allocation's
+ * implicit device-wide synchronization, or an out-of-memory failure in the
+ * middle of a step, is not acceptable. The pages have no counterpart to this
+ * call; it only moves the scratch.
+ *
+ * Same arguments, results and bits as shortconv_backward. The fp32 dW
+ * partials live in a fixed 8 MiB device array inside the library, which
+ * every GPU that loads the library holds until the process exits. The call
+ * allocates nothing and never calls cudaMalloc or cudaFree.
+ *   - Sizes whose shortconv_backward_workspace_bytes(H, K, T) exceeds 8 MiB
+ *     are rejected with SC_EUNSUPPORTED before anything is enqueued (for
+ *     H = 2048, K = 3 that is T above 2,793,472 rows).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture on that device.
+ *   - All calls on a device share the one array and each overwrites it
+ *     before reading it, so no clearing is needed; calls that overlap on the
+ *     GPU (for instance on two streams) race on it and must be serialized
+ *     by the caller.
+ */
+sc_status shortconv_backward_noalloc(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
+                                     const void *w, const void *dy, void *dbcx, float *dw,
+                                     void *stream);
+
+/*
  * Synchronize `stream`, then read and clear the current device's error word.
  * *device_code receives the SC_DEV_* bits seen since the last clear (0 if
  * none). Returns SC_OK if the word was 0, SC_EDEVICE if not, SC_ECUDA if a

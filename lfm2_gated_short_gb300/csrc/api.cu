@@ -200,6 +200,29 @@ sc_status shortconv_backward(sc_dtype dtype, int H, int K, const void *bcx, int6
                                          (cudaStream_t)stream));
 }
 
+sc_status shortconv_backward_noalloc(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
+                                     const void *w, const void *dy, void *dbcx, float *dw,
+                                     void *stream) {
+    sc_status st = check_shape(dtype, H, K);
+    if (st != SC_OK) return st;
+    if (T < 0 || T > INT32_MAX) return SC_EINVAL;
+    if (sc::backward_workspace_bytes(H, K, T) > sc::kNoAllocScratchBytes) return SC_EUNSUPPORTED;
+    const size_t es = elem_size(dtype);
+    const size_t n_bcx = (size_t)T * 3 * H * es, n_dy = (size_t)T * H * es;
+    const size_t n_w = (size_t)H * K * es, n_dw = (size_t)H * K * 4;
+    if (!ptr_ok(bcx, n_bcx, 16) || !ptr_ok(dy, n_dy, 16) || !ptr_ok(w, n_w, 16) ||
+        !ptr_ok(dbcx, n_bcx, 16) || !ptr_ok(dw, n_dw, 4))
+        return SC_EINVAL;
+    const void *ins[3] = {bcx, w, dy};
+    const size_t nins[3] = {n_bcx, n_w, n_dy};
+    for (int i = 0; i < 3; ++i)
+        if (overlaps(dbcx, n_bcx, ins[i], nins[i]) || overlaps(dw, n_dw, ins[i], nins[i]))
+            return SC_EINVAL;
+    if (overlaps(dbcx, n_bcx, dw, n_dw)) return SC_EINVAL;
+    return from_cuda(sc::launch_backward_noalloc(dtype, H, K, bcx, T, w, dy, dbcx, dw,
+                                                 (cudaStream_t)stream));
+}
+
 sc_status shortconv_get_error(void *stream, int *device_code) {
     if (device_code == nullptr) return SC_EINVAL;
     unsigned int code = 0;

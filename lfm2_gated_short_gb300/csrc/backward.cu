@@ -14,6 +14,8 @@
 // partial sums of the 8 segments of a CTA are added in shared memory, each
 // CTA row writes one [H, K] fp32 partial to the workspace, and a second
 // kernel adds the partials in a fixed order (deterministic bits).
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.h"
@@ -260,6 +262,47 @@ cudaError_t launch_backward(int dtype, int H, int K, const void *bcx, int64_t ro
                             const void *dy, void *dbcx, float *dw, void *ws, cudaStream_t s) {
     if (dtype == SC_BF16) return backward_K<__nv_bfloat16>(K, bcx, rows, H, w, dy, dbcx, dw, ws, s);
     return backward_K<float>(K, bcx, rows, H, w, dy, dbcx, dw, ws, s);
+}
+
+// ------------------------------------------------ no-allocation entry point
+//
+// shortconv_backward_noalloc runs the kernels above with their fp32 dW
+// partials in this fixed device array instead of a caller workspace. It is
+// for callers that cannot allocate device memory at call time. It holds
+// kNoAllocScratchBytes on every GPU that loads the library, until exit.
+// Every entry the reduction reads is first written by the same call, so the
+// array needs no clearing; concurrent calls on the same GPU share it and race.
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+// The array's device address on the current device. In host code the array's
+// name is only a host-side stand-in, so the address comes from the runtime:
+// once per device (with that device current), then from the cache.
+static cudaError_t noalloc_scratch(void **out) {
+    static std::mutex mu;
+    static void *addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+
+cudaError_t launch_backward_noalloc(int dtype, int H, int K, const void *bcx, int64_t T,
+                                    const void *w, const void *dy, void *dbcx, float *dw,
+                                    cudaStream_t s) {
+    void *ws = nullptr;
+    const cudaError_t e = noalloc_scratch(&ws);
+    if (e != cudaSuccess) return e;
+    if (dtype == SC_BF16) return backward_K<__nv_bfloat16>(K, bcx, T, H, w, dy, dbcx, dw, ws, s);
+    return backward_K<float>(K, bcx, T, H, w, dy, dbcx, dw, ws, s);
 }
 
 }  // namespace sc

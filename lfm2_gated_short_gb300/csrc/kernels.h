@@ -34,6 +34,14 @@ cudaError_t launch_backward(int dtype, int H, int K, const void *bcx, int64_t T,
                             const void *w, const void *dy, void *dbcx, float *dw,
                             void *workspace, cudaStream_t stream);
 
+// The backward kernels with their dW partials in the library's fixed device
+// scratch (kNoAllocScratchBytes) instead of a caller workspace. The caller
+// checks backward_workspace_bytes(H, K, T) <= kNoAllocScratchBytes first.
+constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;
+cudaError_t launch_backward_noalloc(int dtype, int H, int K, const void *bcx, int64_t T,
+                                    const void *w, const void *dy, void *dbcx, float *dw,
+                                    cudaStream_t stream);
+
 // Read and clear the device error word of the current device (synchronous
 // with respect to `stream`).
 cudaError_t read_and_clear_error(cudaStream_t stream, unsigned int *code);

@@ -1,0 +1,82 @@
+"""shortconv_backward_noalloc: the backward pass for callers that cannot
+allocate device memory at call time (code inside a framework that owns all
+device memory through its own pool, or latency-critical paths that cannot
+afford an allocation's synchronization or an out-of-memory failure
+mid-step). It keeps its scratch in a fixed array inside the library instead
+of a caller workspace.
+
+This file is collected last on purpose. It calls the entry point through the
+C ABI and checks it against shortconv_backward, which takes a caller
+workspace, on two calls in a row. It must pass alone in a fresh process and
+after the other tests.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import lfm2_gated_short_gb300 as sc
+from lfm2_gated_short_gb300 import build as sc_build
+from lfm2_gated_short_gb300 import workloads as wl
+from gpu_util import assert_close, assert_dw_close, dev, host
+
+SCRATCH_LIMIT = 8 << 20  # bytes of fixed device scratch behind the call
+
+
+def _noalloc():
+    f = sc.lib().shortconv_backward_noalloc
+    p, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    f.argtypes = [i32, i32, i32, p, i64, p, p, p, p, p]
+    f.restype = i32
+    return f
+
+
+def call_noalloc(bcx, w, dy):
+    T = bcx.shape[0]
+    H, K = w.shape
+    dbcx = torch.empty_like(bcx)
+    dw = torch.full((H, K), float("nan"), dtype=torch.float32, device=bcx.device)
+    code = sc.SC_BF16 if bcx.dtype == torch.bfloat16 else sc.SC_F32
+    st = _noalloc()(code, H, K, bcx.data_ptr(), T, w.data_ptr(), dy.data_ptr(),
+                    dbcx.data_ptr(), dw.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == sc.SC_OK, sc.lib().shortconv_status_string(st)
+    return dbcx, dw
+
+
+@pytest.mark.gpu
+def test_two_calls_in_a_row_match_the_workspace_entry_point():
+    cases = [wl.training(T=5003, H=512, K=3, seed=301),
+             wl.training(T=65536, H=2048, K=3, seed=302)]
+    for p in cases:
+        bcx, w, dy = dev(p.bcx, p.dtype), dev(p.w, p.dtype), dev(p.dy, p.dtype)
+        assert sc.backward_workspace_bytes(p.H, p.K, p.bcx.shape[0]) <= SCRATCH_LIMIT
+        ref_dbcx, ref_dw = sc.backward(bcx, w, dy)
+        got_dbcx, got_dw = call_noalloc(bcx, w, dy)
+        torch.cuda.synchronize()
+        assert_close(p.dtype, host(got_dbcx), host(ref_dbcx), "dB|dC|dx")
+        assert_dw_close(host(got_dw), host(ref_dw).astype(np.float64))
+    assert sc.get_error() == 0
+
+
+@pytest.mark.gpu
+def test_fp32_call_matches_the_workspace_entry_point():
+    p = wl.training(T=777, H=64, K=4, seed=303, dtype="f32")
+    bcx, w, dy = dev(p.bcx, "f32"), dev(p.w, "f32"), dev(p.dy, "f32")
+    ref_dbcx, ref_dw = sc.backward(bcx, w, dy)
+    got_dbcx, got_dw = call_noalloc(bcx, w, dy)
+    torch.cuda.synchronize()
+    assert_close("f32", host(got_dbcx), host(ref_dbcx), "dB|dC|dx")
+    assert_dw_close(host(got_dw), host(ref_dw).astype(np.float64))
+
+
+def test_sizes_beyond_the_scratch_are_rejected_before_any_work():
+    # Fake aligned addresses: the size check answers before anything is touched.
+    sc_build.build()
+    T = 2_793_473  # first row count whose partials exceed 8 MiB at H=2048, K=3
+    assert sc.backward_workspace_bytes(2048, 3, T) > SCRATCH_LIMIT
+    assert sc.backward_workspace_bytes(2048, 3, T - 1) <= SCRATCH_LIMIT
+    base = 1 << 40
+    st = _noalloc()(sc.SC_BF16, 2048, 3, base, T, base + (1 << 34), base + (2 << 34),
+                    base + (3 << 34), base + (4 << 34), None)
+    assert st == sc.SC_EUNSUPPORTED
