@@ -213,8 +213,10 @@ sc_status shortconv_backward(sc_dtype dtype, int H, int K, const void *bcx, int6
  * every GPU that loads the library holds until the process exits. The call
  * allocates nothing and never calls cudaMalloc or cudaFree.
  *   - Sizes whose shortconv_backward_workspace_bytes(H, K, T) exceeds 8 MiB
- *     are rejected with SC_EUNSUPPORTED before anything is enqueued (for
- *     H = 2048, K = 3 that is T above 2,793,472 rows).
+ *     are rejected with SC_EUNSUPPORTED before anything is enqueued. The
+ *     partials take at most 152 * H * K * 4 bytes, so nothing is rejected
+ *     for H * K <= 13,797 (every T for H = 2048 or H = 4096 with K = 3);
+ *     for H = 8192, K = 4 rows above T = 1024 are.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture on that device.

@@ -3,248 +3,310 @@
 // Liger-Kernel PR #1317, "Kernel changes / Gated short convolution": the B/C
 // gate gradients are fused with the depthwise-conv input gradient in one
 // pass, and the weight gradient of all K taps of a channel is reduced
-// together (no bias). Here one pass over the rows produces dB, dC and dx and
+// together (no bias). One pass over the rows produces dB, dC and dx and
 // accumulates dW in registers:
 //   dC_t = dy_t z_t,  dz_t = dy_t C_t,  du_s = sum_k w_k dz_{s+K-1-k},
 //   dB_s = du_s x_s,  dx_s = du_s B_s,  dW[h,k] = sum_t dz_t u_{t-K+1+k}.
 //
-// Thread = (8 channels, a segment of RB consecutive rows). It walks rows
-// r0-K+1 .. r1+K-2: the K-1 rows before its segment rebuild the u history,
-// the K-1 rows after it supply the dz look-ahead that du needs. The dW
-// partial sums of the 8 segments of a CTA are added in shared memory, each
-// CTA row writes one [H, K] fp32 partial to the workspace, and a second
-// kernel adds the partials in a fixed order (deterministic bits).
+// Same streamed design as the prefill: one persistent CTA per SM owns a
+// balanced range of rows [cr0, cr1) of a slice of up to 2048 channels; a
+// producer warp streams the rows' B|C|x and dy sections -- plus the K-1 rows
+// before the range (u history) and after it (dz look-ahead) -- through a
+// shared-memory ring with 1-D bulk asynchronous copies on full/empty
+// mbarriers; 16 consumer warps, 4 channels per thread, walk the rows. Each
+// thread holds its channels' dW over the whole range in registers and
+// writes one fp32 partial per CTA; a second kernel adds the partials of all
+// CTAs in a fixed order, so dW has the same bits on every call.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
+#include "errors.cuh"
 #include "kernels.h"
 #include "launch.h"
 #include "shortconv.h"
+#include "tma.cuh"
 
 namespace sc {
 
-constexpr int kBwdGroups = 32;   // channel groups per CTA (threadIdx.x): 256 channels
-constexpr int kBwdSegs = 8;      // row segments per CTA (threadIdx.y)
-constexpr int kBwdChunk = 2;     // rows whose loads are issued together
-constexpr int64_t kBwdTargetCtas = 1216;
+constexpr int kBwdCpt = 4;                         // channels per consumer thread
+constexpr int kBwdSlice = 2048;                    // channels per CTA slice
+constexpr int kBwdConsumers = kBwdSlice / kBwdCpt;
+constexpr int kBwdStages = 4;
+constexpr int kBwdMinRows = 16;                    // rows per CTA at least
+constexpr int kBwdRowCtas = 152;                   // row ranges per slice (GB300: one per SM)
+constexpr int kBwdHeader = 256;                    // mbarriers
 
-static int bwd_rows_per_thread(int H, int64_t T) {
-    const int64_t gx = (H / kCh + kBwdGroups - 1) / kBwdGroups;
-    int64_t rb = (T * gx + kBwdSegs * kBwdTargetCtas - 1) / (kBwdSegs * kBwdTargetCtas);
-    if (rb < 4) rb = 4;
-    if (rb > 1024) rb = 1024;
-    return (int)((rb + 3) / 4 * 4);
+template <typename T>
+struct BwdShape {
+    static constexpr int R = sizeof(T) == 2 ? 2 : 1;  // rows per stage (16 / 32 KB per row)
+};
+
+template <typename T>
+constexpr size_t bwd_smem_bytes(int CW) {
+    return (size_t)kBwdHeader + (size_t)kBwdStages * BwdShape<T>::R * 4 * CW * sizeof(T);
 }
 
-static int64_t bwd_row_ctas(int H, int64_t T) {
-    const int64_t rows_per_cta = (int64_t)kBwdSegs * bwd_rows_per_thread(H, T);
-    return (T + rows_per_cta - 1) / rows_per_cta;
+// Row ranges per channel slice; fixed by T alone so the workspace size is.
+static int64_t bwd_row_ctas(int64_t T) {
+    const int64_t n = (T + kBwdMinRows - 1) / kBwdMinRows;
+    return n < 1 ? 1 : (n > kBwdRowCtas ? kBwdRowCtas : n);
 }
 
 size_t backward_workspace_bytes(int H, int K, int64_t T) {
-    return (size_t)bwd_row_ctas(H, T) * (size_t)H * (size_t)K * sizeof(float);
+    return (size_t)bwd_row_ctas(T) * (size_t)H * (size_t)K * sizeof(float);
 }
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kBwdGroups *kBwdSegs)
+__global__ void __launch_bounds__(kBwdConsumers + 32, 1)
     k_backward(const T *__restrict__ bcx, int64_t T_rows, int H, const T *__restrict__ w,
                const T *__restrict__ dy, T *__restrict__ dbcx, float *__restrict__ partial,
-               int RB) {
+               int n_slices, int n_row_ctas) {
+    constexpr int CPT = kBwdCpt;
+    constexpr int NP = CPT / 2;
+    constexpr int R = BwdShape<T>::R;
+    constexpr int NS = kBwdStages;
     constexpr int KH = K > 1 ? K - 1 : 1;  // history / look-ahead depth
-    pdl_wait();
-    const int groups = H / kCh;
-    const int cg = blockIdx.x * kBwdGroups + threadIdx.x;
-    const int h0 = cg * kCh;
-    const int64_t r0 = ((int64_t)blockIdx.y * kBwdSegs + threadIdx.y) * RB;
-    const int64_t r1 = min(r0 + (int64_t)RB, T_rows);
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + 128);
+    T *stage = reinterpret_cast<T *>(smem + kBwdHeader);
+
+    const int tid = threadIdx.x;
+    const int n_consumers = blockDim.x - 32;
+    const bool producer = tid >= n_consumers;
+    const bool lead = tid == n_consumers;
+    const int slice = blockIdx.x % n_slices;
+    const int64_t rc = blockIdx.x / n_slices;
+    const int c0 = slice * kBwdSlice;
+    const int CW = min(kBwdSlice, H);
+    const int cw = min(kBwdSlice, H - c0);
+    const bool active = !producer && tid * CPT < cw;
+    const int h0 = c0 + tid * CPT;
+    const int64_t cr0 = rc * T_rows / n_row_ctas, cr1 = (rc + 1) * T_rows / n_row_ctas;
+    const int64_t sr0 = max((int64_t)0, cr0 - (K - 1));
+    const int64_t sr1 = min(T_rows, cr1 + (K - 1));
+    const int n_chunks = cr0 < cr1 ? (int)((sr1 - sr0 + R - 1) / R) : 0;
+    const uint32_t sec_bytes = (uint32_t)cw * sizeof(T);
     const int64_t ld = 3 * (int64_t)H;
 
-    float acc[kCh][K];
+    if (lead) {
 #pragma unroll
-    for (int ch = 0; ch < kCh; ++ch)
-#pragma unroll
-        for (int k = 0; k < K; ++k) acc[ch][k] = 0.f;
-
-    if (cg < groups && r0 < T_rows) {
-        float wt[kCh][K];
-        load_block<T, K>(w + (int64_t)h0 * K, wt);
-        float uh[kCh][KH], dzq[kCh][KH];  // u and dz of rows t-K+1 .. t-1 (oldest first)
-        Row<T> rbq[KH], rxq[KH];         // B and x of rows t-K+1 .. t-1
-#pragma unroll
-        for (int ch = 0; ch < kCh; ++ch)
-#pragma unroll
-            for (int k = 0; k < KH; ++k) uh[ch][k] = dzq[ch][k] = 0.f;
-
-        // Rows before the segment: only their u (zero before row 0).
-#pragma unroll
-        for (int j = 1; j < K; ++j) {
-            const int64_t t = r0 - K + j;
-            if (t >= 0) {
-                const T *p = bcx + t * ld + h0;
-                const Row<T> rb = load_row(p), rx = load_row(p + 2 * H);
-                float b[kCh], x[kCh];
-                unpack_row(rb, b);
-                unpack_row(rx, x);
-#pragma unroll
-                for (int ch = 0; ch < kCh; ++ch) uh[ch][j - 1] = gate_in<T>(b[ch], x[ch]);
-            }
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], n_consumers / 32);
         }
-
-        // du_s for s = t-K+1 from dz_t and the queued dz, then dB_s, dx_s.
-        auto emit = [&](int64_t t, const float (&dz)[kCh], const Row<T> &rb_s,
-                        const Row<T> &rx_s) {
-            const int64_t s = t - (K - 1);
-            if (s < r0) return;
-            float b[kCh], x[kCh], db[kCh], dx[kCh];
-            unpack_row(rb_s, b);
-            unpack_row(rx_s, x);
-#pragma unroll
-            for (int ch = 0; ch < kCh; ++ch) {
-                float du = wt[ch][0] * dz[ch];
-#pragma unroll
-                for (int k = 1; k < K; ++k) du = fmaf(wt[ch][k], dzq[ch][K - 1 - k], du);
-                db[ch] = du * x[ch];
-                dx[ch] = du * b[ch];
-            }
-            T *q = dbcx + s * ld + h0;
-            store_row(q, db);
-            store_row(q + 2 * H, dx);
-        };
-        auto push = [&](const float (&u)[kCh], const float (&dz)[kCh], const Row<T> &rb,
-                        const Row<T> &rx) {
-            if constexpr (K > 1) {
-#pragma unroll
-                for (int ch = 0; ch < kCh; ++ch) {
-#pragma unroll
-                    for (int k = 0; k + 1 < KH; ++k) {
-                        uh[ch][k] = uh[ch][k + 1];
-                        dzq[ch][k] = dzq[ch][k + 1];
-                    }
-                    uh[ch][KH - 1] = u[ch];
-                    dzq[ch][KH - 1] = dz[ch];
-                }
-#pragma unroll
-                for (int k = 0; k + 1 < KH; ++k) {
-                    rbq[k] = rbq[k + 1];
-                    rxq[k] = rxq[k + 1];
-                }
-                rbq[KH - 1] = rb;
-                rxq[KH - 1] = rx;
-            }
-        };
-
-        // The segment's own rows.
-        for (int64_t t0 = r0; t0 < r1; t0 += kBwdChunk) {
-            Row<T> lb[kBwdChunk], lc[kBwdChunk], lx[kBwdChunk], lg[kBwdChunk];
-#pragma unroll
-            for (int j = 0; j < kBwdChunk; ++j) {
-                if (t0 + j < r1) {
-                    const T *p = bcx + (t0 + j) * ld + h0;
-                    lb[j] = load_row(p);
-                    lc[j] = load_row(p + H);
-                    lx[j] = load_row(p + 2 * H);
-                    lg[j] = load_row(dy + (t0 + j) * (int64_t)H + h0);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < kBwdChunk; ++j) {
-                const int64_t t = t0 + j;
-                if (t < r1) {
-                    float b[kCh], c[kCh], x[kCh], g[kCh], u[kCh], dz[kCh], dc[kCh];
-                    unpack_row(lb[j], b);
-                    unpack_row(lc[j], c);
-                    unpack_row(lx[j], x);
-                    unpack_row(lg[j], g);
-#pragma unroll
-                    for (int ch = 0; ch < kCh; ++ch) {
-                        u[ch] = gate_in<T>(b[ch], x[ch]);
-                        float z = wt[ch][K - 1] * u[ch];
-#pragma unroll
-                        for (int k = 0; k + 1 < K; ++k) z = fmaf(wt[ch][k], uh[ch][k], z);
-                        dc[ch] = g[ch] * z;
-                        dz[ch] = g[ch] * c[ch];
-#pragma unroll
-                        for (int k = 0; k + 1 < K; ++k) acc[ch][k] = fmaf(dz[ch], uh[ch][k], acc[ch][k]);
-                        acc[ch][K - 1] = fmaf(dz[ch], u[ch], acc[ch][K - 1]);
-                    }
-                    store_row(dbcx + t * ld + H + h0, dc);
-                    if constexpr (K == 1)
-                        emit(t, dz, lb[j], lx[j]);
-                    else
-                        emit(t, dz, rbq[0], rxq[0]);
-                    push(u, dz, lb[j], lx[j]);
-                }
-            }
-        }
-
-        // Rows after the segment: only their dz (zero past the last row).
-#pragma unroll
-        for (int j = 0; j + 1 < K; ++j) {
-            const int64_t t = r1 + j;
-            float dz[kCh], u[kCh];
-#pragma unroll
-            for (int ch = 0; ch < kCh; ++ch) dz[ch] = u[ch] = 0.f;
-            if (t < T_rows) {
-                const Row<T> rc = load_row(bcx + t * ld + H + h0);
-                const Row<T> rg = load_row(dy + t * (int64_t)H + h0);
-                float c[kCh], g[kCh];
-                unpack_row(rc, c);
-                unpack_row(rg, g);
-#pragma unroll
-                for (int ch = 0; ch < kCh; ++ch) dz[ch] = g[ch] * c[ch];
-            }
-            emit(t, dz, rbq[0], rxq[0]);
-            push(u, dz, rbq[0], rxq[0]);
-        }
+        mbar_fence_init();
     }
-
-    pdl_launch_dependents();
-    // dW: add the 8 segments of this CTA in a fixed order, one partial per CTA row.
-    __shared__ float red[kBwdSegs][kBwdGroups * kCh * K];
-#pragma unroll
-    for (int ch = 0; ch < kCh; ++ch)
-#pragma unroll
-        for (int k = 0; k < K; ++k) red[threadIdx.y][threadIdx.x * kCh * K + ch * K + k] = acc[ch][k];
     __syncthreads();
-    const int tid = threadIdx.y * kBwdGroups + threadIdx.x;
-    for (int e = tid; e < kBwdGroups * kCh * K; e += kBwdGroups * kBwdSegs) {
-        float s = 0.f;
+    pdl_wait();  // inputs may come from the previous kernel in the stream
+    pdl_launch_dependents();
+
+    // Stage layout per row: B | C | x | dy sections of CW channels.
+    auto issue = [&](int c) {
+        const int s = c % NS;
+        const int64_t rb = sr0 + (int64_t)c * R;
+        const int rows = (int)min((int64_t)R, sr1 - rb);
+        mbar_arrive_expect_tx(&full[s], (uint32_t)rows * 4u * sec_bytes);
+        for (int rr = 0; rr < rows; ++rr) {
+            const T *src = bcx + (rb + rr) * ld + c0;
+            T *dst = stage + (size_t)(s * R + rr) * 4 * CW;
 #pragma unroll
-        for (int j = 0; j < kBwdSegs; ++j) s += red[j][e];
-        const int cg2 = blockIdx.x * kBwdGroups + e / (kCh * K);
-        if (cg2 < groups)
-            partial[(int64_t)blockIdx.y * H * K + (int64_t)cg2 * kCh * K + e % (kCh * K)] = s;
+            for (int q = 0; q < 3; ++q)
+                bulk_copy_g2s(dst + (size_t)q * CW, src + (int64_t)q * H, sec_bytes, &full[s]);
+            bulk_copy_g2s(dst + (size_t)3 * CW, dy + (rb + rr) * (int64_t)H + c0, sec_bytes,
+                          &full[s]);
+        }
+    };
+    auto drain = [&](int from, int to) {
+        for (int c = from; c < to; ++c) mbar_wait_bounded(&full[c % NS], (uint32_t)(c / NS) & 1u);
+    };
+
+    if (producer) {
+        if (!lead) return;
+        int c = 0;
+        for (; c < n_chunks; ++c) {
+            if (c >= NS && !mbar_wait_bounded(&empty[c % NS], (uint32_t)(c / NS - 1) & 1u)) {
+                raise_error(SC_DEV_TIMEOUT);
+                break;
+            }
+            issue(c);
+        }
+        drain(max(0, c - NS), c);
+        return;
     }
+
+    f32x2 wp[K][NP];
+    if (active) load_taps<T, CPT, K>(w + (int64_t)h0 * K, wp);
+    f32x2 uw[K][NP], dzw[K][NP], acc[K][NP];  // u window, dz window (newest last), dW
+    Sec<T, CPT> rbq[KH], rxq[KH];             // B and x of the K-1 rows before t
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+#pragma unroll
+        for (int q = 0; q < NP; ++q) uw[k][q] = dzw[k][q] = acc[k][q] = 0ull;
+
+    // du for row s = t-K+1 from the dz window (dz_t newest), then dB_s, dx_s.
+    auto emit = [&](int64_t t, const Sec<T, CPT> &b_s, const Sec<T, CPT> &x_s) {
+        const int64_t s = t - (K - 1);
+        if (s < cr0 || s >= cr1) return;
+        f32x2 fb[NP], fx[NP], db[NP], dx[NP];
+        Pairs<T, CPT>::widen(b_s, fb);
+        Pairs<T, CPT>::widen(x_s, fx);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            f32x2 du = f2_mul(wp[0][q], dzw[K - 1][q]);
+#pragma unroll
+            for (int k = 1; k < K; ++k) du = f2_fma(wp[k][q], dzw[K - 1 - k][q], du);
+            db[q] = f2_mul(du, fx[q]);
+            dx[q] = f2_mul(du, fb[q]);
+        }
+        T *o = dbcx + s * ld + h0;
+        Pairs<T, CPT>::store(o, db);
+        Pairs<T, CPT>::store(o + 2 * H, dx);
+    };
+    auto push_bx = [&](const Sec<T, CPT> &b, const Sec<T, CPT> &x) {
+        if constexpr (K > 1) {
+#pragma unroll
+            for (int k = 0; k + 1 < KH; ++k) {
+                rbq[k] = rbq[k + 1];
+                rxq[k] = rxq[k + 1];
+            }
+            rbq[KH - 1] = b;
+            rxq[KH - 1] = x;
+        }
+    };
+    auto slide = [&](f32x2 (&win)[K][NP], const f32x2 (&v)[NP]) {
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+#pragma unroll
+            for (int k = 0; k + 1 < K; ++k) win[k][q] = win[k + 1][q];
+            win[K - 1][q] = v[q];
+        }
+    };
+
+    const int lane = tid & 31;
+    const uint32_t base = smem_addr(stage) + (uint32_t)(tid * CPT * sizeof(T));
+    const uint32_t sec = (uint32_t)(CW * sizeof(T));
+    for (int c = 0; c < n_chunks; ++c) {
+        const int s = c % NS;
+        if (!mbar_wait_bounded(&full[s], (uint32_t)(c / NS) & 1u)) {
+            if (lane == 0) raise_error(SC_DEV_TIMEOUT);
+            return;
+        }
+        const int64_t rb = sr0 + (int64_t)c * R;
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            const int64_t t = rb + rr;
+            if (t >= sr1) break;
+            if (!active) continue;
+            const uint32_t a = base + (uint32_t)((s * R + rr) * 4) * sec;
+            const Sec<T, CPT> b = lds_sec<T, CPT>(a), x = lds_sec<T, CPT>(a + 2 * sec);
+            const Sec<T, CPT> cc = lds_sec<T, CPT>(a + sec), g = lds_sec<T, CPT>(a + 3 * sec);
+            f32x2 u[NP], fc[NP], fg[NP], dz[NP];
+            Pairs<T, CPT>::gate(b, x, u);
+            Pairs<T, CPT>::widen(cc, fc);
+            Pairs<T, CPT>::widen(g, fg);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) dz[q] = f2_mul(fg[q], fc[q]);
+            slide(uw, u);
+            slide(dzw, dz);
+            if (t >= cr0 && t < cr1) {
+                f32x2 dc[NP];
+#pragma unroll
+                for (int q = 0; q < NP; ++q) {
+                    f32x2 z = f2_mul(wp[0][q], uw[0][q]);  // the forward's order
+#pragma unroll
+                    for (int k = 1; k < K; ++k) z = f2_fma(wp[k][q], uw[k][q], z);
+                    dc[q] = f2_mul(fg[q], z);
+#pragma unroll
+                    for (int k = 0; k < K; ++k) acc[k][q] = f2_fma(dz[q], uw[k][q], acc[k][q]);
+                }
+                Pairs<T, CPT>::store(dbcx + t * ld + H + h0, dc);
+            }
+            if constexpr (K == 1)
+                emit(t, b, x);
+            else
+                emit(t, rbq[0], rxq[0]);
+            push_bx(b, x);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (!active) return;
+    // Rows past the last one have dz = 0: finish the last K-1 emissions.
+#pragma unroll
+    for (int j = 0; j + 1 < K; ++j) {
+        const int64_t t = sr1 + j;
+        if (cr0 >= cr1 || t >= cr1 + (K - 1)) break;
+        f32x2 zero[NP];
+#pragma unroll
+        for (int q = 0; q < NP; ++q) zero[q] = 0ull;
+        slide(dzw, zero);
+        emit(t, rbq[0], rxq[0]);
+        push_bx(rbq[0], rxq[0]);
+    }
+    // This CTA's dW partial for its channels (zero for an empty range).
+    float *pp = partial + (int64_t)rc * H * K + (int64_t)h0 * K;
+#pragma unroll
+    for (int q = 0; q < NP; ++q)
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            float lo, hi;
+            f2_split(acc[k][q], lo, hi);
+            pp[(2 * q) * K + k] = lo;
+            pp[(2 * q + 1) * K + k] = hi;
+        }
 }
 
-// dw[e] = sum over CTA rows g = 0 .. G-1 of partial[g][e], in that order.
+// dw[e] = sum over CTA rows g = 0 .. G-1 of partial[g][e]: 8 warps take
+// interleaved g for 32 consecutive e, then warp 0 adds the 8 sums in order.
 __global__ void __launch_bounds__(256)
     k_dw_reduce(const float *__restrict__ partial, int64_t G, int HK, float *__restrict__ dw) {
+    __shared__ float part[8][32];
     pdl_wait();
     pdl_launch_dependents();
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= HK) return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int e = blockIdx.x * 32 + lane;
     float s = 0.f;
-    for (int64_t g = 0; g < G; ++g) s += partial[g * HK + e];
-    dw[e] = s;
+    if (e < HK)
+        for (int64_t g = warp; g < G; g += 8) s += partial[g * HK + e];
+    part[warp][lane] = s;
+    __syncthreads();
+    if (warp == 0 && e < HK) {
+        float t = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) t += part[j][lane];
+        dw[e] = t;
+    }
 }
 
 template <typename T, int K>
 static cudaError_t backward_inst(const void *bcx, int64_t rows, int H, const void *w,
                                  const void *dy, void *dbcx, float *dw, void *ws,
                                  cudaStream_t stream) {
-    const int RB = bwd_rows_per_thread(H, rows);
-    const int64_t gy = bwd_row_ctas(H, rows);
-    const int gx = (H / kCh + kBwdGroups - 1) / kBwdGroups;
-    if (gy > 0) {
-        const cudaError_t e = launch_pdl(
-            k_backward<T, K>, dim3(gx, (unsigned)gy), dim3(kBwdGroups, kBwdSegs), 0, stream,
-            (const T *)bcx, rows, H, (const T *)w, (const T *)dy, (T *)dbcx, (float *)ws, RB);
+    const int CW = H < kBwdSlice ? H : kBwdSlice;
+    const int n_slices = (H + kBwdSlice - 1) / kBwdSlice;
+    const int threads = (CW / kBwdCpt + 31) / 32 * 32 + 32;  // consumers + one producer warp
+    const size_t smem = bwd_smem_bytes<T>(CW);
+    const int64_t n_row = bwd_row_ctas(rows);
+    auto kern = k_backward<T, K>;
+    static std::atomic<unsigned long long> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !(configured.load() & (1ull << dev))) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bwd_smem_bytes<T>(kBwdSlice));
         if (e != cudaSuccess) return e;
+        configured.fetch_or(1ull << dev);
     }
+    e = launch_pdl(kern, dim3((unsigned)(n_row * n_slices)), dim3(threads), smem, stream,
+                   (const T *)bcx, rows, H, (const T *)w, (const T *)dy, (T *)dbcx, (float *)ws,
+                   n_slices, (int)n_row);
+    if (e != cudaSuccess) return e;
     const int HK = H * K;
-    return launch_pdl(k_dw_reduce, dim3((HK + 255) / 256), dim3(256), 0, stream,
-                      (const float *)ws, gy, HK, dw);
+    return launch_pdl(k_dw_reduce, dim3((HK + 31) / 32), dim3(256), 0, stream,
+                      (const float *)ws, n_row, HK, dw);
 }
 
 template <typename T>
@@ -258,10 +320,14 @@ static cudaError_t backward_K(int K, const void *bcx, int64_t rows, int H, const
     }
 }
 
-cudaError_t launch_backward(int dtype, int H, int K, const void *bcx, int64_t rows, const void *w,
+cudaError_t launch_backward(int dtype, int H, int K, const void *bcx, int64_t T, const void *w,
                             const void *dy, void *dbcx, float *dw, void *ws, cudaStream_t s) {
-    if (dtype == SC_BF16) return backward_K<__nv_bfloat16>(K, bcx, rows, H, w, dy, dbcx, dw, ws, s);
-    return backward_K<float>(K, bcx, rows, H, w, dy, dbcx, dw, ws, s);
+    if (dtype == SC_BF16) return backward_K<__nv_bfloat16>(K, bcx, T, H, w, dy, dbcx, dw, ws, s);
+    return backward_K<float>(K, bcx, T, H, w, dy, dbcx, dw, ws, s);
+}
+
+cudaError_t take_error_backward(cudaStream_t stream, unsigned int *code) {
+    return take_error_here(stream, code);
 }
 
 // ------------------------------------------------ no-allocation entry point

@@ -13,18 +13,13 @@
 #include <atomic>
 
 #include "common.cuh"
+#include "errors.cuh"
 #include "kernels.h"
 #include "launch.h"
 #include "shortconv.h"
+#include "tma.cuh"
 
 namespace sc {
-
-__device__ unsigned int g_error_word;   // bit mask of SC_DEV_* codes
-__device__ unsigned int g_error_taken;  // last value taken by read_and_clear_error
-
-__device__ __forceinline__ void raise_error(unsigned int code) { atomicOr(&g_error_word, code); }
-
-__global__ void k_take_error() { g_error_taken = atomicExch(&g_error_word, 0u); }
 
 constexpr int kThreads = 256;
 constexpr int kMaxStagedSeqs = 2048;  // cu_seqlens entries staged in shared memory
@@ -482,13 +477,13 @@ cudaError_t launch_rollback(int dtype, int H, int K, int N, int D, const void *w
 // ------------------------------------------------------------ error word
 
 cudaError_t read_and_clear_error(cudaStream_t stream, unsigned int *code) {
-    k_take_error<<<1, 1, 0, stream>>>();
-    cudaError_t e = cudaGetLastError();
+    unsigned int a = 0, b = 0;
+    cudaError_t e = take_error_here(stream, &a);
     if (e != cudaSuccess) return e;
-    e = cudaMemcpyFromSymbolAsync(code, g_error_taken, sizeof(unsigned int), 0,
-                                  cudaMemcpyDeviceToHost, stream);
+    e = take_error_backward(stream, &b);
     if (e != cudaSuccess) return e;
-    return cudaStreamSynchronize(stream);
+    *code = a | b;
+    return cudaSuccess;
 }
 
 }  // namespace sc

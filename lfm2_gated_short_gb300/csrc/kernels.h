@@ -42,6 +42,9 @@ cudaError_t launch_backward_noalloc(int dtype, int H, int K, const void *bcx, in
                                     const void *w, const void *dy, void *dbcx, float *dw,
                                     cudaStream_t stream);
 
+// Take (read and clear) the backward translation unit's error word.
+cudaError_t take_error_backward(cudaStream_t stream, unsigned int *code);
+
 // Read and clear the device error word of the current device (synchronous
 // with respect to `stream`).
 cudaError_t read_and_clear_error(cudaStream_t stream, unsigned int *code);

@@ -20,7 +20,8 @@
 // take their window history from streamed rows of the same sequence.
 //
 // This file is a fragment of forward.cu: it is included inside namespace sc,
-// after the error word, raise_error(), row_u() and kMaxStagedSeqs.
+// after the error word, raise_error(), row_u() and kMaxStagedSeqs; the
+// mbarrier and bulk-copy helpers come from tma.cuh.
 #pragma once
 
 // Build-time shape of the streamed kernel (defaults are the tuned ones):
@@ -41,7 +42,6 @@ constexpr int kStreamSlice = 2048;                         // channels per CTA s
 constexpr int kStreamCuBytes = ((kMaxStagedSeqs + 1) * 4 + 127) / 128 * 128;
 constexpr int kStreamHeader = 256 + kStreamCuBytes + kMaxStagedSeqs * 4;  // barriers, cu, slots
 constexpr int kStreamMinRows = 8;                          // rows per CTA at least
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
 static_assert(kStreamSlice / kStreamCpt + 32 <= 1024, "one CTA holds a slice's consumers");
 
 template <typename T>
@@ -55,72 +55,6 @@ template <typename T>
 constexpr size_t stream_smem_bytes(int CW) {
     return (size_t)kStreamHeader +
            (size_t)StreamShape<T>::NS * StreamShape<T>::R * 3 * CW * sizeof(T);
-}
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_fence_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile(
-        "{\n\t.reg .b64 st;\n\t"
-        "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_addr(bar)),
-        "r"(bytes)
-        : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile(
-        "{\n\t.reg .b64 st;\n\t"
-        "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-// Wait for the phase with this parity to complete; false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-
-__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes,
-                                              uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
 }
 
 template <typename T, int K>

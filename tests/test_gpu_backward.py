@@ -46,12 +46,14 @@ def test_worked_example(dtype):
 
 
 @pytest.mark.parametrize("K", [1, 2, 3, 4])
-@pytest.mark.parametrize("T", [1, 2, 5, 301, 4099])
+@pytest.mark.parametrize("T", [0, 1, 2, 5, 17, 301, 4099])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_backward_small(dtype, T, K):
     p = wl.training(T=T, H=256, K=K, seed=90 + K + T, dtype=dtype)
     dbcx, dw = run(p)
     check_against_oracle(p, dbcx, dw)
+    if T == 0:
+        assert np.all(dw == 0.0)
 
 
 def test_backward_is_deterministic_and_overwrites_dw():
@@ -75,3 +77,10 @@ def test_backward_T65536_H2048_sampled_channels():
     ch = np.sort(np.concatenate([[0, 7, 8, 255, 256, 2047],
                                  rng.choice(np.arange(9, 2040), 58, replace=False)]))
     check_against_oracle(p, dbcx, dw, ch)
+
+
+@pytest.mark.parametrize("H", [2560, 4096])
+def test_backward_channel_slices_wider_than_one_cta(H):
+    p = wl.training(T=333, H=H, K=3, seed=96)
+    dbcx, dw = run(p)
+    check_against_oracle(p, dbcx, dw)

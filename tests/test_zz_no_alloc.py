@@ -71,12 +71,14 @@ def test_fp32_call_matches_the_workspace_entry_point():
 
 
 def test_sizes_beyond_the_scratch_are_rejected_before_any_work():
-    # Fake aligned addresses: the size check answers before anything is touched.
+    # Fake aligned addresses: the size check answers before anything is touched,
+    # and the call is only made once the size is known to exceed the scratch.
     sc_build.build()
-    T = 2_793_473  # first row count whose partials exceed 8 MiB at H=2048, K=3
-    assert sc.backward_workspace_bytes(2048, 3, T) > SCRATCH_LIMIT
-    assert sc.backward_workspace_bytes(2048, 3, T - 1) <= SCRATCH_LIMIT
+    H, K, T = 8192, 4, 1025  # first row count whose partials exceed 8 MiB at H=8192, K=4
+    assert sc.backward_workspace_bytes(H, K, T) > SCRATCH_LIMIT
+    assert sc.backward_workspace_bytes(H, K, T - 1) <= SCRATCH_LIMIT
+    assert sc.backward_workspace_bytes(2048, 3, 2**31 - 1) <= SCRATCH_LIMIT
     base = 1 << 40
-    st = _noalloc()(sc.SC_BF16, 2048, 3, base, T, base + (1 << 34), base + (2 << 34),
+    st = _noalloc()(sc.SC_BF16, H, K, base, T, base + (1 << 34), base + (2 << 34),
                     base + (3 << 34), base + (4 << 34), None)
     assert st == sc.SC_EUNSUPPORTED
