@@ -9,7 +9,7 @@
 //   dB_s = du_s x_s,  dx_s = du_s B_s,  dW[h,k] = sum_t dz_t u_{t-K+1+k}.
 //
 // Same streamed design as the prefill: one persistent CTA per SM owns a
-// balanced range of rows [cr0, cr1) of a slice of up to 2048 channels; a
+// balanced range of rows [cr0, cr1) of a slice of up to 512 channels; a
 // producer warp streams the rows' B|C|x and dy sections -- plus the K-1 rows
 // before the range (u history) and after it (dz look-ahead) -- through a
 // shared-memory ring with 1-D bulk asynchronous copies on full/empty
@@ -29,8 +29,17 @@
 
 namespace sc {
 
+// Build-time shape (defaults are the tuned ones): channels per CTA slice and
+// the CTAs per SM the register budget is sized for.
+#ifndef SC_BWD_SLICE
+#define SC_BWD_SLICE 512
+#endif
+#ifndef SC_BWD_MIN_CTAS
+#define SC_BWD_MIN_CTAS 4
+#endif
+
 constexpr int kBwdCpt = 4;                         // channels per consumer thread
-constexpr int kBwdSlice = 2048;                    // channels per CTA slice
+constexpr int kBwdSlice = SC_BWD_SLICE;            // channels per CTA slice
 constexpr int kBwdConsumers = kBwdSlice / kBwdCpt;
 constexpr int kBwdStages = 4;
 constexpr int kBwdMinRows = 16;                    // rows per CTA at least
@@ -58,7 +67,7 @@ size_t backward_workspace_bytes(int H, int K, int64_t T) {
 }
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kBwdConsumers + 32, 1)
+__global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_MIN_CTAS)
     k_backward(const T *__restrict__ bcx, int64_t T_rows, int H, const T *__restrict__ w,
                const T *__restrict__ dy, T *__restrict__ dbcx, float *__restrict__ partial,
                int n_slices, int n_row_ctas) {

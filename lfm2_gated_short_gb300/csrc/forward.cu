@@ -355,8 +355,11 @@ cudaError_t launch_decode(int dtype, int H, int K, const void *bcx, int N, const
 // ------------------------------------------------------------------- verify
 //
 // Unit = (sequence i, channel group); the D draft steps run in order in
-// registers. Small CTAs spread the few units over all SMs.
+// registers. All draft rows (up to kVerifyRows at a time) are requested
+// before the slot-dependent state load, so a sequence costs two dependent
+// memory round trips. Small CTAs spread the few units over all SMs.
 constexpr int kVerifyThreads = 64;
+constexpr int kVerifyRows = 8;
 
 template <typename T, int K>
 __global__ void __launch_bounds__(kVerifyThreads)
@@ -369,28 +372,39 @@ __global__ void __launch_bounds__(kVerifyThreads)
     const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (unit >= (int64_t)N * groups) return;
     const int i = (int)(unit / groups), cg = (int)(unit % groups), h0 = cg * kCh;
+    const int64_t ld = 3 * (int64_t)H;
     const int slot = slots[i];
+    Row<T> rb[kVerifyRows], rc[kVerifyRows], rx[kVerifyRows];
+#pragma unroll
+    for (int jj = 0; jj < kVerifyRows; ++jj) {
+        if (jj < D) {
+            const T *p = bcx + ((int64_t)i * D + jj) * ld + h0;
+            rb[jj] = load_row(p);
+            rc[jj] = load_row(p + H);
+            rx[jj] = load_row(p + 2 * H);
+        }
+    }
+    float wt[kCh][K], win[kCh][K];
+    load_block<T, K>(w + (int64_t)h0 * K, wt);
     if (slot < 0 || slot >= n_slots) {
         if (cg == 0) raise_error(SC_DEV_BAD_SLOT);
         return;
     }
-    float wt[kCh][K], win[kCh][K];
-    load_block<T, K>(w + (int64_t)h0 * K, wt);
     load_block<T, K>(pool + ((int64_t)slot * H + h0) * K, win);
-    const int64_t ld = 3 * (int64_t)H;
-    for (int j0 = 0; j0 < D; j0 += kChunk) {
-        Row<T> rb[kChunk], rc[kChunk], rx[kChunk];
+    for (int j0 = 0; j0 < D; j0 += kVerifyRows) {
+        if (j0 > 0) {
 #pragma unroll
-        for (int jj = 0; jj < kChunk; ++jj) {
-            if (j0 + jj < D) {
-                const T *p = bcx + ((int64_t)i * D + j0 + jj) * ld + h0;
-                rb[jj] = load_row(p);
-                rc[jj] = load_row(p + H);
-                rx[jj] = load_row(p + 2 * H);
+            for (int jj = 0; jj < kVerifyRows; ++jj) {
+                if (j0 + jj < D) {
+                    const T *p = bcx + ((int64_t)i * D + j0 + jj) * ld + h0;
+                    rb[jj] = load_row(p);
+                    rc[jj] = load_row(p + H);
+                    rx[jj] = load_row(p + 2 * H);
+                }
             }
         }
 #pragma unroll
-        for (int jj = 0; jj < kChunk; ++jj) {
+        for (int jj = 0; jj < kVerifyRows; ++jj) {
             if (j0 + jj < D) {
                 const int64_t t = (int64_t)i * D + j0 + jj;
                 float b[kCh], c[kCh], x[kCh], out[kCh];

@@ -1,8 +1,8 @@
 // prefill_stream.cuh -- the TMA-streamed prefill kernel (included by forward.cu,
 // whose error word and helpers it shares).
 //
-// One CTA per SM (persistent) owns a balanced range of rows [cr0, cr1) of a
-// slice of up to 2048 channels. A producer warp streams the rows it needs --
+// Persistent CTAs (several per SM, as many as fit) each own a balanced range
+// of rows [cr0, cr1) of a slice of up to 512 channels. A producer warp streams the rows it needs --
 // the range plus the K-1 rows before it (window history) and up to K-2 rows
 // after it (the sequence-owner extension) -- through NS shared-memory stages
 // with 1-D bulk asynchronous copies (cp.async.bulk). Each stage has a "full"
@@ -36,11 +36,21 @@
 #ifndef SC_STREAM_STAGES
 #define SC_STREAM_STAGES 4
 #endif
+#ifndef SC_STREAM_SLICE
+#define SC_STREAM_SLICE 512  // channels per CTA slice
+#endif
+#ifndef SC_STREAM_MIN_CTAS
+#define SC_STREAM_MIN_CTAS 4  // CTAs per SM the register budget is sized for
+#endif
+#ifndef SC_STREAM_STAGED
+#define SC_STREAM_STAGED 512  // sequences whose cu_seqlens / slot ids go to shared memory
+#endif
 
 constexpr int kStreamCpt = SC_STREAM_CPT;
-constexpr int kStreamSlice = 2048;                         // channels per CTA slice
-constexpr int kStreamCuBytes = ((kMaxStagedSeqs + 1) * 4 + 127) / 128 * 128;
-constexpr int kStreamHeader = 256 + kStreamCuBytes + kMaxStagedSeqs * 4;  // barriers, cu, slots
+constexpr int kStreamSlice = SC_STREAM_SLICE;
+constexpr int kStreamStaged = SC_STREAM_STAGED;
+constexpr int kStreamCuBytes = ((kStreamStaged + 1) * 4 + 127) / 128 * 128;
+constexpr int kStreamHeader = 256 + kStreamCuBytes + kStreamStaged * 4;  // barriers, cu, slots
 constexpr int kStreamMinRows = 8;                          // rows per CTA at least
 static_assert(kStreamSlice / kStreamCpt + 32 <= 1024, "one CTA holds a slice's consumers");
 
@@ -58,7 +68,7 @@ constexpr size_t stream_smem_bytes(int CW) {
 }
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kStreamSlice / kStreamCpt + 32, 1)
+__global__ void __launch_bounds__(kStreamSlice / kStreamCpt + 32, SC_STREAM_MIN_CTAS)
     k_prefill_stream(const T *__restrict__ bcx, int64_t T_rows, int H, const T *__restrict__ w,
                      const int32_t *__restrict__ cu, int N, const int32_t *__restrict__ slots,
                      T *__restrict__ pool, int n_slots, T *__restrict__ y, int n_slices,
@@ -128,7 +138,7 @@ __global__ void __launch_bounds__(kStreamSlice / kStreamCpt + 32, 1)
         for (int c = from; c < to; ++c) mbar_wait_bounded(&full[c % NS], (uint32_t)(c / NS) & 1u);
     };
 
-    const bool staged = N <= kMaxStagedSeqs;
+    const bool staged = N <= kStreamStaged;
     int bad = 0;
     for (int j = tid; j <= N; j += blockDim.x) {
         const int32_t c = cu[j];
