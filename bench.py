@@ -49,7 +49,8 @@ E = 2  # bf16 bytes
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["lfm2_gated_short_gb300/csrc/forward.cu",
                   "lfm2_gated_short_gb300/csrc/prefill_stream.cuh",
-                  "lfm2_gated_short_gb300/csrc/common.cuh", "lfm2_gated_short_gb300/csrc/launch.h"]
+                  "lfm2_gated_short_gb300/csrc/common.cuh", "lfm2_gated_short_gb300/csrc/launch.h",
+                  "lfm2_gated_short_gb300/csrc/tma.cuh", "lfm2_gated_short_gb300/csrc/errors.cuh"]
 PROFILE = "profiles/prefill_T4096_H2048.txt"
 
 

@@ -8,12 +8,12 @@
 //   dC_t = dy_t z_t,  dz_t = dy_t C_t,  du_s = sum_k w_k dz_{s+K-1-k},
 //   dB_s = du_s x_s,  dx_s = du_s B_s,  dW[h,k] = sum_t dz_t u_{t-K+1+k}.
 //
-// Same streamed design as the prefill: one persistent CTA per SM owns a
-// balanced range of rows [cr0, cr1) of a slice of up to 512 channels; a
+// Same streamed design as the prefill: persistent CTAs (several per SM) each
+// own a balanced range of rows [cr0, cr1) of a slice of up to 512 channels; a
 // producer warp streams the rows' B|C|x and dy sections -- plus the K-1 rows
 // before the range (u history) and after it (dz look-ahead) -- through a
 // shared-memory ring with 1-D bulk asynchronous copies on full/empty
-// mbarriers; 16 consumer warps, 4 channels per thread, walk the rows. Each
+// mbarriers; the consumer warps, 4 channels per thread, walk the rows. Each
 // thread holds its channels' dW over the whole range in registers and
 // writes one fp32 partial per CTA; a second kernel adds the partials of all
 // CTAs in a fixed order, so dW has the same bits on every call.
