@@ -260,3 +260,47 @@ def test_rollback_equals_decoding_the_accepted_prefix_on_gpu():
         if len(take):
             sc.decode(dev(rows[take, j], "bf16"), w, dev(s.slot_ids[take], "i32"), pool_d)
     assert_bits(host(pool_v), host(pool_d), "rollback vs decode")
+
+
+def test_graph_captured_layers_match_eager_calls():
+    """Decode, verify and rollback captured in one CUDA graph (dependent launches
+    chained through the shared pools) give the same bits as eager calls."""
+    s = wl.decode_serving(layers=3, steps=2, batch=64, H=512, K=3, n_slots=128, seed=110)
+    v = wl.verify_serving(layers=3, batch=16, D=4, H=512, K=3, n_slots=128, seed=111)
+
+    def run(graph: bool):
+        pools = [dev(s.pools[l], "bf16") for l in range(3)]
+        w = [dev(s.w[l], "bf16") for l in range(3)]
+        slots = dev(s.slot_ids, "i32")
+        vs = dev(s.slot_ids[:16], "i32")  # verify on slots the decode just wrote (distinct)
+        acc = dev(v.accepted, "i32")
+        bcx = [[dev(s.bcx[l, t], "bf16") for t in range(2)] for l in range(3)]
+        vb = [dev(v.bcx[l], "bf16") for l in range(3)]
+        ys = [torch.empty((64, 512), dtype=torch.bfloat16, device="cuda") for _ in range(6)]
+        wins = [torch.empty((16, 4, 512, 3), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+        yv = [torch.empty((64, 512), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+
+        def body():
+            for t in range(2):
+                for l in range(3):
+                    sc.decode(bcx[l][t], w[l], slots, pools[l], y=ys[3 * t + l])
+            for l in range(3):
+                sc.verify(vb[l], w[l], vs, pools[l], 4, win=wins[l], y=yv[l])
+                sc.rollback(wins[l], acc, vs, pools[l])
+
+        if graph:
+            side = torch.cuda.Stream()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g, stream=side):
+                    body()
+            g.replay()
+        else:
+            body()
+        torch.cuda.synchronize()
+        return [host(t) for t in ys + wins + yv + pools]
+
+    eager, graphed = run(False), run(True)
+    for a, b in zip(eager, graphed):
+        assert_bits(b, a, "graph vs eager")
+    assert sc.get_error() == 0
