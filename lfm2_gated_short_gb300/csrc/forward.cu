@@ -287,10 +287,15 @@ cudaError_t launch_prefill(int dtype, int H, int K, const void *bcx, int64_t row
 
 // ------------------------------------------------------------------- decode
 //
+#ifndef SC_DECODE_THREADS
+#define SC_DECODE_THREADS 256  // threads per CTA (build-time knob)
+#endif
+constexpr int kDecodeThreads = SC_DECODE_THREADS;
+//
 // Unit = (sequence i, channel group). The token's B, C, x loads do not depend
 // on the slot id, so they are issued before the slot-dependent state load.
 template <typename T, int K>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kDecodeThreads)
     k_decode(const T *__restrict__ bcx, int N, int H, const T *__restrict__ w,
              const int32_t *__restrict__ slots, T *__restrict__ pool, int n_slots,
              T *__restrict__ y) {
@@ -328,8 +333,8 @@ static cudaError_t decode_inst(const void *bcx, int N, int H, const void *w,
                                const int32_t *slots, void *pool, int n_slots, void *y,
                                cudaStream_t stream) {
     const int64_t units = (int64_t)N * (H / kCh);
-    const int64_t blocks = (units + kThreads - 1) / kThreads;
-    return launch_pdl(k_decode<T, K>, dim3((unsigned)blocks), dim3(kThreads), 0, stream,
+    const int64_t blocks = (units + kDecodeThreads - 1) / kDecodeThreads;
+    return launch_pdl(k_decode<T, K>, dim3((unsigned)blocks), dim3(kDecodeThreads), 0, stream,
                       (const T *)bcx, N, H, (const T *)w, slots, (T *)pool, n_slots, (T *)y);
 }
 

@@ -5,6 +5,10 @@
 
 #include <utility>
 
+#ifndef SC_USE_PDL
+#define SC_USE_PDL 1  // build-time knob: 0 launches without the attribute
+#endif
+
 namespace sc {
 
 // Launch `kernel` on `stream` allowing it to be scheduled before the previous
@@ -22,7 +26,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = SC_USE_PDL ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
