@@ -67,8 +67,10 @@ def _load():
             lib.orc_verify.argtypes = [i32, i32, i32, p, i32, i32, p, p, p, i32, p, p]
             lib.orc_rollback.argtypes = [i32, i32, i32, i32, i32, p, p, p, p, i32]
             lib.orc_backward.argtypes = [i32, i32, i32, p, i64, p, p, p, p]
+            lib.orc_backward_varlen.argtypes = [i32, i32, i32, p, i64, p, p, i32, p, p, p, p,
+                                                p, p]
             for f in (lib.orc_prefill, lib.orc_decode, lib.orc_verify,
-                      lib.orc_rollback, lib.orc_backward):
+                      lib.orc_rollback, lib.orc_backward, lib.orc_backward_varlen):
                 f.restype = i32
             lib.orc_double_to_bf16.argtypes = [ctypes.c_double]
             lib.orc_double_to_bf16.restype = ctypes.c_uint16
@@ -210,3 +212,35 @@ def backward(dtype, bcx, w, dy):
     st = _load().orc_backward(code, H, K, _ptr(bcx), T, _ptr(w), _ptr(dy),
                               _ptr(dbcx), _ptr(dw))
     return st, dbcx, dw
+
+
+def backward_varlen(dtype, bcx, w, cu_seqlens, dy, init=None, d_final=None):
+    """Packed varlen backward with initial states; returns ``(status, dbcx, dw, d_init)``.
+
+    ``init`` is ``[N, H, K]`` in ``dtype`` (None: zeros); ``d_final`` is
+    ``[N, H, K]`` float64 (None: zeros); ``dw`` and ``d_init`` are float64.
+    """
+    code, npdt = _code(dtype)
+    bcx, w, dy = _arr(bcx, npdt), _arr(w, npdt), _arr(dy, npdt)
+    cu = _idx(cu_seqlens)
+    N = len(cu) - 1
+    T, H3 = bcx.shape
+    H = H3 // 3
+    K = w.shape[1]
+    if init is not None:
+        init = _arr(init, npdt)
+        if init.shape != (N, H, K):
+            raise ValueError("init must be [N, H, K]")
+    if d_final is not None:
+        d_final = _arr(d_final, np.float64)
+        if d_final.shape != (N, H, K):
+            raise ValueError("d_final must be [N, H, K]")
+    dbcx = np.zeros((T, 3 * H), dtype=npdt)
+    dw = np.zeros((H, K), dtype=np.float64)
+    d_init = np.zeros((N, H, K), dtype=np.float64)
+    st = _load().orc_backward_varlen(
+        code, H, K, _ptr(bcx), T, _ptr(w), _ptr(cu), N,
+        _ptr(init) if init is not None else None, _ptr(dy),
+        _ptr(d_final) if d_final is not None else None, _ptr(dbcx), _ptr(dw), _ptr(d_init))
+    return st, dbcx, dw, d_init
+

@@ -373,3 +373,91 @@ int orc_backward(int dt, int H, int K, const void *bcx, int64_t T, const void *w
     free(dz);
     return ORC_OK;
 }
+
+/*
+ * Backward of the packed varlen prefill with initial states (training on
+ * packed sequences, and chunked training that carries the state from one
+ * chunk to the next). Sequence i covers rows cu_seqlens[i] .. cu_seqlens[i+1]-1
+ * and starts from the state init[i] ([N, H, K], NULL = zeros). Writing the
+ * sequence as one array ext = [init_0 .. init_{K-1}, u_0 .. u_{len-1}], the
+ * window at row t is ext[t+1 .. t+K], z_t = sum_k w_k ext[t+1+k] and the final
+ * state is ext[len .. len+K-1]. Given dy and an optional gradient d_final
+ * ([N, H, K] doubles, NULL = zeros) of the final states:
+ *   d ext[j] = sum over (t, k) with t+1+k = j of w_k dz_t,  dz_t = dy_t C_t,
+ *              plus d_final[j - len] for j >= len;
+ *   du_s = d ext[K+s];  dB_s = du_s x_s;  dx_s = du_s B_s;  dC_t = dy_t z_t;
+ *   dW[h,k] = sum over sequences and rows of dz_t ext[t+1+k];
+ *   d_init[i] = d ext[0 .. K-1]  ([N, H, K] doubles, written if not NULL).
+ * The rounding of u is passed straight through. Returns ORC_EDATA (nothing
+ * written) for a cu_seqlens that is not 0 <= ... <= T ending at T.
+ */
+int orc_backward_varlen(int dt, int H, int K, const void *bcx, int64_t T, const void *w,
+                        const int32_t *cu_seqlens, int N, const void *init, const void *dy,
+                        const double *d_final, void *dbcx, double *dw, double *d_init)
+{
+    if (!dtype_ok(dt) || H <= 0 || K <= 0 || T < 0 || N < 0)
+        return ORC_EINVAL;
+    if (cu_seqlens[0] != 0 || cu_seqlens[N] != T)
+        return ORC_EDATA;
+    int64_t maxlen = 0;
+    for (int i = 0; i < N; ++i) {
+        if (cu_seqlens[i + 1] < cu_seqlens[i])
+            return ORC_EDATA;
+        if (cu_seqlens[i + 1] - cu_seqlens[i] > maxlen)
+            maxlen = cu_seqlens[i + 1] - cu_seqlens[i];
+    }
+    size_t n = (size_t)(K + maxlen);
+    double *ext = (double *)malloc(sizeof(double) * n);
+    double *dext = (double *)malloc(sizeof(double) * n);
+    if (!ext || !dext) {
+        free(ext);
+        free(dext);
+        return ORC_EINVAL;
+    }
+    for (int64_t e = 0; e < (int64_t)H * K; ++e)
+        dw[e] = 0.0;
+    for (int i = 0; i < N; ++i) {
+        int64_t row0 = cu_seqlens[i], len = (int64_t)cu_seqlens[i + 1] - cu_seqlens[i];
+        for (int h = 0; h < H; ++h) {
+            int64_t sbase = ((int64_t)i * H + h) * K;
+            for (int m = 0; m < K; ++m)
+                ext[m] = init ? load(dt, init, sbase + m) : 0.0;
+            for (int64_t s = 0; s < len; ++s) {
+                int64_t r = row0 + s;
+                ext[K + s] = round_to(dt, load(dt, bcx, r * 3 * H + h) *
+                                              load(dt, bcx, r * 3 * H + 2 * H + h));
+            }
+            for (int64_t j = 0; j < K + len; ++j)
+                dext[j] = 0.0;
+            for (int64_t t = 0; t < len; ++t) {
+                int64_t r = row0 + t;
+                double z = 0.0;
+                for (int k = 0; k < K; ++k)
+                    z += load(dt, w, (int64_t)h * K + k) * ext[t + 1 + k];
+                double g = load(dt, dy, r * H + h);
+                double dz = g * load(dt, bcx, r * 3 * H + H + h);
+                store(dt, dbcx, r * 3 * H + H + h, g * z);
+                for (int k = 0; k < K; ++k) {
+                    dext[t + 1 + k] += load(dt, w, (int64_t)h * K + k) * dz;
+                    dw[(int64_t)h * K + k] += dz * ext[t + 1 + k];
+                }
+            }
+            if (d_final)
+                for (int k = 0; k < K; ++k)
+                    dext[len + k] += d_final[sbase + k];
+            for (int64_t s = 0; s < len; ++s) {
+                int64_t r = row0 + s;
+                double du = dext[K + s];
+                store(dt, dbcx, r * 3 * H + h, du * load(dt, bcx, r * 3 * H + 2 * H + h));
+                store(dt, dbcx, r * 3 * H + 2 * H + h, du * load(dt, bcx, r * 3 * H + h));
+            }
+            if (d_init)
+                for (int m = 0; m < K; ++m)
+                    d_init[sbase + m] = dext[m];
+        }
+    }
+    free(ext);
+    free(dext);
+    return ORC_OK;
+}
+

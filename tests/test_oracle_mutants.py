@@ -35,6 +35,10 @@ MUTANTS = {
     "backward_du_index": ("int64_t q = s + K - 1 - k;", "int64_t q = s + k;"),
     "backward_dw_tap": ("int64_t p = t - K + 1 + k;\n                if (p >= 0)\n                    acc += dz[t] * u[p];",
                         "int64_t p = t - k;\n                if (p >= 0)\n                    acc += dz[t] * u[p];"),
+    "varlen_init_ignored": ("ext[m] = init ? load(dt, init, sbase + m) : 0.0;",
+                            "ext[m] = 0.0;"),
+    "varlen_final_grad_dropped": ("dext[len + k] += d_final[sbase + k];",
+                                  "dext[len + k] += 0.0 * d_final[sbase + k];"),
     "backward_dx_uses_x": ("store(dt, dbcx, s * 3 * H + 2 * H + h, du * b);",
                            "store(dt, dbcx, s * 3 * H + 2 * H + h, du * x);"),
 }

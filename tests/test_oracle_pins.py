@@ -447,3 +447,116 @@ def test_tiny_fp32_config_prefill_then_decode_matches_conv1d():
     y_ref = (allrows[:, H:2 * H] * z).astype(np.float32)
     np.testing.assert_array_equal(np.concatenate(ys, 0), y_ref)
     np.testing.assert_array_equal(pool[0], u32[-p.K:].T.astype(np.float32))
+
+
+# ------------------------------------------- varlen backward with states
+
+def _torch_varlen_grads(bcx64, w64, cu, dy64, init64, dfin64, round_u=None):
+    """<dy, y> + <d_final, final state> differentiated by torch autograd (float64)."""
+    T, H3 = bcx64.shape
+    H = H3 // 3
+    K = w64.shape[1]
+    bcx = torch.tensor(bcx64, requires_grad=True)
+    w = torch.tensor(w64, requires_grad=True)
+    init = torch.tensor(init64, requires_grad=True)
+    loss = torch.zeros((), dtype=torch.float64)
+    for i in range(len(cu) - 1):
+        a, b = int(cu[i]), int(cu[i + 1])
+        B, C, X = bcx[a:b, :H], bcx[a:b, H:2 * H], bcx[a:b, 2 * H:]
+        u = B * X
+        if round_u is not None:
+            u = u + (round_u(u.detach()) - u.detach())
+        ext = torch.cat([init[i], u.T], dim=1)                    # [H, K + len]
+        if b > a:
+            z = F.conv1d(ext[None, :, 1:], w[:, None, :], groups=H)[0].T
+            loss = loss + (C * z * torch.from_numpy(dy64[a:b])).sum()
+        loss = loss + (ext[:, -K:] * torch.from_numpy(dfin64[i])).sum()
+    loss.backward()
+    return bcx.grad.numpy(), w.grad.numpy(), init.grad.numpy()
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
+def test_backward_varlen_f64_matches_torch_autograd(K):
+    rng = np.random.default_rng(70 + K)
+    H, lengths = 4, [3, 0, 1, 2, 7, 5]
+    cu = np.r_[0, np.cumsum(lengths)].astype(np.int32)
+    T, N = int(cu[-1]), len(lengths)
+    bcx = rng.standard_normal((T, 3 * H))
+    w = rng.standard_normal((H, K))
+    dy = rng.standard_normal((T, H))
+    init = rng.standard_normal((N, H, K))
+    dfin = rng.standard_normal((N, H, K))
+    st, dbcx, dw, dinit = oracle.backward_varlen("f64", bcx, w, cu, dy, init, dfin)
+    assert st == oracle.OK
+    g_bcx, g_w, g_init = _torch_varlen_grads(bcx, w, cu, dy, init, dfin)
+    np.testing.assert_allclose(dbcx, g_bcx, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dw, g_w, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dinit, g_init, rtol=1e-12, atol=1e-12)
+
+
+def test_backward_varlen_reduces_to_the_single_sequence_backward():
+    rng = np.random.default_rng(75)
+    H, K, T = 6, 3, 40
+    bcx = rng.standard_normal((T, 3 * H))
+    w = rng.standard_normal((H, K))
+    dy = rng.standard_normal((T, H))
+    st, dbcx, dw, dinit = oracle.backward_varlen("f64", bcx, w, [0, T], dy)
+    st2, dbcx2, dw2 = oracle.backward("f64", bcx, w, dy)
+    assert st == st2 == oracle.OK
+    np.testing.assert_allclose(dbcx, dbcx2, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dw, dw2, rtol=1e-12, atol=1e-12)
+
+
+def test_backward_varlen_equals_per_sequence_calls():
+    rng = np.random.default_rng(76)
+    H, K, lengths = 8, 4, [5, 1, 0, 9, 2]
+    cu = np.r_[0, np.cumsum(lengths)].astype(np.int32)
+    T, N = int(cu[-1]), len(lengths)
+    bcx = _rand((T, 3 * H), "bf16", rng)
+    w = _rand((H, K), "bf16", rng, wl.WEIGHT_STD)
+    dy = _rand((T, H), "bf16", rng)
+    init = _rand((N, H, K), "bf16", rng)
+    dfin = rng.standard_normal((N, H, K))
+    st, dbcx, dw, dinit = oracle.backward_varlen("bf16", bcx, w, cu, dy, init, dfin)
+    assert st == oracle.OK
+    dw_sum = np.zeros_like(dw)
+    for i in range(N):
+        a, b = int(cu[i]), int(cu[i + 1])
+        st, d1, w1, i1 = oracle.backward_varlen("bf16", bcx[a:b], w, [0, b - a], dy[a:b],
+                                                init[i:i + 1], dfin[i:i + 1])
+        assert st == oracle.OK
+        np.testing.assert_array_equal(dbcx[a:b], d1)
+        np.testing.assert_array_equal(dinit[i], i1[0])
+        dw_sum += w1
+    np.testing.assert_allclose(dw, dw_sum, rtol=1e-12, atol=1e-12)
+
+
+def test_backward_varlen_bf16_matches_autograd_with_straight_through_rounding():
+    rng = np.random.default_rng(77)
+    H, K, lengths = 16, 3, [7, 2, 12]
+    cu = np.r_[0, np.cumsum(lengths)].astype(np.int32)
+    T, N = int(cu[-1]), len(lengths)
+    bcx = _rand((T, 3 * H), "bf16", rng)
+    w = _rand((H, K), "bf16", rng, wl.WEIGHT_STD)
+    dy = _rand((T, H), "bf16", rng)
+    init = _rand((N, H, K), "bf16", rng)
+    dfin = rng.standard_normal((N, H, K))
+    st, dbcx, dw, dinit = oracle.backward_varlen("bf16", bcx, w, cu, dy, init, dfin)
+    assert st == oracle.OK
+    rnd = lambda u: u.float().to(torch.bfloat16).double()
+    g_bcx, g_w, g_init = _torch_varlen_grads(_f64("bf16", bcx), _f64("bf16", w), cu,
+                                             _f64("bf16", dy), _f64("bf16", init), dfin, rnd)
+    np.testing.assert_allclose(dw, g_w, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dinit, g_init, rtol=1e-12, atol=1e-12)
+    g32 = g_bcx.astype(np.float32)
+    ref = torch_bf16_bits(torch.from_numpy(g32))
+    at_tie = (g32.view(np.uint32) & 0xFFFF) == 0x8000
+    assert np.all((dbcx == ref) | at_tie)
+
+
+def test_backward_varlen_rejects_bad_cu_seqlens():
+    rng = np.random.default_rng(78)
+    bcx = rng.standard_normal((6, 12))
+    st, *_ = oracle.backward_varlen("f64", bcx, rng.standard_normal((4, 3)), [0, 4, 3, 6],
+                                    rng.standard_normal((6, 4)))
+    assert st == oracle.EDATA
