@@ -200,6 +200,40 @@ sc_status shortconv_backward(sc_dtype dtype, int H, int K, const void *bcx, int6
                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Backward of the packed varlen prefill with initial states: training on
+ * packed sequences, and chunked training that carries each sequence's state
+ * from one chunk to the next (Liger-Kernel PR #1317's packed SFT workloads
+ * train this layer on packed sequences; the zero-state single-sequence case
+ * is shortconv_backward).
+ *
+ * Sequence i is rows cu_seqlens[i] .. cu_seqlens[i+1]-1 and starts from the
+ * state init_states[i] (as a prefill would have read it from its slot). With
+ * ext = [init_0 .. init_{K-1}, u_0 .. u_{len-1}], row t's window is
+ * ext[t+1 .. t+K] and the final state is ext[len .. len+K-1]. Given dy and an
+ * optional gradient d_final of the final states, the call writes
+ *   dB, dC, dx (as shortconv_backward, history and look-ahead staying inside
+ *   each sequence), dW (fp32, summed over all sequences) and
+ *   d_init[i][h][m] = gradient of init_states[i][h][m] (tap 0 only ever gets
+ *   d_final's share, for empty sequences).
+ * The rounding of u is passed straight through.
+ *
+ *   bcx [T, 3H], w [H, K], dy [T, H]: read (dtype)
+ *   cu_seqlens int32 [N + 1]: read; 0, non-decreasing, ending at T
+ *   init_states [N, H, K] (dtype) or NULL for zero states: read
+ *   d_final [N, H, K] fp32 or NULL for zero: read
+ *   dbcx [T, 3H] (dtype), dw [H, K] fp32: written
+ *   d_init [N, H, K] fp32 or NULL (not computed): written
+ *   workspace: at least shortconv_backward_workspace_bytes(H, K, T) bytes.
+ * Device errors: SC_DEV_BAD_SEQLENS (dw is zeroed; dbcx and d_init are not
+ * written).
+ */
+sc_status shortconv_backward_varlen(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
+                                    const void *w, const int32_t *cu_seqlens, int N,
+                                    const void *init_states, const void *dy,
+                                    const float *d_final, void *dbcx, float *dw, float *d_init,
+                                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * shortconv_backward without a workspace argument, for callers that cannot
  * allocate device memory when they call: code running inside a host
  * framework that owns all device memory through its own pool and forbids

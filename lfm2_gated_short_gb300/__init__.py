@@ -59,11 +59,13 @@ def lib() -> ctypes.CDLL:
             L.shortconv_backward_workspace_bytes.restype = ctypes.c_size_t
             L.shortconv_backward.argtypes = [i32, i32, i32, p, i64, p, p, p, p, p,
                                              ctypes.c_size_t, p]
+            L.shortconv_backward_varlen.argtypes = [i32, i32, i32, p, i64, p, p, i32, p, p, p,
+                                                    p, p, p, p, ctypes.c_size_t, p]
             L.shortconv_get_error.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
             L.shortconv_status_string.argtypes = [i32]
             L.shortconv_status_string.restype = ctypes.c_char_p
             for f in ("prefill", "prefill_tiled", "decode", "verify", "rollback", "backward",
-                      "get_error"):
+                      "backward_varlen", "get_error"):
                 getattr(L, "shortconv_" + f).restype = i32
             _lib = L
     return _lib
@@ -201,6 +203,43 @@ def backward(bcx, w, dy, dbcx=None, dw=None, workspace=None, stream=None):
         _dev(dw, "dw", torch.float32, (H, K)), _dev(workspace, "workspace"),
         workspace.numel(), _stream(stream, bcx.device)))
     return dbcx, dw
+
+
+def backward_varlen(bcx, w, cu_seqlens, dy, init_states=None, d_final=None, dbcx=None,
+                    dw=None, d_init=None, workspace=None, want_d_init=True, stream=None):
+    """Packed varlen backward with initial states; returns ``(dbcx, dw, d_init)``.
+
+    ``init_states`` is ``[N, H, K]`` (the data dtype; None: zeros);
+    ``d_final`` is ``[N, H, K]`` float32 (None: zeros); ``d_init`` is
+    ``[N, H, K]`` float32 (None when ``want_d_init`` is False).
+    """
+    dt = bcx.dtype
+    T, H3 = bcx.shape
+    H, K = w.shape
+    if H3 != 3 * H:
+        raise ValueError("bcx must be [T, 3H] for w [H, K]")
+    N = cu_seqlens.shape[0] - 1
+    need = backward_workspace_bytes(H, K, T)
+    if dbcx is None:
+        dbcx = torch.empty_like(bcx)
+    if dw is None:
+        dw = torch.empty((H, K), dtype=torch.float32, device=bcx.device)
+    if want_d_init and d_init is None:
+        d_init = torch.empty((N, H, K), dtype=torch.float32, device=bcx.device)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=bcx.device)
+    if workspace.dtype != torch.uint8 or workspace.numel() < need:
+        raise ValueError(f"workspace must be a uint8 tensor of at least {need} bytes")
+    init_p = _dev(init_states, "init_states", dt, (N, H, K)) if init_states is not None else None
+    dfin_p = _dev(d_final, "d_final", torch.float32, (N, H, K)) if d_final is not None else None
+    dini_p = _dev(d_init, "d_init", torch.float32, (N, H, K)) if d_init is not None else None
+    _raise_on("shortconv_backward_varlen", lib().shortconv_backward_varlen(
+        _dcode(bcx), H, K, _dev(bcx, "bcx", dt), T, _dev(w, "w", dt),
+        _dev(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,)), N, init_p,
+        _dev(dy, "dy", dt, (T, H)), dfin_p, _dev(dbcx, "dbcx", dt, (T, 3 * H)),
+        _dev(dw, "dw", torch.float32, (H, K)), dini_p, _dev(workspace, "workspace"),
+        workspace.numel(), _stream(stream, bcx.device)))
+    return dbcx, dw, d_init
 
 
 def get_error(stream=None, device=None) -> int:

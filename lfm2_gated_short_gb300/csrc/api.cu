@@ -200,6 +200,44 @@ sc_status shortconv_backward(sc_dtype dtype, int H, int K, const void *bcx, int6
                                          (cudaStream_t)stream));
 }
 
+sc_status shortconv_backward_varlen(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
+                                    const void *w, const int32_t *cu_seqlens, int N,
+                                    const void *init_states, const void *dy,
+                                    const float *d_final, void *dbcx, float *dw, float *d_init,
+                                    void *workspace, size_t workspace_bytes, void *stream) {
+    sc_status st = check_shape(dtype, H, K);
+    if (st != SC_OK) return st;
+    if (T < 0 || T > INT32_MAX || N < 0) return SC_EINVAL;
+    if (N == 0 && T != 0) return SC_EINVAL;
+    const size_t es = elem_size(dtype);
+    const size_t n_bcx = (size_t)T * 3 * H * es, n_dy = (size_t)T * H * es;
+    const size_t n_w = (size_t)H * K * es, n_dw = (size_t)H * K * 4;
+    const size_t n_st = (size_t)N * H * K * es, n_sf = (size_t)N * H * K * 4;
+    const size_t need = sc::backward_workspace_bytes(H, K, T);
+    if (workspace_bytes < need) return SC_EINVAL;
+    if (!ptr_ok(bcx, n_bcx, 16) || !ptr_ok(dy, n_dy, 16) || !ptr_ok(w, n_w, 16) ||
+        !ptr_ok(dbcx, n_bcx, 16) || !ptr_ok(dw, n_dw, 4) || !ptr_ok(workspace, need, 16) ||
+        !ptr_ok(cu_seqlens, (size_t)(N + 1) * 4, 4))
+        return SC_EINVAL;
+    if ((init_states && !aligned(init_states, 4)) || (d_final && !aligned(d_final, 4)) ||
+        (d_init && !aligned(d_init, 4)))
+        return SC_EINVAL;
+    const void *ins[6] = {bcx, w, dy, init_states, d_final, cu_seqlens};
+    const size_t nins[6] = {n_bcx, n_w, n_dy, init_states ? n_st : 0, d_final ? n_sf : 0,
+                            (size_t)(N + 1) * 4};
+    const void *outs[4] = {dbcx, dw, d_init, workspace};
+    const size_t nouts[4] = {n_bcx, n_dw, d_init ? n_sf : 0, need};
+    for (int o = 0; o < 4; ++o) {
+        for (int i = 0; i < 6; ++i)
+            if (overlaps(outs[o], nouts[o], ins[i], nins[i])) return SC_EINVAL;
+        for (int p = o + 1; p < 4; ++p)
+            if (overlaps(outs[o], nouts[o], outs[p], nouts[p])) return SC_EINVAL;
+    }
+    return from_cuda(sc::launch_backward_varlen(dtype, H, K, bcx, T, w, cu_seqlens, N,
+                                                init_states, dy, d_final, dbcx, dw, d_init,
+                                                workspace, (cudaStream_t)stream));
+}
+
 sc_status shortconv_backward_noalloc(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
                                      const void *w, const void *dy, void *dbcx, float *dw,
                                      void *stream) {

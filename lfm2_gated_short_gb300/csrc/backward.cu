@@ -267,6 +267,348 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_MIN_CTAS)
         }
 }
 
+// ------------------------------------------------ packed varlen, with states
+//
+// The backward of the packed varlen prefill (rows cu[i] .. cu[i+1]-1 form
+// sequence i) with initial states init[i] and an optional gradient d_final[i]
+// flowing in through each sequence's final state. Per sequence, with
+// ext = [init_0 .. init_{K-1}, u_0 .. u_{len-1}], row t's window is
+// ext[t+1 .. t+K]; du_s sums w_k dz over rows of the same sequence only, plus
+// d_final[K + s - s1] for the last K rows; d_init[i][m] = sum_{k<m} w_k dz_{m-1-k}
+// (+ d_final[m - len] when m >= len).
+// Work split as in k_backward. A thread follows the sequence pieces of its
+// CTA's stream: a sequence starting inside the stream takes its window from
+// its initial state; at a sequence end K-1 virtual rows with dz = 0 finish the
+// last emissions; the CTA holding a sequence's first row (its owner) writes
+// d_init from the dz of the sequence's first K-1 rows, recorded on the way.
+// Empty sequences get d_init = d_final from the CTA whose range holds their
+// start (the last CTA for those starting at T).
+constexpr int kBwdStaged = 512;  // cu_seqlens entries staged in shared memory
+constexpr int kBwdCuBytes = ((kBwdStaged + 1) * 4 + 127) / 128 * 128;
+
+template <typename T>
+constexpr size_t bwd_varlen_smem_bytes(int CW) {
+    return bwd_smem_bytes<T>(CW) + kBwdCuBytes;
+}
+
+template <typename T, int K>
+__global__ void __launch_bounds__(kBwdConsumers + 32, 3)
+    k_backward_varlen(const T *__restrict__ bcx, int64_t T_rows, int H, const T *__restrict__ w,
+                      const int32_t *__restrict__ cu, int N, const T *__restrict__ init,
+                      const T *__restrict__ dy, const float *__restrict__ d_final,
+                      T *__restrict__ dbcx, float *__restrict__ partial,
+                      float *__restrict__ d_init, int n_slices, int n_row_ctas) {
+    constexpr int CPT = kBwdCpt;
+    constexpr int NP = CPT / 2;
+    constexpr int R = BwdShape<T>::R;
+    constexpr int NS = kBwdStages;
+    constexpr int KH = K > 1 ? K - 1 : 1;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + 128);
+    int32_t *s_cu = reinterpret_cast<int32_t *>(smem + kBwdHeader);
+    T *stage = reinterpret_cast<T *>(smem + kBwdHeader + kBwdCuBytes);
+
+    const int tid = threadIdx.x;
+    const int n_consumers = blockDim.x - 32;
+    const bool producer = tid >= n_consumers;
+    const bool lead = tid == n_consumers;
+    const int slice = blockIdx.x % n_slices;
+    const int64_t rc = blockIdx.x / n_slices;
+    const int c0 = slice * kBwdSlice;
+    const int CW = min(kBwdSlice, H);
+    const int cw = min(kBwdSlice, H - c0);
+    const bool active = !producer && tid * CPT < cw;
+    const int h0 = c0 + tid * CPT;
+    const int64_t cr0 = rc * T_rows / n_row_ctas, cr1 = (rc + 1) * T_rows / n_row_ctas;
+    const int64_t sr0 = max((int64_t)0, cr0 - (K - 1));
+    const int64_t sr1 = min(T_rows, cr1 + (K - 1));
+    const int n_chunks = cr0 < cr1 ? (int)((sr1 - sr0 + R - 1) / R) : 0;
+    const uint32_t sec_bytes = (uint32_t)cw * sizeof(T);
+    const int64_t ld = 3 * (int64_t)H;
+    float *pp = partial + (int64_t)rc * H * K + (int64_t)h0 * K;
+
+    if (lead) {
+#pragma unroll
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], n_consumers / 32);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_launch_dependents();
+
+    auto issue = [&](int c) {
+        const int s = c % NS;
+        const int64_t rb = sr0 + (int64_t)c * R;
+        const int rows = (int)min((int64_t)R, sr1 - rb);
+        mbar_arrive_expect_tx(&full[s], (uint32_t)rows * 4u * sec_bytes);
+        for (int rr = 0; rr < rows; ++rr) {
+            const T *src = bcx + (rb + rr) * ld + c0;
+            T *dst = stage + (size_t)(s * R + rr) * 4 * CW;
+#pragma unroll
+            for (int q = 0; q < 3; ++q)
+                bulk_copy_g2s(dst + (size_t)q * CW, src + (int64_t)q * H, sec_bytes, &full[s]);
+            bulk_copy_g2s(dst + (size_t)3 * CW, dy + (rb + rr) * (int64_t)H + c0, sec_bytes,
+                          &full[s]);
+        }
+    };
+    auto drain = [&](int from, int to) {
+        for (int c = from; c < to; ++c) mbar_wait_bounded(&full[c % NS], (uint32_t)(c / NS) & 1u);
+    };
+    auto write_partial = [&](const f32x2 (&acc)[K][NP]) {
+#pragma unroll
+        for (int q = 0; q < NP; ++q)
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                float lo, hi;
+                f2_split(acc[k][q], lo, hi);
+                pp[(2 * q) * K + k] = lo;
+                pp[(2 * q + 1) * K + k] = hi;
+            }
+    };
+    const int first = min(NS, n_chunks);
+    if (lead)
+        for (int c = 0; c < first; ++c) issue(c);
+
+    const bool staged = N <= kBwdStaged;
+    int bad = 0;
+    for (int j = tid; j <= N; j += blockDim.x) {
+        const int32_t c = cu[j];
+        if (staged) s_cu[j] = c;
+        if (j == 0 && c != 0) bad = 1;
+        if (j == N && (int64_t)c != T_rows) bad = 1;
+        if (j < N && cu[j + 1] < c) bad = 1;
+    }
+    f32x2 acc[K][NP];
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+#pragma unroll
+        for (int q = 0; q < NP; ++q) acc[k][q] = 0ull;
+    if (__syncthreads_or(bad)) {
+        if (blockIdx.x == 0 && tid == 0) raise_error(SC_DEV_BAD_SEQLENS);
+        if (lead) drain(0, first);
+        if (active) write_partial(acc);  // dW becomes 0; dB|dC|dx and d_init are not written
+        return;
+    }
+
+    if (producer) {
+        if (!lead) return;
+        int c = first;
+        for (; c < n_chunks; ++c) {
+            if (!mbar_wait_bounded(&empty[c % NS], (uint32_t)(c / NS - 1) & 1u)) {
+                raise_error(SC_DEV_TIMEOUT);
+                break;
+            }
+            issue(c);
+        }
+        drain(max(0, c - NS), c);
+        return;
+    }
+
+    auto CU = [&](int j) -> int64_t { return staged ? s_cu[j] : cu[j]; };
+    f32x2 wp[K][NP];
+    if (active) load_taps<T, CPT, K>(w + (int64_t)h0 * K, wp);
+    f32x2 uw[K][NP], dzw[K][NP], dzf[KH][NP], dfin[K][NP];
+    Sec<T, CPT> rbq[KH], rxq[KH];
+    int i = 0;
+    int64_t s0 = 0, s1 = 0;
+    bool owner = false;
+
+    auto zero = [&](auto &a) {
+        for (auto &row : a)
+#pragma unroll
+            for (int q = 0; q < NP; ++q) row[q] = 0ull;
+    };
+    auto enter = [&]() {
+        owner = s0 >= cr0 && s0 < cr1;
+        if (s0 >= sr0 && init != nullptr)
+            load_taps<T, CPT, K>(init + ((int64_t)i * H + h0) * K, uw);
+        else
+            zero(uw);
+        zero(dzw);
+        zero(dzf);
+        if (d_final != nullptr && s1 - K < cr1)  // needed only for the last K rows
+            load_taps<float, CPT, K>(d_final + ((int64_t)i * H + h0) * K, dfin);
+        else
+            zero(dfin);
+    };
+    auto slide = [&](f32x2 (&win)[K][NP], const f32x2 (&v)[NP]) {
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+#pragma unroll
+            for (int k = 0; k + 1 < K; ++k) win[k][q] = win[k + 1][q];
+            win[K - 1][q] = v[q];
+        }
+    };
+    auto push_bx = [&](const Sec<T, CPT> &b, const Sec<T, CPT> &x) {
+        if constexpr (K > 1) {
+#pragma unroll
+            for (int k = 0; k + 1 < KH; ++k) {
+                rbq[k] = rbq[k + 1];
+                rxq[k] = rxq[k + 1];
+            }
+            rbq[KH - 1] = b;
+            rxq[KH - 1] = x;
+        }
+    };
+    // du for row s = t-K+1 of the current sequence, then dB_s, dx_s.
+    auto emit = [&](int64_t t, const Sec<T, CPT> &b_s, const Sec<T, CPT> &x_s) {
+        const int64_t s = t - (K - 1);
+        if (s < s0 || s < cr0 || s >= cr1) return;
+        f32x2 fb[NP], fx[NP], db[NP], dx[NP];
+        Pairs<T, CPT>::widen(b_s, fb);
+        Pairs<T, CPT>::widen(x_s, fx);
+        const int64_t f = K + s - s1;  // final-state tap fed by u_s, if in range
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            f32x2 du = f2_mul(wp[0][q], dzw[K - 1][q]);
+#pragma unroll
+            for (int k = 1; k < K; ++k) du = f2_fma(wp[k][q], dzw[K - 1 - k][q], du);
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+                if (f == k) du = f2_fma(f2_make(1.f, 1.f), dfin[k][q], du);
+            db[q] = f2_mul(du, fx[q]);
+            dx[q] = f2_mul(du, fb[q]);
+        }
+        T *o = dbcx + s * ld + h0;
+        Pairs<T, CPT>::store(o, db);
+        Pairs<T, CPT>::store(o + 2 * H, dx);
+    };
+    auto write_d_init = [&]() {
+        const int64_t len = s1 - s0;
+        float *o = d_init + ((int64_t)i * H + h0) * K;
+#pragma unroll
+        for (int q = 0; q < NP; ++q)
+#pragma unroll
+            for (int m = 0; m < K; ++m) {
+                f32x2 g = 0ull;
+#pragma unroll
+                for (int k = 0; k < m; ++k) g = f2_fma(wp[k][q], dzf[m - 1 - k][q], g);
+                if (m >= len) g = f2_fma(f2_make(1.f, 1.f), dfin[m - len][q], g);
+                float lo, hi;
+                f2_split(g, lo, hi);
+                o[(2 * q) * K + m] = lo;
+                o[(2 * q + 1) * K + m] = hi;
+            }
+    };
+    // The sequence ended at s1 inside the stream: K-1 rows with dz = 0 finish
+    // its emissions; its owner writes d_init.
+    auto finish = [&]() {
+        f32x2 zz[NP];
+#pragma unroll
+        for (int q = 0; q < NP; ++q) zz[q] = 0ull;
+#pragma unroll
+        for (int j = 0; j + 1 < K; ++j) {
+            slide(dzw, zz);
+            emit(s1 + j, rbq[0], rxq[0]);
+            push_bx(rbq[0], rxq[0]);
+        }
+        if (owner && d_init != nullptr) write_d_init();
+    };
+
+    if (n_chunks > 0 && active) {
+        int lo = 0, hi = N - 1;  // largest i with cu[i] <= sr0: the sequence holding row sr0
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (CU(mid) <= sr0) lo = mid; else hi = mid - 1;
+        }
+        i = lo;
+        s0 = CU(i);
+        s1 = CU(i + 1);
+        enter();
+    }
+
+    const int lane = tid & 31;
+    const uint32_t base = smem_addr(stage) + (uint32_t)(tid * CPT * sizeof(T));
+    const uint32_t sec = (uint32_t)(CW * sizeof(T));
+    for (int c = 0; c < n_chunks; ++c) {
+        const int s = c % NS;
+        if (!mbar_wait_bounded(&full[s], (uint32_t)(c / NS) & 1u)) {
+            if (lane == 0) raise_error(SC_DEV_TIMEOUT);
+            return;
+        }
+        const int64_t rb = sr0 + (int64_t)c * R;
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            const int64_t t = rb + rr;
+            if (t >= sr1) break;
+            if (!active) continue;
+            if (t >= s1) {
+                finish();
+                do {
+                    ++i;
+                    s0 = CU(i);
+                    s1 = CU(i + 1);
+                } while (t >= s1);
+                enter();
+            }
+            const uint32_t a = base + (uint32_t)((s * R + rr) * 4) * sec;
+            const Sec<T, CPT> b = lds_sec<T, CPT>(a), x = lds_sec<T, CPT>(a + 2 * sec);
+            const Sec<T, CPT> cc = lds_sec<T, CPT>(a + sec), g = lds_sec<T, CPT>(a + 3 * sec);
+            f32x2 u[NP], fc[NP], fg[NP], dz[NP];
+            Pairs<T, CPT>::gate(b, x, u);
+            Pairs<T, CPT>::widen(cc, fc);
+            Pairs<T, CPT>::widen(g, fg);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) dz[q] = f2_mul(fg[q], fc[q]);
+            slide(uw, u);
+            slide(dzw, dz);
+            const int64_t r = t - s0;
+#pragma unroll
+            for (int k = 0; k < KH; ++k)
+                if (K > 1 && r == k)
+#pragma unroll
+                    for (int q = 0; q < NP; ++q) dzf[k][q] = dz[q];
+            if (t >= cr0 && t < cr1) {
+                f32x2 dc[NP];
+#pragma unroll
+                for (int q = 0; q < NP; ++q) {
+                    f32x2 z = f2_mul(wp[0][q], uw[0][q]);
+#pragma unroll
+                    for (int k = 1; k < K; ++k) z = f2_fma(wp[k][q], uw[k][q], z);
+                    dc[q] = f2_mul(fg[q], z);
+#pragma unroll
+                    for (int k = 0; k < K; ++k) acc[k][q] = f2_fma(dz[q], uw[k][q], acc[k][q]);
+                }
+                Pairs<T, CPT>::store(dbcx + t * ld + H + h0, dc);
+            }
+            if constexpr (K == 1)
+                emit(t, b, x);
+            else
+                emit(t, rbq[0], rxq[0]);
+            push_bx(b, x);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (!active) return;
+    if (n_chunks > 0) {
+        if (s1 <= sr1)
+            finish();
+        else if (owner && d_init != nullptr)
+            write_d_init();  // its first K-1 rows were streamed; the rest is another CTA's
+    }
+    // Empty sequences starting in this CTA's range (or at T, for the last CTA).
+    if (d_init != nullptr) {
+        int lo = 0, hi = N;  // first j with cu[j] >= cr0
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (CU(mid) < cr0) lo = mid + 1; else hi = mid;
+        }
+        const bool last = rc == n_row_ctas - 1;
+        for (int j = lo; j < N && (CU(j) < cr1 || (last && CU(j) == T_rows)); ++j) {
+            if (CU(j + 1) != CU(j)) continue;
+            float *o = d_init + ((int64_t)j * H + h0) * K;
+            for (int e = 0; e < CPT * K; ++e)
+                o[e] = d_final != nullptr ? d_final[((int64_t)j * H + h0) * K + e] : 0.f;
+        }
+    }
+    write_partial(acc);
+}
+
 // dw[e] = sum over CTA rows g = 0 .. G-1 of partial[g][e]: 8 warps take
 // interleaved g for 32 consecutive e, then warp 0 adds the 8 sums in order.
 __global__ void __launch_bounds__(256)
@@ -316,6 +658,61 @@ static cudaError_t backward_inst(const void *bcx, int64_t rows, int H, const voi
     const int HK = H * K;
     return launch_pdl(k_dw_reduce, dim3((HK + 31) / 32), dim3(256), 0, stream,
                       (const float *)ws, n_row, HK, dw);
+}
+
+template <typename T, int K>
+static cudaError_t backward_varlen_inst(const void *bcx, int64_t rows, int H, const void *w,
+                                        const int32_t *cu, int N, const void *init,
+                                        const void *dy, const float *d_final, void *dbcx,
+                                        float *dw, float *d_init, void *ws,
+                                        cudaStream_t stream) {
+    const int CW = H < kBwdSlice ? H : kBwdSlice;
+    const int n_slices = (H + kBwdSlice - 1) / kBwdSlice;
+    const int threads = (CW / kBwdCpt + 31) / 32 * 32 + 32;
+    const size_t smem = bwd_varlen_smem_bytes<T>(CW);
+    const int64_t n_row = bwd_row_ctas(rows);
+    auto kern = k_backward_varlen<T, K>;
+    static std::atomic<unsigned long long> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !(configured.load() & (1ull << dev))) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bwd_varlen_smem_bytes<T>(kBwdSlice));
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(1ull << dev);
+    }
+    e = launch_pdl(kern, dim3((unsigned)(n_row * n_slices)), dim3(threads), smem, stream,
+                   (const T *)bcx, rows, H, (const T *)w, cu, N, (const T *)init, (const T *)dy,
+                   d_final, (T *)dbcx, (float *)ws, d_init, n_slices, (int)n_row);
+    if (e != cudaSuccess) return e;
+    const int HK = H * K;
+    return launch_pdl(k_dw_reduce, dim3((HK + 31) / 32), dim3(256), 0, stream,
+                      (const float *)ws, n_row, HK, dw);
+}
+
+template <typename T>
+static cudaError_t backward_varlen_K(int K, const void *bcx, int64_t rows, int H, const void *w,
+                                     const int32_t *cu, int N, const void *init, const void *dy,
+                                     const float *d_final, void *dbcx, float *dw, float *d_init,
+                                     void *ws, cudaStream_t s) {
+    switch (K) {
+        case 1: return backward_varlen_inst<T, 1>(bcx, rows, H, w, cu, N, init, dy, d_final, dbcx, dw, d_init, ws, s);
+        case 2: return backward_varlen_inst<T, 2>(bcx, rows, H, w, cu, N, init, dy, d_final, dbcx, dw, d_init, ws, s);
+        case 3: return backward_varlen_inst<T, 3>(bcx, rows, H, w, cu, N, init, dy, d_final, dbcx, dw, d_init, ws, s);
+        default: return backward_varlen_inst<T, 4>(bcx, rows, H, w, cu, N, init, dy, d_final, dbcx, dw, d_init, ws, s);
+    }
+}
+
+cudaError_t launch_backward_varlen(int dtype, int H, int K, const void *bcx, int64_t T,
+                                   const void *w, const int32_t *cu, int N, const void *init,
+                                   const void *dy, const float *d_final, void *dbcx, float *dw,
+                                   float *d_init, void *ws, cudaStream_t s) {
+    if (dtype == SC_BF16)
+        return backward_varlen_K<__nv_bfloat16>(K, bcx, T, H, w, cu, N, init, dy, d_final, dbcx,
+                                                dw, d_init, ws, s);
+    return backward_varlen_K<float>(K, bcx, T, H, w, cu, N, init, dy, d_final, dbcx, dw, d_init,
+                                    ws, s);
 }
 
 template <typename T>

@@ -34,6 +34,15 @@ cudaError_t launch_backward(int dtype, int H, int K, const void *bcx, int64_t T,
                             const void *w, const void *dy, void *dbcx, float *dw,
                             void *workspace, cudaStream_t stream);
 
+// Packed varlen backward with initial states (NULL: zeros), an optional
+// final-state gradient (NULL: zeros) and an optional initial-state gradient
+// output (NULL: not written). Same workspace size as launch_backward.
+cudaError_t launch_backward_varlen(int dtype, int H, int K, const void *bcx, int64_t T,
+                                   const void *w, const int32_t *cu_seqlens, int N,
+                                   const void *init, const void *dy, const float *d_final,
+                                   void *dbcx, float *dw, float *d_init, void *workspace,
+                                   cudaStream_t stream);
+
 // The backward kernels with their dW partials in the library's fixed device
 // scratch (kNoAllocScratchBytes) instead of a caller workspace. The caller
 // checks backward_workspace_bytes(H, K, T) <= kNoAllocScratchBytes first.

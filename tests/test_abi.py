@@ -38,6 +38,8 @@ def L():
     lib.shortconv_backward_workspace_bytes.argtypes = [i32, i32, i64]
     lib.shortconv_backward_workspace_bytes.restype = ctypes.c_size_t
     lib.shortconv_backward.argtypes = [i32, i32, i32, p, i64, p, p, p, p, p, ctypes.c_size_t, p]
+    lib.shortconv_backward_varlen.argtypes = [i32, i32, i32, p, i64, p, p, i32, p, p, p, p, p,
+                                              p, p, ctypes.c_size_t, p]
     lib.shortconv_get_error.argtypes = [p, p]
     lib.shortconv_status_string.argtypes = [i32]
     lib.shortconv_status_string.restype = ctypes.c_char_p
@@ -118,6 +120,24 @@ def test_backward_workspace_and_errors(L):
     need = L.shortconv_backward_workspace_bytes(256, 3, 64)
     assert L.shortconv_backward(BF16, 256, 3, A, 64, Bp, Cp, Dp, Ep, Fp, need - 1, None) == SC_EINVAL
     assert L.shortconv_backward(BF16, 256, 3, A, 64, Bp, Cp, A, Ep, Fp, need, None) == SC_EINVAL
+
+
+def test_backward_varlen_argument_errors(L):
+    need = L.shortconv_backward_workspace_bytes(256, 3, 64)
+    ok = dict(dtype=BF16, H=256, K=3, bcx=A, T=64, w=Bp, cu=Cp, N=2, init=None, dy=Dp,
+              dfin=None, dbcx=Ep, dw=Fp, dinit=None, ws=Gp, wsb=need)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return L.shortconv_backward_varlen(a["dtype"], a["H"], a["K"], a["bcx"], a["T"], a["w"],
+                                           a["cu"], a["N"], a["init"], a["dy"], a["dfin"],
+                                           a["dbcx"], a["dw"], a["dinit"], a["ws"], a["wsb"],
+                                           None)
+    assert call(N=0) == SC_EINVAL                 # rows but no sequences
+    assert call(wsb=need - 1) == SC_EINVAL
+    assert call(dbcx=A) == SC_EINVAL              # output aliases bcx
+    assert call(dinit=Bp) == SC_EINVAL            # d_init aliases w
+    assert call(K=5) == SC_EUNSUPPORTED
 
 
 def test_status_strings_and_get_error_null(L):

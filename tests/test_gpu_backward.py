@@ -84,3 +84,94 @@ def test_backward_channel_slices_wider_than_one_cta(H):
     p = wl.training(T=333, H=H, K=3, seed=96)
     dbcx, dw = run(p)
     check_against_oracle(p, dbcx, dw)
+
+
+# ------------------------------------------- packed varlen, with states
+
+def _varlen_case(lengths, H, K, seed, dtype="bf16", with_init=True, with_final=True):
+    rng = np.random.default_rng(seed)
+    lengths = np.asarray(lengths, np.int64)
+    cu = np.r_[0, np.cumsum(lengths)].astype(np.int32)
+    T, N = int(cu[-1]), len(lengths)
+    bcx = wl.normal(rng, (T, 3 * H), 1.0, dtype)
+    w = wl.normal(rng, (H, K), wl.WEIGHT_STD, dtype)
+    dy = wl.normal(rng, (T, H), 1.0, dtype)
+    init = wl.normal(rng, (N, H, K), 1.0, dtype) if with_init else None
+    dfin = rng.standard_normal((N, H, K)).astype(np.float32) if with_final else None
+    return dict(dtype=dtype, H=H, K=K, cu=cu, bcx=bcx, w=w, dy=dy, init=init, dfin=dfin)
+
+
+def _run_varlen(c):
+    dt = c["dtype"]
+    out = sc.backward_varlen(dev(c["bcx"], dt), dev(c["w"], dt), dev(c["cu"], "i32"),
+                             dev(c["dy"], dt),
+                             init_states=None if c["init"] is None else dev(c["init"], dt),
+                             d_final=None if c["dfin"] is None else dev(c["dfin"], "f32"))
+    torch.cuda.synchronize()
+    return host(out[0]), host(out[1]), host(out[2])
+
+
+def _check_varlen(c, dbcx, dw, dinit, channels=None):
+    H = c["H"]
+    ch = np.arange(H) if channels is None else np.asarray(channels)
+    cols = np.concatenate([ch, H + ch, 2 * H + ch])
+    init = None if c["init"] is None else np.ascontiguousarray(c["init"][:, ch])
+    dfin = None if c["dfin"] is None else np.ascontiguousarray(c["dfin"][:, ch].astype(np.float64))
+    st, d_ref, dw_ref, di_ref = oracle.backward_varlen(
+        c["dtype"], np.ascontiguousarray(c["bcx"][:, cols]), np.ascontiguousarray(c["w"][ch]),
+        c["cu"], np.ascontiguousarray(c["dy"][:, ch]), init, dfin)
+    assert st == oracle.OK
+    assert_close(c["dtype"], dbcx[:, cols], d_ref, "dB|dC|dx")
+    assert_dw_close(dw[ch], dw_ref)
+    assert_dw_close(dinit[:, ch], di_ref, "d_init")
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_backward_varlen_mixed_lengths(dtype, K):
+    lengths = [5, 0, 1, 2, 3, 40, 0, 7, 64, 1, 130, 2]
+    c = _varlen_case(lengths, 256, K, 200 + K, dtype)
+    _check_varlen(c, *_run_varlen(c))
+
+
+@pytest.mark.parametrize("with_init,with_final", [(False, False), (True, False), (False, True)])
+def test_backward_varlen_optional_states(with_init, with_final):
+    c = _varlen_case([17, 3, 0, 250, 9], 512, 3, 210, "bf16", with_init, with_final)
+    _check_varlen(c, *_run_varlen(c))
+
+
+def test_backward_varlen_many_sequences_across_row_ranges():
+    rng = np.random.default_rng(211)
+    lengths = rng.integers(0, 60, size=300)
+    c = _varlen_case(lengths, 256, 4, 212)
+    _check_varlen(c, *_run_varlen(c))
+
+
+def test_backward_varlen_one_fresh_sequence_matches_the_single_sequence_kernel():
+    c = _varlen_case([3001], 512, 3, 213, with_init=False, with_final=False)
+    dbcx, dw, _ = _run_varlen(c)
+    d2, w2 = sc.backward(dev(c["bcx"], "bf16"), dev(c["w"], "bf16"), dev(c["dy"], "bf16"))
+    assert_bits(dbcx, host(d2), "dbcx")
+    np.testing.assert_array_equal(dw, host(w2))
+
+
+def test_backward_varlen_packed_lfm2_shapes_sampled_channels():
+    """16 packed sequences, lengths U{64..2048}, H=2048, K=3, with states; 64 channels checked."""
+    rng = np.random.default_rng(214)
+    c = _varlen_case(rng.integers(64, 2048, size=16, endpoint=True), 2048, 3, 215)
+    dbcx, dw, dinit = _run_varlen(c)
+    ch = np.sort(np.concatenate([[0, 7, 8, 511, 512, 2047],
+                                 rng.choice(np.arange(9, 2040), 58, replace=False)]))
+    _check_varlen(c, dbcx, dw, dinit, ch)
+
+
+def test_backward_varlen_bad_seqlens_zero_dw_and_set_the_error():
+    c = _varlen_case([4, 5, 6], 64, 3, 216)
+    bad = c["cu"].copy()
+    bad[1], bad[2] = 9, 4                               # not non-decreasing
+    dbcx0 = torch.full((15, 192), 3.0, dtype=torch.bfloat16, device="cuda")
+    dbcx, dw, _ = sc.backward_varlen(dev(c["bcx"], "bf16"), dev(c["w"], "bf16"),
+                                     dev(bad, "i32"), dev(c["dy"], "bf16"), dbcx=dbcx0)
+    assert sc.get_error() == sc.DEV_BAD_SEQLENS
+    assert np.all(host(dw) == 0.0)
+    assert np.all(host(dbcx).view(np.uint16) == np.uint16(0x4040))  # 3.0 untouched
