@@ -474,6 +474,44 @@ def training_section(sc, device, T_, reps, sets_n):
                 fwd_bwd_gbs=(fb + bb) / (fb_us * 1e-6) / 1e9, fwd_bytes=fb, bwd_bytes=bb)
 
 
+def packed_training_section(sc, device, T_=65536, reps=10):
+    """Packed training: fresh sequences with lengths U{64..2048} filling T_ rows;
+    varlen prefill forward, then the varlen backward (no state gradients)."""
+    rng = np.random.default_rng(7)
+    lengths = []
+    while sum(lengths) < T_:
+        lengths.append(int(rng.integers(64, 2048, endpoint=True)))
+    lengths[-1] -= sum(lengths) - T_
+    N = len(lengths)
+    cu = torch.tensor(np.r_[0, np.cumsum(lengths)].astype(np.int32), device=device)
+    slots = torch.arange(N, dtype=torch.int32, device=device)
+    g = torch.Generator(device=device).manual_seed(8)
+    w = randn_bf16((H, K), g, device, wl.WEIGHT_STD)
+    bcx = randn_bf16((T_, 3 * H), g, device)
+    dy = randn_bf16((T_, H), g, device)
+    y = torch.empty((T_, H), dtype=torch.bfloat16, device=device)
+    dbcx = torch.empty_like(bcx)
+    dw = torch.empty((H, K), dtype=torch.float32, device=device)
+    pool = torch.zeros((N, H, K), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(sc.backward_workspace_bytes(H, K, T_), dtype=torch.uint8, device=device)
+
+    def fwd(i):
+        sc.prefill(bcx, w, cu, slots, pool, y=y)
+
+    def bwd(i):
+        sc.backward_varlen(bcx, w, cu, dy, dbcx=dbcx, dw=dw, workspace=ws, want_d_init=False)
+
+    for i in range(3):
+        fwd(i)
+        bwd(i)
+    torch.cuda.synchronize()
+    f_us, b_us = time_loop(fwd, reps), time_loop(bwd, reps)
+    assert sc.get_error() == 0
+    fb, bb = prefill_bytes(T_, H, K, N), backward_bytes(T_, H, K)
+    return dict(T=T_, n_seqs=N, fwd_us=f_us, bwd_us=b_us, fwd_gbs=fb / (f_us * 1e-6) / 1e9,
+                bwd_gbs=bb / (b_us * 1e-6) / 1e9, fwd_bwd_ms=(f_us + b_us) / 1e3)
+
+
 def cpu_baseline(seconds=10.0):
     """The CPU oracle as it stands, single-threaded, on the headline workload."""
     import oracle
@@ -586,6 +624,7 @@ def main():
     extras["varlen"] = varlen_section(sc, device)
     extras["train_T4096"] = training_section(sc, device, 4096, 20, 4)
     extras["train_T65536"] = training_section(sc, device, 65536, 10, 1)
+    extras["train_packed_T65536"] = packed_training_section(sc, device)
     clk = clocks.stop()
     del flush_buf
     torch.cuda.empty_cache()
