@@ -70,6 +70,7 @@ typedef enum { SC_F32 = 0, SC_BF16 = 1 } sc_dtype;
 #define SC_DEV_BAD_SEQLENS 0x2u   /* cu_seqlens not 0 = c0 <= c1 <= ... <= cN = T: call skipped */
 #define SC_DEV_BAD_ACCEPTED 0x4u  /* an accepted length outside [0, D]: that sequence skipped */
 #define SC_DEV_TIMEOUT 0x8u       /* a bounded wait on an asynchronous copy gave up: output incomplete */
+#define SC_DEV_NO_SLOT 0x10u      /* a claim asked for more slots than were free: nothing claimed */
 
 /*
  * Packed variable-length prefill (continued prefill from each slot's state).
@@ -262,6 +263,41 @@ sc_status shortconv_backward_varlen(sc_dtype dtype, int H, int K, const void *bc
 sc_status shortconv_backward_noalloc(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
                                      const void *w, const void *dy, void *dbcx, float *dw,
                                      void *stream);
+
+/*
+ * Conv-state slot pool on the device (MAX LFM2 article, section "推理状态管理：
+ * ConvStateCache 与卷积状态生命周期": a request claims a free slot -- an error
+ * when none is free --, starts from a zero state, and releases the slot when
+ * it finishes). The in-use set is a caller-owned device bitmap of
+ * (n_slots + 31) / 32 uint32 words, bit (s % 32) of word s / 32 set while slot
+ * s is in use; bits past n_slots are ignored and kept. Calls on one bitmap
+ * must be ordered (one stream), like any read-modify-write of device memory.
+ *
+ * shortconv_slots_claim: take the n_claim lowest-numbered free slots, in
+ * increasing order, mark them in use and write them to slots_out [n_claim];
+ * if pool is not NULL (a [n_slots, H, K] pool of `dtype`) their states are
+ * zeroed. All-or-nothing: with fewer than n_claim free slots nothing is
+ * claimed, slots_out is all -1 and SC_DEV_NO_SLOT is set. 0 <= n_claim <= n_slots.
+ */
+sc_status shortconv_slots_claim(uint32_t *in_use, int n_slots, int n_claim, int32_t *slots_out,
+                                sc_dtype dtype, int H, int K, void *pool, void *stream);
+
+/*
+ * shortconv_slots_release: mark slot_ids [n] free. An id out of range or not
+ * in use sets SC_DEV_BAD_SLOT and is skipped; the others are released.
+ */
+sc_status shortconv_slots_release(uint32_t *in_use, int n_slots, const int32_t *slot_ids, int n,
+                                  void *stream);
+
+/*
+ * shortconv_pool_copy: pool[dst_slots[i]] = pool[src_slots[i]] for i < n (a
+ * state snapshot, e.g. to reuse the state reached at a shared prefix).
+ * Destinations must be distinct and not among the sources (not checked). An
+ * id out of range sets SC_DEV_BAD_SLOT and skips that pair.
+ */
+sc_status shortconv_pool_copy(sc_dtype dtype, int H, int K, void *pool, int n_slots,
+                              const int32_t *src_slots, const int32_t *dst_slots, int n,
+                              void *stream);
 
 /*
  * Synchronize `stream`, then read and clear the current device's error word.

@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libshortconv.so")
 
 SC_OK, SC_EINVAL, SC_EUNSUPPORTED, SC_ECUDA, SC_EDEVICE = 0, 1, 2, 3, 4
 SC_F32, SC_BF16 = 0, 1
-DEV_BAD_SLOT, DEV_BAD_SEQLENS, DEV_BAD_ACCEPTED = 0x1, 0x2, 0x4
+DEV_BAD_SLOT, DEV_BAD_SEQLENS, DEV_BAD_ACCEPTED, DEV_TIMEOUT, DEV_NO_SLOT = 0x1, 0x2, 0x4, 0x8, 0x10
 
 _lock = threading.Lock()
 _lib = None
@@ -61,11 +61,15 @@ def lib() -> ctypes.CDLL:
                                              ctypes.c_size_t, p]
             L.shortconv_backward_varlen.argtypes = [i32, i32, i32, p, i64, p, p, i32, p, p, p,
                                                     p, p, p, p, ctypes.c_size_t, p]
+            L.shortconv_slots_claim.argtypes = [p, i32, i32, p, i32, i32, i32, p, p]
+            L.shortconv_slots_release.argtypes = [p, i32, p, i32, p]
+            L.shortconv_pool_copy.argtypes = [i32, i32, i32, p, i32, p, p, i32, p]
             L.shortconv_get_error.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
             L.shortconv_status_string.argtypes = [i32]
             L.shortconv_status_string.restype = ctypes.c_char_p
             for f in ("prefill", "prefill_tiled", "decode", "verify", "rollback", "backward",
-                      "backward_varlen", "get_error"):
+                      "backward_varlen", "slots_claim", "slots_release", "pool_copy",
+                      "get_error"):
                 getattr(L, "shortconv_" + f).restype = i32
             _lib = L
     return _lib
@@ -240,6 +244,45 @@ def backward_varlen(bcx, w, cu_seqlens, dy, init_states=None, d_final=None, dbcx
         _dev(dw, "dw", torch.float32, (H, K)), dini_p, _dev(workspace, "workspace"),
         workspace.numel(), _stream(stream, bcx.device)))
     return dbcx, dw, d_init
+
+
+def slot_bitmap(n_slots: int, device="cuda") -> torch.Tensor:
+    """An all-free in-use bitmap for ``n_slots`` slots (int32 words, bit per slot)."""
+    return torch.zeros(((n_slots + 31) // 32,), dtype=torch.int32, device=device)
+
+
+def slots_claim(in_use, n_slots, n_claim, pool=None, slots_out=None, stream=None):
+    """Claim ``n_claim`` free slots (lowest first, all-or-nothing); zero their
+    states in ``pool`` if given. Returns the int32 slot ids (-1s if none)."""
+    if slots_out is None:
+        slots_out = torch.empty((n_claim,), dtype=torch.int32, device=in_use.device)
+    dt, H, K, pp = SC_BF16, 8, 1, None
+    if pool is not None:
+        dt, H, K = _dcode(pool), pool.shape[1], pool.shape[2]
+        pp = _dev(pool, "pool", pool.dtype, (n_slots, H, K))
+    _raise_on("shortconv_slots_claim", lib().shortconv_slots_claim(
+        _dev(in_use, "in_use", torch.int32, ((n_slots + 31) // 32,)), n_slots, n_claim,
+        _dev(slots_out, "slots_out", torch.int32, (n_claim,)), dt, H, K, pp,
+        _stream(stream, in_use.device)))
+    return slots_out
+
+
+def slots_release(in_use, n_slots, slot_ids, stream=None):
+    """Mark ``slot_ids`` free."""
+    n = slot_ids.shape[0]
+    _raise_on("shortconv_slots_release", lib().shortconv_slots_release(
+        _dev(in_use, "in_use", torch.int32, ((n_slots + 31) // 32,)), n_slots,
+        _dev(slot_ids, "slot_ids", torch.int32, (n,)), n, _stream(stream, in_use.device)))
+
+
+def pool_copy(pool, src_slots, dst_slots, stream=None):
+    """``pool[dst[i]] = pool[src[i]]`` (destinations distinct, not among sources)."""
+    n_slots, H, K = pool.shape
+    n = src_slots.shape[0]
+    _raise_on("shortconv_pool_copy", lib().shortconv_pool_copy(
+        _dcode(pool), H, K, _dev(pool, "pool", pool.dtype, (n_slots, H, K)), n_slots,
+        _dev(src_slots, "src_slots", torch.int32, (n,)),
+        _dev(dst_slots, "dst_slots", torch.int32, (n,)), n, _stream(stream, pool.device)))
 
 
 def get_error(stream=None, device=None) -> int:

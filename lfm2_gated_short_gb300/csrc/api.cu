@@ -261,6 +261,56 @@ sc_status shortconv_backward_noalloc(sc_dtype dtype, int H, int K, const void *b
                                                  (cudaStream_t)stream));
 }
 
+sc_status shortconv_slots_claim(uint32_t *in_use, int n_slots, int n_claim, int32_t *slots_out,
+                                sc_dtype dtype, int H, int K, void *pool, void *stream) {
+    if (n_slots <= 0 || n_claim < 0 || n_claim > n_slots) return SC_EINVAL;
+    const size_t n_bm = (size_t)(n_slots + 31) / 32 * 4;
+    if (!ptr_ok(in_use, n_bm, 4) || !ptr_ok(slots_out, (size_t)n_claim * 4, 4)) return SC_EINVAL;
+    size_t n_pool = 0;
+    int64_t state_bytes = 0;
+    if (pool != nullptr) {
+        const sc_status st = check_shape(dtype, H, K);
+        if (st != SC_OK) return st;
+        state_bytes = (int64_t)H * K * elem_size(dtype);
+        n_pool = (size_t)n_slots * state_bytes;
+        if (!aligned(pool, 16)) return SC_EINVAL;
+    }
+    if (overlaps(in_use, n_bm, slots_out, (size_t)n_claim * 4) ||
+        overlaps(in_use, n_bm, pool, n_pool) || overlaps(slots_out, (size_t)n_claim * 4, pool, n_pool))
+        return SC_EINVAL;
+    return from_cuda(sc::launch_slots_claim(in_use, n_slots, n_claim, slots_out, pool,
+                                            state_bytes, (cudaStream_t)stream));
+}
+
+sc_status shortconv_slots_release(uint32_t *in_use, int n_slots, const int32_t *slot_ids, int n,
+                                  void *stream) {
+    if (n_slots <= 0 || n < 0) return SC_EINVAL;
+    const size_t n_bm = (size_t)(n_slots + 31) / 32 * 4;
+    if (!ptr_ok(in_use, n_bm, 4) || !ptr_ok(slot_ids, (size_t)n * 4, 4)) return SC_EINVAL;
+    if (overlaps(in_use, n_bm, slot_ids, (size_t)n * 4)) return SC_EINVAL;
+    if (n == 0) return SC_OK;
+    return from_cuda(sc::launch_slots_release(in_use, n_slots, slot_ids, n, (cudaStream_t)stream));
+}
+
+sc_status shortconv_pool_copy(sc_dtype dtype, int H, int K, void *pool, int n_slots,
+                              const int32_t *src_slots, const int32_t *dst_slots, int n,
+                              void *stream) {
+    const sc_status st = check_shape(dtype, H, K);
+    if (st != SC_OK) return st;
+    if (n_slots <= 0 || n < 0) return SC_EINVAL;
+    const int64_t state_bytes = (int64_t)H * K * elem_size(dtype);
+    const size_t n_pool = (size_t)n_slots * state_bytes;
+    if (!ptr_ok(pool, n_pool, 16) || !ptr_ok(src_slots, (size_t)n * 4, 4) ||
+        !ptr_ok(dst_slots, (size_t)n * 4, 4))
+        return SC_EINVAL;
+    if (overlaps(pool, n_pool, src_slots, (size_t)n * 4) ||
+        overlaps(pool, n_pool, dst_slots, (size_t)n * 4))
+        return SC_EINVAL;
+    if (n == 0) return SC_OK;
+    return from_cuda(sc::launch_pool_copy(src_slots, dst_slots, n, state_bytes, pool, n_slots,
+                                          (cudaStream_t)stream));
+}
+
 sc_status shortconv_get_error(void *stream, int *device_code) {
     if (device_code == nullptr) return SC_EINVAL;
     unsigned int code = 0;

@@ -54,6 +54,16 @@ cudaError_t launch_backward_noalloc(int dtype, int H, int K, const void *bcx, in
 // Take (read and clear) the backward translation unit's error word.
 cudaError_t take_error_backward(cudaStream_t stream, unsigned int *code);
 
+// Slot pool: claim n_claim free slots (lowest first, all-or-nothing) and
+// zero their states when pool != NULL; release slots; copy states.
+cudaError_t launch_slots_claim(uint32_t *in_use, int n_slots, int n_claim, int32_t *out,
+                               void *pool, int64_t state_bytes, cudaStream_t stream);
+cudaError_t launch_slots_release(uint32_t *in_use, int n_slots, const int32_t *slots, int n,
+                                 cudaStream_t stream);
+cudaError_t launch_pool_copy(const int32_t *src, const int32_t *dst, int n, int64_t state_bytes,
+                             void *pool, int n_slots, cudaStream_t stream);
+cudaError_t take_error_slots(cudaStream_t stream, unsigned int *code);
+
 // Read and clear the device error word of the current device (synchronous
 // with respect to `stream`).
 cudaError_t read_and_clear_error(cudaStream_t stream, unsigned int *code);
