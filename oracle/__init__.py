@@ -62,13 +62,13 @@ def _load():
             # to check that the pins catch the mistake.
             lib = ctypes.CDLL(os.environ.get("SHORTCONV_ORACLE_LIB") or build())
             p, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
-            lib.orc_prefill.argtypes = [i32, i32, i32, p, i64, p, p, i32, p, p, i32, p]
-            lib.orc_decode.argtypes = [i32, i32, i32, p, i32, p, p, p, i32, p]
-            lib.orc_verify.argtypes = [i32, i32, i32, p, i32, i32, p, p, p, i32, p, p]
+            lib.orc_prefill.argtypes = [i32, i32, i32, p, i64, p, p, p, i32, p, p, i32, p]
+            lib.orc_decode.argtypes = [i32, i32, i32, p, i32, p, p, p, p, i32, p]
+            lib.orc_verify.argtypes = [i32, i32, i32, p, i32, i32, p, p, p, p, i32, p, p]
             lib.orc_rollback.argtypes = [i32, i32, i32, i32, i32, p, p, p, p, i32]
-            lib.orc_backward.argtypes = [i32, i32, i32, p, i64, p, p, p, p]
-            lib.orc_backward_varlen.argtypes = [i32, i32, i32, p, i64, p, p, i32, p, p, p, p,
-                                                p, p]
+            lib.orc_backward.argtypes = [i32, i32, i32, p, i64, p, p, p, p, p, p]
+            lib.orc_backward_varlen.argtypes = [i32, i32, i32, p, i64, p, p, p, i32, p, p, p, p,
+                                                p, p, p]
             for f in (lib.orc_prefill, lib.orc_decode, lib.orc_verify,
                       lib.orc_rollback, lib.orc_backward, lib.orc_backward_varlen):
                 f.restype = i32
@@ -102,6 +102,16 @@ def _idx(a) -> np.ndarray:
     return out
 
 
+def _opt(a, npdt, shape, name):
+    """Pointer of an optional array (None: NULL)."""
+    if a is None:
+        return None, None
+    a = _arr(a, npdt)
+    if a.shape != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}")
+    return a, _ptr(a)
+
+
 def _code(dtype: str):
     if dtype not in DTYPES:
         raise ValueError(f"dtype must be one of {sorted(DTYPES)}")
@@ -129,8 +139,11 @@ def to_f64(dtype: str, a: np.ndarray) -> np.ndarray:
     return bf16_to_f64(a) if dtype == "bf16" else np.asarray(a, dtype=np.float64)
 
 
-def prefill(dtype, bcx, w, cu_seqlens, slot_ids, pool, y=None):
-    """Varlen prefill. ``pool`` is updated in place; returns ``(status, y)``."""
+def prefill(dtype, bcx, w, cu_seqlens, slot_ids, pool, y=None, bias=None):
+    """Varlen prefill. ``pool`` is updated in place; returns ``(status, y)``.
+
+    ``bias`` is an optional ``[H]`` array of ``dtype`` added to the conv output.
+    """
     code, npdt = _code(dtype)
     bcx, w, pool = _arr(bcx, npdt), _arr(w, npdt), pool
     if pool.dtype != npdt or not pool.flags.c_contiguous:
@@ -144,12 +157,13 @@ def prefill(dtype, bcx, w, cu_seqlens, slot_ids, pool, y=None):
     K = w.shape[1]
     if y is None:
         y = np.zeros((T, H), dtype=npdt)
-    st = _load().orc_prefill(code, H, K, _ptr(bcx), T, _ptr(w), _ptr(cu),
+    bias, bp = _opt(bias, npdt, (H,), "bias")
+    st = _load().orc_prefill(code, H, K, _ptr(bcx), T, _ptr(w), bp, _ptr(cu),
                              len(slots), _ptr(slots), _ptr(pool), pool.shape[0], _ptr(y))
     return st, y
 
 
-def decode(dtype, bcx, w, slot_ids, pool, y=None):
+def decode(dtype, bcx, w, slot_ids, pool, y=None, bias=None):
     """One token per sequence (row i of ``bcx`` for sequence i), pool in place."""
     code, npdt = _code(dtype)
     bcx, w = _arr(bcx, npdt), _arr(w, npdt)
@@ -161,12 +175,13 @@ def decode(dtype, bcx, w, slot_ids, pool, y=None):
     K = w.shape[1]
     if y is None:
         y = np.zeros((N, H), dtype=npdt)
-    st = _load().orc_decode(code, H, K, _ptr(bcx), N, _ptr(w), _ptr(slots),
+    bias, bp = _opt(bias, npdt, (H,), "bias")
+    st = _load().orc_decode(code, H, K, _ptr(bcx), N, _ptr(w), bp, _ptr(slots),
                             _ptr(pool), pool.shape[0], _ptr(y))
     return st, y
 
 
-def verify(dtype, bcx, w, slot_ids, pool, D, win=None, y=None):
+def verify(dtype, bcx, w, slot_ids, pool, D, win=None, y=None, bias=None):
     """Speculative verify over ``[N*D, 3H]`` draft rows; returns ``(status, win, y)``."""
     code, npdt = _code(dtype)
     bcx, w, pool = _arr(bcx, npdt), _arr(w, npdt), _arr(pool, npdt)
@@ -178,7 +193,8 @@ def verify(dtype, bcx, w, slot_ids, pool, D, win=None, y=None):
         win = np.zeros((N, D, H, K), dtype=npdt)
     if y is None:
         y = np.zeros((N * D, H), dtype=npdt)
-    st = _load().orc_verify(code, H, K, _ptr(bcx), N, D, _ptr(w), _ptr(slots),
+    bias, bp = _opt(bias, npdt, (H,), "bias")
+    st = _load().orc_verify(code, H, K, _ptr(bcx), N, D, _ptr(w), bp, _ptr(slots),
                             _ptr(pool), pool.shape[0], _ptr(win), _ptr(y))
     return st, win, y
 
@@ -196,11 +212,12 @@ def rollback(dtype, win, accepted, slot_ids, pool):
                                 _ptr(pool), pool.shape[0])
 
 
-def backward(dtype, bcx, w, dy):
-    """Single-sequence backward from a zero state; returns ``(status, dbcx, dw)``.
+def backward(dtype, bcx, w, dy, bias=None, with_dbias=False):
+    """Single-sequence backward from a zero state; returns ``(status, dbcx, dw)``,
+    or ``(status, dbcx, dw, dbias)`` when ``with_dbias``.
 
     ``dbcx`` has the ``[T, 3H]`` layout ``dB | dC | dx`` in ``dtype``; ``dw``
-    is ``[H, K]`` float64.
+    is ``[H, K]`` float64; ``dbias`` is ``[H]`` float64.
     """
     code, npdt = _code(dtype)
     bcx, w, dy = _arr(bcx, npdt), _arr(w, npdt), _arr(dy, npdt)
@@ -209,13 +226,17 @@ def backward(dtype, bcx, w, dy):
     K = w.shape[1]
     dbcx = np.zeros((T, 3 * H), dtype=npdt)
     dw = np.zeros((H, K), dtype=np.float64)
-    st = _load().orc_backward(code, H, K, _ptr(bcx), T, _ptr(w), _ptr(dy),
-                              _ptr(dbcx), _ptr(dw))
-    return st, dbcx, dw
+    dbias = np.zeros((H,), dtype=np.float64)
+    bias, bp = _opt(bias, npdt, (H,), "bias")
+    st = _load().orc_backward(code, H, K, _ptr(bcx), T, _ptr(w), bp, _ptr(dy),
+                              _ptr(dbcx), _ptr(dw), _ptr(dbias) if with_dbias else None)
+    return (st, dbcx, dw, dbias) if with_dbias else (st, dbcx, dw)
 
 
-def backward_varlen(dtype, bcx, w, cu_seqlens, dy, init=None, d_final=None):
-    """Packed varlen backward with initial states; returns ``(status, dbcx, dw, d_init)``.
+def backward_varlen(dtype, bcx, w, cu_seqlens, dy, init=None, d_final=None, bias=None,
+                    with_dbias=False):
+    """Packed varlen backward with initial states; returns ``(status, dbcx, dw, d_init)``,
+    or ``(status, dbcx, dw, d_init, dbias)`` when ``with_dbias``.
 
     ``init`` is ``[N, H, K]`` in ``dtype`` (None: zeros); ``d_final`` is
     ``[N, H, K]`` float64 (None: zeros); ``dw`` and ``d_init`` are float64.
@@ -238,9 +259,12 @@ def backward_varlen(dtype, bcx, w, cu_seqlens, dy, init=None, d_final=None):
     dbcx = np.zeros((T, 3 * H), dtype=npdt)
     dw = np.zeros((H, K), dtype=np.float64)
     d_init = np.zeros((N, H, K), dtype=np.float64)
+    dbias = np.zeros((H,), dtype=np.float64)
+    bias, bp = _opt(bias, npdt, (H,), "bias")
     st = _load().orc_backward_varlen(
-        code, H, K, _ptr(bcx), T, _ptr(w), _ptr(cu), N,
+        code, H, K, _ptr(bcx), T, _ptr(w), bp, _ptr(cu), N,
         _ptr(init) if init is not None else None, _ptr(dy),
-        _ptr(d_final) if d_final is not None else None, _ptr(dbcx), _ptr(dw), _ptr(d_init))
-    return st, dbcx, dw, d_init
+        _ptr(d_final) if d_final is not None else None, _ptr(dbcx), _ptr(dw),
+        _ptr(dbias) if with_dbias else None, _ptr(d_init))
+    return (st, dbcx, dw, d_init, dbias) if with_dbias else (st, dbcx, dw, d_init)
 

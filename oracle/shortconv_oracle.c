@@ -128,13 +128,16 @@ static int dtype_ok(int dt) { return dt == ORC_F32 || dt == ORC_BF16 || dt == OR
 
 /*
  * One sequence, one channel h: the per-token sliding window of the MAX
- * definition. win[0..K-1] enters holding the slot's state (oldest first) and
+ * definition. An optional per-channel bias (NULL: none) is added to the conv
+ * output before the C gate, the place conv1d's bias takes in the SGLang verify
+ * listing (causal_conv1d_update(..., conv_bias, activation=None), gated by C
+ * afterwards). win[0..K-1] enters holding the slot's state (oldest first) and
  * leaves holding the last K values of [state; u_0 .. u_{len-1}].
  * Row t of bcx is [B(0..H-1) | C(H..2H-1) | x(2H..3H-1)].
  */
 static void run_channel(int dt, int H, int K, const void *bcx, int64_t row0,
-                        int64_t len, const void *w, int h, double *win, void *y,
-                        int64_t y_row0)
+                        int64_t len, const void *w, const void *bias, int h, double *win,
+                        void *y, int64_t y_row0)
 {
     for (int64_t r = 0; r < len; ++r) {
         int64_t t = row0 + r;
@@ -148,6 +151,8 @@ static void run_channel(int dt, int H, int K, const void *bcx, int64_t row0,
         double z = 0.0;
         for (int k = 0; k < K; ++k)
             z += load(dt, w, (int64_t)h * K + k) * win[k];
+        if (bias)
+            z += load(dt, bias, h);
         store(dt, y, (y_row0 + r) * H + h, c * z);
     }
 }
@@ -165,7 +170,7 @@ static void run_channel(int dt, int H, int K, const void *bcx, int64_t row0,
  * returned after the others are done.
  */
 int orc_prefill(int dt, int H, int K, const void *bcx, int64_t T, const void *w,
-                const int32_t *cu_seqlens, int N, const int32_t *slot_ids,
+                const void *bias, const int32_t *cu_seqlens, int N, const int32_t *slot_ids,
                 void *pool, int n_slots, void *y)
 {
     if (!dtype_ok(dt) || H <= 0 || K <= 0 || T < 0 || N < 0 || n_slots <= 0)
@@ -190,7 +195,7 @@ int orc_prefill(int dt, int H, int K, const void *bcx, int64_t T, const void *w,
             int64_t base = ((int64_t)s * H + h) * K;
             for (int k = 0; k < K; ++k)
                 win[k] = load(dt, pool, base + k);
-            run_channel(dt, H, K, bcx, row0, len, w, h, win, y, row0);
+            run_channel(dt, H, K, bcx, row0, len, w, bias, h, win, y, row0);
             for (int k = 0; k < K; ++k)
                 store(dt, pool, base + k, win[k]);
         }
@@ -203,7 +208,7 @@ int orc_prefill(int dt, int H, int K, const void *bcx, int64_t T, const void *w,
  * Decode: one new token per sequence, rows 0..N-1 of bcx, in place on the
  * pool. This is the prefill loop with one-token sequences.
  */
-int orc_decode(int dt, int H, int K, const void *bcx, int N, const void *w,
+int orc_decode(int dt, int H, int K, const void *bcx, int N, const void *w, const void *bias,
                const int32_t *slot_ids, void *pool, int n_slots, void *y)
 {
     if (!dtype_ok(dt) || H <= 0 || K <= 0 || N < 0 || n_slots <= 0)
@@ -222,7 +227,7 @@ int orc_decode(int dt, int H, int K, const void *bcx, int N, const void *w,
             int64_t base = ((int64_t)s * H + h) * K;
             for (int k = 0; k < K; ++k)
                 win[k] = load(dt, pool, base + k);
-            run_channel(dt, H, K, bcx, i, 1, w, h, win, y, i);
+            run_channel(dt, H, K, bcx, i, 1, w, bias, h, win, y, i);
             for (int k = 0; k < K; ++k)
                 store(dt, pool, base + k, win[k]);
         }
@@ -238,8 +243,8 @@ int orc_decode(int dt, int H, int K, const void *bcx, int N, const void *w,
  * y gets the step's output. The pool is only read.
  */
 int orc_verify(int dt, int H, int K, const void *bcx, int N, int D, const void *w,
-               const int32_t *slot_ids, const void *pool, int n_slots, void *win_out,
-               void *y)
+               const void *bias, const int32_t *slot_ids, const void *pool, int n_slots,
+               void *win_out, void *y)
 {
     if (!dtype_ok(dt) || H <= 0 || K <= 0 || N < 0 || D <= 0 || n_slots <= 0)
         return ORC_EINVAL;
@@ -259,7 +264,7 @@ int orc_verify(int dt, int H, int K, const void *bcx, int N, int D, const void *
                 win[k] = load(dt, pool, base + k);
             for (int j = 0; j < D; ++j) {
                 int64_t t = (int64_t)i * D + j;
-                run_channel(dt, H, K, bcx, t, 1, w, h, win, y, t);
+                run_channel(dt, H, K, bcx, t, 1, w, bias, h, win, y, t);
                 for (int k = 0; k < K; ++k)
                     store(dt, win_out, (t * H + h) * K + k, win[k]);
             }
@@ -310,10 +315,12 @@ int orc_rollback(int dt, int H, int K, int N, int D, const void *win_in,
  *   dB_s   = du_s * x_s,   dx_s = du_s * B_s
  *   dW_h,k = sum_t dz_t u_{t-K+1+k}         (all K taps of a channel together)
  * The rounding of u is passed straight through (its derivative taken as 1).
- * dbcx has bcx's [T, 3H] layout (dB | dC | dx); dw is [H, K] in double.
+ * dbcx has bcx's [T, 3H] layout (dB | dC | dx); dw is [H, K] in double. With
+ * a bias (NULL: none) z_t includes it, and dbias[h] = sum_t dz_t (dbias NULL:
+ * not written).
  */
 int orc_backward(int dt, int H, int K, const void *bcx, int64_t T, const void *w,
-                 const void *dy, void *dbcx, double *dw)
+                 const void *bias, const void *dy, void *dbcx, double *dw, double *dbias)
 {
     if (!dtype_ok(dt) || H <= 0 || K <= 0 || T < 0)
         return ORC_EINVAL;
@@ -338,7 +345,7 @@ int orc_backward(int dt, int H, int K, const void *bcx, int64_t T, const void *w
                 if (p >= 0)
                     acc += load(dt, w, (int64_t)h * K + k) * u[p];
             }
-            z[t] = acc;
+            z[t] = bias ? acc + load(dt, bias, h) : acc;
         }
         for (int64_t t = 0; t < T; ++t) {
             double g = load(dt, dy, t * H + h);
@@ -367,6 +374,12 @@ int orc_backward(int dt, int H, int K, const void *bcx, int64_t T, const void *w
             }
             dw[(int64_t)h * K + k] = acc;
         }
+        if (dbias) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < T; ++t)
+                acc += dz[t];
+            dbias[h] = acc;
+        }
     }
     free(u);
     free(z);
@@ -387,13 +400,15 @@ int orc_backward(int dt, int H, int K, const void *bcx, int64_t T, const void *w
  *              plus d_final[j - len] for j >= len;
  *   du_s = d ext[K+s];  dB_s = du_s x_s;  dx_s = du_s B_s;  dC_t = dy_t z_t;
  *   dW[h,k] = sum over sequences and rows of dz_t ext[t+1+k];
- *   d_init[i] = d ext[0 .. K-1]  ([N, H, K] doubles, written if not NULL).
+ *   d_init[i] = d ext[0 .. K-1]  ([N, H, K] doubles, written if not NULL);
+ * with a bias (NULL: none) z_t includes it and dbias[h] = sum of dz_t.
  * The rounding of u is passed straight through. Returns ORC_EDATA (nothing
  * written) for a cu_seqlens that is not 0 <= ... <= T ending at T.
  */
 int orc_backward_varlen(int dt, int H, int K, const void *bcx, int64_t T, const void *w,
-                        const int32_t *cu_seqlens, int N, const void *init, const void *dy,
-                        const double *d_final, void *dbcx, double *dw, double *d_init)
+                        const void *bias, const int32_t *cu_seqlens, int N, const void *init,
+                        const void *dy, const double *d_final, void *dbcx, double *dw,
+                        double *dbias, double *d_init)
 {
     if (!dtype_ok(dt) || H <= 0 || K <= 0 || T < 0 || N < 0)
         return ORC_EINVAL;
@@ -416,6 +431,9 @@ int orc_backward_varlen(int dt, int H, int K, const void *bcx, int64_t T, const 
     }
     for (int64_t e = 0; e < (int64_t)H * K; ++e)
         dw[e] = 0.0;
+    if (dbias)
+        for (int h = 0; h < H; ++h)
+            dbias[h] = 0.0;
     for (int i = 0; i < N; ++i) {
         int64_t row0 = cu_seqlens[i], len = (int64_t)cu_seqlens[i + 1] - cu_seqlens[i];
         for (int h = 0; h < H; ++h) {
@@ -434,8 +452,12 @@ int orc_backward_varlen(int dt, int H, int K, const void *bcx, int64_t T, const 
                 double z = 0.0;
                 for (int k = 0; k < K; ++k)
                     z += load(dt, w, (int64_t)h * K + k) * ext[t + 1 + k];
+                if (bias)
+                    z += load(dt, bias, h);
                 double g = load(dt, dy, r * H + h);
                 double dz = g * load(dt, bcx, r * 3 * H + H + h);
+                if (dbias)
+                    dbias[h] += dz;
                 store(dt, dbcx, r * 3 * H + H + h, g * z);
                 for (int k = 0; k < K; ++k) {
                     dext[t + 1 + k] += load(dt, w, (int64_t)h * K + k) * dz;

@@ -26,8 +26,8 @@ MUTANTS = {
                                 "double u = b * x;"),
     "window_not_reset_per_sequence": (
         "            for (int k = 0; k < K; ++k)\n                win[k] = load(dt, pool, base + k);\n"
-        "            run_channel(dt, H, K, bcx, row0, len, w, h, win, y, row0);",
-        "            run_channel(dt, H, K, bcx, row0, len, w, h, win, y, row0);"),
+        "            run_channel(dt, H, K, bcx, row0, len, w, bias, h, win, y, row0);",
+        "            run_channel(dt, H, K, bcx, row0, len, w, bias, h, win, y, row0);"),
     "bf16_truncates": ("double r = nearbyint(d / spacing) * spacing;",
                        "double r = trunc(d / spacing) * spacing;"),
     "rollback_off_by_one": ("int64_t src = (((int64_t)i * D + (a - 1)) * H) * K;",
@@ -39,6 +39,10 @@ MUTANTS = {
                             "ext[m] = 0.0;"),
     "varlen_final_grad_dropped": ("dext[len + k] += d_final[sbase + k];",
                                   "dext[len + k] += 0.0 * d_final[sbase + k];"),
+    "bias_ignored": ("        if (bias)\n            z += load(dt, bias, h);\n        store(dt, y,",
+                     "        store(dt, y,"),
+    "dbias_weighted": ("            for (int64_t t = 0; t < T; ++t)\n                acc += dz[t];\n            dbias[h] = acc;",
+                       "            for (int64_t t = 0; t < T; ++t)\n                acc += dz[t] * u[t];\n            dbias[h] = acc;"),
     "backward_dx_uses_x": ("store(dt, dbcx, s * 3 * H + 2 * H + h, du * b);",
                            "store(dt, dbcx, s * 3 * H + 2 * H + h, du * x);"),
 }

@@ -560,3 +560,116 @@ def test_backward_varlen_rejects_bad_cu_seqlens():
     st, *_ = oracle.backward_varlen("f64", bcx, rng.standard_normal((4, 3)), [0, 4, 3, 6],
                                     rng.standard_normal((6, 4)))
     assert st == oracle.EDATA
+
+
+# ----------------------------------------------------------- conv bias
+
+@pytest.mark.parametrize("K", [1, 3, 4])
+def test_forward_bias_f64_matches_torch_conv1d_with_bias(K):
+    rng = np.random.default_rng(80 + K)
+    H, T = 5, 13
+    bcx = rng.standard_normal((T, 3 * H))
+    w = rng.standard_normal((H, K))
+    b = rng.standard_normal(H)
+    state = rng.standard_normal((1, H, K))
+    pool = state.copy()
+    st, y = oracle.prefill("f64", bcx, w, [0, T], [0], pool, bias=b)
+    assert st == oracle.OK
+    u = bcx[:, :H] * bcx[:, 2 * H:]
+    ext = np.concatenate([state[0, :, 1:], u.T], axis=1)
+    z = F.conv1d(torch.from_numpy(ext)[None], torch.from_numpy(w)[:, None, :],
+                 bias=torch.from_numpy(b), groups=H)[0].numpy().T
+    np.testing.assert_allclose(y, bcx[:, H:2 * H] * z, rtol=1e-13, atol=1e-13)
+    # the state keeps u, so the bias never reaches it
+    np.testing.assert_array_equal(pool[0], np.concatenate([state[0], u.T], 1)[:, -K:])
+
+
+def test_forward_bias_bf16_matches_library_casts():
+    rng = np.random.default_rng(85)
+    H, K, T = 16, 3, 50
+    bcx = _rand((T, 3 * H), "bf16", rng)
+    w = _rand((H, K), "bf16", rng, wl.WEIGHT_STD)
+    b = _rand((H,), "bf16", rng)
+    pool = np.zeros((1, H, K), np.uint16)
+    st, y = oracle.prefill("bf16", bcx, w, [0, T], [0], pool, bias=b)
+    assert st == oracle.OK
+    b64 = _f64("bf16", bcx)
+    u64 = _f64("bf16", torch_bf16_bits(torch.from_numpy((b64[:, :H] * b64[:, 2 * H:]).astype(np.float32))))
+    z = F.conv1d(F.pad(torch.from_numpy(u64.T)[None], (K - 1, 0)),
+                 torch.from_numpy(_f64("bf16", w))[:, None, :],
+                 bias=torch.from_numpy(_f64("bf16", b)), groups=H)[0].numpy().T
+    y32 = (b64[:, H:2 * H] * z).astype(np.float32)
+    ref = torch_bf16_bits(torch.from_numpy(y32))
+    at_tie = (y32.view(np.uint32) & 0xFFFF) == 0x8000
+    assert np.all((y == ref) | at_tie)
+
+
+def test_bias_keeps_prefill_equal_to_prefill_plus_decode_and_verify_windows():
+    rng = np.random.default_rng(86)
+    H, K, T = 8, 3, 9
+    bcx = _rand((T, 3 * H), "bf16", rng)
+    w = _rand((H, K), "bf16", rng, wl.WEIGHT_STD)
+    b = _rand((H,), "bf16", rng)
+    state = _rand((1, H, K), "bf16", rng)
+    full = state.copy()
+    _, y_full = oracle.prefill("bf16", bcx, w, [0, T], [0], full, bias=b)
+    pool = state.copy()
+    _, y1 = oracle.prefill("bf16", bcx[:4], w, [0, 4], [0], pool, bias=b)
+    ys = [y1] + [oracle.decode("bf16", bcx[t:t + 1], w, [0], pool, bias=b)[1] for t in range(4, T)]
+    np.testing.assert_array_equal(np.concatenate(ys), y_full)
+    np.testing.assert_array_equal(pool, full)
+    st, win_b, yv = oracle.verify("bf16", bcx, w, [0], state, T, bias=b)
+    st, win_0, _ = oracle.verify("bf16", bcx, w, [0], state, T)
+    np.testing.assert_array_equal(win_b, win_0)       # the tape holds u: no bias in it
+    np.testing.assert_array_equal(yv, y_full)
+
+
+def _torch_bias_grads(bcx64, w64, b64, dy64):
+    T, H3 = bcx64.shape
+    H = H3 // 3
+    K = w64.shape[1]
+    bcx = torch.tensor(bcx64, requires_grad=True)
+    w = torch.tensor(w64, requires_grad=True)
+    b = torch.tensor(b64, requires_grad=True)
+    u = bcx[:, :H] * bcx[:, 2 * H:]
+    z = F.conv1d(F.pad(u.T[None], (K - 1, 0)), w[:, None, :], bias=b, groups=H)[0].T
+    ((bcx[:, H:2 * H] * z) * torch.from_numpy(dy64)).sum().backward()
+    return bcx.grad.numpy(), w.grad.numpy(), b.grad.numpy()
+
+
+@pytest.mark.parametrize("K", [1, 3, 4])
+def test_backward_bias_f64_matches_torch_autograd(K):
+    rng = np.random.default_rng(87 + K)
+    H, T = 6, 21
+    bcx = rng.standard_normal((T, 3 * H))
+    w = rng.standard_normal((H, K))
+    b = rng.standard_normal(H)
+    dy = rng.standard_normal((T, H))
+    st, dbcx, dw, db = oracle.backward("f64", bcx, w, dy, bias=b, with_dbias=True)
+    assert st == oracle.OK
+    g_bcx, g_w, g_b = _torch_bias_grads(bcx, w, b, dy)
+    np.testing.assert_allclose(dbcx, g_bcx, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dw, g_w, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(db, g_b, rtol=1e-12, atol=1e-12)
+
+
+def test_backward_varlen_bias_matches_per_sequence_sums():
+    rng = np.random.default_rng(90)
+    H, K, lengths = 6, 3, [4, 0, 9, 2]
+    cu = np.r_[0, np.cumsum(lengths)].astype(np.int32)
+    T, N = int(cu[-1]), len(lengths)
+    bcx = rng.standard_normal((T, 3 * H))
+    w = rng.standard_normal((H, K))
+    b = rng.standard_normal(H)
+    dy = rng.standard_normal((T, H))
+    st, dbcx, dw, di, db = oracle.backward_varlen("f64", bcx, w, cu, dy, bias=b, with_dbias=True)
+    assert st == oracle.OK
+    g_b = np.zeros(H)
+    for i in range(N):
+        a, e = int(cu[i]), int(cu[i + 1])
+        if e > a:
+            s2, d1, w1, b1 = oracle.backward("f64", bcx[a:e], w, dy[a:e], bias=b, with_dbias=True)
+            np.testing.assert_allclose(dbcx[a:e], d1, rtol=1e-12, atol=1e-12)
+            g_b += b1
+    np.testing.assert_allclose(db, g_b, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(db, _torch_bias_grads(bcx, w, b, dy)[2] * 0 + g_b, rtol=1e-12)
