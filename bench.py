@@ -439,9 +439,12 @@ def varlen_section(sc, device, reps=20):
     return dict(T=p.T, n_seqs=p.N, us=us, bytes=nb, gbs=nb / (us * 1e-6) / 1e9)
 
 
-def training_section(sc, device, T_, reps, sets_n):
+def training_section(sc, device, T_, reps, sets_n, bias=False):
+    """Forward + backward of one sequence; with ``bias``, a conv bias and dbias too."""
     g = torch.Generator(device=device).manual_seed(6)
     w = randn_bf16((H, K), g, device, wl.WEIGHT_STD)
+    b = randn_bf16((H,), g, device, 0.5) if bias else None
+    db = torch.empty((H,), dtype=torch.float32, device=device) if bias else None
     cu = torch.tensor([0, T_], dtype=torch.int32, device=device)
     slot = torch.zeros(1, dtype=torch.int32, device=device)
     ws = torch.empty(max(16, sc.backward_workspace_bytes(H, K, T_)), dtype=torch.uint8,
@@ -455,10 +458,11 @@ def training_section(sc, device, T_, reps, sets_n):
                          pool=torch.zeros((1, H, K), dtype=torch.bfloat16, device=device)))
 
     def fwd(s):
-        sc.prefill(s["bcx"], w, cu, slot, s["pool"], y=s["y"])
+        sc.prefill(s["bcx"], w, cu, slot, s["pool"], y=s["y"], bias=b)
 
     def bwd(s):
-        sc.backward(s["bcx"], w, s["dy"], dbcx=s["dbcx"], dw=dw, workspace=ws)
+        sc.backward(s["bcx"], w, s["dy"], dbcx=s["dbcx"], dw=dw, workspace=ws, bias=b,
+                    with_dbias=bias, dbias=db)
 
     for i in range(3):
         fwd(sets[i % sets_n])
@@ -469,7 +473,9 @@ def training_section(sc, device, T_, reps, sets_n):
     fb_us = time_loop(lambda i: (fwd(sets[i % sets_n]), bwd(sets[i % sets_n])), reps)
     assert sc.get_error() == 0
     fb, bb = prefill_bytes(T_, H, K, 1), backward_bytes(T_, H, K)
-    return dict(T=T_, fwd_us=f_us, bwd_us=b_us, fwd_bwd_ms=fb_us / 1e3,
+    if bias:
+        fb, bb = fb + H * E, bb + H * E + H * 4  # bias read; bias read and dbias written
+    return dict(T=T_, bias=bias, fwd_us=f_us, bwd_us=b_us, fwd_bwd_ms=fb_us / 1e3,
                 fwd_gbs=fb / (f_us * 1e-6) / 1e9, bwd_gbs=bb / (b_us * 1e-6) / 1e9,
                 fwd_bwd_gbs=(fb + bb) / (fb_us * 1e-6) / 1e9, fwd_bytes=fb, bwd_bytes=bb)
 
@@ -624,6 +630,8 @@ def main():
     extras["varlen"] = varlen_section(sc, device)
     extras["train_T4096"] = training_section(sc, device, 4096, 20, 4)
     extras["train_T65536"] = training_section(sc, device, 65536, 10, 1)
+    extras["train_T4096_bias"] = training_section(sc, device, 4096, 20, 4, bias=True)
+    extras["train_T65536_bias"] = training_section(sc, device, 65536, 10, 1, bias=True)
     extras["train_packed_T65536"] = packed_training_section(sc, device)
     clk = clocks.stop()
     del flush_buf

@@ -73,6 +73,19 @@ typedef enum { SC_F32 = 0, SC_BF16 = 1 } sc_dtype;
 #define SC_DEV_NO_SLOT 0x10u      /* a claim asked for more slots than were free: nothing claimed */
 
 /*
+ * The optional conv bias. Every forward and backward call below takes
+ * `bias`: device [H] of the call's dtype, 16-byte aligned, read only; NULL
+ * means no bias. A bias is added to the depthwise conv output of its channel
+ * before the C gate: z_t = sum_k w_k u_{t-K+1+k} + bias[h], y_t = C_t z_t
+ * (the MAX LFM2 article, section "批处理与权重适配", maps a checkpoint's
+ * conv.conv.bias to the layer's conv_bias; the SGLang PR #31041 verify code,
+ * section "实现拆解 2", passes conv_bias to the conv update with no
+ * activation and gates by C afterwards). The released LFM2 checkpoints have
+ * no conv bias; NULL gives exactly the bias-free results. With a bias, the
+ * sum is rounded once in fp32 after the K-tap chain.
+ */
+
+/*
  * Packed variable-length prefill (continued prefill from each slot's state).
  *
  * Sequence i (0 <= i < N) is rows cu_seqlens[i] .. cu_seqlens[i+1]-1 of bcx
@@ -89,6 +102,7 @@ typedef enum { SC_F32 = 0, SC_BF16 = 1 } sc_dtype;
  *   bcx         device [T, 3H]           read
  *   T           total rows, 0 <= T < 2^31
  *   w           device [H, K]            read
+ *   bias        device [H] or NULL       read (see above)
  *   cu_seqlens  device int32 [N + 1]     read; must be 0, non-decreasing, end at T
  *   N           number of sequences, >= 0 (N = 0 requires T = 0)
  *   slot_ids    device int32 [N]         read
@@ -103,7 +117,7 @@ typedef enum { SC_F32 = 0, SC_BF16 = 1 } sc_dtype;
  * for the register-tiled alternative; both give identical bits).
  */
 sc_status shortconv_prefill(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
-                            const void *w, const int32_t *cu_seqlens, int N,
+                            const void *w, const void *bias, const int32_t *cu_seqlens, int N,
                             const int32_t *slot_ids, void *pool, int n_slots, void *y,
                             void *stream);
 
@@ -114,9 +128,9 @@ sc_status shortconv_prefill(sc_dtype dtype, int H, int K, const void *bcx, int64
  * kernel. Every choice gives identical bits; only the speed differs.
  */
 sc_status shortconv_prefill_tiled(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
-                                  const void *w, const int32_t *cu_seqlens, int N,
-                                  const int32_t *slot_ids, void *pool, int n_slots, void *y,
-                                  int rows_per_thread, void *stream);
+                                  const void *w, const void *bias, const int32_t *cu_seqlens,
+                                  int N, const int32_t *slot_ids, void *pool, int n_slots,
+                                  void *y, int rows_per_thread, void *stream);
 
 /*
  * Decode: one new token per sequence, in place on the pool.
@@ -127,13 +141,14 @@ sc_status shortconv_prefill_tiled(sc_dtype dtype, int H, int K, const void *bcx,
  * request's state, drop the oldest column, append bx_t, scatter back) for a
  * single token.
  *
- *   bcx [N, 3H] read; w [H, K] read; slot_ids int32 [N] read;
- *   pool [n_slots, H, K] read and written; y [N, H] written.
+ *   bcx [N, 3H] read; w [H, K] read; bias [H] or NULL read;
+ *   slot_ids int32 [N] read; pool [n_slots, H, K] read and written;
+ *   y [N, H] written.
  * Device errors: SC_DEV_BAD_SLOT (that sequence skipped).
  */
 sc_status shortconv_decode(sc_dtype dtype, int H, int K, const void *bcx, int N,
-                           const void *w, const int32_t *slot_ids, void *pool,
-                           int n_slots, void *y, void *stream);
+                           const void *w, const void *bias, const int32_t *slot_ids,
+                           void *pool, int n_slots, void *y, void *stream);
 
 /*
  * Speculative verify: D draft tokens per sequence, recording the conv window
@@ -147,13 +162,14 @@ sc_status shortconv_decode(sc_dtype dtype, int H, int K, const void *bcx, int N,
  * win[i, j, :, :] and the draft's output to y[i*D + j]. The pool is only
  * read; shortconv_rollback commits the accepted prefix.
  *
- *   bcx [N*D, 3H] read; w [H, K] read; slot_ids int32 [N] read;
- *   pool [n_slots, H, K] read; win [N, D, H, K] written; y [N*D, H] written.
+ *   bcx [N*D, 3H] read; w [H, K] read; bias [H] or NULL read;
+ *   slot_ids int32 [N] read; pool [n_slots, H, K] read;
+ *   win [N, D, H, K] written; y [N*D, H] written.
  * Device errors: SC_DEV_BAD_SLOT (that sequence's win and y rows not written).
  */
 sc_status shortconv_verify(sc_dtype dtype, int H, int K, const void *bcx, int N, int D,
-                           const void *w, const int32_t *slot_ids, const void *pool,
-                           int n_slots, void *win, void *y, void *stream);
+                           const void *w, const void *bias, const int32_t *slot_ids,
+                           const void *pool, int n_slots, void *win, void *y, void *stream);
 
 /*
  * Rollback after verify: sequence i accepted accepted[i] of its D drafts
@@ -170,9 +186,10 @@ sc_status shortconv_rollback(sc_dtype dtype, int H, int K, int N, int D, const v
                              int n_slots, void *stream);
 
 /*
- * Bytes of device workspace shortconv_backward needs for these sizes
- * (fp32 partial weight gradients). Host-only; no CUDA call; depends only on
- * the arguments. Returns 0 for invalid sizes.
+ * Bytes of device workspace shortconv_backward and shortconv_backward_varlen
+ * need for these sizes (fp32 partial weight and bias gradients, one block per
+ * row range). Host-only; no CUDA call; depends only on the arguments.
+ * Returns 0 for invalid sizes.
  */
 size_t shortconv_backward_workspace_bytes(int H, int K, int64_t T);
 
@@ -181,24 +198,26 @@ size_t shortconv_backward_workspace_bytes(int H, int K, int64_t T);
  * training path: Liger-Kernel PR #1317, "Kernel changes / Gated short
  * convolution": the B/C gate gradients fused with the depthwise-conv input
  * gradient, and the weight gradient of all K taps of a channel reduced
- * together, bias-free). With z_t = sum_k w_k u_{t-K+1+k} (u before row 0 is 0):
+ * together). With z_t = sum_k w_k u_{t-K+1+k} (+ bias[h]; u before row 0 is 0):
  *   dC_t = dy_t z_t;  dz_t = dy_t C_t;  du_s = sum_k w_k dz_{s+K-1-k}
  *   (terms past row T-1 are 0);  dB_s = du_s x_s;  dx_s = du_s B_s;
- *   dW[h,k] = sum_t dz_t u_{t-K+1+k}.
+ *   dW[h,k] = sum_t dz_t u_{t-K+1+k};  dbias[h] = sum_t dz_t.
  * The rounding of u is passed straight through.
  *
- *   bcx [T, 3H] read; w [H, K] read; dy [T, H] read;
+ *   bcx [T, 3H] read; w [H, K] read; bias [H] or NULL read; dy [T, H] read;
  *   dbcx [T, 3H] written (dB | dC | dx, same dtype as bcx);
  *   dw [H, K] fp32 written (overwritten, not accumulated);
+ *   dbias [H] fp32 written, or NULL (not computed; independent of bias);
  *   workspace: device scratch of at least
  *   shortconv_backward_workspace_bytes(H, K, T) bytes, 16-byte aligned,
  *   owned by the caller, contents ignored on entry and unspecified after.
- * The weight gradient is reduced in a fixed order: repeated calls give
- * identical bits.
+ * The weight and bias gradients are reduced in a fixed order: repeated calls
+ * give identical bits.
  */
 sc_status shortconv_backward(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
-                             const void *w, const void *dy, void *dbcx, float *dw,
-                             void *workspace, size_t workspace_bytes, void *stream);
+                             const void *w, const void *bias, const void *dy, void *dbcx,
+                             float *dw, float *dbias, void *workspace, size_t workspace_bytes,
+                             void *stream);
 
 /*
  * Backward of the packed varlen prefill with initial states: training on
@@ -213,26 +232,29 @@ sc_status shortconv_backward(sc_dtype dtype, int H, int K, const void *bcx, int6
  * ext[t+1 .. t+K] and the final state is ext[len .. len+K-1]. Given dy and an
  * optional gradient d_final of the final states, the call writes
  *   dB, dC, dx (as shortconv_backward, history and look-ahead staying inside
- *   each sequence), dW (fp32, summed over all sequences) and
+ *   each sequence), dW and dbias (fp32, summed over all sequences) and
  *   d_init[i][h][m] = gradient of init_states[i][h][m] (tap 0 only ever gets
  *   d_final's share, for empty sequences).
  * The rounding of u is passed straight through.
  *
  *   bcx [T, 3H], w [H, K], dy [T, H]: read (dtype)
+ *   bias [H] (dtype) or NULL: read
  *   cu_seqlens int32 [N + 1]: read; 0, non-decreasing, ending at T
  *   init_states [N, H, K] (dtype) or NULL for zero states: read
  *   d_final [N, H, K] fp32 or NULL for zero: read
  *   dbcx [T, 3H] (dtype), dw [H, K] fp32: written
+ *   dbias [H] fp32 or NULL (not computed): written
  *   d_init [N, H, K] fp32 or NULL (not computed): written
  *   workspace: at least shortconv_backward_workspace_bytes(H, K, T) bytes.
- * Device errors: SC_DEV_BAD_SEQLENS (dw is zeroed; dbcx and d_init are not
- * written).
+ * Device errors: SC_DEV_BAD_SEQLENS (dw and dbias are zeroed; dbcx and
+ * d_init are not written).
  */
 sc_status shortconv_backward_varlen(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
-                                    const void *w, const int32_t *cu_seqlens, int N,
-                                    const void *init_states, const void *dy,
-                                    const float *d_final, void *dbcx, float *dw, float *d_init,
-                                    void *workspace, size_t workspace_bytes, void *stream);
+                                    const void *w, const void *bias, const int32_t *cu_seqlens,
+                                    int N, const void *init_states, const void *dy,
+                                    const float *d_final, void *dbcx, float *dw, float *dbias,
+                                    float *d_init, void *workspace, size_t workspace_bytes,
+                                    void *stream);
 
 /*
  * shortconv_backward without a workspace argument, for callers that cannot
@@ -243,13 +265,14 @@ sc_status shortconv_backward_varlen(sc_dtype dtype, int H, int K, const void *bc
  * middle of a step, is not acceptable. The pages have no counterpart to this
  * call; it only moves the scratch.
  *
- * Same arguments, results and bits as shortconv_backward. The fp32 dW
- * partials live in a fixed 8 MiB device array inside the library, which
- * every GPU that loads the library holds until the process exits. The call
- * allocates nothing and never calls cudaMalloc or cudaFree.
- *   - Sizes whose shortconv_backward_workspace_bytes(H, K, T) exceeds 8 MiB
- *     are rejected with SC_EUNSUPPORTED before anything is enqueued. The
- *     partials take at most 152 * H * K * 4 bytes, so nothing is rejected
+ * Same results and bits as shortconv_backward with bias = dbias = NULL, and
+ * its arguments less those and the workspace. The fp32 dW partials live in
+ * a fixed 8 MiB device array inside the library, which every GPU that loads
+ * the library holds until the process exits. The call allocates nothing and
+ * never calls cudaMalloc or cudaFree.
+ *   - Sizes whose dW partials exceed 8 MiB are rejected with
+ *     SC_EUNSUPPORTED before anything is enqueued. The partials take
+ *     min(ceil(T / 16), 152) * H * K * 4 bytes, so nothing is rejected
  *     for H * K <= 13,797 (every T for H = 2048 or H = 4096 with K = 3);
  *     for H = 8192, K = 4 rows above T = 1024 are.
  *   - The first call on a device looks up the array's device address

@@ -10,6 +10,8 @@ an exception is raised.
 Layouts (row-major, contiguous, one dtype per call: torch.bfloat16 or
 torch.float32): ``bcx [T, 3H]`` (B | C | x), ``w [H, K]``, state pool
 ``[n_slots, H, K]`` (tap K-1 newest), ``y [T, H]``; index arrays are int32.
+Every forward and backward call takes an optional conv ``bias [H]`` (the data
+dtype; None for none), added to the conv output before the C gate.
 """
 from __future__ import annotations
 
@@ -49,18 +51,19 @@ def lib() -> ctypes.CDLL:
                     "`python -m lfm2_gated_short_gb300.build` (nvcc, sm_103a)")
             L = ctypes.CDLL(LIB_PATH)
             p, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
-            L.shortconv_prefill.argtypes = [i32, i32, i32, p, i64, p, p, i32, p, p, i32, p, p]
-            L.shortconv_prefill_tiled.argtypes = [i32, i32, i32, p, i64, p, p, i32, p, p, i32,
-                                                  p, i32, p]
-            L.shortconv_decode.argtypes = [i32, i32, i32, p, i32, p, p, p, i32, p, p]
-            L.shortconv_verify.argtypes = [i32, i32, i32, p, i32, i32, p, p, p, i32, p, p, p]
+            L.shortconv_prefill.argtypes = [i32, i32, i32, p, i64, p, p, p, i32, p, p, i32, p, p]
+            L.shortconv_prefill_tiled.argtypes = [i32, i32, i32, p, i64, p, p, p, i32, p, p,
+                                                  i32, p, i32, p]
+            L.shortconv_decode.argtypes = [i32, i32, i32, p, i32, p, p, p, p, i32, p, p]
+            L.shortconv_verify.argtypes = [i32, i32, i32, p, i32, i32, p, p, p, p, i32, p, p,
+                                           p]
             L.shortconv_rollback.argtypes = [i32, i32, i32, i32, i32, p, p, p, p, i32, p]
             L.shortconv_backward_workspace_bytes.argtypes = [i32, i32, i64]
             L.shortconv_backward_workspace_bytes.restype = ctypes.c_size_t
-            L.shortconv_backward.argtypes = [i32, i32, i32, p, i64, p, p, p, p, p,
+            L.shortconv_backward.argtypes = [i32, i32, i32, p, i64, p, p, p, p, p, p, p,
                                              ctypes.c_size_t, p]
-            L.shortconv_backward_varlen.argtypes = [i32, i32, i32, p, i64, p, p, i32, p, p, p,
-                                                    p, p, p, p, ctypes.c_size_t, p]
+            L.shortconv_backward_varlen.argtypes = [i32, i32, i32, p, i64, p, p, p, i32, p, p,
+                                                    p, p, p, p, p, p, ctypes.c_size_t, p]
             L.shortconv_slots_claim.argtypes = [p, i32, i32, p, i32, i32, i32, p, p]
             L.shortconv_slots_release.argtypes = [p, i32, p, i32, p]
             L.shortconv_pool_copy.argtypes = [i32, i32, i32, p, i32, p, p, i32, p]
@@ -108,7 +111,12 @@ def _stream(stream, device) -> int:
     return s.cuda_stream
 
 
-def prefill(bcx, w, cu_seqlens, slot_ids, pool, y=None, rows_per_thread=0, stream=None):
+def _bias(bias, dt, H):
+    return None if bias is None else _dev(bias, "bias", dt, (H,))
+
+
+def prefill(bcx, w, cu_seqlens, slot_ids, pool, y=None, rows_per_thread=0, stream=None,
+            bias=None):
     """Packed varlen prefill; updates ``pool`` in place and returns ``y [T, H]``."""
     dt = bcx.dtype
     T, H3 = bcx.shape
@@ -118,7 +126,7 @@ def prefill(bcx, w, cu_seqlens, slot_ids, pool, y=None, rows_per_thread=0, strea
     N = slot_ids.shape[0]
     if y is None:
         y = torch.empty((T, H), dtype=dt, device=bcx.device)
-    args = (_dcode(bcx), H, K, _dev(bcx, "bcx", dt), T, _dev(w, "w", dt),
+    args = (_dcode(bcx), H, K, _dev(bcx, "bcx", dt), T, _dev(w, "w", dt), _bias(bias, dt, H),
             _dev(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,)), N,
             _dev(slot_ids, "slot_ids", torch.int32, (N,)),
             _dev(pool, "pool", dt, (pool.shape[0], H, K)), pool.shape[0],
@@ -132,7 +140,7 @@ def prefill(bcx, w, cu_seqlens, slot_ids, pool, y=None, rows_per_thread=0, strea
     return y
 
 
-def decode(bcx, w, slot_ids, pool, y=None, stream=None):
+def decode(bcx, w, slot_ids, pool, y=None, stream=None, bias=None):
     """One token per sequence; updates ``pool`` in place and returns ``y [N, H]``."""
     dt = bcx.dtype
     N, H3 = bcx.shape
@@ -142,14 +150,14 @@ def decode(bcx, w, slot_ids, pool, y=None, stream=None):
     if y is None:
         y = torch.empty((N, H), dtype=dt, device=bcx.device)
     _raise_on("shortconv_decode", lib().shortconv_decode(
-        _dcode(bcx), H, K, _dev(bcx, "bcx", dt), N, _dev(w, "w", dt),
+        _dcode(bcx), H, K, _dev(bcx, "bcx", dt), N, _dev(w, "w", dt), _bias(bias, dt, H),
         _dev(slot_ids, "slot_ids", torch.int32, (N,)),
         _dev(pool, "pool", dt, (pool.shape[0], H, K)), pool.shape[0],
         _dev(y, "y", dt, (N, H)), _stream(stream, bcx.device)))
     return y
 
 
-def verify(bcx, w, slot_ids, pool, D, win=None, y=None, stream=None):
+def verify(bcx, w, slot_ids, pool, D, win=None, y=None, stream=None, bias=None):
     """Speculative verify of ``D`` drafts per sequence; returns ``(win, y)``. Pool is read only."""
     dt = bcx.dtype
     H, K = w.shape
@@ -161,7 +169,7 @@ def verify(bcx, w, slot_ids, pool, D, win=None, y=None, stream=None):
     if y is None:
         y = torch.empty((N * D, H), dtype=dt, device=bcx.device)
     _raise_on("shortconv_verify", lib().shortconv_verify(
-        _dcode(bcx), H, K, _dev(bcx, "bcx", dt), N, D, _dev(w, "w", dt),
+        _dcode(bcx), H, K, _dev(bcx, "bcx", dt), N, D, _dev(w, "w", dt), _bias(bias, dt, H),
         _dev(slot_ids, "slot_ids", torch.int32, (N,)),
         _dev(pool, "pool", dt, (pool.shape[0], H, K)), pool.shape[0],
         _dev(win, "win", dt, (N, D, H, K)), _dev(y, "y", dt, (N * D, H)),
@@ -185,8 +193,10 @@ def backward_workspace_bytes(H: int, K: int, T: int) -> int:
     return int(lib().shortconv_backward_workspace_bytes(H, K, T))
 
 
-def backward(bcx, w, dy, dbcx=None, dw=None, workspace=None, stream=None):
-    """Backward from a zero state; returns ``(dbcx [T, 3H], dw [H, K] fp32)``."""
+def backward(bcx, w, dy, dbcx=None, dw=None, workspace=None, stream=None, bias=None,
+             with_dbias=False, dbias=None):
+    """Backward from a zero state; returns ``(dbcx [T, 3H], dw [H, K] fp32)``,
+    plus ``dbias [H] fp32`` when ``with_dbias``."""
     dt = bcx.dtype
     T, H3 = bcx.shape
     H, K = w.shape
@@ -197,21 +207,26 @@ def backward(bcx, w, dy, dbcx=None, dw=None, workspace=None, stream=None):
         dbcx = torch.empty_like(bcx)
     if dw is None:
         dw = torch.empty((H, K), dtype=torch.float32, device=bcx.device)
+    if with_dbias and dbias is None:
+        dbias = torch.empty((H,), dtype=torch.float32, device=bcx.device)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=bcx.device)
     if workspace.dtype != torch.uint8 or workspace.numel() < need:
         raise ValueError(f"workspace must be a uint8 tensor of at least {need} bytes")
+    db_p = _dev(dbias, "dbias", torch.float32, (H,)) if with_dbias else None
     _raise_on("shortconv_backward", lib().shortconv_backward(
-        _dcode(bcx), H, K, _dev(bcx, "bcx", dt), T, _dev(w, "w", dt),
+        _dcode(bcx), H, K, _dev(bcx, "bcx", dt), T, _dev(w, "w", dt), _bias(bias, dt, H),
         _dev(dy, "dy", dt, (T, H)), _dev(dbcx, "dbcx", dt, (T, 3 * H)),
-        _dev(dw, "dw", torch.float32, (H, K)), _dev(workspace, "workspace"),
+        _dev(dw, "dw", torch.float32, (H, K)), db_p, _dev(workspace, "workspace"),
         workspace.numel(), _stream(stream, bcx.device)))
-    return dbcx, dw
+    return (dbcx, dw, dbias) if with_dbias else (dbcx, dw)
 
 
 def backward_varlen(bcx, w, cu_seqlens, dy, init_states=None, d_final=None, dbcx=None,
-                    dw=None, d_init=None, workspace=None, want_d_init=True, stream=None):
-    """Packed varlen backward with initial states; returns ``(dbcx, dw, d_init)``.
+                    dw=None, d_init=None, workspace=None, want_d_init=True, stream=None,
+                    bias=None, with_dbias=False, dbias=None):
+    """Packed varlen backward with initial states; returns ``(dbcx, dw, d_init)``,
+    plus ``dbias [H] fp32`` when ``with_dbias``.
 
     ``init_states`` is ``[N, H, K]`` (the data dtype; None: zeros);
     ``d_final`` is ``[N, H, K]`` float32 (None: zeros); ``d_init`` is
@@ -230,6 +245,8 @@ def backward_varlen(bcx, w, cu_seqlens, dy, init_states=None, d_final=None, dbcx
         dw = torch.empty((H, K), dtype=torch.float32, device=bcx.device)
     if want_d_init and d_init is None:
         d_init = torch.empty((N, H, K), dtype=torch.float32, device=bcx.device)
+    if with_dbias and dbias is None:
+        dbias = torch.empty((H,), dtype=torch.float32, device=bcx.device)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=bcx.device)
     if workspace.dtype != torch.uint8 or workspace.numel() < need:
@@ -237,13 +254,14 @@ def backward_varlen(bcx, w, cu_seqlens, dy, init_states=None, d_final=None, dbcx
     init_p = _dev(init_states, "init_states", dt, (N, H, K)) if init_states is not None else None
     dfin_p = _dev(d_final, "d_final", torch.float32, (N, H, K)) if d_final is not None else None
     dini_p = _dev(d_init, "d_init", torch.float32, (N, H, K)) if d_init is not None else None
+    db_p = _dev(dbias, "dbias", torch.float32, (H,)) if with_dbias else None
     _raise_on("shortconv_backward_varlen", lib().shortconv_backward_varlen(
-        _dcode(bcx), H, K, _dev(bcx, "bcx", dt), T, _dev(w, "w", dt),
+        _dcode(bcx), H, K, _dev(bcx, "bcx", dt), T, _dev(w, "w", dt), _bias(bias, dt, H),
         _dev(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,)), N, init_p,
         _dev(dy, "dy", dt, (T, H)), dfin_p, _dev(dbcx, "dbcx", dt, (T, 3 * H)),
-        _dev(dw, "dw", torch.float32, (H, K)), dini_p, _dev(workspace, "workspace"),
+        _dev(dw, "dw", torch.float32, (H, K)), db_p, dini_p, _dev(workspace, "workspace"),
         workspace.numel(), _stream(stream, bcx.device)))
-    return dbcx, dw, d_init
+    return (dbcx, dw, d_init, dbias) if with_dbias else (dbcx, dw, d_init)
 
 
 def slot_bitmap(n_slots: int, device="cuda") -> torch.Tensor:

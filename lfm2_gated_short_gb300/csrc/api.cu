@@ -30,6 +30,9 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 
 size_t elem_size(sc_dtype d) { return d == SC_BF16 ? 2 : 4; }
 
+// An optional array: NULL (absent) or aligned.
+bool opt_ok(const void *p, uintptr_t align) { return p == nullptr || aligned(p, align); }
+
 // Common size checks: dtype, H, K.
 sc_status check_shape(sc_dtype dtype, int H, int K) {
     if (dtype != SC_F32 && dtype != SC_BF16) return SC_EUNSUPPORTED;
@@ -56,8 +59,9 @@ int sm_count_of_current_device() {
 sc_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SC_OK : SC_ECUDA; }
 
 sc_status prefill_impl(sc_dtype dtype, int H, int K, const void *bcx, int64_t T, const void *w,
-                       const int32_t *cu_seqlens, int N, const int32_t *slot_ids, void *pool,
-                       int n_slots, void *y, int rows_per_thread, void *stream) {
+                       const void *bias, const int32_t *cu_seqlens, int N,
+                       const int32_t *slot_ids, void *pool, int n_slots, void *y,
+                       int rows_per_thread, void *stream) {
     sc_status st = check_shape(dtype, H, K);
     if (st != SC_OK) return st;
     if (T < 0 || T > INT32_MAX || N < 0 || n_slots <= 0) return SC_EINVAL;
@@ -68,19 +72,21 @@ sc_status prefill_impl(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
     const size_t es = elem_size(dtype);
     const size_t n_bcx = (size_t)T * 3 * H * es, n_y = (size_t)T * H * es;
     const size_t n_w = (size_t)H * K * es, n_pool = (size_t)n_slots * H * K * es;
+    const size_t n_b = bias ? (size_t)H * es : 0;
     if (!ptr_ok(bcx, n_bcx, 16) || !ptr_ok(y, n_y, 16) || !ptr_ok(w, n_w, 16) ||
         !ptr_ok(pool, n_pool, 16) || !ptr_ok(cu_seqlens, (size_t)(N + 1) * 4, 4) ||
-        !ptr_ok(slot_ids, (size_t)N * 4, 4))
+        !ptr_ok(slot_ids, (size_t)N * 4, 4) || !opt_ok(bias, 16))
         return SC_EINVAL;
     if (overlaps(y, n_y, bcx, n_bcx) || overlaps(y, n_y, pool, n_pool) ||
         overlaps(y, n_y, w, n_w) || overlaps(pool, n_pool, bcx, n_bcx) ||
-        overlaps(pool, n_pool, w, n_w))
+        overlaps(pool, n_pool, w, n_w) || overlaps(y, n_y, bias, n_b) ||
+        overlaps(pool, n_pool, bias, n_b))
         return SC_EINVAL;
     if (N == 0) return SC_OK;
     const int sms = sm_count_of_current_device();
     if (sms <= 0) return SC_ECUDA;
-    return from_cuda(sc::launch_prefill(dtype, H, K, bcx, T, w, cu_seqlens, N, slot_ids, pool,
-                                        n_slots, y, rows_per_thread, sms,
+    return from_cuda(sc::launch_prefill(dtype, H, K, bcx, T, w, bias, cu_seqlens, N, slot_ids,
+                                        pool, n_slots, y, rows_per_thread, sms,
                                         (cudaStream_t)stream));
 }
 
@@ -89,45 +95,47 @@ sc_status prefill_impl(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
 extern "C" {
 
 sc_status shortconv_prefill(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
-                            const void *w, const int32_t *cu_seqlens, int N,
+                            const void *w, const void *bias, const int32_t *cu_seqlens, int N,
                             const int32_t *slot_ids, void *pool, int n_slots, void *y,
                             void *stream) {
-    return prefill_impl(dtype, H, K, bcx, T, w, cu_seqlens, N, slot_ids, pool, n_slots, y, 0,
-                        stream);
+    return prefill_impl(dtype, H, K, bcx, T, w, bias, cu_seqlens, N, slot_ids, pool, n_slots, y,
+                        0, stream);
 }
 
 sc_status shortconv_prefill_tiled(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
-                                  const void *w, const int32_t *cu_seqlens, int N,
-                                  const int32_t *slot_ids, void *pool, int n_slots, void *y,
-                                  int rows_per_thread, void *stream) {
-    return prefill_impl(dtype, H, K, bcx, T, w, cu_seqlens, N, slot_ids, pool, n_slots, y,
+                                  const void *w, const void *bias, const int32_t *cu_seqlens,
+                                  int N, const int32_t *slot_ids, void *pool, int n_slots,
+                                  void *y, int rows_per_thread, void *stream) {
+    return prefill_impl(dtype, H, K, bcx, T, w, bias, cu_seqlens, N, slot_ids, pool, n_slots, y,
                         rows_per_thread, stream);
 }
 
 sc_status shortconv_decode(sc_dtype dtype, int H, int K, const void *bcx, int N, const void *w,
-                           const int32_t *slot_ids, void *pool, int n_slots, void *y,
-                           void *stream) {
+                           const void *bias, const int32_t *slot_ids, void *pool, int n_slots,
+                           void *y, void *stream) {
     sc_status st = check_shape(dtype, H, K);
     if (st != SC_OK) return st;
     if (N < 0 || n_slots <= 0) return SC_EINVAL;
     const size_t es = elem_size(dtype);
     const size_t n_bcx = (size_t)N * 3 * H * es, n_y = (size_t)N * H * es;
     const size_t n_w = (size_t)H * K * es, n_pool = (size_t)n_slots * H * K * es;
+    const size_t n_b = bias ? (size_t)H * es : 0;
     if (!ptr_ok(bcx, n_bcx, 16) || !ptr_ok(y, n_y, 16) || !ptr_ok(w, n_w, 16) ||
-        !ptr_ok(pool, n_pool, 16) || !ptr_ok(slot_ids, (size_t)N * 4, 4))
+        !ptr_ok(pool, n_pool, 16) || !ptr_ok(slot_ids, (size_t)N * 4, 4) || !opt_ok(bias, 16))
         return SC_EINVAL;
     if (overlaps(y, n_y, bcx, n_bcx) || overlaps(y, n_y, pool, n_pool) ||
         overlaps(y, n_y, w, n_w) || overlaps(pool, n_pool, bcx, n_bcx) ||
-        overlaps(pool, n_pool, w, n_w))
+        overlaps(pool, n_pool, w, n_w) || overlaps(y, n_y, bias, n_b) ||
+        overlaps(pool, n_pool, bias, n_b))
         return SC_EINVAL;
     if (N == 0) return SC_OK;
-    return from_cuda(sc::launch_decode(dtype, H, K, bcx, N, w, slot_ids, pool, n_slots, y,
+    return from_cuda(sc::launch_decode(dtype, H, K, bcx, N, w, bias, slot_ids, pool, n_slots, y,
                                        (cudaStream_t)stream));
 }
 
 sc_status shortconv_verify(sc_dtype dtype, int H, int K, const void *bcx, int N, int D,
-                           const void *w, const int32_t *slot_ids, const void *pool,
-                           int n_slots, void *win, void *y, void *stream) {
+                           const void *w, const void *bias, const int32_t *slot_ids,
+                           const void *pool, int n_slots, void *win, void *y, void *stream) {
     sc_status st = check_shape(dtype, H, K);
     if (st != SC_OK) return st;
     if (N < 0 || D <= 0 || n_slots <= 0) return SC_EINVAL;
@@ -138,17 +146,17 @@ sc_status shortconv_verify(sc_dtype dtype, int H, int K, const void *bcx, int N,
     const size_t n_w = (size_t)H * K * es, n_pool = (size_t)n_slots * H * K * es;
     if (!ptr_ok(bcx, n_bcx, 16) || !ptr_ok(y, n_y, 16) || !ptr_ok(w, n_w, 16) ||
         !ptr_ok(pool, n_pool, 16) || !ptr_ok(win, n_win, 16) ||
-        !ptr_ok(slot_ids, (size_t)N * 4, 4))
+        !ptr_ok(slot_ids, (size_t)N * 4, 4) || !opt_ok(bias, 16))
         return SC_EINVAL;
-    const void *ins[3] = {bcx, w, pool};
-    const size_t nins[3] = {n_bcx, n_w, n_pool};
-    for (int i = 0; i < 3; ++i)
+    const void *ins[4] = {bcx, w, pool, bias};
+    const size_t nins[4] = {n_bcx, n_w, n_pool, bias ? (size_t)H * es : 0};
+    for (int i = 0; i < 4; ++i)
         if (overlaps(y, n_y, ins[i], nins[i]) || overlaps(win, n_win, ins[i], nins[i]))
             return SC_EINVAL;
     if (overlaps(y, n_y, win, n_win)) return SC_EINVAL;
     if (N == 0) return SC_OK;
-    return from_cuda(sc::launch_verify(dtype, H, K, bcx, N, D, w, slot_ids, pool, n_slots, win,
-                                       y, (cudaStream_t)stream));
+    return from_cuda(sc::launch_verify(dtype, H, K, bcx, N, D, w, bias, slot_ids, pool, n_slots,
+                                       win, y, (cudaStream_t)stream));
 }
 
 sc_status shortconv_rollback(sc_dtype dtype, int H, int K, int N, int D, const void *win,
@@ -174,8 +182,9 @@ size_t shortconv_backward_workspace_bytes(int H, int K, int64_t T) {
 }
 
 sc_status shortconv_backward(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
-                             const void *w, const void *dy, void *dbcx, float *dw,
-                             void *workspace, size_t workspace_bytes, void *stream) {
+                             const void *w, const void *bias, const void *dy, void *dbcx,
+                             float *dw, float *dbias, void *workspace, size_t workspace_bytes,
+                             void *stream) {
     sc_status st = check_shape(dtype, H, K);
     if (st != SC_OK) return st;
     if (T < 0 || T > INT32_MAX) return SC_EINVAL;
@@ -185,26 +194,29 @@ sc_status shortconv_backward(sc_dtype dtype, int H, int K, const void *bcx, int6
     const size_t need = sc::backward_workspace_bytes(H, K, T);
     if (workspace_bytes < need) return SC_EINVAL;
     if (!ptr_ok(bcx, n_bcx, 16) || !ptr_ok(dy, n_dy, 16) || !ptr_ok(w, n_w, 16) ||
-        !ptr_ok(dbcx, n_bcx, 16) || !ptr_ok(dw, n_dw, 4) || !ptr_ok(workspace, need, 16))
+        !ptr_ok(dbcx, n_bcx, 16) || !ptr_ok(dw, n_dw, 4) || !ptr_ok(workspace, need, 16) ||
+        !opt_ok(bias, 16) || !opt_ok(dbias, 4))
         return SC_EINVAL;
-    const void *ins[3] = {bcx, w, dy};
-    const size_t nins[3] = {n_bcx, n_w, n_dy};
-    for (int i = 0; i < 3; ++i)
-        if (overlaps(dbcx, n_bcx, ins[i], nins[i]) || overlaps(dw, n_dw, ins[i], nins[i]) ||
-            overlaps(workspace, need, ins[i], nins[i]))
-            return SC_EINVAL;
-    if (overlaps(dbcx, n_bcx, dw, n_dw) || overlaps(dbcx, n_bcx, workspace, need) ||
-        overlaps(dw, n_dw, workspace, need))
-        return SC_EINVAL;
-    return from_cuda(sc::launch_backward(dtype, H, K, bcx, T, w, dy, dbcx, dw, workspace,
-                                         (cudaStream_t)stream));
+    const void *ins[4] = {bcx, w, dy, bias};
+    const size_t nins[4] = {n_bcx, n_w, n_dy, bias ? (size_t)H * es : 0};
+    const void *outs[4] = {dbcx, dw, dbias, workspace};
+    const size_t nouts[4] = {n_bcx, n_dw, dbias ? (size_t)H * 4 : 0, need};
+    for (int o = 0; o < 4; ++o) {
+        for (int i = 0; i < 4; ++i)
+            if (overlaps(outs[o], nouts[o], ins[i], nins[i])) return SC_EINVAL;
+        for (int p = o + 1; p < 4; ++p)
+            if (overlaps(outs[o], nouts[o], outs[p], nouts[p])) return SC_EINVAL;
+    }
+    return from_cuda(sc::launch_backward(dtype, H, K, bcx, T, w, bias, dy, dbcx, dw, dbias,
+                                         workspace, (cudaStream_t)stream));
 }
 
 sc_status shortconv_backward_varlen(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
-                                    const void *w, const int32_t *cu_seqlens, int N,
-                                    const void *init_states, const void *dy,
-                                    const float *d_final, void *dbcx, float *dw, float *d_init,
-                                    void *workspace, size_t workspace_bytes, void *stream) {
+                                    const void *w, const void *bias, const int32_t *cu_seqlens,
+                                    int N, const void *init_states, const void *dy,
+                                    const float *d_final, void *dbcx, float *dw, float *dbias,
+                                    float *d_init, void *workspace, size_t workspace_bytes,
+                                    void *stream) {
     sc_status st = check_shape(dtype, H, K);
     if (st != SC_OK) return st;
     if (T < 0 || T > INT32_MAX || N < 0) return SC_EINVAL;
@@ -219,23 +231,23 @@ sc_status shortconv_backward_varlen(sc_dtype dtype, int H, int K, const void *bc
         !ptr_ok(dbcx, n_bcx, 16) || !ptr_ok(dw, n_dw, 4) || !ptr_ok(workspace, need, 16) ||
         !ptr_ok(cu_seqlens, (size_t)(N + 1) * 4, 4))
         return SC_EINVAL;
-    if ((init_states && !aligned(init_states, 4)) || (d_final && !aligned(d_final, 4)) ||
-        (d_init && !aligned(d_init, 4)))
+    if (!opt_ok(init_states, 4) || !opt_ok(d_final, 4) || !opt_ok(d_init, 4) ||
+        !opt_ok(bias, 16) || !opt_ok(dbias, 4))
         return SC_EINVAL;
-    const void *ins[6] = {bcx, w, dy, init_states, d_final, cu_seqlens};
-    const size_t nins[6] = {n_bcx, n_w, n_dy, init_states ? n_st : 0, d_final ? n_sf : 0,
-                            (size_t)(N + 1) * 4};
-    const void *outs[4] = {dbcx, dw, d_init, workspace};
-    const size_t nouts[4] = {n_bcx, n_dw, d_init ? n_sf : 0, need};
-    for (int o = 0; o < 4; ++o) {
-        for (int i = 0; i < 6; ++i)
+    const void *ins[7] = {bcx, w, dy, init_states, d_final, cu_seqlens, bias};
+    const size_t nins[7] = {n_bcx, n_w, n_dy, init_states ? n_st : 0, d_final ? n_sf : 0,
+                            (size_t)(N + 1) * 4, bias ? (size_t)H * es : 0};
+    const void *outs[5] = {dbcx, dw, d_init, workspace, dbias};
+    const size_t nouts[5] = {n_bcx, n_dw, d_init ? n_sf : 0, need, dbias ? (size_t)H * 4 : 0};
+    for (int o = 0; o < 5; ++o) {
+        for (int i = 0; i < 7; ++i)
             if (overlaps(outs[o], nouts[o], ins[i], nins[i])) return SC_EINVAL;
-        for (int p = o + 1; p < 4; ++p)
+        for (int p = o + 1; p < 5; ++p)
             if (overlaps(outs[o], nouts[o], outs[p], nouts[p])) return SC_EINVAL;
     }
-    return from_cuda(sc::launch_backward_varlen(dtype, H, K, bcx, T, w, cu_seqlens, N,
-                                                init_states, dy, d_final, dbcx, dw, d_init,
-                                                workspace, (cudaStream_t)stream));
+    return from_cuda(sc::launch_backward_varlen(dtype, H, K, bcx, T, w, bias, cu_seqlens, N,
+                                                init_states, dy, d_final, dbcx, dw, dbias,
+                                                d_init, workspace, (cudaStream_t)stream));
 }
 
 sc_status shortconv_backward_noalloc(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
@@ -244,7 +256,8 @@ sc_status shortconv_backward_noalloc(sc_dtype dtype, int H, int K, const void *b
     sc_status st = check_shape(dtype, H, K);
     if (st != SC_OK) return st;
     if (T < 0 || T > INT32_MAX) return SC_EINVAL;
-    if (sc::backward_workspace_bytes(H, K, T) > sc::kNoAllocScratchBytes) return SC_EUNSUPPORTED;
+    if (sc::backward_partial_bytes(H, K, T, false) > sc::kNoAllocScratchBytes)
+        return SC_EUNSUPPORTED;
     const size_t es = elem_size(dtype);
     const size_t n_bcx = (size_t)T * 3 * H * es, n_dy = (size_t)T * H * es;
     const size_t n_w = (size_t)H * K * es, n_dw = (size_t)H * K * 4;

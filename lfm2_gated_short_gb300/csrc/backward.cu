@@ -3,10 +3,11 @@
 // Liger-Kernel PR #1317, "Kernel changes / Gated short convolution": the B/C
 // gate gradients are fused with the depthwise-conv input gradient in one
 // pass, and the weight gradient of all K taps of a channel is reduced
-// together (no bias). One pass over the rows produces dB, dC and dx and
-// accumulates dW in registers:
-//   dC_t = dy_t z_t,  dz_t = dy_t C_t,  du_s = sum_k w_k dz_{s+K-1-k},
-//   dB_s = du_s x_s,  dx_s = du_s B_s,  dW[h,k] = sum_t dz_t u_{t-K+1+k}.
+// together. One pass over the rows produces dB, dC and dx and accumulates dW
+// (and, with the optional conv bias b, dbias) in registers:
+//   z_t = sum_k w_k u_{t-K+1+k} (+ b),  dC_t = dy_t z_t,  dz_t = dy_t C_t,
+//   du_s = sum_k w_k dz_{s+K-1-k},  dB_s = du_s x_s,  dx_s = du_s B_s,
+//   dW[h,k] = sum_t dz_t u_{t-K+1+k},  dbias[h] = sum_t dz_t.
 //
 // Same streamed design as the prefill: persistent CTAs (several per SM) each
 // own a balanced range of rows [cr0, cr1) of a slice of up to 512 channels; a
@@ -14,9 +15,11 @@
 // before the range (u history) and after it (dz look-ahead) -- through a
 // shared-memory ring with 1-D bulk asynchronous copies on full/empty
 // mbarriers; the consumer warps, 4 channels per thread, walk the rows. Each
-// thread holds its channels' dW over the whole range in registers and
-// writes one fp32 partial per CTA; a second kernel adds the partials of all
-// CTAs in a fixed order, so dW has the same bits on every call.
+// thread holds its channels' dW (and dbias) over the whole range in registers
+// and writes one fp32 partial per CTA; a second kernel adds the partials of
+// all CTAs in a fixed order, so dW and dbias have the same bits on every call.
+// Partial layout per row range: H*K dW entries, then H dbias entries when the
+// caller asked for dbias.
 #include <atomic>
 #include <mutex>
 
@@ -62,15 +65,57 @@ static int64_t bwd_row_ctas(int64_t T) {
     return n < 1 ? 1 : (n > kBwdRowCtas ? kBwdRowCtas : n);
 }
 
-size_t backward_workspace_bytes(int H, int K, int64_t T) {
-    return (size_t)bwd_row_ctas(T) * (size_t)H * (size_t)K * sizeof(float);
+size_t backward_partial_bytes(int H, int K, int64_t T, bool with_dbias) {
+    return (size_t)bwd_row_ctas(T) * (size_t)H * (size_t)(K + (with_dbias ? 1 : 0)) *
+           sizeof(float);
 }
 
-template <typename T, int K>
+size_t backward_workspace_bytes(int H, int K, int64_t T) {
+    return backward_partial_bytes(H, K, T, true);
+}
+
+// The conv bias of a thread's CPT channels as pairs (zeros without a bias).
+template <typename T, int CPT>
+__device__ __forceinline__ void load_bias_pairs(const T *__restrict__ bias, int h0,
+                                                f32x2 (&bp)[CPT / 2]) {
+#pragma unroll
+    for (int q = 0; q < CPT / 2; ++q)
+        bp[q] = bias != nullptr
+                    ? f2_make(ld_elem(bias + h0 + 2 * q), ld_elem(bias + h0 + 2 * q + 1))
+                    : 0ull;
+}
+
+// One row range's dW (and dbias) partial for a thread's CPT channels.
+template <int K, int CPT>
+__device__ __forceinline__ void store_partial(float *__restrict__ part, int H, int h0,
+                                              bool with_dbias, const f32x2 (&acc)[K][CPT / 2],
+                                              const f32x2 (&accb)[CPT / 2]) {
+    float *pp = part + (int64_t)h0 * K;
+#pragma unroll
+    for (int q = 0; q < CPT / 2; ++q) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            float lo, hi;
+            f2_split(acc[k][q], lo, hi);
+            pp[(2 * q) * K + k] = lo;
+            pp[(2 * q + 1) * K + k] = hi;
+        }
+        if (with_dbias) {
+            float lo, hi;
+            f2_split(accb[q], lo, hi);
+            part[(int64_t)H * K + h0 + 2 * q] = lo;
+            part[(int64_t)H * K + h0 + 2 * q + 1] = hi;
+        }
+    }
+}
+
+// HB: a conv bias is given or dbias is wanted. The instance without carries
+// no bias registers or branches; with_dbias then is false.
+template <typename T, int K, bool HB>
 __global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_MIN_CTAS)
     k_backward(const T *__restrict__ bcx, int64_t T_rows, int H, const T *__restrict__ w,
-               const T *__restrict__ dy, T *__restrict__ dbcx, float *__restrict__ partial,
-               int n_slices, int n_row_ctas) {
+               const T *__restrict__ bias, const T *__restrict__ dy, T *__restrict__ dbcx,
+               float *__restrict__ partial, bool with_dbias, int n_slices, int n_row_ctas) {
     constexpr int CPT = kBwdCpt;
     constexpr int NP = CPT / 2;
     constexpr int R = BwdShape<T>::R;
@@ -145,14 +190,20 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_MIN_CTAS)
         return;
     }
 
-    f32x2 wp[K][NP];
-    if (active) load_taps<T, CPT, K>(w + (int64_t)h0 * K, wp);
+    f32x2 wp[K][NP], bp[NP], accb[NP];  // taps, conv bias, dbias
+    if (active) {
+        load_taps<T, CPT, K>(w + (int64_t)h0 * K, wp);
+        if constexpr (HB) load_bias_pairs<T, CPT>(bias, h0, bp);
+    }
     f32x2 uw[K][NP], dzw[K][NP], acc[K][NP];  // u window, dz window (newest last), dW
     Sec<T, CPT> rbq[KH], rxq[KH];             // B and x of the K-1 rows before t
 #pragma unroll
-    for (int k = 0; k < K; ++k)
+    for (int q = 0; q < NP; ++q) {
+        accb[q] = 0ull;
 #pragma unroll
-        for (int q = 0; q < NP; ++q) uw[k][q] = dzw[k][q] = acc[k][q] = 0ull;
+        for (int k = 0; k < K; ++k) uw[k][q] = dzw[k][q] = acc[k][q] = 0ull;
+    }
+    const f32x2 one2 = f2_make(1.f, 1.f);
 
     // du for row s = t-K+1 from the dz window (dz_t newest), then dB_s, dx_s.
     auto emit = [&](int64_t t, const Sec<T, CPT> &b_s, const Sec<T, CPT> &x_s) {
@@ -226,9 +277,12 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_MIN_CTAS)
                     f32x2 z = f2_mul(wp[0][q], uw[0][q]);  // the forward's order
 #pragma unroll
                     for (int k = 1; k < K; ++k) z = f2_fma(wp[k][q], uw[k][q], z);
+                    if constexpr (HB)
+                        if (bias != nullptr) z = f2_fma(one2, bp[q], z);
                     dc[q] = f2_mul(fg[q], z);
 #pragma unroll
                     for (int k = 0; k < K; ++k) acc[k][q] = f2_fma(dz[q], uw[k][q], acc[k][q]);
+                    if constexpr (HB) accb[q] = f2_fma(one2, dz[q], accb[q]);
                 }
                 Pairs<T, CPT>::store(dbcx + t * ld + H + h0, dc);
             }
@@ -254,17 +308,9 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_MIN_CTAS)
         emit(t, rbq[0], rxq[0]);
         push_bx(rbq[0], rxq[0]);
     }
-    // This CTA's dW partial for its channels (zero for an empty range).
-    float *pp = partial + (int64_t)rc * H * K + (int64_t)h0 * K;
-#pragma unroll
-    for (int q = 0; q < NP; ++q)
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-            float lo, hi;
-            f2_split(acc[k][q], lo, hi);
-            pp[(2 * q) * K + k] = lo;
-            pp[(2 * q + 1) * K + k] = hi;
-        }
+    // This CTA's dW (and dbias) partial for its channels (zero for an empty range).
+    store_partial<K, CPT>(partial + rc * (int64_t)H * (K + (with_dbias ? 1 : 0)), H, h0,
+                          HB && with_dbias, acc, accb);
 }
 
 // ------------------------------------------------ packed varlen, with states
@@ -291,13 +337,14 @@ constexpr size_t bwd_varlen_smem_bytes(int CW) {
     return bwd_smem_bytes<T>(CW) + kBwdCuBytes;
 }
 
-template <typename T, int K>
+template <typename T, int K, bool HB>
 __global__ void __launch_bounds__(kBwdConsumers + 32, 3)
     k_backward_varlen(const T *__restrict__ bcx, int64_t T_rows, int H, const T *__restrict__ w,
-                      const int32_t *__restrict__ cu, int N, const T *__restrict__ init,
-                      const T *__restrict__ dy, const float *__restrict__ d_final,
-                      T *__restrict__ dbcx, float *__restrict__ partial,
-                      float *__restrict__ d_init, int n_slices, int n_row_ctas) {
+                      const T *__restrict__ bias, const int32_t *__restrict__ cu, int N,
+                      const T *__restrict__ init, const T *__restrict__ dy,
+                      const float *__restrict__ d_final, T *__restrict__ dbcx,
+                      float *__restrict__ partial, bool with_dbias, float *__restrict__ d_init,
+                      int n_slices, int n_row_ctas) {
     constexpr int CPT = kBwdCpt;
     constexpr int NP = CPT / 2;
     constexpr int R = BwdShape<T>::R;
@@ -326,7 +373,7 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, 3)
     const int n_chunks = cr0 < cr1 ? (int)((sr1 - sr0 + R - 1) / R) : 0;
     const uint32_t sec_bytes = (uint32_t)cw * sizeof(T);
     const int64_t ld = 3 * (int64_t)H;
-    float *pp = partial + (int64_t)rc * H * K + (int64_t)h0 * K;
+    float *part = partial + rc * (int64_t)H * (K + (with_dbias ? 1 : 0));
 
     if (lead) {
 #pragma unroll
@@ -358,17 +405,6 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, 3)
     auto drain = [&](int from, int to) {
         for (int c = from; c < to; ++c) mbar_wait_bounded(&full[c % NS], (uint32_t)(c / NS) & 1u);
     };
-    auto write_partial = [&](const f32x2 (&acc)[K][NP]) {
-#pragma unroll
-        for (int q = 0; q < NP; ++q)
-#pragma unroll
-            for (int k = 0; k < K; ++k) {
-                float lo, hi;
-                f2_split(acc[k][q], lo, hi);
-                pp[(2 * q) * K + k] = lo;
-                pp[(2 * q + 1) * K + k] = hi;
-            }
-    };
     const int first = min(NS, n_chunks);
     if (lead)
         for (int c = 0; c < first; ++c) issue(c);
@@ -382,15 +418,18 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, 3)
         if (j == N && (int64_t)c != T_rows) bad = 1;
         if (j < N && cu[j + 1] < c) bad = 1;
     }
-    f32x2 acc[K][NP];
+    f32x2 acc[K][NP], accb[NP];
 #pragma unroll
-    for (int k = 0; k < K; ++k)
+    for (int q = 0; q < NP; ++q) {
+        accb[q] = 0ull;
 #pragma unroll
-        for (int q = 0; q < NP; ++q) acc[k][q] = 0ull;
+        for (int k = 0; k < K; ++k) acc[k][q] = 0ull;
+    }
     if (__syncthreads_or(bad)) {
         if (blockIdx.x == 0 && tid == 0) raise_error(SC_DEV_BAD_SEQLENS);
         if (lead) drain(0, first);
-        if (active) write_partial(acc);  // dW becomes 0; dB|dC|dx and d_init are not written
+        // dW and dbias become 0; dB|dC|dx and d_init are not written
+        if (active) store_partial<K, CPT>(part, H, h0, HB && with_dbias, acc, accb);
         return;
     }
 
@@ -409,8 +448,12 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, 3)
     }
 
     auto CU = [&](int j) -> int64_t { return staged ? s_cu[j] : cu[j]; };
-    f32x2 wp[K][NP];
-    if (active) load_taps<T, CPT, K>(w + (int64_t)h0 * K, wp);
+    f32x2 wp[K][NP], bp[NP];
+    if (active) {
+        load_taps<T, CPT, K>(w + (int64_t)h0 * K, wp);
+        if constexpr (HB) load_bias_pairs<T, CPT>(bias, h0, bp);
+    }
+    const f32x2 one2 = f2_make(1.f, 1.f);
     f32x2 uw[K][NP], dzw[K][NP], dzf[KH][NP], dfin[K][NP];
     Sec<T, CPT> rbq[KH], rxq[KH];
     int i = 0;
@@ -569,9 +612,12 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, 3)
                     f32x2 z = f2_mul(wp[0][q], uw[0][q]);
 #pragma unroll
                     for (int k = 1; k < K; ++k) z = f2_fma(wp[k][q], uw[k][q], z);
+                    if constexpr (HB)
+                        if (bias != nullptr) z = f2_fma(one2, bp[q], z);
                     dc[q] = f2_mul(fg[q], z);
 #pragma unroll
                     for (int k = 0; k < K; ++k) acc[k][q] = f2_fma(dz[q], uw[k][q], acc[k][q]);
+                    if constexpr (HB) accb[q] = f2_fma(one2, dz[q], accb[q]);
                 }
                 Pairs<T, CPT>::store(dbcx + t * ld + H + h0, dc);
             }
@@ -606,41 +652,53 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, 3)
                 o[e] = d_final != nullptr ? d_final[((int64_t)j * H + h0) * K + e] : 0.f;
         }
     }
-    write_partial(acc);
+    store_partial<K, CPT>(part, H, h0, HB && with_dbias, acc, accb);
 }
 
-// dw[e] = sum over CTA rows g = 0 .. G-1 of partial[g][e]: 8 warps take
-// interleaved g for 32 consecutive e, then warp 0 adds the 8 sums in order.
+// out[e] = sum over row ranges g = 0 .. G-1 of partial[g][e] for the P
+// entries of a partial (dW's HK first, then dbias's): 8 warps take interleaved
+// g for 32 consecutive e, then warp 0 adds the 8 sums in order.
 __global__ void __launch_bounds__(256)
-    k_dw_reduce(const float *__restrict__ partial, int64_t G, int HK, float *__restrict__ dw) {
+    k_dw_reduce(const float *__restrict__ partial, int64_t G, int HK, int P,
+                float *__restrict__ dw, float *__restrict__ dbias) {
     __shared__ float part[8][32];
     pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int e = blockIdx.x * 32 + lane;
     float s = 0.f;
-    if (e < HK)
-        for (int64_t g = warp; g < G; g += 8) s += partial[g * HK + e];
+    if (e < P)
+        for (int64_t g = warp; g < G; g += 8) s += partial[g * P + e];
     part[warp][lane] = s;
     __syncthreads();
-    if (warp == 0 && e < HK) {
+    if (warp == 0 && e < P) {
         float t = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) t += part[j][lane];
-        dw[e] = t;
+        if (e < HK)
+            dw[e] = t;
+        else
+            dbias[e - HK] = t;
     }
 }
 
-template <typename T, int K>
+static cudaError_t launch_reduce(const void *ws, int64_t n_row, int H, int K, float *dw,
+                                 float *dbias, cudaStream_t stream) {
+    const int HK = H * K, P = HK + (dbias != nullptr ? H : 0);
+    return launch_pdl(k_dw_reduce, dim3((unsigned)((P + 31) / 32)), dim3(256), 0, stream,
+                      (const float *)ws, n_row, HK, P, dw, dbias);
+}
+
+template <typename T, int K, bool HB>
 static cudaError_t backward_inst(const void *bcx, int64_t rows, int H, const void *w,
-                                 const void *dy, void *dbcx, float *dw, void *ws,
-                                 cudaStream_t stream) {
+                                 const void *bias, const void *dy, void *dbcx, float *dw,
+                                 float *dbias, void *ws, cudaStream_t stream) {
     const int CW = H < kBwdSlice ? H : kBwdSlice;
     const int n_slices = (H + kBwdSlice - 1) / kBwdSlice;
     const int threads = (CW / kBwdCpt + 31) / 32 * 32 + 32;  // consumers + one producer warp
     const size_t smem = bwd_smem_bytes<T>(CW);
     const int64_t n_row = bwd_row_ctas(rows);
-    auto kern = k_backward<T, K>;
+    auto kern = k_backward<T, K, HB>;
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -652,26 +710,24 @@ static cudaError_t backward_inst(const void *bcx, int64_t rows, int H, const voi
         configured.fetch_or(1ull << dev);
     }
     e = launch_pdl(kern, dim3((unsigned)(n_row * n_slices)), dim3(threads), smem, stream,
-                   (const T *)bcx, rows, H, (const T *)w, (const T *)dy, (T *)dbcx, (float *)ws,
-                   n_slices, (int)n_row);
+                   (const T *)bcx, rows, H, (const T *)w, (const T *)bias, (const T *)dy,
+                   (T *)dbcx, (float *)ws, dbias != nullptr, n_slices, (int)n_row);
     if (e != cudaSuccess) return e;
-    const int HK = H * K;
-    return launch_pdl(k_dw_reduce, dim3((HK + 31) / 32), dim3(256), 0, stream,
-                      (const float *)ws, n_row, HK, dw);
+    return launch_reduce(ws, n_row, H, K, dw, dbias, stream);
 }
 
-template <typename T, int K>
+template <typename T, int K, bool HB>
 static cudaError_t backward_varlen_inst(const void *bcx, int64_t rows, int H, const void *w,
-                                        const int32_t *cu, int N, const void *init,
-                                        const void *dy, const float *d_final, void *dbcx,
-                                        float *dw, float *d_init, void *ws,
-                                        cudaStream_t stream) {
+                                        const void *bias, const int32_t *cu, int N,
+                                        const void *init, const void *dy, const float *d_final,
+                                        void *dbcx, float *dw, float *dbias, float *d_init,
+                                        void *ws, cudaStream_t stream) {
     const int CW = H < kBwdSlice ? H : kBwdSlice;
     const int n_slices = (H + kBwdSlice - 1) / kBwdSlice;
     const int threads = (CW / kBwdCpt + 31) / 32 * 32 + 32;
     const size_t smem = bwd_varlen_smem_bytes<T>(CW);
     const int64_t n_row = bwd_row_ctas(rows);
-    auto kern = k_backward_varlen<T, K>;
+    auto kern = k_backward_varlen<T, K, HB>;
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -683,53 +739,70 @@ static cudaError_t backward_varlen_inst(const void *bcx, int64_t rows, int H, co
         configured.fetch_or(1ull << dev);
     }
     e = launch_pdl(kern, dim3((unsigned)(n_row * n_slices)), dim3(threads), smem, stream,
-                   (const T *)bcx, rows, H, (const T *)w, cu, N, (const T *)init, (const T *)dy,
-                   d_final, (T *)dbcx, (float *)ws, d_init, n_slices, (int)n_row);
+                   (const T *)bcx, rows, H, (const T *)w, (const T *)bias, cu, N,
+                   (const T *)init, (const T *)dy, d_final, (T *)dbcx, (float *)ws,
+                   dbias != nullptr, d_init, n_slices, (int)n_row);
     if (e != cudaSuccess) return e;
-    const int HK = H * K;
-    return launch_pdl(k_dw_reduce, dim3((HK + 31) / 32), dim3(256), 0, stream,
-                      (const float *)ws, n_row, HK, dw);
+    return launch_reduce(ws, n_row, H, K, dw, dbias, stream);
 }
 
+#define SC_VARLEN_ARGS bcx, rows, H, w, bias, cu, N, init, dy, d_final, dbcx, dw, dbias, d_init, ws, s
 template <typename T>
 static cudaError_t backward_varlen_K(int K, const void *bcx, int64_t rows, int H, const void *w,
-                                     const int32_t *cu, int N, const void *init, const void *dy,
-                                     const float *d_final, void *dbcx, float *dw, float *d_init,
-                                     void *ws, cudaStream_t s) {
+                                     const void *bias, const int32_t *cu, int N,
+                                     const void *init, const void *dy, const float *d_final,
+                                     void *dbcx, float *dw, float *dbias, float *d_init, void *ws,
+                                     cudaStream_t s) {
+    const bool hb = bias != nullptr || dbias != nullptr;
+#define SC_VARLEN_CASE(k)                                                        \
+    return hb ? backward_varlen_inst<T, k, true>(SC_VARLEN_ARGS)                 \
+              : backward_varlen_inst<T, k, false>(SC_VARLEN_ARGS)
     switch (K) {
-        case 1: return backward_varlen_inst<T, 1>(bcx, rows, H, w, cu, N, init, dy, d_final, dbcx, dw, d_init, ws, s);
-        case 2: return backward_varlen_inst<T, 2>(bcx, rows, H, w, cu, N, init, dy, d_final, dbcx, dw, d_init, ws, s);
-        case 3: return backward_varlen_inst<T, 3>(bcx, rows, H, w, cu, N, init, dy, d_final, dbcx, dw, d_init, ws, s);
-        default: return backward_varlen_inst<T, 4>(bcx, rows, H, w, cu, N, init, dy, d_final, dbcx, dw, d_init, ws, s);
+        case 1: SC_VARLEN_CASE(1);
+        case 2: SC_VARLEN_CASE(2);
+        case 3: SC_VARLEN_CASE(3);
+        default: SC_VARLEN_CASE(4);
     }
+#undef SC_VARLEN_CASE
 }
+#undef SC_VARLEN_ARGS
 
 cudaError_t launch_backward_varlen(int dtype, int H, int K, const void *bcx, int64_t T,
-                                   const void *w, const int32_t *cu, int N, const void *init,
-                                   const void *dy, const float *d_final, void *dbcx, float *dw,
-                                   float *d_init, void *ws, cudaStream_t s) {
+                                   const void *w, const void *bias, const int32_t *cu, int N,
+                                   const void *init, const void *dy, const float *d_final,
+                                   void *dbcx, float *dw, float *dbias, float *d_init, void *ws,
+                                   cudaStream_t s) {
     if (dtype == SC_BF16)
-        return backward_varlen_K<__nv_bfloat16>(K, bcx, T, H, w, cu, N, init, dy, d_final, dbcx,
-                                                dw, d_init, ws, s);
-    return backward_varlen_K<float>(K, bcx, T, H, w, cu, N, init, dy, d_final, dbcx, dw, d_init,
-                                    ws, s);
+        return backward_varlen_K<__nv_bfloat16>(K, bcx, T, H, w, bias, cu, N, init, dy, d_final,
+                                                dbcx, dw, dbias, d_init, ws, s);
+    return backward_varlen_K<float>(K, bcx, T, H, w, bias, cu, N, init, dy, d_final, dbcx, dw,
+                                    dbias, d_init, ws, s);
 }
 
 template <typename T>
 static cudaError_t backward_K(int K, const void *bcx, int64_t rows, int H, const void *w,
-                              const void *dy, void *dbcx, float *dw, void *ws, cudaStream_t s) {
+                              const void *bias, const void *dy, void *dbcx, float *dw,
+                              float *dbias, void *ws, cudaStream_t s) {
+    const bool hb = bias != nullptr || dbias != nullptr;
+#define SC_BWD_ARGS bcx, rows, H, w, bias, dy, dbcx, dw, dbias, ws, s
+#define SC_BWD_CASE(k)                                                         \
+    return hb ? backward_inst<T, k, true>(SC_BWD_ARGS) : backward_inst<T, k, false>(SC_BWD_ARGS)
     switch (K) {
-        case 1: return backward_inst<T, 1>(bcx, rows, H, w, dy, dbcx, dw, ws, s);
-        case 2: return backward_inst<T, 2>(bcx, rows, H, w, dy, dbcx, dw, ws, s);
-        case 3: return backward_inst<T, 3>(bcx, rows, H, w, dy, dbcx, dw, ws, s);
-        default: return backward_inst<T, 4>(bcx, rows, H, w, dy, dbcx, dw, ws, s);
+        case 1: SC_BWD_CASE(1);
+        case 2: SC_BWD_CASE(2);
+        case 3: SC_BWD_CASE(3);
+        default: SC_BWD_CASE(4);
     }
+#undef SC_BWD_CASE
+#undef SC_BWD_ARGS
 }
 
 cudaError_t launch_backward(int dtype, int H, int K, const void *bcx, int64_t T, const void *w,
-                            const void *dy, void *dbcx, float *dw, void *ws, cudaStream_t s) {
-    if (dtype == SC_BF16) return backward_K<__nv_bfloat16>(K, bcx, T, H, w, dy, dbcx, dw, ws, s);
-    return backward_K<float>(K, bcx, T, H, w, dy, dbcx, dw, ws, s);
+                            const void *bias, const void *dy, void *dbcx, float *dw,
+                            float *dbias, void *ws, cudaStream_t s) {
+    if (dtype == SC_BF16)
+        return backward_K<__nv_bfloat16>(K, bcx, T, H, w, bias, dy, dbcx, dw, dbias, ws, s);
+    return backward_K<float>(K, bcx, T, H, w, bias, dy, dbcx, dw, dbias, ws, s);
 }
 
 cudaError_t take_error_backward(cudaStream_t stream, unsigned int *code) {
@@ -738,8 +811,9 @@ cudaError_t take_error_backward(cudaStream_t stream, unsigned int *code) {
 
 // ------------------------------------------------ no-allocation entry point
 //
-// shortconv_backward_noalloc runs the kernels above with their fp32 dW
-// partials in this fixed device array instead of a caller workspace. It is
+// shortconv_backward_noalloc runs the kernels above (without a conv bias) with
+// their fp32 dW partials in this fixed device array instead of a caller
+// workspace. It is
 // for callers that cannot allocate device memory at call time. It holds
 // kNoAllocScratchBytes on every GPU that loads the library, until exit.
 // Every entry the reduction reads is first written by the same call, so the
@@ -773,8 +847,9 @@ cudaError_t launch_backward_noalloc(int dtype, int H, int K, const void *bcx, in
     void *ws = nullptr;
     const cudaError_t e = noalloc_scratch(&ws);
     if (e != cudaSuccess) return e;
-    if (dtype == SC_BF16) return backward_K<__nv_bfloat16>(K, bcx, T, H, w, dy, dbcx, dw, ws, s);
-    return backward_K<float>(K, bcx, T, H, w, dy, dbcx, dw, ws, s);
+    if (dtype == SC_BF16)
+        return backward_K<__nv_bfloat16>(K, bcx, T, H, w, nullptr, dy, dbcx, dw, nullptr, ws, s);
+    return backward_K<float>(K, bcx, T, H, w, nullptr, dy, dbcx, dw, nullptr, ws, s);
 }
 
 }  // namespace sc

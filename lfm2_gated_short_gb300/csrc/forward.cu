@@ -38,11 +38,23 @@ __device__ __forceinline__ void row_u(const T *__restrict__ bcx, int64_t row, in
     for (int c = 0; c < kCh; ++c) u[c] = gate_in<T>(b[c], x[c]);
 }
 
+// The optional per-channel conv bias of 8 channels (zeros when absent).
+template <typename T>
+__device__ __forceinline__ void load_bias8(const T *__restrict__ bias, int h0, float (&bh)[kCh]) {
+    if (bias != nullptr) {
+        unpack_row(load_row(bias + h0), bh);
+    } else {
+#pragma unroll
+        for (int c = 0; c < kCh; ++c) bh[c] = 0.f;
+    }
+}
+
 // Rows [a, e) of one sequence for 8 channels; `win` enters holding the last K
 // values of u before row a and leaves holding the last K up to row e-1.
 template <typename T, int K>
 __device__ __forceinline__ void run_rows(const T *__restrict__ bcx, int H, int h0, int64_t a,
                                          int64_t e, const float (&wt)[kCh][K],
+                                         const float (&bh)[kCh], bool has_bias,
                                          float (&win)[kCh][K], T *__restrict__ y) {
     const int64_t ld = 3 * (int64_t)H;
     for (int64_t r = a; r < e; r += kChunk) {
@@ -66,7 +78,9 @@ __device__ __forceinline__ void run_rows(const T *__restrict__ bcx, int H, int h
 #pragma unroll
                 for (int ch = 0; ch < kCh; ++ch) {
                     const float u = gate_in<T>(b[ch], x[ch]);
-                    out[ch] = c[ch] * slide_dot<K>(win[ch], wt[ch], u);
+                    float z = slide_dot<K>(win[ch], wt[ch], u);
+                    if (has_bias) z = z + bh[ch];
+                    out[ch] = c[ch] * z;
                 }
                 store_row(y + (r + j) * (int64_t)H + h0, out);
             }
@@ -91,8 +105,9 @@ __device__ __forceinline__ void run_rows(const T *__restrict__ bcx, int H, int h
 template <typename T, int K, int L>
 __global__ void __launch_bounds__(kThreads)
     k_prefill(const T *__restrict__ bcx, int64_t T_rows, int H, const T *__restrict__ w,
-              const int32_t *__restrict__ cu, int N, const int32_t *__restrict__ slots,
-              T *__restrict__ pool, int n_slots, T *__restrict__ y) {
+              const T *__restrict__ bias, const int32_t *__restrict__ cu, int N,
+              const int32_t *__restrict__ slots, T *__restrict__ pool, int n_slots,
+              T *__restrict__ y) {
     __shared__ int32_t s_cu[kMaxStagedSeqs + 1];
     const bool staged = N <= kMaxStagedSeqs;
     pdl_wait();
@@ -129,8 +144,10 @@ __global__ void __launch_bounds__(kThreads)
         if (CU(mid) <= r0) lo = mid; else hi = mid - 1;
     }
 
-    float wt[kCh][K];
+    float wt[kCh][K], bh[kCh];
     load_block<T, K>(w + (int64_t)h0 * K, wt);
+    load_bias8<T>(bias, h0, bh);
+    const bool has_bias = bias != nullptr;
 
     for (int i = lo; i < N; ++i) {
         const int64_t s0 = CU(i), s1 = CU(i + 1);
@@ -166,7 +183,7 @@ __global__ void __launch_bounds__(kThreads)
                 for (int ch = 0; ch < kCh; ++ch) win[ch][k] = u[ch];
             }
         }
-        run_rows<T, K>(bcx, H, h0, a, e, wt, win, y);
+        run_rows<T, K>(bcx, H, h0, a, e, wt, bh, has_bias, win, y);
         if (owner) {
             if (e < s1) {  // the sequence ends in a later tile: rebuild its last K values
 #pragma unroll
@@ -184,50 +201,51 @@ __global__ void __launch_bounds__(kThreads)
 
 template <typename T, int K, int L>
 static cudaError_t prefill_inst(const void *bcx, int64_t rows, int H, const void *w,
-                                const int32_t *cu, int N, const int32_t *slots, void *pool,
-                                int n_slots, void *y, cudaStream_t stream) {
+                                const void *bias, const int32_t *cu, int N,
+                                const int32_t *slots, void *pool, int n_slots, void *y,
+                                cudaStream_t stream) {
     const int64_t units = (rows + L - 1) / L * (H / kCh);
     int64_t blocks = (units + kThreads - 1) / kThreads;
     if (blocks < 1) blocks = 1;  // still validates cu_seqlens
     return launch_pdl(k_prefill<T, K, L>, dim3((unsigned)blocks), dim3(kThreads), 0, stream,
-                      (const T *)bcx, rows, H, (const T *)w, cu, N, slots, (T *)pool, n_slots,
-                      (T *)y);
+                      (const T *)bcx, rows, H, (const T *)w, (const T *)bias, cu, N, slots,
+                      (T *)pool, n_slots, (T *)y);
 }
 
 template <typename T, int K>
 static cudaError_t prefill_L(int L, const void *bcx, int64_t rows, int H, const void *w,
-                             const int32_t *cu, int N, const int32_t *slots, void *pool,
-                             int n_slots, void *y, cudaStream_t s) {
+                             const void *bias, const int32_t *cu, int N, const int32_t *slots,
+                             void *pool, int n_slots, void *y, cudaStream_t s) {
     switch (L) {
-        case 4: return prefill_inst<T, K, 4>(bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
-        case 8: return prefill_inst<T, K, 8>(bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
-        case 16: return prefill_inst<T, K, 16>(bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
-        default: return prefill_inst<T, K, 32>(bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
+        case 4: return prefill_inst<T, K, 4>(bcx, rows, H, w, bias, cu, N, slots, pool, n_slots, y, s);
+        case 8: return prefill_inst<T, K, 8>(bcx, rows, H, w, bias, cu, N, slots, pool, n_slots, y, s);
+        case 16: return prefill_inst<T, K, 16>(bcx, rows, H, w, bias, cu, N, slots, pool, n_slots, y, s);
+        default: return prefill_inst<T, K, 32>(bcx, rows, H, w, bias, cu, N, slots, pool, n_slots, y, s);
     }
 }
 
 template <typename T>
 static cudaError_t prefill_K(int K, int L, const void *bcx, int64_t rows, int H, const void *w,
-                             const int32_t *cu, int N, const int32_t *slots, void *pool,
-                             int n_slots, void *y, cudaStream_t s) {
+                             const void *bias, const int32_t *cu, int N, const int32_t *slots,
+                             void *pool, int n_slots, void *y, cudaStream_t s) {
     switch (K) {
-        case 1: return prefill_L<T, 1>(L, bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
-        case 2: return prefill_L<T, 2>(L, bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
-        case 3: return prefill_L<T, 3>(L, bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
-        default: return prefill_L<T, 4>(L, bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
+        case 1: return prefill_L<T, 1>(L, bcx, rows, H, w, bias, cu, N, slots, pool, n_slots, y, s);
+        case 2: return prefill_L<T, 2>(L, bcx, rows, H, w, bias, cu, N, slots, pool, n_slots, y, s);
+        case 3: return prefill_L<T, 3>(L, bcx, rows, H, w, bias, cu, N, slots, pool, n_slots, y, s);
+        default: return prefill_L<T, 4>(L, bcx, rows, H, w, bias, cu, N, slots, pool, n_slots, y, s);
     }
 }
 
-template <typename T, int K>
+template <typename T, int K, bool HB>
 static cudaError_t prefill_stream_inst(const void *bcx, int64_t rows, int H, const void *w,
-                                       const int32_t *cu, int N, const int32_t *slots,
-                                       void *pool, int n_slots, void *y, int sm_count,
-                                       cudaStream_t stream) {
+                                       const void *bias, const int32_t *cu, int N,
+                                       const int32_t *slots, void *pool, int n_slots, void *y,
+                                       int sm_count, cudaStream_t stream) {
     const int CW = std::min(kStreamSlice, H);
     const int n_slices = (H + kStreamSlice - 1) / kStreamSlice;
     const int threads = (CW / kStreamCpt + 31) / 32 * 32 + 32;  // consumers + one producer warp
     const size_t smem = stream_smem_bytes<T>(CW);
-    auto kern = k_prefill_stream<T, K>;
+    auto kern = k_prefill_stream<T, K, HB>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -254,35 +272,44 @@ static cudaError_t prefill_stream_inst(const void *bcx, int64_t rows, int H, con
                                       (int64_t)sm_count * occ / n_slices);
     if (n_row < 1) n_row = 1;
     return launch_pdl(kern, dim3((unsigned)(n_row * n_slices)), dim3(threads), smem, stream,
-                      (const T *)bcx, rows, H, (const T *)w, cu, N, slots, (T *)pool, n_slots,
-                      (T *)y, n_slices, (int)n_row);
+                      (const T *)bcx, rows, H, (const T *)w, (const T *)bias, cu, N, slots,
+                      (T *)pool, n_slots, (T *)y, n_slices, (int)n_row);
 }
 
 template <typename T>
 static cudaError_t prefill_stream_K(int K, const void *bcx, int64_t rows, int H, const void *w,
-                                    const int32_t *cu, int N, const int32_t *slots, void *pool,
-                                    int n_slots, void *y, int sms, cudaStream_t s) {
+                                    const void *bias, const int32_t *cu, int N,
+                                    const int32_t *slots, void *pool, int n_slots, void *y,
+                                    int sms, cudaStream_t s) {
+#define SC_STREAM_ARGS bcx, rows, H, w, bias, cu, N, slots, pool, n_slots, y, sms, s
+#define SC_STREAM_CASE(k)                                                   \
+    return bias != nullptr ? prefill_stream_inst<T, k, true>(SC_STREAM_ARGS) \
+                           : prefill_stream_inst<T, k, false>(SC_STREAM_ARGS)
     switch (K) {
-        case 1: return prefill_stream_inst<T, 1>(bcx, rows, H, w, cu, N, slots, pool, n_slots, y, sms, s);
-        case 2: return prefill_stream_inst<T, 2>(bcx, rows, H, w, cu, N, slots, pool, n_slots, y, sms, s);
-        case 3: return prefill_stream_inst<T, 3>(bcx, rows, H, w, cu, N, slots, pool, n_slots, y, sms, s);
-        default: return prefill_stream_inst<T, 4>(bcx, rows, H, w, cu, N, slots, pool, n_slots, y, sms, s);
+        case 1: SC_STREAM_CASE(1);
+        case 2: SC_STREAM_CASE(2);
+        case 3: SC_STREAM_CASE(3);
+        default: SC_STREAM_CASE(4);
     }
+#undef SC_STREAM_CASE
+#undef SC_STREAM_ARGS
 }
 
 cudaError_t launch_prefill(int dtype, int H, int K, const void *bcx, int64_t rows, const void *w,
-                           const int32_t *cu, int N, const int32_t *slots, void *pool,
-                           int n_slots, void *y, int L, int sm_count, cudaStream_t s) {
+                           const void *bias, const int32_t *cu, int N, const int32_t *slots,
+                           void *pool, int n_slots, void *y, int L, int sm_count,
+                           cudaStream_t s) {
     if (L == 0) {
         if (dtype == SC_BF16)
-            return prefill_stream_K<__nv_bfloat16>(K, bcx, rows, H, w, cu, N, slots, pool,
+            return prefill_stream_K<__nv_bfloat16>(K, bcx, rows, H, w, bias, cu, N, slots, pool,
                                                    n_slots, y, sm_count, s);
-        return prefill_stream_K<float>(K, bcx, rows, H, w, cu, N, slots, pool, n_slots, y,
+        return prefill_stream_K<float>(K, bcx, rows, H, w, bias, cu, N, slots, pool, n_slots, y,
                                        sm_count, s);
     }
     if (dtype == SC_BF16)
-        return prefill_K<__nv_bfloat16>(K, L, bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
-    return prefill_K<float>(K, L, bcx, rows, H, w, cu, N, slots, pool, n_slots, y, s);
+        return prefill_K<__nv_bfloat16>(K, L, bcx, rows, H, w, bias, cu, N, slots, pool, n_slots,
+                                        y, s);
+    return prefill_K<float>(K, L, bcx, rows, H, w, bias, cu, N, slots, pool, n_slots, y, s);
 }
 
 // ------------------------------------------------------------------- decode
@@ -297,8 +324,8 @@ constexpr int kDecodeThreads = SC_DECODE_THREADS;
 template <typename T, int K>
 __global__ void __launch_bounds__(kDecodeThreads)
     k_decode(const T *__restrict__ bcx, int N, int H, const T *__restrict__ w,
-             const int32_t *__restrict__ slots, T *__restrict__ pool, int n_slots,
-             T *__restrict__ y) {
+             const T *__restrict__ bias, const int32_t *__restrict__ slots,
+             T *__restrict__ pool, int n_slots, T *__restrict__ y) {
     pdl_wait();
     pdl_launch_dependents();
     const int groups = H / kCh;
@@ -308,8 +335,9 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const T *p = bcx + (int64_t)i * 3 * H + h0;
     const Row<T> rb = load_row(p), rc = load_row(p + H), rx = load_row(p + 2 * H);
     const int slot = slots[i];
-    float wt[kCh][K];
+    float wt[kCh][K], bh[kCh];
     load_block<T, K>(w + (int64_t)h0 * K, wt);
+    load_bias8<T>(bias, h0, bh);
     if (slot < 0 || slot >= n_slots) {
         if (cg == 0) raise_error(SC_DEV_BAD_SLOT);
         return;
@@ -322,39 +350,44 @@ __global__ void __launch_bounds__(kDecodeThreads)
     unpack_row(rc, c);
     unpack_row(rx, x);
 #pragma unroll
-    for (int ch = 0; ch < kCh; ++ch)
-        out[ch] = c[ch] * slide_dot<K>(win[ch], wt[ch], gate_in<T>(b[ch], x[ch]));
+    for (int ch = 0; ch < kCh; ++ch) {
+        float z = slide_dot<K>(win[ch], wt[ch], gate_in<T>(b[ch], x[ch]));
+        if (bias != nullptr) z = z + bh[ch];
+        out[ch] = c[ch] * z;
+    }
     store_row(y + (int64_t)i * H + h0, out);
     store_block<T, K>(st, win);
 }
 
 template <typename T, int K>
-static cudaError_t decode_inst(const void *bcx, int N, int H, const void *w,
+static cudaError_t decode_inst(const void *bcx, int N, int H, const void *w, const void *bias,
                                const int32_t *slots, void *pool, int n_slots, void *y,
                                cudaStream_t stream) {
     const int64_t units = (int64_t)N * (H / kCh);
     const int64_t blocks = (units + kDecodeThreads - 1) / kDecodeThreads;
     return launch_pdl(k_decode<T, K>, dim3((unsigned)blocks), dim3(kDecodeThreads), 0, stream,
-                      (const T *)bcx, N, H, (const T *)w, slots, (T *)pool, n_slots, (T *)y);
+                      (const T *)bcx, N, H, (const T *)w, (const T *)bias, slots, (T *)pool,
+                      n_slots, (T *)y);
 }
 
 template <typename T>
 static cudaError_t decode_K(int K, const void *bcx, int N, int H, const void *w,
-                            const int32_t *slots, void *pool, int n_slots, void *y,
-                            cudaStream_t s) {
+                            const void *bias, const int32_t *slots, void *pool, int n_slots,
+                            void *y, cudaStream_t s) {
     switch (K) {
-        case 1: return decode_inst<T, 1>(bcx, N, H, w, slots, pool, n_slots, y, s);
-        case 2: return decode_inst<T, 2>(bcx, N, H, w, slots, pool, n_slots, y, s);
-        case 3: return decode_inst<T, 3>(bcx, N, H, w, slots, pool, n_slots, y, s);
-        default: return decode_inst<T, 4>(bcx, N, H, w, slots, pool, n_slots, y, s);
+        case 1: return decode_inst<T, 1>(bcx, N, H, w, bias, slots, pool, n_slots, y, s);
+        case 2: return decode_inst<T, 2>(bcx, N, H, w, bias, slots, pool, n_slots, y, s);
+        case 3: return decode_inst<T, 3>(bcx, N, H, w, bias, slots, pool, n_slots, y, s);
+        default: return decode_inst<T, 4>(bcx, N, H, w, bias, slots, pool, n_slots, y, s);
     }
 }
 
 cudaError_t launch_decode(int dtype, int H, int K, const void *bcx, int N, const void *w,
-                          const int32_t *slots, void *pool, int n_slots, void *y,
-                          cudaStream_t s) {
-    if (dtype == SC_BF16) return decode_K<__nv_bfloat16>(K, bcx, N, H, w, slots, pool, n_slots, y, s);
-    return decode_K<float>(K, bcx, N, H, w, slots, pool, n_slots, y, s);
+                          const void *bias, const int32_t *slots, void *pool, int n_slots,
+                          void *y, cudaStream_t s) {
+    if (dtype == SC_BF16)
+        return decode_K<__nv_bfloat16>(K, bcx, N, H, w, bias, slots, pool, n_slots, y, s);
+    return decode_K<float>(K, bcx, N, H, w, bias, slots, pool, n_slots, y, s);
 }
 
 // ------------------------------------------------------------------- verify
@@ -369,8 +402,9 @@ constexpr int kVerifyRows = 8;
 template <typename T, int K>
 __global__ void __launch_bounds__(kVerifyThreads)
     k_verify(const T *__restrict__ bcx, int N, int D, int H, const T *__restrict__ w,
-             const int32_t *__restrict__ slots, const T *__restrict__ pool, int n_slots,
-             T *__restrict__ win_out, T *__restrict__ y) {
+             const T *__restrict__ bias, const int32_t *__restrict__ slots,
+             const T *__restrict__ pool, int n_slots, T *__restrict__ win_out,
+             T *__restrict__ y) {
     pdl_wait();
     pdl_launch_dependents();
     const int groups = H / kCh;
@@ -389,8 +423,9 @@ __global__ void __launch_bounds__(kVerifyThreads)
             rx[jj] = load_row(p + 2 * H);
         }
     }
-    float wt[kCh][K], win[kCh][K];
+    float wt[kCh][K], win[kCh][K], bh[kCh];
     load_block<T, K>(w + (int64_t)h0 * K, wt);
+    load_bias8<T>(bias, h0, bh);
     if (slot < 0 || slot >= n_slots) {
         if (cg == 0) raise_error(SC_DEV_BAD_SLOT);
         return;
@@ -417,8 +452,11 @@ __global__ void __launch_bounds__(kVerifyThreads)
                 unpack_row(rc[jj], c);
                 unpack_row(rx[jj], x);
 #pragma unroll
-                for (int ch = 0; ch < kCh; ++ch)
-                    out[ch] = c[ch] * slide_dot<K>(win[ch], wt[ch], gate_in<T>(b[ch], x[ch]));
+                for (int ch = 0; ch < kCh; ++ch) {
+                    float z = slide_dot<K>(win[ch], wt[ch], gate_in<T>(b[ch], x[ch]));
+                    if (bias != nullptr) z = z + bh[ch];
+                    out[ch] = c[ch] * z;
+                }
                 store_row(y + t * H + h0, out);
                 store_block<T, K>(win_out + (t * H + h0) * K, win);
             }
@@ -428,33 +466,33 @@ __global__ void __launch_bounds__(kVerifyThreads)
 
 template <typename T, int K>
 static cudaError_t verify_inst(const void *bcx, int N, int D, int H, const void *w,
-                               const int32_t *slots, const void *pool, int n_slots, void *win,
-                               void *y, cudaStream_t stream) {
+                               const void *bias, const int32_t *slots, const void *pool,
+                               int n_slots, void *win, void *y, cudaStream_t stream) {
     const int64_t units = (int64_t)N * (H / kCh);
     const int64_t blocks = (units + kVerifyThreads - 1) / kVerifyThreads;
     return launch_pdl(k_verify<T, K>, dim3((unsigned)blocks), dim3(kVerifyThreads), 0, stream,
-                      (const T *)bcx, N, D, H, (const T *)w, slots, (const T *)pool, n_slots,
-                      (T *)win, (T *)y);
+                      (const T *)bcx, N, D, H, (const T *)w, (const T *)bias, slots,
+                      (const T *)pool, n_slots, (T *)win, (T *)y);
 }
 
 template <typename T>
 static cudaError_t verify_K(int K, const void *bcx, int N, int D, int H, const void *w,
-                            const int32_t *slots, const void *pool, int n_slots, void *win,
-                            void *y, cudaStream_t s) {
+                            const void *bias, const int32_t *slots, const void *pool,
+                            int n_slots, void *win, void *y, cudaStream_t s) {
     switch (K) {
-        case 1: return verify_inst<T, 1>(bcx, N, D, H, w, slots, pool, n_slots, win, y, s);
-        case 2: return verify_inst<T, 2>(bcx, N, D, H, w, slots, pool, n_slots, win, y, s);
-        case 3: return verify_inst<T, 3>(bcx, N, D, H, w, slots, pool, n_slots, win, y, s);
-        default: return verify_inst<T, 4>(bcx, N, D, H, w, slots, pool, n_slots, win, y, s);
+        case 1: return verify_inst<T, 1>(bcx, N, D, H, w, bias, slots, pool, n_slots, win, y, s);
+        case 2: return verify_inst<T, 2>(bcx, N, D, H, w, bias, slots, pool, n_slots, win, y, s);
+        case 3: return verify_inst<T, 3>(bcx, N, D, H, w, bias, slots, pool, n_slots, win, y, s);
+        default: return verify_inst<T, 4>(bcx, N, D, H, w, bias, slots, pool, n_slots, win, y, s);
     }
 }
 
 cudaError_t launch_verify(int dtype, int H, int K, const void *bcx, int N, int D, const void *w,
-                          const int32_t *slots, const void *pool, int n_slots, void *win,
-                          void *y, cudaStream_t s) {
+                          const void *bias, const int32_t *slots, const void *pool, int n_slots,
+                          void *win, void *y, cudaStream_t s) {
     if (dtype == SC_BF16)
-        return verify_K<__nv_bfloat16>(K, bcx, N, D, H, w, slots, pool, n_slots, win, y, s);
-    return verify_K<float>(K, bcx, N, D, H, w, slots, pool, n_slots, win, y, s);
+        return verify_K<__nv_bfloat16>(K, bcx, N, D, H, w, bias, slots, pool, n_slots, win, y, s);
+    return verify_K<float>(K, bcx, N, D, H, w, bias, slots, pool, n_slots, win, y, s);
 }
 
 // ----------------------------------------------------------------- rollback

@@ -11,41 +11,49 @@ namespace sc {
 
 // Prefill: rows_per_thread 0 selects the TMA-streamed kernel (one CTA per SM),
 // 4/8/16/32 the register-tiled kernel with that many rows per thread.
+// bias (here and below) is the optional per-channel conv bias, NULL for none.
 cudaError_t launch_prefill(int dtype, int H, int K, const void *bcx, int64_t T, const void *w,
-                           const int32_t *cu_seqlens, int N, const int32_t *slot_ids,
-                           void *pool, int n_slots, void *y, int rows_per_thread,
-                           int sm_count, cudaStream_t stream);
+                           const void *bias, const int32_t *cu_seqlens, int N,
+                           const int32_t *slot_ids, void *pool, int n_slots, void *y,
+                           int rows_per_thread, int sm_count, cudaStream_t stream);
 
 cudaError_t launch_decode(int dtype, int H, int K, const void *bcx, int N, const void *w,
-                          const int32_t *slot_ids, void *pool, int n_slots, void *y,
-                          cudaStream_t stream);
+                          const void *bias, const int32_t *slot_ids, void *pool, int n_slots,
+                          void *y, cudaStream_t stream);
 
 cudaError_t launch_verify(int dtype, int H, int K, const void *bcx, int N, int D,
-                          const void *w, const int32_t *slot_ids, const void *pool,
-                          int n_slots, void *win, void *y, cudaStream_t stream);
+                          const void *w, const void *bias, const int32_t *slot_ids,
+                          const void *pool, int n_slots, void *win, void *y,
+                          cudaStream_t stream);
 
 cudaError_t launch_rollback(int dtype, int H, int K, int N, int D, const void *win,
                             const int32_t *accepted, const int32_t *slot_ids, void *pool,
                             int n_slots, cudaStream_t stream);
 
+// Bytes of fp32 partials the backward writes: one H*K dW block per row range,
+// plus H dbias entries per row range when dbias is wanted.
+size_t backward_partial_bytes(int H, int K, int64_t T, bool with_dbias);
+// The caller-workspace size: room for both.
 size_t backward_workspace_bytes(int H, int K, int64_t T);
 
+// dbias (fp32 [H]) is written when non-NULL.
 cudaError_t launch_backward(int dtype, int H, int K, const void *bcx, int64_t T,
-                            const void *w, const void *dy, void *dbcx, float *dw,
-                            void *workspace, cudaStream_t stream);
+                            const void *w, const void *bias, const void *dy, void *dbcx,
+                            float *dw, float *dbias, void *workspace, cudaStream_t stream);
 
 // Packed varlen backward with initial states (NULL: zeros), an optional
 // final-state gradient (NULL: zeros) and an optional initial-state gradient
 // output (NULL: not written). Same workspace size as launch_backward.
 cudaError_t launch_backward_varlen(int dtype, int H, int K, const void *bcx, int64_t T,
-                                   const void *w, const int32_t *cu_seqlens, int N,
-                                   const void *init, const void *dy, const float *d_final,
-                                   void *dbcx, float *dw, float *d_init, void *workspace,
-                                   cudaStream_t stream);
+                                   const void *w, const void *bias, const int32_t *cu_seqlens,
+                                   int N, const void *init, const void *dy,
+                                   const float *d_final, void *dbcx, float *dw, float *dbias,
+                                   float *d_init, void *workspace, cudaStream_t stream);
 
-// The backward kernels with their dW partials in the library's fixed device
-// scratch (kNoAllocScratchBytes) instead of a caller workspace. The caller
-// checks backward_workspace_bytes(H, K, T) <= kNoAllocScratchBytes first.
+// The bias-free backward kernels with their dW partials in the library's
+// fixed device scratch (kNoAllocScratchBytes) instead of a caller workspace.
+// The caller checks backward_partial_bytes(H, K, T, false) <=
+// kNoAllocScratchBytes first.
 constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;
 cudaError_t launch_backward_noalloc(int dtype, int H, int K, const void *bcx, int64_t T,
                                     const void *w, const void *dy, void *dbcx, float *dw,

@@ -67,12 +67,14 @@ constexpr size_t stream_smem_bytes(int CW) {
            (size_t)StreamShape<T>::NS * StreamShape<T>::R * 3 * CW * sizeof(T);
 }
 
-template <typename T, int K>
+// HB: a conv bias is given (bias != NULL); the bias-free instance carries no
+// bias registers or branches.
+template <typename T, int K, bool HB>
 __global__ void __launch_bounds__(kStreamSlice / kStreamCpt + 32, SC_STREAM_MIN_CTAS)
     k_prefill_stream(const T *__restrict__ bcx, int64_t T_rows, int H, const T *__restrict__ w,
-                     const int32_t *__restrict__ cu, int N, const int32_t *__restrict__ slots,
-                     T *__restrict__ pool, int n_slots, T *__restrict__ y, int n_slices,
-                     int n_row_ctas) {
+                     const T *__restrict__ bias, const int32_t *__restrict__ cu, int N,
+                     const int32_t *__restrict__ slots, T *__restrict__ pool, int n_slots,
+                     T *__restrict__ y, int n_slices, int n_row_ctas) {
     constexpr int CPT = kStreamCpt;
     constexpr int NP = CPT / 2;
     constexpr int R = StreamShape<T>::R;
@@ -113,8 +115,15 @@ __global__ void __launch_bounds__(kStreamSlice / kStreamCpt + 32, SC_STREAM_MIN_
     pdl_wait();  // everything below may read what earlier kernels in the stream wrote
     pdl_launch_dependents();
 
-    f32x2 wp[K][NP], win[K][NP];
-    if (active) load_taps<T, CPT, K>(w + (int64_t)h0 * K, wp);  // in flight during the checks
+    f32x2 wp[K][NP], win[K][NP], bp[NP];
+    if (active) {
+        load_taps<T, CPT, K>(w + (int64_t)h0 * K, wp);  // in flight during the checks
+        if constexpr (HB) {
+#pragma unroll
+            for (int q = 0; q < NP; ++q)
+                bp[q] = f2_make(ld_elem(bias + h0 + 2 * q), ld_elem(bias + h0 + 2 * q + 1));
+        }
+    }
 
     auto issue = [&](int c) {
         const int s = c % NS;
@@ -233,6 +242,7 @@ __global__ void __launch_bounds__(kStreamSlice / kStreamCpt + 32, SC_STREAM_MIN_
                 f32x2 z = f2_mul(wp[0][q], win[0][q]);
 #pragma unroll
                 for (int k = 1; k < K; ++k) z = f2_fma(wp[k][q], win[k][q], z);
+                if constexpr (HB) z = f2_fma(f2_make(1.f, 1.f), bp[q], z);  // z + b, one rounding
                 yv[q] = f2_mul(cz[q], z);
             }
             Pairs<T, CPT>::store(y + row * (int64_t)H + h0, yv);

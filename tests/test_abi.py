@@ -30,16 +30,18 @@ def L():
     path = sc_build.build()
     lib = ctypes.CDLL(path)
     p, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
-    lib.shortconv_prefill.argtypes = [i32, i32, i32, p, i64, p, p, i32, p, p, i32, p, p]
-    lib.shortconv_prefill_tiled.argtypes = [i32, i32, i32, p, i64, p, p, i32, p, p, i32, p, i32, p]
-    lib.shortconv_decode.argtypes = [i32, i32, i32, p, i32, p, p, p, i32, p, p]
-    lib.shortconv_verify.argtypes = [i32, i32, i32, p, i32, i32, p, p, p, i32, p, p, p]
+    lib.shortconv_prefill.argtypes = [i32, i32, i32, p, i64, p, p, p, i32, p, p, i32, p, p]
+    lib.shortconv_prefill_tiled.argtypes = [i32, i32, i32, p, i64, p, p, p, i32, p, p, i32, p,
+                                            i32, p]
+    lib.shortconv_decode.argtypes = [i32, i32, i32, p, i32, p, p, p, p, i32, p, p]
+    lib.shortconv_verify.argtypes = [i32, i32, i32, p, i32, i32, p, p, p, p, i32, p, p, p]
     lib.shortconv_rollback.argtypes = [i32, i32, i32, i32, i32, p, p, p, p, i32, p]
     lib.shortconv_backward_workspace_bytes.argtypes = [i32, i32, i64]
     lib.shortconv_backward_workspace_bytes.restype = ctypes.c_size_t
-    lib.shortconv_backward.argtypes = [i32, i32, i32, p, i64, p, p, p, p, p, ctypes.c_size_t, p]
-    lib.shortconv_backward_varlen.argtypes = [i32, i32, i32, p, i64, p, p, i32, p, p, p, p, p,
-                                              p, p, ctypes.c_size_t, p]
+    lib.shortconv_backward.argtypes = [i32, i32, i32, p, i64, p, p, p, p, p, p, p,
+                                       ctypes.c_size_t, p]
+    lib.shortconv_backward_varlen.argtypes = [i32, i32, i32, p, i64, p, p, p, i32, p, p, p, p,
+                                              p, p, p, p, ctypes.c_size_t, p]
     lib.shortconv_get_error.argtypes = [p, p]
     lib.shortconv_status_string.argtypes = [i32]
     lib.shortconv_status_string.restype = ctypes.c_char_p
@@ -66,9 +68,10 @@ BASE = 1 << 40
 A, Bp, Cp, Dp, Ep, Fp, Gp = (BASE + i * (1 << 32) for i in range(7))
 
 
-def prefill(L, dtype=BF16, H=256, K=3, bcx=A, T=64, w=Bp, cu=Cp, N=1, slots=Dp, pool=Ep,
-            n_slots=4, y=Fp):
-    return L.shortconv_prefill(dtype, H, K, bcx, T, w, cu, N, slots, pool, n_slots, y, None)
+def prefill(L, dtype=BF16, H=256, K=3, bcx=A, T=64, w=Bp, bias=None, cu=Cp, N=1, slots=Dp,
+            pool=Ep, n_slots=4, y=Fp):
+    return L.shortconv_prefill(dtype, H, K, bcx, T, w, bias, cu, N, slots, pool, n_slots, y,
+                               None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -87,6 +90,9 @@ def prefill(L, dtype=BF16, H=256, K=3, bcx=A, T=64, w=Bp, cu=Cp, N=1, slots=Dp, 
     (dict(cu=Cp + 2), SC_EINVAL),           # int32 array not 4-byte aligned
     (dict(y=A + 64), SC_EINVAL),            # y overlaps bcx
     (dict(pool=Bp), SC_EINVAL),             # pool overlaps w
+    (dict(bias=Gp + 8), SC_EINVAL),         # bias not 16-byte aligned
+    (dict(bias=Fp + 64), SC_EINVAL),        # bias overlaps y
+    (dict(bias=Ep), SC_EINVAL),             # bias overlaps pool
 ])
 def test_prefill_argument_errors(L, kw, status):
     assert prefill(L, **kw) == status
@@ -97,16 +103,22 @@ def test_prefill_empty_call_is_ok_without_a_device(L):
 
 
 def test_prefill_tiled_rejects_unbuilt_tiles(L):
-    st = L.shortconv_prefill_tiled(BF16, 256, 3, A, 64, Bp, Cp, 1, Dp, Ep, 4, Fp, 12, None)
+    st = L.shortconv_prefill_tiled(BF16, 256, 3, A, 64, Bp, None, Cp, 1, Dp, Ep, 4, Fp, 12, None)
     assert st == SC_EINVAL
 
 
 def test_decode_verify_rollback_argument_errors(L):
-    assert L.shortconv_decode(BF16, 256, 3, A, 4, Bp, Dp, Ep, 4, A + 16, None) == SC_EINVAL
-    assert L.shortconv_decode(BF16, 256, 3, A, 4, Bp, Dp, Ep, 0, Fp, None) == SC_EINVAL
-    assert L.shortconv_decode(BF16, 256, 3, A, 0, Bp, 0, Ep, 4, 0, None) == SC_OK
-    assert L.shortconv_verify(BF16, 256, 3, A, 4, 0, Bp, Dp, Ep, 4, Fp, Gp, None) == SC_EINVAL
-    assert L.shortconv_verify(BF16, 256, 3, A, 4, 2, Bp, Dp, Ep, 4, Fp, Fp, None) == SC_EINVAL
+    assert L.shortconv_decode(BF16, 256, 3, A, 4, Bp, None, Dp, Ep, 4, A + 16, None) == SC_EINVAL
+    assert L.shortconv_decode(BF16, 256, 3, A, 4, Bp, None, Dp, Ep, 0, Fp, None) == SC_EINVAL
+    assert L.shortconv_decode(BF16, 256, 3, A, 4, Bp, Gp + 4, Dp, Ep, 4, Fp, None) == SC_EINVAL
+    assert L.shortconv_decode(BF16, 256, 3, A, 4, Bp, Fp + 64, Dp, Ep, 4, Fp, None) == SC_EINVAL
+    assert L.shortconv_decode(BF16, 256, 3, A, 0, Bp, None, 0, Ep, 4, 0, None) == SC_OK
+    assert L.shortconv_verify(BF16, 256, 3, A, 4, 0, Bp, None, Dp, Ep, 4, Fp, Gp,
+                              None) == SC_EINVAL
+    assert L.shortconv_verify(BF16, 256, 3, A, 4, 2, Bp, None, Dp, Ep, 4, Fp, Fp,
+                              None) == SC_EINVAL
+    assert L.shortconv_verify(BF16, 256, 3, A, 4, 2, Bp, Gp, Dp, Ep, 4, Fp, Gp,
+                              None) == SC_EINVAL                       # y aliases bias
     assert L.shortconv_rollback(BF16, 256, 3, 4, 2, Fp, Cp, Dp, Fp, 4, None) == SC_EINVAL
     assert L.shortconv_rollback(F32, 256, 3, 0, 2, 0, 0, 0, Ep, 4, None) == SC_OK
 
@@ -118,26 +130,39 @@ def test_backward_workspace_and_errors(L):
     assert L.shortconv_backward_workspace_bytes(12, 3, 100) == 0
     assert L.shortconv_backward_workspace_bytes(2048, 3, -1) == 0
     need = L.shortconv_backward_workspace_bytes(256, 3, 64)
-    assert L.shortconv_backward(BF16, 256, 3, A, 64, Bp, Cp, Dp, Ep, Fp, need - 1, None) == SC_EINVAL
-    assert L.shortconv_backward(BF16, 256, 3, A, 64, Bp, Cp, A, Ep, Fp, need, None) == SC_EINVAL
+    assert need == 4 * 256 * 4 * 4      # 4 row ranges x (dW 3 + dbias 1) x H fp32
+
+    def bwd(bias=None, dbcx=Dp, dw=Ep, dbias=None, ws=Fp, wsb=need):
+        return L.shortconv_backward(BF16, 256, 3, A, 64, Bp, bias, Cp, dbcx, dw, dbias, ws, wsb,
+                                    None)
+    assert bwd(wsb=need - 1) == SC_EINVAL
+    assert bwd(dbcx=A) == SC_EINVAL                  # dbcx aliases bcx
+    assert bwd(bias=Gp + 8) == SC_EINVAL             # misaligned bias
+    assert bwd(dbias=Gp + 2) == SC_EINVAL            # misaligned dbias
+    assert bwd(dbias=Ep + 64) == SC_EINVAL           # dbias overlaps dw
+    assert bwd(bias=Gp, dbias=Gp) == SC_EINVAL       # dbias aliases bias
+    assert bwd(dbias=Fp + 16) == SC_EINVAL           # dbias inside the workspace
 
 
 def test_backward_varlen_argument_errors(L):
     need = L.shortconv_backward_workspace_bytes(256, 3, 64)
-    ok = dict(dtype=BF16, H=256, K=3, bcx=A, T=64, w=Bp, cu=Cp, N=2, init=None, dy=Dp,
-              dfin=None, dbcx=Ep, dw=Fp, dinit=None, ws=Gp, wsb=need)
+    ok = dict(dtype=BF16, H=256, K=3, bcx=A, T=64, w=Bp, bias=None, cu=Cp, N=2, init=None,
+              dy=Dp, dfin=None, dbcx=Ep, dw=Fp, dbias=None, dinit=None, ws=Gp, wsb=need)
 
     def call(**kw):
         a = dict(ok, **kw)
         return L.shortconv_backward_varlen(a["dtype"], a["H"], a["K"], a["bcx"], a["T"], a["w"],
-                                           a["cu"], a["N"], a["init"], a["dy"], a["dfin"],
-                                           a["dbcx"], a["dw"], a["dinit"], a["ws"], a["wsb"],
-                                           None)
+                                           a["bias"], a["cu"], a["N"], a["init"], a["dy"],
+                                           a["dfin"], a["dbcx"], a["dw"], a["dbias"], a["dinit"],
+                                           a["ws"], a["wsb"], None)
     assert call(N=0) == SC_EINVAL                 # rows but no sequences
     assert call(wsb=need - 1) == SC_EINVAL
     assert call(dbcx=A) == SC_EINVAL              # output aliases bcx
     assert call(dinit=Bp) == SC_EINVAL            # d_init aliases w
     assert call(K=5) == SC_EUNSUPPORTED
+    assert call(bias=Fp + 4) == SC_EINVAL         # misaligned bias
+    assert call(dbias=Bp) == SC_EINVAL            # dbias aliases w
+    assert call(dbias=Fp + 8) == SC_EINVAL        # dbias overlaps dw
 
 
 def test_status_strings_and_get_error_null(L):

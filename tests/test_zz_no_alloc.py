@@ -24,6 +24,12 @@ from gpu_util import assert_close, assert_dw_close, dev, host
 SCRATCH_LIMIT = 8 << 20  # bytes of fixed device scratch behind the call
 
 
+def partial_bytes(H, K, T):
+    """The fp32 dW partials the call keeps in its scratch, as the header states:
+    one H*K block per row range, min(ceil(T / 16), 152) row ranges."""
+    return min(max(-(-T // 16), 1), 152) * H * K * 4
+
+
 def _noalloc():
     f = sc.lib().shortconv_backward_noalloc
     p, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
@@ -50,7 +56,7 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point():
              wl.training(T=65536, H=2048, K=3, seed=302)]
     for p in cases:
         bcx, w, dy = dev(p.bcx, p.dtype), dev(p.w, p.dtype), dev(p.dy, p.dtype)
-        assert sc.backward_workspace_bytes(p.H, p.K, p.bcx.shape[0]) <= SCRATCH_LIMIT
+        assert partial_bytes(p.H, p.K, p.bcx.shape[0]) <= SCRATCH_LIMIT
         ref_dbcx, ref_dw = sc.backward(bcx, w, dy)
         got_dbcx, got_dw = call_noalloc(bcx, w, dy)
         torch.cuda.synchronize()
@@ -75,9 +81,11 @@ def test_sizes_beyond_the_scratch_are_rejected_before_any_work():
     # and the call is only made once the size is known to exceed the scratch.
     sc_build.build()
     H, K, T = 8192, 4, 1025  # first row count whose partials exceed 8 MiB at H=8192, K=4
-    assert sc.backward_workspace_bytes(H, K, T) > SCRATCH_LIMIT
-    assert sc.backward_workspace_bytes(H, K, T - 1) <= SCRATCH_LIMIT
-    assert sc.backward_workspace_bytes(2048, 3, 2**31 - 1) <= SCRATCH_LIMIT
+    assert partial_bytes(H, K, T) > SCRATCH_LIMIT
+    assert partial_bytes(H, K, T - 1) <= SCRATCH_LIMIT
+    assert partial_bytes(2048, 3, 2**31 - 1) <= SCRATCH_LIMIT
+    # the caller-workspace size also holds the bias-gradient partials
+    assert sc.backward_workspace_bytes(H, K, T) == partial_bytes(H, K, T) // K * (K + 1)
     base = 1 << 40
     st = _noalloc()(sc.SC_BF16, H, K, base, T, base + (1 << 34), base + (2 << 34),
                     base + (3 << 34), base + (4 << 34), None)
