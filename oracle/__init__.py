@@ -76,6 +76,9 @@ def _load():
             lib.orc_double_to_bf16.restype = ctypes.c_uint16
             lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
             lib.orc_bf16_to_double.restype = ctypes.c_double
+            lib.orc_round_bf16_array.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
+                                                 ctypes.c_int64]
+            lib.orc_round_bf16_array.restype = None
             _lib = lib
     return _lib
 
@@ -120,12 +123,10 @@ def _code(dtype: str):
 
 def round_bf16(values) -> np.ndarray:
     """Round doubles to bf16 bit patterns (ties to even) with the oracle's routine."""
-    lib = _load()
-    v = np.asarray(values, dtype=np.float64).ravel()
+    v = np.ascontiguousarray(values, dtype=np.float64)
     out = np.empty(v.shape, dtype=np.uint16)
-    for i, d in enumerate(v):
-        out[i] = lib.orc_double_to_bf16(float(d))
-    return out.reshape(np.shape(values))
+    _load().orc_round_bf16_array(_ptr(v), _ptr(out), v.size)
+    return out
 
 
 def bf16_to_f64(bits) -> np.ndarray:

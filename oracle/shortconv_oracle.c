@@ -83,6 +83,13 @@ uint16_t orc_double_to_bf16(double d)
 
 double orc_bf16_to_double(uint16_t b) { return bf16_bits_to_double(b); }
 
+/* orc_double_to_bf16 over an array of n values. */
+void orc_round_bf16_array(const double *in, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_double_to_bf16(in[i]);
+}
+
 static double round_to(int dt, double v)
 {
     switch (dt) {
