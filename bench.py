@@ -47,6 +47,7 @@ WORKLOAD = "ShortConv prefill, 1 sequence, T=4096 H=2048 K=3 bf16, zero state (L
 H, K, T = 2048, 3, 4096
 E = 2  # bf16 bytes
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCES = ["lfm2_gated_short_gb300/csrc/forward.cu",
                   "lfm2_gated_short_gb300/csrc/prefill_stream.cuh",
                   "lfm2_gated_short_gb300/csrc/common.cuh", "lfm2_gated_short_gb300/csrc/launch.h",
@@ -518,6 +519,65 @@ def packed_training_section(sc, device, T_=65536, reps=10):
                 bwd_gbs=bb / (b_us * 1e-6) / 1e9, fwd_bwd_ms=(f_us + b_us) / 1e3)
 
 
+def peak_bf16():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def layer_section(sc, device, T_, reps=20):
+    """The whole ShortConv layer at LFM2-1.2B width (D = H = 2048): in_proj fused
+    with the conv (tensor cores), against the same work unfused (a cuBLAS
+    projection through torch.matmul, then the conv kernel); out_proj against
+    torch.matmul."""
+    D = H
+    g = torch.Generator(device=device).manual_seed(9)
+    hidden = randn_bf16((T_, D), g, device)
+    w_in = randn_bf16((3 * H, D), g, device, D ** -0.5)
+    w_out = randn_bf16((D, H), g, device, H ** -0.5)
+    w = randn_bf16((H, K), g, device, wl.WEIGHT_STD)
+    cu = torch.tensor([0, T_], dtype=torch.int32, device=device)
+    slot = torch.zeros(1, dtype=torch.int32, device=device)
+    pool = torch.zeros((1, H, K), dtype=torch.bfloat16, device=device)
+    y = torch.empty((T_, H), dtype=torch.bfloat16, device=device)
+    bcx = torch.empty((T_, 3 * H), dtype=torch.bfloat16, device=device)
+    out = torch.empty((T_, D), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(max(16, sc.in_proj_workspace_bytes(H, K, 1)), dtype=torch.uint8,
+                     device=device)
+
+    def fused(i):
+        sc.in_proj_prefill(hidden, w_in, w, cu, slot, pool, y=y, workspace=ws)
+
+    def unfused(i):
+        torch.matmul(hidden, w_in.t(), out=bcx)
+        sc.prefill(bcx, w, cu, slot, pool, y=y)
+
+    def ours_out(i):
+        sc.out_proj(y, w_out, out=out)
+
+    def torch_out(i):
+        torch.matmul(y, w_out.t(), out=out)
+
+    for f in (fused, unfused, ours_out, torch_out):
+        for i in range(3):
+            f(i)
+    torch.cuda.synchronize()
+    us = {f.__name__: time_loop(f, reps) for f in (fused, unfused, ours_out, torch_out)}
+    assert sc.get_error() == 0
+    peak, src = peak_bf16()
+    f_in, f_out = 2.0 * T_ * 3 * H * D, 2.0 * T_ * D * H
+    tf = lambda flops, u: flops / (u * 1e-6) / 1e12
+    return dict(T=T_, D=D, H=H, fused_in_proj_conv_us=us["fused"],
+                fused_tflops=tf(f_in, us["fused"]), fused_frac=tf(f_in, us["fused"]) / peak,
+                unfused_matmul_plus_conv_us=us["unfused"],
+                out_proj_us=us["ours_out"], out_proj_tflops=tf(f_out, us["ours_out"]),
+                out_proj_frac=tf(f_out, us["ours_out"]) / peak,
+                torch_matmul_out_proj_us=us["torch_out"], peak_tflops=peak,
+                peak_source=f"{src} bf16_tflops")
+
+
 def cpu_baseline(seconds=10.0):
     """The CPU oracle as it stands, single-threaded, on the headline workload."""
     import oracle
@@ -633,6 +693,8 @@ def main():
     extras["train_T4096_bias"] = training_section(sc, device, 4096, 20, 4, bias=True)
     extras["train_T65536_bias"] = training_section(sc, device, 65536, 10, 1, bias=True)
     extras["train_packed_T65536"] = packed_training_section(sc, device)
+    extras["layer_T4096"] = layer_section(sc, device, 4096)
+    extras["layer_T16384"] = layer_section(sc, device, 16384, reps=10)
     clk = clocks.stop()
     del flush_buf
     torch.cuda.empty_cache()

@@ -288,6 +288,52 @@ sc_status shortconv_backward_noalloc(sc_dtype dtype, int H, int K, const void *b
                                      void *stream);
 
 /*
+ * The layer's projections on the tensor cores (bf16 only).
+ *
+ * The MAX LFM2 article (section "短卷积实现（LFM2ShortConv）") gives the
+ * layer: in_proj maps the hidden state to three parts b, c, xv; bx = b * xv
+ * goes through the causal conv; y = c * conv_out goes through out_proj.
+ * Neither projection has a bias there. A projection from n to m features
+ * has the weight [m, n] (row-major), so in_proj's is [3H, D] (rows 0..H-1
+ * give b, H..2H-1 c, 2H..3H-1 xv) and out_proj's is [D, H].
+ *
+ * shortconv_in_proj_prefill computes in_proj and the whole packed varlen
+ * prefill of shortconv_prefill in one pass: the [T, 3H] projection is
+ * accumulated in fp32, rounded to bf16 (the values a separate in_proj
+ * would store) and consumed in the GEMM's epilogue; it never reaches
+ * memory. Results are those of shortconv_prefill on that projection, so
+ * they differ from in_proj followed by shortconv_prefill only where the
+ * fp32 accumulation order of the projection changes a bf16 rounding.
+ *
+ *   D, H, K      model width (D % 64 == 0), channels (H % 64 == 0), taps
+ *   hidden       device [T, D] bf16            read
+ *   w_in         device [3H, D] bf16           read
+ *   w, bias      as shortconv_prefill (bias [H] or NULL)
+ *   cu_seqlens, N, slot_ids, pool, n_slots, y: as shortconv_prefill
+ *   workspace    device scratch of at least
+ *                shortconv_in_proj_workspace_bytes(H, K, N) bytes, 16-byte
+ *                aligned, owned by the caller (the last K values of u per
+ *                sequence, from which the slots' new states are written
+ *                after all rows are done)
+ * Device errors: as shortconv_prefill, plus SC_DEV_TIMEOUT (a bounded wait
+ * on a tensor copy or on the tensor cores gave up; output incomplete).
+ */
+size_t shortconv_in_proj_workspace_bytes(int H, int K, int N);
+sc_status shortconv_in_proj_prefill(sc_dtype dtype, int D, int H, int K, const void *hidden,
+                                    int64_t T, const void *w_in, const void *w, const void *bias,
+                                    const int32_t *cu_seqlens, int N, const int32_t *slot_ids,
+                                    void *pool, int n_slots, void *y, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
+/*
+ * out_proj: out = y w_out^T, fp32 accumulation, rounded once to bf16.
+ *   y [T, H] bf16 read (H % 64 == 0); w_out [D, H] bf16 read
+ *   (D % 256 == 0); out [T, D] bf16 written.
+ */
+sc_status shortconv_out_proj(sc_dtype dtype, int H, int D, const void *y, int64_t T,
+                             const void *w_out, void *out, void *stream);
+
+/*
  * Conv-state slot pool on the device (MAX LFM2 article, section "推理状态管理：
  * ConvStateCache 与卷积状态生命周期": a request claims a free slot -- an error
  * when none is free --, starts from a zero state, and releases the slot when

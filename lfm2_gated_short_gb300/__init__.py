@@ -64,6 +64,11 @@ def lib() -> ctypes.CDLL:
                                              ctypes.c_size_t, p]
             L.shortconv_backward_varlen.argtypes = [i32, i32, i32, p, i64, p, p, p, i32, p, p,
                                                     p, p, p, p, p, p, ctypes.c_size_t, p]
+            L.shortconv_in_proj_workspace_bytes.argtypes = [i32, i32, i32]
+            L.shortconv_in_proj_workspace_bytes.restype = ctypes.c_size_t
+            L.shortconv_in_proj_prefill.argtypes = [i32, i32, i32, i32, p, i64, p, p, p, p, i32,
+                                                    p, p, i32, p, p, ctypes.c_size_t, p]
+            L.shortconv_out_proj.argtypes = [i32, i32, i32, p, i64, p, p, p]
             L.shortconv_slots_claim.argtypes = [p, i32, i32, p, i32, i32, i32, p, p]
             L.shortconv_slots_release.argtypes = [p, i32, p, i32, p]
             L.shortconv_pool_copy.argtypes = [i32, i32, i32, p, i32, p, p, i32, p]
@@ -71,8 +76,8 @@ def lib() -> ctypes.CDLL:
             L.shortconv_status_string.argtypes = [i32]
             L.shortconv_status_string.restype = ctypes.c_char_p
             for f in ("prefill", "prefill_tiled", "decode", "verify", "rollback", "backward",
-                      "backward_varlen", "slots_claim", "slots_release", "pool_copy",
-                      "get_error"):
+                      "backward_varlen", "in_proj_prefill", "out_proj", "slots_claim",
+                      "slots_release", "pool_copy", "get_error"):
                 getattr(L, "shortconv_" + f).restype = i32
             _lib = L
     return _lib
@@ -262,6 +267,48 @@ def backward_varlen(bcx, w, cu_seqlens, dy, init_states=None, d_final=None, dbcx
         _dev(dw, "dw", torch.float32, (H, K)), db_p, dini_p, _dev(workspace, "workspace"),
         workspace.numel(), _stream(stream, bcx.device)))
     return (dbcx, dw, d_init, dbias) if with_dbias else (dbcx, dw, d_init)
+
+
+def in_proj_workspace_bytes(H: int, K: int, N: int) -> int:
+    return int(lib().shortconv_in_proj_workspace_bytes(H, K, N))
+
+
+def in_proj_prefill(hidden, w_in, w, cu_seqlens, slot_ids, pool, y=None, bias=None,
+                    workspace=None, stream=None):
+    """in_proj fused with the packed varlen prefill (bf16); updates ``pool`` and
+    returns ``y [T, H]``. ``hidden [T, D]``, ``w_in [3H, D]`` (rows b | c | xv)."""
+    dt = torch.bfloat16
+    T, D = hidden.shape
+    H, K = w.shape
+    N = slot_ids.shape[0]
+    need = in_proj_workspace_bytes(H, K, N)
+    if y is None:
+        y = torch.empty((T, H), dtype=dt, device=hidden.device)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=hidden.device)
+    if workspace.dtype != torch.uint8 or workspace.numel() < need:
+        raise ValueError(f"workspace must be a uint8 tensor of at least {need} bytes")
+    _raise_on("shortconv_in_proj_prefill", lib().shortconv_in_proj_prefill(
+        _dcode(hidden), D, H, K, _dev(hidden, "hidden", dt), T,
+        _dev(w_in, "w_in", dt, (3 * H, D)), _dev(w, "w", dt), _bias(bias, dt, H),
+        _dev(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,)), N,
+        _dev(slot_ids, "slot_ids", torch.int32, (N,)),
+        _dev(pool, "pool", dt, (pool.shape[0], H, K)), pool.shape[0], _dev(y, "y", dt, (T, H)),
+        _dev(workspace, "workspace"), workspace.numel(), _stream(stream, hidden.device)))
+    return y
+
+
+def out_proj(y, w_out, out=None, stream=None):
+    """out = y w_out^T (bf16, fp32 accumulation): ``y [T, H]``, ``w_out [D, H]``."""
+    dt = torch.bfloat16
+    T, H = y.shape
+    D = w_out.shape[0]
+    if out is None:
+        out = torch.empty((T, D), dtype=dt, device=y.device)
+    _raise_on("shortconv_out_proj", lib().shortconv_out_proj(
+        _dcode(y), H, D, _dev(y, "y", dt), T, _dev(w_out, "w_out", dt, (D, H)),
+        _dev(out, "out", dt, (T, D)), _stream(stream, y.device)))
+    return out
 
 
 def slot_bitmap(n_slots: int, device="cuda") -> torch.Tensor:

@@ -274,6 +274,62 @@ sc_status shortconv_backward_noalloc(sc_dtype dtype, int H, int K, const void *b
                                                  (cudaStream_t)stream));
 }
 
+size_t shortconv_in_proj_workspace_bytes(int H, int K, int N) {
+    if (H <= 0 || H % 64 != 0 || K <= 0 || K > 4 || N < 0) return 0;
+    return sc::in_proj_workspace_bytes(H, K, N);
+}
+
+sc_status shortconv_in_proj_prefill(sc_dtype dtype, int D, int H, int K, const void *hidden,
+                                    int64_t T, const void *w_in, const void *w, const void *bias,
+                                    const int32_t *cu_seqlens, int N, const int32_t *slot_ids,
+                                    void *pool, int n_slots, void *y, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
+    if (dtype != SC_BF16 && dtype != SC_F32) return SC_EUNSUPPORTED;
+    if (D <= 0 || H <= 0 || K <= 0) return SC_EINVAL;
+    if (dtype != SC_BF16 || D % 64 != 0 || H % 64 != 0 || K > 4) return SC_EUNSUPPORTED;
+    if ((int64_t)H * 3 > INT32_MAX / 2 || D > INT32_MAX / 2) return SC_EUNSUPPORTED;
+    if (T < 0 || T > INT32_MAX || N < 0 || n_slots <= 0) return SC_EINVAL;
+    if (N == 0 && T != 0) return SC_EINVAL;
+    const size_t n_h = (size_t)T * D * 2, n_win = (size_t)3 * H * D * 2, n_w = (size_t)H * K * 2;
+    const size_t n_y = (size_t)T * H * 2, n_pool = (size_t)n_slots * H * K * 2;
+    const size_t need = sc::in_proj_workspace_bytes(H, K, N);
+    if (workspace_bytes < need) return SC_EINVAL;
+    if (!ptr_ok(hidden, n_h, 16) || !ptr_ok(w_in, n_win, 16) || !ptr_ok(w, n_w, 16) ||
+        !ptr_ok(y, n_y, 16) || !ptr_ok(pool, n_pool, 16) || !ptr_ok(workspace, need, 16) ||
+        !ptr_ok(cu_seqlens, (size_t)(N + 1) * 4, 4) || !ptr_ok(slot_ids, (size_t)N * 4, 4) ||
+        !opt_ok(bias, 16))
+        return SC_EINVAL;
+    const void *ins[6] = {hidden, w_in, w, bias, cu_seqlens, slot_ids};
+    const size_t nins[6] = {n_h, n_win, n_w, bias ? (size_t)H * 2 : 0, (size_t)(N + 1) * 4,
+                            (size_t)N * 4};
+    const void *outs[3] = {y, pool, workspace};
+    const size_t nouts[3] = {n_y, n_pool, need};
+    for (int o = 0; o < 3; ++o) {
+        for (int i = 0; i < 6; ++i)
+            if (overlaps(outs[o], nouts[o], ins[i], nins[i])) return SC_EINVAL;
+        for (int p = o + 1; p < 3; ++p)
+            if (overlaps(outs[o], nouts[o], outs[p], nouts[p])) return SC_EINVAL;
+    }
+    if (N == 0) return SC_OK;
+    return from_cuda(sc::launch_in_proj_prefill(D, H, K, hidden, T, w_in, w, bias, cu_seqlens, N,
+                                                slot_ids, pool, n_slots, y, workspace,
+                                                (cudaStream_t)stream));
+}
+
+sc_status shortconv_out_proj(sc_dtype dtype, int H, int D, const void *y, int64_t T,
+                             const void *w_out, void *out, void *stream) {
+    if (dtype != SC_BF16 && dtype != SC_F32) return SC_EUNSUPPORTED;
+    if (D <= 0 || H <= 0) return SC_EINVAL;
+    if (dtype != SC_BF16 || H % 64 != 0 || D % 256 != 0) return SC_EUNSUPPORTED;
+    if (H > INT32_MAX / 2 || D > INT32_MAX / 2) return SC_EUNSUPPORTED;
+    if (T < 0 || T > INT32_MAX) return SC_EINVAL;
+    const size_t n_y = (size_t)T * H * 2, n_wo = (size_t)D * H * 2, n_out = (size_t)T * D * 2;
+    if (!ptr_ok(y, n_y, 16) || !ptr_ok(w_out, n_wo, 16) || !ptr_ok(out, n_out, 16))
+        return SC_EINVAL;
+    if (overlaps(out, n_out, y, n_y) || overlaps(out, n_out, w_out, n_wo)) return SC_EINVAL;
+    return from_cuda(sc::launch_out_proj(H, D, y, T, w_out, out, (cudaStream_t)stream));
+}
+
 sc_status shortconv_slots_claim(uint32_t *in_use, int n_slots, int n_claim, int32_t *slots_out,
                                 sc_dtype dtype, int H, int K, void *pool, void *stream) {
     if (n_slots <= 0 || n_claim < 0 || n_claim > n_slots) return SC_EINVAL;

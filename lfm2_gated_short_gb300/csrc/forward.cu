@@ -534,15 +534,16 @@ cudaError_t launch_rollback(int dtype, int H, int K, int N, int D, const void *w
 // ------------------------------------------------------------ error word
 
 cudaError_t read_and_clear_error(cudaStream_t stream, unsigned int *code) {
-    unsigned int a = 0, b = 0;  // forward, backward and slot-pool words
+    unsigned int a = 0, b = 0, c = 0, d = 0;  // forward, backward, slot-pool, projection words
     cudaError_t e = take_error_here(stream, &a);
     if (e != cudaSuccess) return e;
     e = take_error_backward(stream, &b);
     if (e != cudaSuccess) return e;
-    unsigned int c = 0;
     e = take_error_slots(stream, &c);
     if (e != cudaSuccess) return e;
-    *code = a | b | c;
+    e = take_error_proj(stream, &d);
+    if (e != cudaSuccess) return e;
+    *code = a | b | c | d;
     return cudaSuccess;
 }
 

@@ -59,6 +59,19 @@ cudaError_t launch_backward_noalloc(int dtype, int H, int K, const void *bcx, in
                                     const void *w, const void *dy, void *dbcx, float *dw,
                                     cudaStream_t stream);
 
+// The layer's projections (bf16): in_proj fused with the ShortConv, writing y
+// and, through k_commit_states, the slots' new states (workspace: the last K
+// values of u per sequence, in_proj_workspace_bytes); out_proj a plain GEMM.
+size_t in_proj_workspace_bytes(int H, int K, int N);
+cudaError_t launch_in_proj_prefill(int D, int H, int K, const void *hidden, int64_t T,
+                                   const void *w_in, const void *w, const void *bias,
+                                   const int32_t *cu_seqlens, int N, const int32_t *slot_ids,
+                                   void *pool, int n_slots, void *y, void *workspace,
+                                   cudaStream_t stream);
+cudaError_t launch_out_proj(int H, int D, const void *y, int64_t T, const void *w_out, void *out,
+                            cudaStream_t stream);
+cudaError_t take_error_proj(cudaStream_t stream, unsigned int *code);
+
 // Take (read and clear) the backward translation unit's error word.
 cudaError_t take_error_backward(cudaStream_t stream, unsigned int *code);
 

@@ -1,0 +1,143 @@
+// tcgen05.cuh -- 5th-generation tensor core (tcgen05), tensor memory (TMEM)
+// and tiled bulk tensor copy (TMA) helpers for sm_100-family GPUs (inline PTX).
+//
+// Operand tiles are K-major bf16 with the 128-byte swizzle: a row holds 64
+// consecutive K values (128 B), 8 rows form a 1024-byte swizzle atom, atoms
+// follow each other along M (or N). A 2-D tiled TMA copy with
+// CU_TENSOR_MAP_SWIZZLE_128B and a {64, rows} box writes exactly this layout
+// into shared memory (base 1024-byte aligned).
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "tma.cuh"
+
+namespace sc {
+
+// ------------------------------------------------------------ tiled TMA
+
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Copy the box at element coordinates (x = inner, y = outer) of `map` into
+// shared memory at `dst`, completing `bytes` on the mbarrier. x must be a
+// multiple of 8 (16 bytes of bf16); y may be negative or past the end (the
+// box is zero-filled there).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+// ------------------------------------------------------------ descriptors
+
+// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled tile whose
+// 8-row atoms are 1024 bytes apart: start address >> 4 in bits [0, 14),
+// leading byte offset (unused by this layout; 16 B) in [16, 30), stride byte
+// offset 1024 >> 4 in [32, 46), descriptor version 1 in [46, 48), swizzle
+// mode 2 (128 B) in [61, 64). Adding 2 to the descriptor moves the start 32
+// bytes (16 bf16) along K inside the swizzle atom.
+__device__ __forceinline__ uint64_t sdesc_k128(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B (both K-major) and an
+// fp32 accumulator: D format 1 (f32) in bits [4, 6), A format 1 (bf16) in
+// [7, 10), B format 1 (bf16) in [10, 13), N >> 3 in [17, 23), M >> 4 in
+// [24, 29).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// ------------------------------------------------------------ TMEM
+
+// Allocate `ncols` TMEM columns (a power of two >= 32); the whole warp calls
+// this; the TMEM address is written to *slot (shared memory).
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+// Free what tmem_alloc took; the whole warp that allocated calls this.
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one M x N x 16 step; issued by one thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far
+// has completed.
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(bar))
+        : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane (warp-collective;
+// taddr = base + (first lane of the warp's quarter << 16) + column).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Named barrier over `count` threads (ids 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// OR of `pred` over the `count` threads of named barrier `id`.
+__device__ __forceinline__ bool named_or(int id, int count, bool pred) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(out)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return out != 0;
+}
+
+}  // namespace sc

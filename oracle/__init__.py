@@ -126,7 +126,7 @@ def round_bf16(values) -> np.ndarray:
     v = np.ascontiguousarray(values, dtype=np.float64)
     out = np.empty(v.shape, dtype=np.uint16)
     _load().orc_round_bf16_array(_ptr(v), _ptr(out), v.size)
-    return out
+    return out.reshape(np.shape(values))
 
 
 def bf16_to_f64(bits) -> np.ndarray:

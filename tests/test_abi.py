@@ -42,6 +42,11 @@ def L():
                                        ctypes.c_size_t, p]
     lib.shortconv_backward_varlen.argtypes = [i32, i32, i32, p, i64, p, p, p, i32, p, p, p, p,
                                               p, p, p, p, ctypes.c_size_t, p]
+    lib.shortconv_in_proj_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.shortconv_in_proj_workspace_bytes.restype = ctypes.c_size_t
+    lib.shortconv_in_proj_prefill.argtypes = [i32, i32, i32, i32, p, i64, p, p, p, p, i32, p, p,
+                                              i32, p, p, ctypes.c_size_t, p]
+    lib.shortconv_out_proj.argtypes = [i32, i32, i32, p, i64, p, p, p]
     lib.shortconv_get_error.argtypes = [p, p]
     lib.shortconv_status_string.argtypes = [i32]
     lib.shortconv_status_string.restype = ctypes.c_char_p
@@ -163,6 +168,45 @@ def test_backward_varlen_argument_errors(L):
     assert call(bias=Fp + 4) == SC_EINVAL         # misaligned bias
     assert call(dbias=Bp) == SC_EINVAL            # dbias aliases w
     assert call(dbias=Fp + 8) == SC_EINVAL        # dbias overlaps dw
+
+
+def test_in_proj_prefill_argument_errors(L):
+    need = L.shortconv_in_proj_workspace_bytes(128, 3, 2)
+    assert need == 2 * 128 * 3 * 2
+    assert L.shortconv_in_proj_workspace_bytes(100, 3, 2) == 0
+    ok = dict(dtype=BF16, D=256, H=128, K=3, hid=A, T=64, w_in=Bp, w=Cp, bias=None, cu=Dp, N=2,
+              slots=Dp + 4096, pool=Ep, n_slots=4, y=Fp, ws=Gp, wsb=need)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return L.shortconv_in_proj_prefill(a["dtype"], a["D"], a["H"], a["K"], a["hid"], a["T"],
+                                           a["w_in"], a["w"], a["bias"], a["cu"], a["N"],
+                                           a["slots"], a["pool"], a["n_slots"], a["y"], a["ws"],
+                                           a["wsb"], None)
+    assert call(dtype=F32) == SC_EUNSUPPORTED      # bf16 only
+    assert call(D=100) == SC_EUNSUPPORTED          # D % 64
+    assert call(H=72) == SC_EUNSUPPORTED           # H % 64
+    assert call(K=5) == SC_EUNSUPPORTED
+    assert call(K=0) == SC_EINVAL
+    assert call(N=0) == SC_EINVAL                  # rows but no sequences
+    assert call(wsb=need - 1) == SC_EINVAL
+    assert call(hid=A + 8) == SC_EINVAL            # not 16-byte aligned
+    assert call(y=A) == SC_EINVAL                  # y aliases hidden
+    assert call(pool=Bp) == SC_EINVAL              # pool overlaps w_in
+    assert call(ws=Fp + 64) == SC_EINVAL           # workspace overlaps y
+    assert call(bias=Fp + 32) == SC_EINVAL         # y overlaps bias
+    assert call(T=0, N=0, hid=0, y=0) == SC_OK     # nothing to do
+
+
+def test_out_proj_argument_errors(L):
+    def call(dtype=BF16, H=128, D=512, y=A, T=64, wo=Bp, out=Cp):
+        return L.shortconv_out_proj(dtype, H, D, y, T, wo, out, None)
+    assert call(dtype=F32) == SC_EUNSUPPORTED
+    assert call(D=300) == SC_EUNSUPPORTED          # D % 256
+    assert call(H=100) == SC_EUNSUPPORTED          # H % 64
+    assert call(T=-1) == SC_EINVAL
+    assert call(out=A + 1024) == SC_EINVAL         # out overlaps y
+    assert call(wo=Bp + 8) == SC_EINVAL            # misaligned
 
 
 def test_status_strings_and_get_error_null(L):

@@ -1,0 +1,261 @@
+"""The layer's projections on the GPU (tensor cores) against the layer oracle.
+
+shortconv_in_proj_prefill computes in_proj (fp32 accumulation on the tensor
+cores), rounds the projection to bf16 and runs the ShortConv in the GEMM's
+epilogue. With dyadic inputs (small integers times powers of two, bounded so
+that every partial sum of the projection is exact in fp32), the projection is
+exact in any accumulation order. Then its bf16 rounding is the oracle's, the
+states must match bit for bit and y must meet the bf16 tolerance. With
+normal inputs the projection is exact only up to fp32 accumulation error: a
+projection value within that error of a bf16 rounding boundary may round
+either way, and outputs that use such a value are excluded (they are
+counted, and rare).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import layer
+import lfm2_gated_short_gb300 as sc
+from gpu_util import assert_bits, assert_close, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+def dyadic(rng, shape, lim, exp):
+    """Integers in [-lim, lim] times 2**exp, as bf16 bits (exact)."""
+    return oracle.round_bf16(rng.integers(-lim, lim, size=shape, endpoint=True) * 2.0 ** exp)
+
+
+def make_case(rng, lengths, D, H, K, extra_slots=5, exact=True, state=True):
+    lengths = np.asarray(lengths, np.int64)
+    cu = np.r_[0, np.cumsum(lengths)].astype(np.int32)
+    T, N = int(cu[-1]), len(lengths)
+    if exact:  # products are multiples of 2^-9 below 2^-3, sums of D <= 4096 are exact
+        hidden = dyadic(rng, (T, D), 8, -3)
+        w_in = dyadic(rng, (3 * H, D), 8, -6)
+    else:
+        hidden = oracle.round_bf16(rng.standard_normal((T, D)))
+        w_in = oracle.round_bf16(rng.standard_normal((3 * H, D)) / np.sqrt(D))
+    w = oracle.round_bf16(rng.standard_normal((H, K)) * np.sqrt(1 / 3))
+    n_slots = N + extra_slots
+    slots = rng.permutation(n_slots)[:N].astype(np.int32)
+    pool = np.full((n_slots, H, K), 0xDEAD, np.uint16)  # untouched slots keep this
+    for s in slots:
+        pool[s] = oracle.round_bf16(rng.standard_normal((H, K))) if state else 0
+    return dict(hidden=hidden, w_in=w_in, w=w, cu=cu, slots=slots, pool=pool, D=D, H=H, K=K)
+
+
+def run_gpu(c, bias=None):
+    pool = dev(c["pool"], "bf16")
+    y = sc.in_proj_prefill(dev(c["hidden"], "bf16"), dev(c["w_in"], "bf16"), dev(c["w"], "bf16"),
+                           dev(c["cu"], "i32"), dev(c["slots"], "i32"), pool,
+                           bias=None if bias is None else dev(bias, "bf16"))
+    torch.cuda.synchronize()
+    return host(y), host(pool)
+
+
+def run_oracle(c, bias=None):
+    pool = c["pool"].copy()
+    st, y = layer.in_proj_prefill("bf16", c["hidden"], c["w_in"], c["w"], c["cu"], c["slots"],
+                                  pool, bias=bias)
+    assert st == oracle.OK
+    return y, pool
+
+
+def test_tiny_single_tile():
+    c = make_case(np.random.default_rng(800), [50], 64, 64, 3, state=False)
+    y, pool = run_gpu(c)
+    y_ref, pool_ref = run_oracle(c)
+    assert sc.get_error() == 0
+    assert_close("bf16", y, y_ref, "y")
+    assert_bits(pool, pool_ref, "pool")
+
+
+TILE_EDGE_LENGTHS = [1, 2, 0, 130, 5, 126, 127, 128, 3, 260, 0, 4]
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
+def test_varlen_exact_inputs(K):
+    c = make_case(np.random.default_rng(810 + K), TILE_EDGE_LENGTHS, 128, 128, K)
+    y, pool = run_gpu(c)
+    y_ref, pool_ref = run_oracle(c)
+    assert sc.get_error() == 0
+    assert_close("bf16", y, y_ref, "y")
+    assert_bits(pool, pool_ref, "pool (states bit-exact, untouched slots unchanged)")
+
+
+def test_varlen_exact_inputs_with_bias():
+    rng = np.random.default_rng(820)
+    c = make_case(rng, TILE_EDGE_LENGTHS, 192, 256, 3)
+    b = oracle.round_bf16(rng.standard_normal(256) * 0.5)
+    y, pool = run_gpu(c, b)
+    y_ref, pool_ref = run_oracle(c, b)
+    assert_close("bf16", y, y_ref, "y")
+    assert_bits(pool, pool_ref, "pool")
+
+
+def test_fused_equals_the_conv_kernel_on_the_same_projection():
+    """With an exact projection, the fused epilogue gives the bits of the
+    streamed prefill kernel run on the projection (same operation order)."""
+    c = make_case(np.random.default_rng(830), TILE_EDGE_LENGTHS, 128, 192, 3)
+    y, pool = run_gpu(c)
+    bcx = layer.in_proj("bf16", c["hidden"], c["w_in"])
+    pool2 = dev(c["pool"], "bf16")
+    y2 = sc.prefill(dev(bcx, "bf16"), dev(c["w"], "bf16"), dev(c["cu"], "i32"),
+                    dev(c["slots"], "i32"), pool2)
+    torch.cuda.synchronize()
+    assert_bits(y, host(y2), "y")
+    assert_bits(pool, host(pool2), "pool")
+
+
+def test_one_token_per_sequence_equals_decode():
+    rng = np.random.default_rng(840)
+    c = make_case(rng, [1] * 37, 128, 128, 3)
+    y, pool = run_gpu(c)
+    bcx = layer.in_proj("bf16", c["hidden"], c["w_in"])
+    pool2 = dev(c["pool"], "bf16")
+    y2 = sc.decode(dev(bcx, "bf16"), dev(c["w"], "bf16"), dev(c["slots"], "i32"), pool2)
+    torch.cuda.synchronize()
+    assert_bits(y, host(y2), "y")
+    assert_bits(pool, host(pool2), "pool")
+
+
+def test_lfm2_shape_T4096_D2048_H2048_sampled_channels():
+    """One 4096-token sequence at LFM2-1.2B's width; oracle on 64 channels."""
+    rng = np.random.default_rng(850)
+    D = H = 2048
+    c = make_case(rng, [4096], D, H, 3, extra_slots=0, state=False)
+    y, pool = run_gpu(c)
+    ch = np.sort(np.concatenate([[0, 63, 64, 1023, 1024, 2047],
+                                 rng.choice(np.arange(65, 2040), 58, replace=False)]))
+    rows = np.concatenate([ch, H + ch, 2 * H + ch])
+    sub = dict(c, w_in=c["w_in"][rows], w=np.ascontiguousarray(c["w"][ch]),
+               pool=np.ascontiguousarray(c["pool"][:, ch]))
+    y_ref, pool_ref = run_oracle(sub)
+    assert_close("bf16", y[:, ch], y_ref, "y")
+    assert_bits(pool[:, ch], pool_ref, "pool")
+
+
+def _ambiguous(exact, bound):
+    """True where [exact - bound, exact + bound] holds a bf16 rounding boundary
+    (rounding is monotone, so exactly where its two ends round apart)."""
+    return oracle.round_bf16(exact - bound) != oracle.round_bf16(exact + bound)
+
+
+def test_normal_inputs_outside_rounding_ambiguity():
+    """Normal inputs: outputs whose projection values are all farther than the
+    accumulation bound from a bf16 rounding boundary meet the tolerance; their
+    states match bit for bit."""
+    rng = np.random.default_rng(860)
+    D, H, K = 128, 128, 3
+    c = make_case(rng, [200, 0, 3, 333, 64], D, H, K, exact=False)
+    y, pool = run_gpu(c)
+    y_ref, pool_ref = run_oracle(c)
+    h = oracle.bf16_to_f64(c["hidden"])
+    wi = oracle.bf16_to_f64(c["w_in"])
+    exact = h @ wi.T
+    # fp32 accumulation of D products: |error| <= lam sqrt(D) 2^-24 sum|terms| except
+    # with probability below 2 exp(-lam^2 / 2) (Higham and Mary's probabilistic
+    # rounding-error bound); lam = 8 puts that below 1e-13 per sum. The worst-case
+    # bound (D in place of lam sqrt(D)) spans a quarter of a bf16 step here and
+    # would exclude nearly every output. The ambiguous share grows with D.
+    bound = 8 * np.sqrt(D) * 2.0 ** -24 * (np.abs(h) @ np.abs(wi).T)
+    amb = _ambiguous(exact, bound)
+    amb_b, amb_c, amb_x = amb[:, :H], amb[:, H:2 * H], amb[:, 2 * H:]
+    u_amb = amb_b | amb_x
+    T = y.shape[0]
+    bad_in = np.zeros((T, H), bool)  # output (t, h) uses C_t and u of rows t-K+1 .. t
+    for k in range(K):
+        bad_in[k:] |= u_amb[:T - k] if k else u_amb
+    bad_in |= amb_c
+    keep = ~bad_in
+    assert keep.mean() > 0.5, keep.mean()  # each output uses 2K + 1 projection values
+    g, r = oracle.bf16_to_f64(y), oracle.bf16_to_f64(y_ref)
+    ok = np.abs(g - r) <= 1e-2 + 2.0 ** -7 * np.abs(r)
+    assert ok[keep].all(), f"{int((~ok[keep]).sum())} unambiguous outputs out of tolerance"
+    # states: the last K u of each sequence, where unambiguous
+    cu = c["cu"]
+    for i, s in enumerate(c["slots"]):
+        n = cu[i + 1] - cu[i]
+        for m in range(K):
+            t = cu[i + 1] - K + m
+            if n + m < K or t < cu[i]:
+                continue
+            sel = ~u_amb[t]
+            np.testing.assert_array_equal(pool[s, sel, m], pool_ref[s, sel, m])
+
+
+def test_errors_write_nothing():
+    rng = np.random.default_rng(870)
+    c = make_case(rng, [5, 9, 4], 64, 64, 3)
+    bad = c["cu"].copy()
+    bad[1], bad[2] = 9, 5  # not non-decreasing
+    pool = dev(c["pool"], "bf16")
+    y0 = torch.full((18, 64), 3.0, dtype=torch.bfloat16, device="cuda")
+    sc.in_proj_prefill(dev(c["hidden"], "bf16"), dev(c["w_in"], "bf16"), dev(c["w"], "bf16"),
+                       dev(bad, "i32"), dev(c["slots"], "i32"), pool, y=y0)
+    assert sc.get_error() == sc.DEV_BAD_SEQLENS
+    assert np.all(host(y0) == np.uint16(0x4040))
+    assert_bits(host(pool), c["pool"], "pool")
+    # a bad slot skips that sequence only
+    slots = c["slots"].copy()
+    slots[1] = 10 ** 6
+    y1 = torch.full((18, 64), 3.0, dtype=torch.bfloat16, device="cuda")
+    pool = dev(c["pool"], "bf16")
+    sc.in_proj_prefill(dev(c["hidden"], "bf16"), dev(c["w_in"], "bf16"), dev(c["w"], "bf16"),
+                       dev(c["cu"], "i32"), dev(slots, "i32"), pool, y=y1)
+    assert sc.get_error() == sc.DEV_BAD_SLOT
+    yh = host(y1)
+    assert np.all(yh[5:14] == np.uint16(0x4040))
+    pool_ref = c["pool"].copy()
+    cut = dict(c, cu=np.array([0, 5], np.int32), slots=c["slots"][:1], hidden=c["hidden"][:5])
+    y_ref, p_ref = run_oracle(dict(cut, pool=pool_ref))
+    assert_close("bf16", yh[:5], y_ref, "y of the good sequence")
+
+
+def test_no_rows_with_sequences():
+    c = make_case(np.random.default_rng(880), [0, 0, 0], 64, 64, 3)
+    y, pool = run_gpu(c)
+    assert y.shape == (0, 64)
+    assert_bits(pool, c["pool"], "pool")
+    assert sc.get_error() == 0
+
+
+# ----------------------------------------------------------------- out_proj
+
+@pytest.mark.parametrize("T", [1, 127, 300])
+def test_out_proj_exact_inputs(T):
+    rng = np.random.default_rng(890 + T)
+    H, D = 192, 512
+    y = dyadic(rng, (T, H), 8, -3)
+    wo = dyadic(rng, (D, H), 8, -6)
+    out = sc.out_proj(dev(y, "bf16"), dev(wo, "bf16"))
+    torch.cuda.synchronize()
+    assert_bits(host(out), layer.out_proj("bf16", y, wo), "out")
+
+
+def test_out_proj_lfm2_shape_sampled_columns():
+    rng = np.random.default_rng(895)
+    T, H, D = 4096, 2048, 2048
+    y = dyadic(rng, (T, H), 8, -3)
+    wo = dyadic(rng, (D, H), 8, -6)
+    out = host(sc.out_proj(dev(y, "bf16"), dev(wo, "bf16")))
+    cols = np.sort(rng.choice(D, 48, replace=False))
+    assert_bits(out[:, cols], layer.out_proj("bf16", y, wo[cols]), "out")
+
+
+def test_layer_chain_against_the_oracle():
+    """in_proj + conv, then out_proj: the whole ShortConv layer."""
+    rng = np.random.default_rng(899)
+    c = make_case(rng, [70, 1, 190], 256, 128, 3)
+    wo = dyadic(rng, (256, 128), 8, -6)
+    pool = dev(c["pool"], "bf16")
+    y = sc.in_proj_prefill(dev(c["hidden"], "bf16"), dev(c["w_in"], "bf16"), dev(c["w"], "bf16"),
+                           dev(c["cu"], "i32"), dev(c["slots"], "i32"), pool)
+    out = host(sc.out_proj(y, dev(wo, "bf16")))
+    y_ref, _ = run_oracle(c)
+    out_ref = layer.out_proj("bf16", y_ref, wo)
+    # y may differ from the oracle's by one bf16 rounding; out inherits that
+    assert_close("bf16", out, out_ref, "out")
