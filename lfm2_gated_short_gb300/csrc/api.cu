@@ -311,8 +311,10 @@ sc_status shortconv_in_proj_prefill(sc_dtype dtype, int D, int H, int K, const v
             if (overlaps(outs[o], nouts[o], outs[p], nouts[p])) return SC_EINVAL;
     }
     if (N == 0) return SC_OK;
+    const int sms = sm_count_of_current_device();
+    if (sms <= 0) return SC_ECUDA;
     return from_cuda(sc::launch_in_proj_prefill(D, H, K, hidden, T, w_in, w, bias, cu_seqlens, N,
-                                                slot_ids, pool, n_slots, y, workspace,
+                                                slot_ids, pool, n_slots, y, workspace, sms,
                                                 (cudaStream_t)stream));
 }
 
@@ -327,7 +329,10 @@ sc_status shortconv_out_proj(sc_dtype dtype, int H, int D, const void *y, int64_
     if (!ptr_ok(y, n_y, 16) || !ptr_ok(w_out, n_wo, 16) || !ptr_ok(out, n_out, 16))
         return SC_EINVAL;
     if (overlaps(out, n_out, y, n_y) || overlaps(out, n_out, w_out, n_wo)) return SC_EINVAL;
-    return from_cuda(sc::launch_out_proj(H, D, y, T, w_out, out, (cudaStream_t)stream));
+    if (T == 0) return SC_OK;
+    const int sms = sm_count_of_current_device();
+    if (sms <= 0) return SC_ECUDA;
+    return from_cuda(sc::launch_out_proj(H, D, y, T, w_out, out, sms, (cudaStream_t)stream));
 }
 
 sc_status shortconv_slots_claim(uint32_t *in_use, int n_slots, int n_claim, int32_t *slots_out,

@@ -67,9 +67,9 @@ cudaError_t launch_in_proj_prefill(int D, int H, int K, const void *hidden, int6
                                    const void *w_in, const void *w, const void *bias,
                                    const int32_t *cu_seqlens, int N, const int32_t *slot_ids,
                                    void *pool, int n_slots, void *y, void *workspace,
-                                   cudaStream_t stream);
+                                   int sm_count, cudaStream_t stream);
 cudaError_t launch_out_proj(int H, int D, const void *y, int64_t T, const void *w_out, void *out,
-                            cudaStream_t stream);
+                            int sm_count, cudaStream_t stream);
 cudaError_t take_error_proj(cudaStream_t stream, unsigned int *code);
 
 // Take (read and clear) the backward translation unit's error word.

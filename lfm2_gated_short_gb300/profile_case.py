@@ -4,6 +4,8 @@
     python -m lfm2_gated_short_gb300.profile_case decode   --N 256  --launches 6
     python -m lfm2_gated_short_gb300.profile_case verify   --N 64 --D 8 --launches 6
     python -m lfm2_gated_short_gb300.profile_case backward --T 65536 --launches 3
+    python -m lfm2_gated_short_gb300.profile_case in_proj  --T 4096 --launches 3
+    python -m lfm2_gated_short_gb300.profile_case out_proj --T 4096 --launches 3
 
 Inputs are drawn on the device with a seeded generator (bf16, N(0,1) data,
 N(0,1/3) weights, N(0,1) pools). Consecutive launches rotate over three input
@@ -21,7 +23,8 @@ import lfm2_gated_short_gb300 as sc
 
 def main() -> None:
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["prefill", "prefill_tiled", "decode", "verify", "backward"])
+    ap.add_argument("op", choices=["prefill", "prefill_tiled", "decode", "verify", "backward",
+                                   "in_proj", "out_proj"])
     ap.add_argument("--T", type=int, default=4096)
     ap.add_argument("--H", type=int, default=2048)
     ap.add_argument("--K", type=int, default=3)
@@ -39,6 +42,9 @@ def main() -> None:
 
     H, K = a.H, a.K
     w = rnd(H, K, std=(1 / 3) ** 0.5)
+    Dm = H  # model width of the projections (LFM2-1.2B: D = H)
+    w_in = rnd(3 * H, Dm, std=Dm ** -0.5) if a.op == "in_proj" else None
+    w_out = rnd(Dm, H, std=H ** -0.5) if a.op == "out_proj" else None
     sets = []
     for _ in range(3):
         if a.op in ("prefill", "prefill_tiled"):
@@ -49,6 +55,12 @@ def main() -> None:
             sets.append(dict(bcx=rnd(a.N, 3 * H), pool=rnd(a.slots, H, K)))
         elif a.op == "verify":
             sets.append(dict(bcx=rnd(a.N * a.D, 3 * H), pool=rnd(a.slots, H, K)))
+        elif a.op == "in_proj":
+            sets.append(dict(hidden=rnd(a.T, Dm), y=torch.empty(a.T, H, dtype=torch.bfloat16,
+                                                                 device=dev),
+                             pool=torch.zeros(1, H, K, dtype=torch.bfloat16, device=dev)))
+        elif a.op == "out_proj":
+            sets.append(dict(y=rnd(a.T, H)))
         else:
             sets.append(dict(bcx=rnd(a.T, 3 * H), dy=rnd(a.T, H)))
     cu = torch.tensor([0, a.T], dtype=torch.int32, device=dev)
@@ -65,6 +77,10 @@ def main() -> None:
             sc.decode(s["bcx"], w, slots, s["pool"])
         elif a.op == "verify":
             sc.verify(s["bcx"], w, slots, s["pool"], a.D)
+        elif a.op == "in_proj":
+            sc.in_proj_prefill(s["hidden"], w_in, w, cu, slot0, s["pool"], y=s["y"])
+        elif a.op == "out_proj":
+            sc.out_proj(s["y"], w_out)
         else:
             sc.backward(s["bcx"], w, s["dy"])
     torch.cuda.synchronize()
