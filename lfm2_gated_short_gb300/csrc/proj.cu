@@ -44,28 +44,51 @@ namespace sc {
 
 typedef __nv_bfloat16 bf16;
 
-constexpr int kPBM = 128;                     // rows per tile = TMEM lanes
+constexpr int kPBM = 128;                     // rows per CTA tile = TMEM lanes
 constexpr int kPBK = 64;                      // K per stage: one 128-byte swizzle row
-constexpr int kPStages = 4;
 constexpr int kPThreads = 192;
-constexpr uint32_t kPTmemCols = 512;  // two 256-column accumulator buffers
 constexpr uint32_t kPABytes = kPBM * kPBK * 2;  // 16 KB
+
+#ifndef SC_PROJ_CLUSTER
+#define SC_PROJ_CLUSTER 2  // 2: CTA pairs run 256-row MMAs (cta_group::2); 1: single CTAs
+#endif
+#ifndef SC_PROJ_ACC_BUFS
+#define SC_PROJ_ACC_BUFS 2  // TMEM accumulator buffers of 256 columns
+#endif
+#ifndef SC_INPROJ_STAGES
+#define SC_INPROJ_STAGES (SC_PROJ_CLUSTER == 2 ? 6 : 4)  // stage ring depth, fused in_proj
+#endif
+#ifndef SC_OUTPROJ_STAGES
+#define SC_OUTPROJ_STAGES (SC_PROJ_CLUSTER == 2 ? 6 : 4)  // stage ring depth, out_proj
+#endif
+constexpr int kPCluster = SC_PROJ_CLUSTER;
+constexpr int kAccBufs = SC_PROJ_ACC_BUFS;
+constexpr uint32_t kPTmemCols = 256u * kAccBufs;
+constexpr int kInStages = SC_INPROJ_STAGES;
+constexpr int kOutStages = SC_OUTPROJ_STAGES;
+constexpr int kMaxStages = 8;
+static_assert(kPCluster == 1 || kPCluster == 2, "CTA pairs or single CTAs");
+static_assert(kAccBufs == 1 || kAccBufs == 2, "one or two accumulator buffers");
 
 constexpr int kConvCh = 64;                   // channels per fused tile
 constexpr int kConvN = 3 * kConvCh;           // GEMM N: B | C | x of those channels
-constexpr uint32_t kConvStage = kPABytes + kConvN * kPBK * 2;  // 40 KB
+constexpr int kConvBoxRows = kConvCh / kPCluster;  // B rows per TMA box (3 boxes a CTA)
+constexpr uint32_t kConvBox = kConvBoxRows * kPBK * 2;
+constexpr uint32_t kConvStage = kPABytes + 3 * kConvBox;  // 40 KB single, 28 KB a pair CTA
 constexpr int kUStride = 144;                 // bytes per u row: 128 + 16, conflict-free
 constexpr int kProjCuStaged = 512;
 
 constexpr int kOutN = 256;                    // out_proj N per tile
-constexpr uint32_t kOutStage = kPABytes + kOutN * kPBK * 2;    // 48 KB
+constexpr int kOutBoxRows = kOutN / kPCluster;
+constexpr uint32_t kOutBox = kOutBoxRows * kPBK * 2;
+constexpr uint32_t kOutStage = kPABytes + kOutBox;  // 48 KB single, 32 KB a pair CTA
 
 // Shared memory after the stage ring: barriers and flags. The accumulator
 // is double-buffered in TMEM (columns 0.. and 256..): the MMA lane fills one
 // buffer while the epilogue warps drain the other.
 struct PipeState {
-    uint64_t full[kPStages];   // stage loaded (TMA bytes)
-    uint64_t empty[kPStages];  // stage consumed (MMA commit)
+    uint64_t full[kMaxStages];   // stage loaded (TMA bytes)
+    uint64_t empty[kMaxStages];  // stage consumed (MMA commit)
     uint64_t tfull[2];         // accumulator buffer ready (MMA commit)
     uint64_t tempty[2];        // accumulator buffer drained (128 epilogue threads)
     uint64_t mma_done;         // every MMA of this CTA completed
@@ -78,81 +101,130 @@ constexpr size_t kConvExtra = (size_t)kPBM * kUStride          // u tile
                               + kConvCh * sizeof(float)        // bias
                               + (kProjCuStaged + 8) * 4;       // staged cu_seqlens
 constexpr size_t conv_smem_bytes() {
-    return 1024 + (size_t)kPStages * kConvStage + kConvExtra + sizeof(PipeState);
+    return 1024 + (size_t)kInStages * kConvStage + kConvExtra + sizeof(PipeState);
 }
 constexpr size_t out_smem_bytes() {
-    return 1024 + (size_t)kPStages * kOutStage + sizeof(PipeState);
+    return 1024 + (size_t)kOutStages * kOutStage + sizeof(PipeState);
 }
+static_assert(conv_smem_bytes() <= 232448 && out_smem_bytes() <= 232448,
+              "stage ring larger than a CTA's shared memory");
+static_assert(kInStages <= kMaxStages && kOutStages <= kMaxStages, "too many stages");
 
 // ------------------------------------------------------------ persistent mainloop
 //
-// A CTA takes tiles blockIdx.x, blockIdx.x + gridDim.x, ...; the stage ring
-// runs on across tiles (k-block counter g over all of the CTA's tiles).
+// CL = 1: one CTA runs 128-row MMAs (cta_group::1). CL = 2: the two CTAs of a
+// cluster run 256-row MMAs as a pair (cta_group::2): each stages its own 128
+// rows of A and half of B's N rows, the leader (rank 0) issues the MMAs, and
+// each CTA's TMEM receives its own rows of the result. Per SM that halves the
+// B bytes staged and read by the tensor core. The CTAs of a cluster take CL
+// consecutive row tiles of one column tile; clusters walk the tile groups c,
+// c + n_clusters, ...; the stage ring runs on across tiles (k-block counter g
+// over all of the CTA's tiles).
 
-__device__ __forceinline__ void pipe_init(PipeState *ps) {
+struct TileWalk {
+    int first, step, n_groups, rank, CL;
+    // Row tile and column tile of the group's tile for this CTA.
+    __device__ __forceinline__ void at(int grp, int n_col_tiles, int &mt, int &ct) const {
+        ct = grp % n_col_tiles;
+        mt = (grp / n_col_tiles) * CL + rank;
+    }
+};
+
+template <int CL>
+__device__ __forceinline__ TileWalk tile_walk(int n_row_tiles, int n_col_tiles) {
+    TileWalk w;
+    w.CL = CL;
+    w.rank = CL > 1 ? (int)cluster_ctarank() : 0;
+    w.first = blockIdx.x / CL;
+    w.step = gridDim.x / CL;
+    w.n_groups = (n_row_tiles + CL - 1) / CL * n_col_tiles;
+    return w;
+}
+
+__device__ __forceinline__ void pipe_init(PipeState *ps, int CL) {
 #pragma unroll
-    for (int s = 0; s < kPStages; ++s) {
-        mbar_init(&ps->full[s], 1);
-        mbar_init(&ps->empty[s], 1);
+    for (int s = 0; s < kMaxStages; ++s) {
+        mbar_init(&ps->full[s], 1);   // the (leader's) producer; bytes of both CTAs
+        mbar_init(&ps->empty[s], 1);  // the (leader's) MMA commit
     }
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
         mbar_init(&ps->tfull[b], 1);
-        mbar_init(&ps->tempty[b], 128);
+        mbar_init(&ps->tempty[b], 4 * CL);  // one lane per epilogue warp of each CTA
     }
     mbar_init(&ps->mma_done, 1);
     ps->abort = 0;
     mbar_fence_init();
 }
 
-// Warp 0, one lane. coords(tile, a_row, b_rows) gives a tile's A row and the
-// first rows of its NB boxes of B.
-template <int NB, typename Coords>
+// Warp 0, one lane. coords(mt, ct, a_row, rows) gives the tile's A row and the
+// first rows of this CTA's NB boxes of B (box_bytes each); a stage holds A,
+// then the boxes.
+template <int S, int NB, int CL, typename Coords>
 __device__ __forceinline__ void produce_tiles(const CUtensorMap *ma, const CUtensorMap *mb,
                                               uint32_t stages, uint32_t stage_bytes,
-                                              PipeState *ps, int nk, int n_tiles,
-                                              uint32_t box_bytes, Coords coords) {
+                                              PipeState *ps, int nk, const TileWalk &tw,
+                                              int n_col_tiles, uint32_t box_bytes,
+                                              Coords coords) {
+    const bool leader = tw.rank == 0;
     uint32_t g = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        int a_row, b_rows[NB];
-        coords(tile, a_row, b_rows);
+    for (int grp = tw.first; grp < tw.n_groups && ok; grp += tw.step) {
+        int mt, ct, a_row, rows[NB];
+        tw.at(grp, n_col_tiles, mt, ct);
+        coords(mt, ct, a_row, rows);
         for (int kb = 0; kb < nk; ++kb, ++g) {
-            const uint32_t s = g % kPStages;
-            if (g >= kPStages &&
-                !mbar_wait_bounded(&ps->empty[s], (g / kPStages - 1) & 1u)) {
+            const uint32_t s = g % S;
+            if (g >= S && !mbar_wait_bounded(&ps->empty[s], (g / S - 1) & 1u)) {
                 raise_error(SC_DEV_TIMEOUT);
                 ps->abort = 1;
                 ok = false;
                 break;
             }
             const uint32_t st = stages + s * stage_bytes;
-            mbar_arrive_expect_tx(&ps->full[s], kPABytes + NB * box_bytes);
-            tma_load_2d(st, ma, &ps->full[s], kb * kPBK, a_row);
+            if constexpr (CL == 1) {
+                mbar_arrive_expect_tx(&ps->full[s], stage_bytes);
+                tma_load_2d(st, ma, &ps->full[s], kb * kPBK, a_row);
 #pragma unroll
-            for (int i = 0; i < NB; ++i)
-                tma_load_2d(st + kPABytes + i * box_bytes, mb, &ps->full[s], kb * kPBK,
-                            b_rows[i]);
+                for (int i = 0; i < NB; ++i)
+                    tma_load_2d(st + kPABytes + i * box_bytes, mb, &ps->full[s], kb * kPBK,
+                                rows[i]);
+            } else {  // both CTAs' bytes count on the leader's barrier
+                const uint32_t bar = cluster_map(smem_addr(&ps->full[s]), 0);
+                if (leader) mbar_arrive_expect_tx(&ps->full[s], 2 * stage_bytes);
+                tma_load_2d_pair(st, ma, bar, kb * kPBK, a_row);
+#pragma unroll
+                for (int i = 0; i < NB; ++i)
+                    tma_load_2d_pair(st + kPABytes + i * box_bytes, mb, bar, kb * kPBK, rows[i]);
+            }
         }
     }
-    // The copies still in flight land before the CTA may leave.
-    for (uint32_t c = g > kPStages ? g - kPStages : 0; c < g; ++c)
-        mbar_wait_bounded(&ps->full[c % kPStages], (c / kPStages) & 1u);
+    // The copies in flight land before the CTA may leave (the leader's barrier
+    // counts both CTAs' bytes), and so do the MMA-commit arrivals that release
+    // the last stages.
+    if (CL == 1 || leader)
+        for (uint32_t c = g > S ? g - S : 0; c < g; ++c)
+            mbar_wait_bounded(&ps->full[c % S], (c / S) & 1u);
+    if (ok)
+        for (uint32_t c = g > S ? g - S : 0; c < g; ++c)
+            mbar_wait_bounded(&ps->empty[c % S], (c / S) & 1u);
 }
 
-// Warp 1, one lane: per K block, 4 MMAs of K = 16 into accumulator buffer
-// it & 1 (it = the CTA's tile count); a stage is released when its MMAs
-// complete, a buffer is announced full when all of the tile's have.
-template <int N>
+// Warp 1, one lane of the (leader) CTA: per K block, 4 MMAs of K = 16 into
+// accumulator buffer it % kAccBufs (it = the CTA's tile count); a stage is
+// released when its MMAs complete, a buffer is announced full when all of
+// the tile's have.
+template <int S, int N, int CL>
 __device__ __forceinline__ void mma_tiles(uint32_t tmem, uint32_t stages, uint32_t stage_bytes,
-                                          PipeState *ps, int nk, int n_tiles) {
-    constexpr uint32_t idesc = idesc_bf16_f32(kPBM, N);
+                                          PipeState *ps, int nk, const TileWalk &tw) {
+    constexpr uint32_t idesc = idesc_bf16_f32(kPBM * CL, N);
+    constexpr uint16_t both = 3;
     uint32_t g = 0;
     int it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++it) {
-        const int b = it & 1;
-        if (it >= 2 && !mbar_wait_bounded(&ps->tempty[b], (uint32_t)((it >> 1) - 1) & 1u)) {
+    for (int grp = tw.first; grp < tw.n_groups && ok; grp += tw.step, ++it) {
+        const int b = it % kAccBufs, use = it / kAccBufs;
+        if (use >= 1 && !mbar_wait_bounded(&ps->tempty[b], (uint32_t)(use - 1) & 1u)) {
             raise_error(SC_DEV_TIMEOUT);
             ps->abort = 1;
             break;
@@ -160,8 +232,8 @@ __device__ __forceinline__ void mma_tiles(uint32_t tmem, uint32_t stages, uint32
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)b * 256u;
         for (int kb = 0; kb < nk; ++kb, ++g) {
-            const uint32_t s = g % kPStages;
-            if (!mbar_wait_bounded(&ps->full[s], (g / kPStages) & 1u)) {
+            const uint32_t s = g % S;
+            if (!mbar_wait_bounded(&ps->full[s], (g / S) & 1u)) {
                 raise_error(SC_DEV_TIMEOUT);
                 ps->abort = 1;
                 ok = false;
@@ -171,32 +243,57 @@ __device__ __forceinline__ void mma_tiles(uint32_t tmem, uint32_t stages, uint32
             const uint32_t st = stages + s * stage_bytes;
             const uint64_t da = sdesc_k128(st), db = sdesc_k128(st + kPABytes);
 #pragma unroll
-            for (int j = 0; j < kPBK / 16; ++j)
-                mma_bf16(d, da + 2 * j, db + 2 * j, idesc, (kb | j) != 0);
-            mma_commit(&ps->empty[s]);
+            for (int j = 0; j < kPBK / 16; ++j) {
+                if constexpr (CL == 1)
+                    mma_bf16(d, da + 2 * j, db + 2 * j, idesc, (kb | j) != 0);
+                else
+                    mma_bf16_pair(d, da + 2 * j, db + 2 * j, idesc, (kb | j) != 0);
+            }
+            if constexpr (CL == 1)
+                mma_commit(&ps->empty[s]);
+            else
+                mma_commit_pair(&ps->empty[s], both);  // the stage of both CTAs
         }
-        if (ok) mma_commit(&ps->tfull[b]);
+        if (ok) {
+            if constexpr (CL == 1)
+                mma_commit(&ps->tfull[b]);
+            else
+                mma_commit_pair(&ps->tfull[b], both);
+        }
     }
     // No MMA may still write TMEM when it is freed.
-    mma_commit(&ps->mma_done);
+    if constexpr (CL == 1)
+        mma_commit(&ps->mma_done);
+    else
+        mma_commit_pair(&ps->mma_done, 1);
     mbar_wait_bounded(&ps->mma_done, 0);
 }
 
-// Epilogue threads: wait for accumulator buffer b of the CTA's it-th tile.
+// Epilogue threads: wait for the accumulator buffer of the CTA's it-th tile.
 // The decision to go on is taken together (barrier-OR over the 128 threads),
 // so no thread waits at a named barrier the others have left.
 __device__ __forceinline__ bool epi_acquire(PipeState *ps, int it) {
-    const bool ok = mbar_wait_bounded(&ps->tfull[it & 1], (uint32_t)(it >> 1) & 1u);
+    const bool ok =
+        mbar_wait_bounded(&ps->tfull[it % kAccBufs], (uint32_t)(it / kAccBufs) & 1u);
     const bool fail = named_or(1, 128, !ok || ps->abort != 0);
     if (!ok) raise_error(SC_DEV_TIMEOUT);
     tc_fence_after();
     return !fail;
 }
 
-// Every tcgen05.ld of the buffer has completed (tmem_ld16 waits): release it.
-__device__ __forceinline__ void epi_release(PipeState *ps, int it) {
+// Every tcgen05.ld of the buffer has completed (tmem_ld16 waits): one lane
+// per warp releases it on the (leader's) barrier.
+template <int CL>
+__device__ __forceinline__ void epi_release(PipeState *ps, int it, int rank) {
     tc_fence_before();
-    mbar_arrive(&ps->tempty[it & 1]);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+        uint64_t *bar = &ps->tempty[it % kAccBufs];
+        if (CL == 1 || rank == 0)
+            mbar_arrive(bar);
+        else
+            mbar_arrive_cluster(cluster_map(smem_addr(bar), 0));
+    }
 }
 
 __device__ __forceinline__ unsigned char *align1024(unsigned char *raw) {
@@ -204,48 +301,63 @@ __device__ __forceinline__ unsigned char *align1024(unsigned char *raw) {
     return raw + (((a + 1023u) & ~1023u) - a);
 }
 
-// Shared start of both kernels: barriers, TMEM (2 x 256 columns), PDL wait.
+// Shared start of both kernels: barriers, TMEM, PDL wait; with pairs, no CTA
+// goes on before every CTA's barriers exist.
+template <int CL>
 __device__ __forceinline__ uint32_t pipe_start(PipeState *ps, const CUtensorMap *m0,
                                                const CUtensorMap *m1) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) pipe_init(ps);
+    if (threadIdx.x == 0) pipe_init(ps, CL);
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(m0);
         tma_prefetch_map(m1);
     }
-    if (warp == 1) tmem_alloc(&ps->tmem, kPTmemCols);
+    if (warp == 1) {
+        if constexpr (CL == 1)
+            tmem_alloc(&ps->tmem, kPTmemCols);
+        else
+            tmem_alloc_pair(&ps->tmem, kPTmemCols);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if constexpr (CL > 1) cluster_sync();
     const uint32_t tmem = ps->tmem;
     pdl_wait();  // inputs may come from the previous kernel in the stream
     pdl_launch_dependents();
     return tmem;
 }
 
+// With pairs, no CTA leaves while the other may still write its shared
+// memory or arrive on its barriers; the pair frees its TMEM together.
+template <int CL>
 __device__ __forceinline__ void pipe_finish(uint32_t tmem) {
     tc_fence_before();
     __syncthreads();
+    if constexpr (CL > 1) cluster_sync();
     if ((threadIdx.x >> 5) == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, kPTmemCols);
+        if constexpr (CL == 1)
+            tmem_dealloc(tmem, kPTmemCols);
+        else
+            tmem_dealloc_pair(tmem, kPTmemCols);
     }
 }
 
 // ------------------------------------------------------------ fused in_proj + conv
 
-template <int K>
+template <int K, int CL>
 __global__ void __launch_bounds__(kPThreads, 1)
     k_in_proj_conv(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
                    int64_t T_rows, int D, int H, const bf16 *__restrict__ w,
                    const bf16 *__restrict__ bias, const int32_t *__restrict__ cu, int N,
                    const int32_t *__restrict__ slots, const bf16 *__restrict__ pool, int n_slots,
-                   bf16 *__restrict__ y, bf16 *__restrict__ tail, int n_ctiles, int n_tiles) {
+                   bf16 *__restrict__ y, bf16 *__restrict__ tail, int n_ctiles, int n_mtiles) {
     constexpr int OUT = kPBM - (K - 1);  // output rows per tile
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = align1024(smem_raw);
-    unsigned char *u_tile = base + (size_t)kPStages * kConvStage;
+    unsigned char *u_tile = base + (size_t)kInStages * kConvStage;
     float *wts = reinterpret_cast<float *>(u_tile + kPBM * kUStride);  // [kConvCh][K]
     float *bsm = wts + kConvCh * 4;
     int32_t *s_cu = reinterpret_cast<int32_t *>(bsm + kConvCh);
@@ -253,20 +365,28 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t stages = smem_addr(base);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = D / kPBK;
-    const uint32_t tmem = pipe_start(ps, &map_h, &map_w);
+    const uint32_t tmem = pipe_start<CL>(ps, &map_h, &map_w);
+    const TileWalk tw = tile_walk<CL>(n_mtiles, n_ctiles);
 
     if (warp == 0) {
         if (lane == 0)
-            produce_tiles<3>(&map_h, &map_w, stages, kConvStage, ps, nk, n_tiles,
-                             kConvCh * kPBK * 2, [&](int tile, int &a_row, int (&rows)[3]) {
-                                 const int h0 = (tile % n_ctiles) * kConvCh;
-                                 a_row = (tile / n_ctiles) * OUT - (K - 1);
-                                 rows[0] = h0;
-                                 rows[1] = H + h0;
-                                 rows[2] = 2 * H + h0;
-                             });
+            produce_tiles<kInStages, 3, CL>(
+                &map_h, &map_w, stages, kConvStage, ps, nk, tw, n_ctiles, kConvBox,
+                [&](int mt, int ct, int &a_row, int (&rows)[3]) {
+                    // The B tile is [B | C | x] of 64 channels: 3 * CL chunks of
+                    // kConvBoxRows rows; this CTA loads chunks 3 rank .. 3 rank + 2.
+                    const int h0 = ct * kConvCh;
+                    a_row = mt * OUT - (K - 1);
+#pragma unroll
+                    for (int i = 0; i < 3; ++i) {
+                        const int chunk = 3 * tw.rank + i;
+                        const int per = kConvCh / kConvBoxRows;  // chunks per block
+                        rows[i] = (chunk / per) * H + h0 + (chunk % per) * kConvBoxRows;
+                    }
+                });
     } else if (warp == 1) {
-        if (lane == 0) mma_tiles<kConvN>(tmem, stages, kConvStage, ps, nk, n_tiles);
+        if (lane == 0 && tw.rank == 0)
+            mma_tiles<kInStages, kConvN, CL>(tmem, stages, kConvStage, ps, nk, tw);
         __syncwarp();
     } else {
         // ---------------- epilogue: warps 2..5
@@ -289,16 +409,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
         unsigned char *urow = u_tile + r * kUStride;
 
         int it = 0;
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
-            const int h0 = (tile % n_ctiles) * kConvCh;
-            const int64_t t = (int64_t)(tile / n_ctiles) * OUT - (K - 1) + r;  // global row
+        for (int grp = tw.first; grp < tw.n_groups; grp += tw.step, ++it) {
+            int mt, ct;
+            tw.at(grp, n_ctiles, mt, ct);
+            const int h0 = ct * kConvCh;
+            const int64_t t = (int64_t)mt * OUT - (K - 1) + r;  // global row (past T: no output)
             // This tile's taps and bias (the previous tile is done with them).
             for (int e = et; e < kConvCh * K; e += 128)
                 wts[e] = __bfloat162float(w[(int64_t)h0 * K + e]);
             if (bias != nullptr)
                 for (int e = et; e < kConvCh; e += 128) bsm[e] = __bfloat162float(bias[h0 + e]);
             if (!epi_acquire(ps, it)) break;
-            const uint32_t trow = tmem + (uint32_t)(it & 1) * 256u + ((uint32_t)(q * 32) << 16);
+            const uint32_t trow =
+                tmem + (uint32_t)(it % kAccBufs) * 256u + ((uint32_t)(q * 32) << 16);
 
             // Phase A: u = round(round(B) round(x)) of every tile row into u_tile.
             __syncwarp();  // tcgen05.ld is warp-collective: lanes converge first
@@ -329,7 +452,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) cv[cc * 16 + j] = Dt<bf16>::round(tmp[j]);
             }
-            epi_release(ps, it);
+            epi_release<CL>(ps, it, tw.rank);
             named_sync(1, 128);  // u_tile, taps and bias complete
 
             // Phase B: outputs of rows K-1 .. 127 of the tile.
@@ -411,7 +534,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             named_sync(1, 128);  // u_tile, taps and bias free for the next tile
         }
     }
-    pipe_finish(tmem);
+    pipe_finish<CL>(tmem);
 }
 
 // New state of sequence i = the last K entries of [old state; u of its rows]:
@@ -462,36 +585,43 @@ __global__ void __launch_bounds__(256)
 
 // ------------------------------------------------------------ out_proj
 
+template <int CL>
 __global__ void __launch_bounds__(kPThreads, 1)
     k_out_proj(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                int64_t M_rows, int Kdim, int N_cols, bf16 *__restrict__ out, int n_ntiles,
-               int n_tiles) {
+               int n_mtiles) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = align1024(smem_raw);
-    PipeState *ps = reinterpret_cast<PipeState *>(base + (size_t)kPStages * kOutStage);
+    PipeState *ps = reinterpret_cast<PipeState *>(base + (size_t)kOutStages * kOutStage);
     const uint32_t stages = smem_addr(base);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = Kdim / kPBK;
-    const uint32_t tmem = pipe_start(ps, &map_a, &map_b);
+    const uint32_t tmem = pipe_start<CL>(ps, &map_a, &map_b);
+    const TileWalk tw = tile_walk<CL>(n_mtiles, n_ntiles);
 
     if (warp == 0) {
         if (lane == 0)
-            produce_tiles<1>(&map_a, &map_b, stages, kOutStage, ps, nk, n_tiles,
-                             kOutN * kPBK * 2, [&](int tile, int &a_row, int (&rows)[1]) {
-                                 a_row = (tile / n_ntiles) * kPBM;
-                                 rows[0] = (tile % n_ntiles) * kOutN;
-                             });
+            produce_tiles<kOutStages, 1, CL>(
+                &map_a, &map_b, stages, kOutStage, ps, nk, tw, n_ntiles, kOutBox,
+                [&](int mt, int nt, int &a_row, int (&rows)[1]) {
+                    a_row = mt * kPBM;
+                    rows[0] = nt * kOutN + tw.rank * kOutBoxRows;
+                });
     } else if (warp == 1) {
-        if (lane == 0) mma_tiles<kOutN>(tmem, stages, kOutStage, ps, nk, n_tiles);
+        if (lane == 0 && tw.rank == 0)
+            mma_tiles<kOutStages, kOutN, CL>(tmem, stages, kOutStage, ps, nk, tw);
         __syncwarp();
     } else {
         const int q = warp & 3;
         int it = 0;
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
-            const int64_t t = (int64_t)(tile / n_ntiles) * kPBM + q * 32 + lane;
-            const int col0 = (tile % n_ntiles) * kOutN;
+        for (int grp = tw.first; grp < tw.n_groups; grp += tw.step, ++it) {
+            int mt, nt;
+            tw.at(grp, n_ntiles, mt, nt);
+            const int64_t t = (int64_t)mt * kPBM + q * 32 + lane;  // past M_rows: no store
+            const int col0 = nt * kOutN;
             if (!epi_acquire(ps, it)) break;
-            const uint32_t trow = tmem + (uint32_t)(it & 1) * 256u + ((uint32_t)(q * 32) << 16);
+            const uint32_t trow =
+                tmem + (uint32_t)(it % kAccBufs) * 256u + ((uint32_t)(q * 32) << 16);
             const bool store = t < M_rows;
 #pragma unroll 1
             for (int cc = 0; cc < kOutN / 16; ++cc) {
@@ -506,11 +636,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
-            __syncwarp();
-            epi_release(ps, it);
+            epi_release<CL>(ps, it, tw.rank);
         }
     }
-    pipe_finish(tmem);
+    pipe_finish<CL>(tmem);
 }
 
 // ------------------------------------------------------------ host side
@@ -563,6 +692,40 @@ static cudaError_t smem_opt_in(F kern, size_t bytes, std::atomic<unsigned long l
     return e;
 }
 
+// How many clusters of kPCluster CTAs of `kern` fit on the device at once
+// (the persistent grid), cached per device.
+template <typename F>
+static cudaError_t max_clusters(F kern, size_t smem, int sm_count, std::atomic<int> (&cache)[64],
+                                int *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && cache[dev].load() > 0) {
+        *out = cache[dev].load();
+        return cudaSuccess;
+    }
+    int n = sm_count / kPCluster;
+    if (kPCluster > 1) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(kPCluster * (sm_count / kPCluster)));
+        cfg.blockDim = dim3(kPThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kPCluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaOccupancyMaxActiveClusters(&n, (const void *)kern, &cfg);
+        if (e != cudaSuccess) return e;
+    }
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    if (dev >= 0 && dev < 64) cache[dev].store(n);
+    *out = n;
+    return cudaSuccess;
+}
+
 size_t in_proj_workspace_bytes(int H, int K, int N) { return (size_t)N * H * K * 2; }
 
 template <int K>
@@ -573,16 +736,22 @@ static cudaError_t in_proj_inst(const CUtensorMap &mh, const CUtensorMap &mw, in
     constexpr int OUT = kPBM - (K - 1);
     cudaError_t e;
     if (T > 0) {
+        auto kern = k_in_proj_conv<K, kPCluster>;
         static std::atomic<unsigned long long> done{0};
-        e = smem_opt_in(k_in_proj_conv<K>, conv_smem_bytes(), done);
+        e = smem_opt_in(kern, conv_smem_bytes(), done);
+        if (e != cudaSuccess) return e;
+        static std::atomic<int> cache[64];
+        int clusters = 0;
+        e = max_clusters(kern, conv_smem_bytes(), sm_count, cache, &clusters);
         if (e != cudaSuccess) return e;
         const int n_ctiles = H / kConvCh;
-        const int64_t n_tiles = (T + OUT - 1) / OUT * n_ctiles;
-        const int grid = (int)(n_tiles < sm_count ? n_tiles : sm_count);  // persistent
-        e = launch_pdl(k_in_proj_conv<K>, dim3((unsigned)grid), dim3(kPThreads),
-                       conv_smem_bytes(), stream, mh, mw, T, D, H, (const bf16 *)w,
-                       (const bf16 *)bias, cu, N, slots, (const bf16 *)pool, n_slots, (bf16 *)y,
-                       (bf16 *)tail, n_ctiles, (int)n_tiles);
+        const int64_t n_mtiles = (T + OUT - 1) / OUT;
+        const int64_t groups = (n_mtiles + kPCluster - 1) / kPCluster * n_ctiles;
+        const int grid = kPCluster * (int)(groups < clusters ? groups : clusters);  // persistent
+        e = launch_pdl_cluster(kern, dim3((unsigned)grid), dim3(kPThreads), conv_smem_bytes(),
+                               stream, kPCluster, mh, mw, T, D, H, (const bf16 *)w,
+                               (const bf16 *)bias, cu, N, slots, (const bf16 *)pool, n_slots,
+                               (bf16 *)y, (bf16 *)tail, n_ctiles, (int)n_mtiles);
         if (e != cudaSuccess) return e;
     }
     const int64_t units = (int64_t)N * (H / kCh);
@@ -601,7 +770,7 @@ cudaError_t launch_in_proj_prefill(int D, int H, int K, const void *hidden, int6
     if (T > 0) {
         cudaError_t e = map_2d(&mh, hidden, (uint64_t)D, (uint64_t)T, kPBM);
         if (e != cudaSuccess) return e;
-        e = map_2d(&mw, w_in, (uint64_t)D, (uint64_t)3 * H, kConvCh);
+        e = map_2d(&mw, w_in, (uint64_t)D, (uint64_t)3 * H, kConvBoxRows);
         if (e != cudaSuccess) return e;
     }
     switch (K) {
@@ -618,16 +787,23 @@ cudaError_t launch_out_proj(int H, int D, const void *y, int64_t T, const void *
     CUtensorMap ma, mb;
     cudaError_t e = map_2d(&ma, y, (uint64_t)H, (uint64_t)T, kPBM);
     if (e != cudaSuccess) return e;
-    e = map_2d(&mb, w_out, (uint64_t)H, (uint64_t)D, kOutN);
+    e = map_2d(&mb, w_out, (uint64_t)H, (uint64_t)D, kOutBoxRows);
     if (e != cudaSuccess) return e;
+    auto kern = k_out_proj<kPCluster>;
     static std::atomic<unsigned long long> done{0};
-    e = smem_opt_in(k_out_proj, out_smem_bytes(), done);
+    e = smem_opt_in(kern, out_smem_bytes(), done);
+    if (e != cudaSuccess) return e;
+    static std::atomic<int> cache[64];
+    int clusters = 0;
+    e = max_clusters(kern, out_smem_bytes(), sm_count, cache, &clusters);
     if (e != cudaSuccess) return e;
     const int n_ntiles = D / kOutN;
-    const int64_t n_tiles = (T + kPBM - 1) / kPBM * n_ntiles;
-    const int grid = (int)(n_tiles < sm_count ? n_tiles : sm_count);  // persistent
-    return launch_pdl(k_out_proj, dim3((unsigned)grid), dim3(kPThreads), out_smem_bytes(), stream,
-                      ma, mb, T, H, D, (bf16 *)out, n_ntiles, (int)n_tiles);
+    const int64_t n_mtiles = (T + kPBM - 1) / kPBM;
+    const int64_t groups = (n_mtiles + kPCluster - 1) / kPCluster * n_ntiles;
+    const int grid = kPCluster * (int)(groups < clusters ? groups : clusters);  // persistent
+    return launch_pdl_cluster(kern, dim3((unsigned)grid), dim3(kPThreads), out_smem_bytes(),
+                              stream, kPCluster, ma, mb, T, H, D, (bf16 *)out, n_ntiles,
+                              (int)n_mtiles);
 }
 
 cudaError_t take_error_proj(cudaStream_t stream, unsigned int *code) {
