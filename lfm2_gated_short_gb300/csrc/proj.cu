@@ -22,10 +22,12 @@
 // k_out_proj is the plain out_proj GEMM (128 x 256 tiles) on the same
 // mainloop, with a store epilogue.
 //
-// Warp roles (192 threads): warp 0 issues the TMA copies, warp 1 owns the
-// TMEM allocation and one of its lanes issues the MMAs, warps 2-5 run the
-// epilogue (warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31). Every
-// mbarrier wait gives up after 2 s (SC_DEV_TIMEOUT); the TMEM is always freed.
+// Warp roles: warp 0 issues the TMA copies, warp 1 owns the TMEM allocation
+// and one of its lanes issues the MMAs, the other warps run the epilogue
+// (warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31): 8 epilogue warps in
+// the fused kernel, two per lane quarter with 32 channels each, so the conv
+// epilogue keeps pace with the tensor cores; 4 in out_proj. Every mbarrier
+// wait gives up after 2 s (SC_DEV_TIMEOUT); the TMEM is always freed.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -46,7 +48,7 @@ typedef __nv_bfloat16 bf16;
 
 constexpr int kPBM = 128;                     // rows per CTA tile = TMEM lanes
 constexpr int kPBK = 64;                      // K per stage: one 128-byte swizzle row
-constexpr int kPThreads = 192;
+constexpr int kOutThreads = 192;              // producer, MMA and 4 epilogue warps
 constexpr uint32_t kPABytes = kPBM * kPBK * 2;  // 16 KB
 
 #ifndef SC_PROJ_CLUSTER
@@ -77,6 +79,16 @@ constexpr uint32_t kConvBox = kConvBoxRows * kPBK * 2;
 constexpr uint32_t kConvStage = kPABytes + 3 * kConvBox;  // 40 KB single, 28 KB a pair CTA
 constexpr int kUStride = 144;                 // bytes per u row: 128 + 16, conflict-free
 constexpr int kProjCuStaged = 512;
+#ifndef SC_INPROJ_EPI_WARPS
+#define SC_INPROJ_EPI_WARPS 8  // epilogue warps of the fused kernel: 4 or 8
+#endif
+// Epilogue warp w reads TMEM lanes 32 (w % 4) ..; with 8 warps two share each
+// lane quarter and each takes half of the tile's 64 channels.
+constexpr int kInEpiWarps = SC_INPROJ_EPI_WARPS;
+constexpr int kInEpiThreads = 32 * kInEpiWarps;
+constexpr int kInThreads = 64 + kInEpiThreads;
+constexpr int kChPerWarp = kConvCh * 4 / kInEpiWarps;  // channels per epilogue warp
+static_assert(kInEpiWarps == 4 || kInEpiWarps == 8, "4 or 8 epilogue warps");
 
 constexpr int kOutN = 256;                    // out_proj N per tile
 constexpr int kOutBoxRows = kOutN / kPCluster;
@@ -97,7 +109,7 @@ struct PipeState {
 };
 
 constexpr size_t kConvExtra = (size_t)kPBM * kUStride          // u tile
-                              + kConvCh * 4 * sizeof(float)    // taps
+                              + kConvCh * 4 * sizeof(float)    // taps, tap-major
                               + kConvCh * sizeof(float)        // bias
                               + (kProjCuStaged + 8) * 4;       // staged cu_seqlens
 constexpr size_t conv_smem_bytes() {
@@ -141,7 +153,7 @@ __device__ __forceinline__ TileWalk tile_walk(int n_row_tiles, int n_col_tiles) 
     return w;
 }
 
-__device__ __forceinline__ void pipe_init(PipeState *ps, int CL) {
+__device__ __forceinline__ void pipe_init(PipeState *ps, int CL, int epi_warps) {
 #pragma unroll
     for (int s = 0; s < kMaxStages; ++s) {
         mbar_init(&ps->full[s], 1);   // the (leader's) producer; bytes of both CTAs
@@ -150,7 +162,7 @@ __device__ __forceinline__ void pipe_init(PipeState *ps, int CL) {
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
         mbar_init(&ps->tfull[b], 1);
-        mbar_init(&ps->tempty[b], 4 * CL);  // one lane per epilogue warp of each CTA
+        mbar_init(&ps->tempty[b], epi_warps * CL);  // one lane per epilogue warp of each CTA
     }
     mbar_init(&ps->mma_done, 1);
     ps->abort = 0;
@@ -272,10 +284,10 @@ __device__ __forceinline__ void mma_tiles(uint32_t tmem, uint32_t stages, uint32
 // Epilogue threads: wait for the accumulator buffer of the CTA's it-th tile.
 // The decision to go on is taken together (barrier-OR over the 128 threads),
 // so no thread waits at a named barrier the others have left.
-__device__ __forceinline__ bool epi_acquire(PipeState *ps, int it) {
+__device__ __forceinline__ bool epi_acquire(PipeState *ps, int it, int epi_threads) {
     const bool ok =
         mbar_wait_bounded(&ps->tfull[it % kAccBufs], (uint32_t)(it / kAccBufs) & 1u);
-    const bool fail = named_or(1, 128, !ok || ps->abort != 0);
+    const bool fail = named_or(1, epi_threads, !ok || ps->abort != 0);
     if (!ok) raise_error(SC_DEV_TIMEOUT);
     tc_fence_after();
     return !fail;
@@ -305,9 +317,9 @@ __device__ __forceinline__ unsigned char *align1024(unsigned char *raw) {
 // goes on before every CTA's barriers exist.
 template <int CL>
 __device__ __forceinline__ uint32_t pipe_start(PipeState *ps, const CUtensorMap *m0,
-                                               const CUtensorMap *m1) {
+                                               const CUtensorMap *m1, int epi_warps) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) pipe_init(ps, CL);
+    if (threadIdx.x == 0) pipe_init(ps, CL, epi_warps);
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(m0);
         tma_prefetch_map(m1);
@@ -348,7 +360,7 @@ __device__ __forceinline__ void pipe_finish(uint32_t tmem) {
 // ------------------------------------------------------------ fused in_proj + conv
 
 template <int K, int CL>
-__global__ void __launch_bounds__(kPThreads, 1)
+__global__ void __launch_bounds__(kInThreads, 1)
     k_in_proj_conv(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
                    int64_t T_rows, int D, int H, const bf16 *__restrict__ w,
                    const bf16 *__restrict__ bias, const int32_t *__restrict__ cu, int N,
@@ -365,7 +377,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t stages = smem_addr(base);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = D / kPBK;
-    const uint32_t tmem = pipe_start<CL>(ps, &map_h, &map_w);
+    const uint32_t tmem = pipe_start<CL>(ps, &map_h, &map_w, kInEpiWarps);
     const TileWalk tw = tile_walk<CL>(n_mtiles, n_ctiles);
 
     if (warp == 0) {
@@ -389,21 +401,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mma_tiles<kInStages, kConvN, CL>(tmem, stages, kConvStage, ps, nk, tw);
         __syncwarp();
     } else {
-        // ---------------- epilogue: warps 2..5
-        const int et = threadIdx.x - 64;  // 0..127
-        const int q = warp & 3;
-        const int r = q * 32 + lane;      // tile row = TMEM lane
+        // ---------------- epilogue: warps 2 .. 2 + kInEpiWarps - 1
+        const int et = threadIdx.x - 64;        // 0 .. kInEpiThreads - 1
+        const int q = warp & 3;                 // TMEM lane quarter
+        const int r = q * 32 + lane;            // tile row = TMEM lane
+        const int cw = ((warp - 2) >> 2) * kChPerWarp;  // this warp's first channel
         // cu_seqlens: staged and checked once per CTA.
         const bool staged = N <= kProjCuStaged;
         bool bad = false;
-        for (int j = et; j <= N; j += 128) {
+        for (int j = et; j <= N; j += kInEpiThreads) {
             const int32_t c = cu[j];
             if (staged) s_cu[j] = c;
             if (j == 0 && c != 0) bad = true;
             if (j == N && (int64_t)c != T_rows) bad = true;
             if (j < N && cu[j + 1] < c) bad = true;
         }
-        bad = named_or(1, 128, bad);  // also orders the staging above
+        bad = named_or(1, kInEpiThreads, bad);  // also orders the staging above
         if (bad && blockIdx.x == 0 && et == 0) raise_error(SC_DEV_BAD_SEQLENS);
         auto CU = [&](int j) -> int64_t { return staged ? s_cu[j] : cu[j]; };
         unsigned char *urow = u_tile + r * kUStride;
@@ -414,48 +427,58 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tw.at(grp, n_ctiles, mt, ct);
             const int h0 = ct * kConvCh;
             const int64_t t = (int64_t)mt * OUT - (K - 1) + r;  // global row (past T: no output)
-            // This tile's taps and bias (the previous tile is done with them).
-            for (int e = et; e < kConvCh * K; e += 128)
-                wts[e] = __bfloat162float(w[(int64_t)h0 * K + e]);
+            // This tile's taps (tap-major: wts[k * 64 + c]) and bias; the previous
+            // tile is done with them.
+            for (int e = et; e < kConvCh * K; e += kInEpiThreads)
+                wts[(e % K) * kConvCh + e / K] = __bfloat162float(w[(int64_t)h0 * K + e]);
             if (bias != nullptr)
-                for (int e = et; e < kConvCh; e += 128) bsm[e] = __bfloat162float(bias[h0 + e]);
-            if (!epi_acquire(ps, it)) break;
+                for (int e = et; e < kConvCh; e += kInEpiThreads)
+                    bsm[e] = __bfloat162float(bias[h0 + e]);
+            if (!epi_acquire(ps, it, kInEpiThreads)) break;
             const uint32_t trow =
-                tmem + (uint32_t)(it % kAccBufs) * 256u + ((uint32_t)(q * 32) << 16);
+                tmem + (uint32_t)(it % kAccBufs) * 256u + ((uint32_t)(q * 32) << 16) + cw;
 
-            // Phase A: u = round(round(B) round(x)) of every tile row into u_tile.
+            // Phase A: this warp's channels of B, C and x, all loads in flight at
+            // once; u = round(round(B) round(x)) into u_tile; C kept rounded.
+            constexpr int NC = kChPerWarp / 16;  // 16-channel chunks of this warp
+            uint32_t rb[NC][16], rx[NC][16], rc[NC][16];
             __syncwarp();  // tcgen05.ld is warp-collective: lanes converge first
 #pragma unroll
-            for (int cc = 0; cc < kConvCh / 16; ++cc) {
-                float bv[16], xv[16];
-                tmem_ld16(trow + cc * 16, bv);
-                tmem_ld16(trow + 2 * kConvCh + cc * 16, xv);
+            for (int cc = 0; cc < NC; ++cc) {
+                tmem_ld16_nowait(trow + cc * 16, rb[cc]);
+                tmem_ld16_nowait(trow + 2 * kConvCh + cc * 16, rx[cc]);
+                tmem_ld16_nowait(trow + kConvCh + cc * 16, rc[cc]);
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc) {
+                tmem_regs_ready(rb[cc]);
+                tmem_regs_ready(rx[cc]);
+                tmem_regs_ready(rc[cc]);
+            }
+            epi_release<CL>(ps, it, tw.rank);  // the accumulator buffer is read
+            float cv[NC][16];
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc) {
                 uint32_t pk[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float u0 =
-                        __fmul_rn(Dt<bf16>::round(bv[2 * j]), Dt<bf16>::round(xv[2 * j]));
-                    const float u1 = __fmul_rn(Dt<bf16>::round(bv[2 * j + 1]),
-                                               Dt<bf16>::round(xv[2 * j + 1]));
+                    const float u0 = __fmul_rn(Dt<bf16>::round(__uint_as_float(rb[cc][2 * j])),
+                                               Dt<bf16>::round(__uint_as_float(rx[cc][2 * j])));
+                    const float u1 =
+                        __fmul_rn(Dt<bf16>::round(__uint_as_float(rb[cc][2 * j + 1])),
+                                  Dt<bf16>::round(__uint_as_float(rx[cc][2 * j + 1])));
                     pk[j] = pack_bf16(u0, u1);
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(urow + cc * 32);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) cv[cc][j] = Dt<bf16>::round(__uint_as_float(rc[cc][j]));
+                uint4 *dst = reinterpret_cast<uint4 *>(urow + (cw + cc * 16) * 2);
                 dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
-            // C of this row, then the buffer goes back to the MMA lane.
-            float cv[kConvCh];
-#pragma unroll
-            for (int cc = 0; cc < kConvCh / 16; ++cc) {
-                float tmp[16];
-                tmem_ld16(trow + kConvCh + cc * 16, tmp);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) cv[cc * 16 + j] = Dt<bf16>::round(tmp[j]);
-            }
-            epi_release<CL>(ps, it, tw.rank);
-            named_sync(1, 128);  // u_tile, taps and bias complete
+            named_sync(1, kInEpiThreads);  // u_tile, taps and bias complete
 
-            // Phase B: outputs of rows K-1 .. 127 of the tile.
+            // Phase B: outputs of rows K-1 .. 127 of the tile, this warp's channels.
             bool out_row = r >= K - 1 && t < T_rows && !bad;
             int i = 0, slot = 0;
             int64_t s0 = 0, s1 = 0;
@@ -477,19 +500,29 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (out_row) {
                 const bool fresh_hist = t - s0 >= K - 1;  // whole window inside the sequence
 #pragma unroll
-                for (int cc = 0; cc < kConvCh / 16; ++cc) {
-                    float win[K][16];
+                for (int sc8 = 0; sc8 < kChPerWarp / 8; ++sc8) {  // 8-channel sub-chunks
+                    const int c0 = cw + sc8 * 8;  // first channel of the sub-chunk in the tile
+                    float win[K][8], wk[K][8], bv[8];
 #pragma unroll
                     for (int k = 0; k < K; ++k) {
-                        const uint4 *src = reinterpret_cast<const uint4 *>(
-                            u_tile + (r - (K - 1) + k) * kUStride + cc * 32);
-                        const uint4 a = src[0], b2 = src[1];
-                        const uint32_t wd[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
+                        const uint4 a = *reinterpret_cast<const uint4 *>(
+                            u_tile + (r - (K - 1) + k) * kUStride + c0 * 2);
+                        const uint32_t wd[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
+                        for (int j = 0; j < 4; ++j) {
                             win[k][2 * j] = bf16_lo(wd[j]);
                             win[k][2 * j + 1] = bf16_hi(wd[j]);
                         }
+                        const float4 *tp = reinterpret_cast<const float4 *>(wts + k * kConvCh + c0);
+                        const float4 t0 = tp[0], t1 = tp[1];
+                        wk[k][0] = t0.x; wk[k][1] = t0.y; wk[k][2] = t0.z; wk[k][3] = t0.w;
+                        wk[k][4] = t1.x; wk[k][5] = t1.y; wk[k][6] = t1.z; wk[k][7] = t1.w;
+                    }
+                    if (bias != nullptr) {
+                        const float4 *bp = reinterpret_cast<const float4 *>(bsm + c0);
+                        const float4 b0 = bp[0], b1 = bp[1];
+                        bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w;
+                        bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
                     }
                     if (!fresh_hist) {  // window positions before the sequence start: its slot
                         const int64_t rs = t - s0;
@@ -498,40 +531,38 @@ __global__ void __launch_bounds__(kPThreads, 1)
                             const int64_t e = rs + 1 + k;  // index into [state; u_s0 ...]
                             if (e < K)
 #pragma unroll
-                                for (int j = 0; j < 16; ++j)
+                                for (int j = 0; j < 8; ++j)
                                     win[k][j] = __bfloat162float(
-                                        pool[((int64_t)slot * H + h0 + cc * 16 + j) * K + e]);
+                                        pool[((int64_t)slot * H + h0 + c0 + j) * K + e]);
                         }
                     }
-                    uint32_t pk[8];
+                    uint32_t pk[4];
 #pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
+                    for (int j = 0; j < 8; j += 2) {
                         float o[2];
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
-                            const int c = cc * 16 + j + hh;
-                            float z = wts[c * K] * win[0][j + hh];
+                            float z = wk[0][j + hh] * win[0][j + hh];
 #pragma unroll
-                            for (int k = 1; k < K; ++k) z = fmaf(wts[c * K + k], win[k][j + hh], z);
-                            if (bias != nullptr) z = z + bsm[c];
-                            o[hh] = cv[c] * z;
+                            for (int k = 1; k < K; ++k) z = fmaf(wk[k][j + hh], win[k][j + hh], z);
+                            if (bias != nullptr) z = z + bv[j + hh];
+                            o[hh] = cv[sc8 >> 1][(sc8 & 1) * 8 + j + hh] * z;
                         }
                         pk[j / 2] = pack_bf16(o[0], o[1]);
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>(y + t * (int64_t)H + h0 + cc * 16);
-                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    *reinterpret_cast<uint4 *>(y + t * (int64_t)H + h0 + c0) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     if (t >= s1 - K) {  // one of the sequence's last K rows: its u to the tail
                         const int m = (int)(K - (s1 - t));
-                        const uint16_t *ur = reinterpret_cast<const uint16_t *>(urow + cc * 32);
+                        const uint16_t *ur = reinterpret_cast<const uint16_t *>(urow + c0 * 2);
                         uint16_t *tl = reinterpret_cast<uint16_t *>(tail);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            tl[((int64_t)i * H + h0 + cc * 16 + j) * K + m] = ur[j];
+                        for (int j = 0; j < 8; ++j)
+                            tl[((int64_t)i * H + h0 + c0 + j) * K + m] = ur[j];
                     }
                 }
             }
-            named_sync(1, 128);  // u_tile, taps and bias free for the next tile
+            named_sync(1, kInEpiThreads);  // u_tile, taps and bias free for the next tile
         }
     }
     pipe_finish<CL>(tmem);
@@ -586,7 +617,7 @@ __global__ void __launch_bounds__(256)
 // ------------------------------------------------------------ out_proj
 
 template <int CL>
-__global__ void __launch_bounds__(kPThreads, 1)
+__global__ void __launch_bounds__(kOutThreads, 1)
     k_out_proj(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                int64_t M_rows, int Kdim, int N_cols, bf16 *__restrict__ out, int n_ntiles,
                int n_mtiles) {
@@ -596,7 +627,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t stages = smem_addr(base);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = Kdim / kPBK;
-    const uint32_t tmem = pipe_start<CL>(ps, &map_a, &map_b);
+    const uint32_t tmem = pipe_start<CL>(ps, &map_a, &map_b, 4);
     const TileWalk tw = tile_walk<CL>(n_mtiles, n_ntiles);
 
     if (warp == 0) {
@@ -619,7 +650,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tw.at(grp, n_ntiles, mt, nt);
             const int64_t t = (int64_t)mt * kPBM + q * 32 + lane;  // past M_rows: no store
             const int col0 = nt * kOutN;
-            if (!epi_acquire(ps, it)) break;
+            if (!epi_acquire(ps, it, 128)) break;
             const uint32_t trow =
                 tmem + (uint32_t)(it % kAccBufs) * 256u + ((uint32_t)(q * 32) << 16);
             const bool store = t < M_rows;
@@ -695,7 +726,8 @@ static cudaError_t smem_opt_in(F kern, size_t bytes, std::atomic<unsigned long l
 // How many clusters of kPCluster CTAs of `kern` fit on the device at once
 // (the persistent grid), cached per device.
 template <typename F>
-static cudaError_t max_clusters(F kern, size_t smem, int sm_count, std::atomic<int> (&cache)[64],
+static cudaError_t max_clusters(F kern, size_t smem, int threads, int sm_count,
+                                std::atomic<int> (&cache)[64],
                                 int *out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -708,7 +740,7 @@ static cudaError_t max_clusters(F kern, size_t smem, int sm_count, std::atomic<i
     if (kPCluster > 1) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(kPCluster * (sm_count / kPCluster)));
-        cfg.blockDim = dim3(kPThreads);
+        cfg.blockDim = dim3((unsigned)threads);
         cfg.dynamicSmemBytes = smem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -742,13 +774,13 @@ static cudaError_t in_proj_inst(const CUtensorMap &mh, const CUtensorMap &mw, in
         if (e != cudaSuccess) return e;
         static std::atomic<int> cache[64];
         int clusters = 0;
-        e = max_clusters(kern, conv_smem_bytes(), sm_count, cache, &clusters);
+        e = max_clusters(kern, conv_smem_bytes(), kInThreads, sm_count, cache, &clusters);
         if (e != cudaSuccess) return e;
         const int n_ctiles = H / kConvCh;
         const int64_t n_mtiles = (T + OUT - 1) / OUT;
         const int64_t groups = (n_mtiles + kPCluster - 1) / kPCluster * n_ctiles;
         const int grid = kPCluster * (int)(groups < clusters ? groups : clusters);  // persistent
-        e = launch_pdl_cluster(kern, dim3((unsigned)grid), dim3(kPThreads), conv_smem_bytes(),
+        e = launch_pdl_cluster(kern, dim3((unsigned)grid), dim3(kInThreads), conv_smem_bytes(),
                                stream, kPCluster, mh, mw, T, D, H, (const bf16 *)w,
                                (const bf16 *)bias, cu, N, slots, (const bf16 *)pool, n_slots,
                                (bf16 *)y, (bf16 *)tail, n_ctiles, (int)n_mtiles);
@@ -795,13 +827,13 @@ cudaError_t launch_out_proj(int H, int D, const void *y, int64_t T, const void *
     if (e != cudaSuccess) return e;
     static std::atomic<int> cache[64];
     int clusters = 0;
-    e = max_clusters(kern, out_smem_bytes(), sm_count, cache, &clusters);
+    e = max_clusters(kern, out_smem_bytes(), kOutThreads, sm_count, cache, &clusters);
     if (e != cudaSuccess) return e;
     const int n_ntiles = D / kOutN;
     const int64_t n_mtiles = (T + kPBM - 1) / kPBM;
     const int64_t groups = (n_mtiles + kPCluster - 1) / kPCluster * n_ntiles;
     const int grid = kPCluster * (int)(groups < clusters ? groups : clusters);  // persistent
-    return launch_pdl_cluster(kern, dim3((unsigned)grid), dim3(kPThreads), out_smem_bytes(),
+    return launch_pdl_cluster(kern, dim3((unsigned)grid), dim3(kOutThreads), out_smem_bytes(),
                               stream, kPCluster, ma, mb, T, H, D, (bf16 *)out, n_ntiles,
                               (int)n_mtiles);
 }
