@@ -5,7 +5,7 @@
 // through the causal depthwise conv; c * conv_out goes through out_proj.
 //
 // k_in_proj_conv fuses everything up to out_proj into the in_proj GEMM: a CTA
-// computes the 128 x 192 product block [B | C | x] of 64 channels for 128
+// pair computes the [B | C | x] product block of 128 channels for 2 x 128
 // rows (bf16 operands streamed by tiled TMA through a 4-stage ring, fp32
 // accumulators in TMEM), and its epilogue rounds B, C, x to bf16 (the values
 // a separate in_proj would store), forms u = round(B x), runs the K-tap conv
@@ -54,30 +54,34 @@ constexpr uint32_t kPABytes = kPBM * kPBK * 2;  // 16 KB
 #ifndef SC_PROJ_CLUSTER
 #define SC_PROJ_CLUSTER 2  // 2: CTA pairs run 256-row MMAs (cta_group::2); 1: single CTAs
 #endif
-#ifndef SC_PROJ_ACC_BUFS
-#define SC_PROJ_ACC_BUFS 2  // TMEM accumulator buffers of 256 columns
-#endif
 #ifndef SC_INPROJ_STAGES
-#define SC_INPROJ_STAGES (SC_PROJ_CLUSTER == 2 ? 6 : 4)  // stage ring depth, fused in_proj
+#define SC_INPROJ_STAGES 4  // stage ring depth of the fused in_proj (40 KB a stage)
 #endif
 #ifndef SC_OUTPROJ_STAGES
 #define SC_OUTPROJ_STAGES (SC_PROJ_CLUSTER == 2 ? 6 : 4)  // stage ring depth, out_proj
 #endif
 constexpr int kPCluster = SC_PROJ_CLUSTER;
-constexpr int kAccBufs = SC_PROJ_ACC_BUFS;
-constexpr uint32_t kPTmemCols = 256u * kAccBufs;
+constexpr uint32_t kPTmemCols = 512;  // all of TMEM: accumulator buffers of 256 columns
 constexpr int kInStages = SC_INPROJ_STAGES;
 constexpr int kOutStages = SC_OUTPROJ_STAGES;
 constexpr int kMaxStages = 8;
 static_assert(kPCluster == 1 || kPCluster == 2, "CTA pairs or single CTAs");
-static_assert(kAccBufs == 1 || kAccBufs == 2, "one or two accumulator buffers");
 
-constexpr int kConvCh = 64;                   // channels per fused tile
-constexpr int kConvN = 3 * kConvCh;           // GEMM N: B | C | x of those channels
-constexpr int kConvBoxRows = kConvCh / kPCluster;  // B rows per TMA box (3 boxes a CTA)
-constexpr uint32_t kConvBox = kConvBoxRows * kPBK * 2;
-constexpr uint32_t kConvStage = kPABytes + 3 * kConvBox;  // 40 KB single, 28 KB a pair CTA
-constexpr int kUStride = 144;                 // bytes per u row: 128 + 16, conflict-free
+// Fused tile: the B | C | x product columns of kConvCh channels, laid out in
+// TMEM as [B | C | x] (column c, kConvCh + c, 2 kConvCh + c for channel c).
+// CTA pairs: 128 channels, one N = 256 MMA (B | C) into columns 0.. and one
+// N = 128 MMA (x) into columns 256..; 384 columns, one accumulator buffer.
+// Single CTAs: 64 channels, one N = 192 MMA; two buffers of 256 columns.
+// Either way a CTA stages A and three 64-row boxes of w_in (40 KB a stage).
+constexpr int kConvCh = kPCluster == 2 ? 128 : 64;
+constexpr int kConvN1 = kPCluster == 2 ? 256 : 192;   // first MMA's N
+constexpr int kConvN2 = kPCluster == 2 ? 128 : 0;     // second MMA's N (0: none)
+constexpr int kInBufs = kPCluster == 2 ? 1 : 2;       // accumulator buffers
+constexpr int kConvBoxRows = 64;
+constexpr uint32_t kConvBox = kConvBoxRows * kPBK * 2;   // 8 KB
+constexpr uint32_t kConvStage = kPABytes + 3 * kConvBox;  // 40 KB
+constexpr int kOutBufs = 2;
+constexpr int kUStride = kConvCh * 2 + 16;    // bytes per u row (+16: conflict-free)
 constexpr int kProjCuStaged = 512;
 #ifndef SC_INPROJ_EPI_WARPS
 #define SC_INPROJ_EPI_WARPS 8  // epilogue warps of the fused kernel: 4 or 8
@@ -88,6 +92,7 @@ constexpr int kInEpiWarps = SC_INPROJ_EPI_WARPS;
 constexpr int kInEpiThreads = 32 * kInEpiWarps;
 constexpr int kInThreads = 64 + kInEpiThreads;
 constexpr int kChPerWarp = kConvCh * 4 / kInEpiWarps;  // channels per epilogue warp
+constexpr int kChPass = 32;  // channels of one TMEM read pass (3 x 32 registers in flight)
 static_assert(kInEpiWarps == 4 || kInEpiWarps == 8, "4 or 8 epilogue warps");
 
 constexpr int kOutN = 256;                    // out_proj N per tile
@@ -222,27 +227,32 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap *ma, const CUten
             mbar_wait_bounded(&ps->empty[c % S], (c / S) & 1u);
 }
 
-// Warp 1, one lane of the (leader) CTA: per K block, 4 MMAs of K = 16 into
-// accumulator buffer it % kAccBufs (it = the CTA's tile count); a stage is
-// released when its MMAs complete, a buffer is announced full when all of
-// the tile's have.
-template <int S, int N, int CL>
+// Warp 1, one lane of the (leader) CTA: per 16-deep K step one MMA of N1
+// columns (B rows 0 .. N1/CL - 1 of the CTA's stage) into the buffer's
+// columns 0.., and, if N2 > 0, one of N2 columns (the next N2/CL B rows)
+// into columns 256..; into accumulator buffer it % NBUF (it = the CTA's tile
+// count, buffers 256 columns apart). A stage is released when its MMAs
+// complete, a buffer is announced full when all of the tile's have.
+template <int S, int N1, int N2, int CL, int NBUF>
 __device__ __forceinline__ void mma_tiles(uint32_t tmem, uint32_t stages, uint32_t stage_bytes,
                                           PipeState *ps, int nk, const TileWalk &tw) {
-    constexpr uint32_t idesc = idesc_bf16_f32(kPBM * CL, N);
+    static_assert(N2 == 0 || NBUF == 1, "a second MMA uses the second 256 columns");
+    constexpr uint32_t idesc1 = idesc_bf16_f32(kPBM * CL, N1);
+    constexpr uint32_t idesc2 = idesc_bf16_f32(kPBM * CL, N2 > 0 ? N2 : 16);
+    constexpr uint32_t b2_off = (uint32_t)(N1 / CL) * kPBK * 2;  // bytes to the second B part
     constexpr uint16_t both = 3;
     uint32_t g = 0;
     int it = 0;
     bool ok = true;
     for (int grp = tw.first; grp < tw.n_groups && ok; grp += tw.step, ++it) {
-        const int b = it % kAccBufs, use = it / kAccBufs;
+        const int b = it % NBUF, use = it / NBUF;
         if (use >= 1 && !mbar_wait_bounded(&ps->tempty[b], (uint32_t)(use - 1) & 1u)) {
             raise_error(SC_DEV_TIMEOUT);
             ps->abort = 1;
             break;
         }
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)b * 256u;
+        const uint32_t d = tmem + (uint32_t)b * 256u;  // NBUF == 1: b == 0
         for (int kb = 0; kb < nk; ++kb, ++g) {
             const uint32_t s = g % S;
             if (!mbar_wait_bounded(&ps->full[s], (g / S) & 1u)) {
@@ -254,12 +264,18 @@ __device__ __forceinline__ void mma_tiles(uint32_t tmem, uint32_t stages, uint32
             tc_fence_after();
             const uint32_t st = stages + s * stage_bytes;
             const uint64_t da = sdesc_k128(st), db = sdesc_k128(st + kPABytes);
+            const uint64_t db2 = sdesc_k128(st + kPABytes + b2_off);
 #pragma unroll
             for (int j = 0; j < kPBK / 16; ++j) {
-                if constexpr (CL == 1)
-                    mma_bf16(d, da + 2 * j, db + 2 * j, idesc, (kb | j) != 0);
-                else
-                    mma_bf16_pair(d, da + 2 * j, db + 2 * j, idesc, (kb | j) != 0);
+                const uint32_t acc = (kb | j) != 0;
+                if constexpr (CL == 1) {
+                    mma_bf16(d, da + 2 * j, db + 2 * j, idesc1, acc);
+                    if constexpr (N2 > 0) mma_bf16(d + 256u, da + 2 * j, db2 + 2 * j, idesc2, acc);
+                } else {
+                    mma_bf16_pair(d, da + 2 * j, db + 2 * j, idesc1, acc);
+                    if constexpr (N2 > 0)
+                        mma_bf16_pair(d + 256u, da + 2 * j, db2 + 2 * j, idesc2, acc);
+                }
             }
             if constexpr (CL == 1)
                 mma_commit(&ps->empty[s]);
@@ -284,9 +300,9 @@ __device__ __forceinline__ void mma_tiles(uint32_t tmem, uint32_t stages, uint32
 // Epilogue threads: wait for the accumulator buffer of the CTA's it-th tile.
 // The decision to go on is taken together (barrier-OR over the 128 threads),
 // so no thread waits at a named barrier the others have left.
+template <int NBUF>
 __device__ __forceinline__ bool epi_acquire(PipeState *ps, int it, int epi_threads) {
-    const bool ok =
-        mbar_wait_bounded(&ps->tfull[it % kAccBufs], (uint32_t)(it / kAccBufs) & 1u);
+    const bool ok = mbar_wait_bounded(&ps->tfull[it % NBUF], (uint32_t)(it / NBUF) & 1u);
     const bool fail = named_or(1, epi_threads, !ok || ps->abort != 0);
     if (!ok) raise_error(SC_DEV_TIMEOUT);
     tc_fence_after();
@@ -295,12 +311,12 @@ __device__ __forceinline__ bool epi_acquire(PipeState *ps, int it, int epi_threa
 
 // Every tcgen05.ld of the buffer has completed (tmem_ld16 waits): one lane
 // per warp releases it on the (leader's) barrier.
-template <int CL>
+template <int CL, int NBUF>
 __device__ __forceinline__ void epi_release(PipeState *ps, int it, int rank) {
     tc_fence_before();
     __syncwarp();
     if ((threadIdx.x & 31) == 0) {
-        uint64_t *bar = &ps->tempty[it % kAccBufs];
+        uint64_t *bar = &ps->tempty[it % NBUF];
         if (CL == 1 || rank == 0)
             mbar_arrive(bar);
         else
@@ -385,20 +401,23 @@ __global__ void __launch_bounds__(kInThreads, 1)
             produce_tiles<kInStages, 3, CL>(
                 &map_h, &map_w, stages, kConvStage, ps, nk, tw, n_ctiles, kConvBox,
                 [&](int mt, int ct, int &a_row, int (&rows)[3]) {
-                    // The B tile is [B | C | x] of 64 channels: 3 * CL chunks of
-                    // kConvBoxRows rows; this CTA loads chunks 3 rank .. 3 rank + 2.
                     const int h0 = ct * kConvCh;
                     a_row = mt * OUT - (K - 1);
+                    if constexpr (CL == 2) {
+                        // First MMA's B rows (B | C of 128 channels): rank 0 holds the
+                        // 128 of B, rank 1 the 128 of C; second MMA's (x): 64 each.
+                        rows[0] = tw.rank * H + h0;
+                        rows[1] = tw.rank * H + h0 + 64;
+                        rows[2] = 2 * H + h0 + 64 * tw.rank;
+                    } else {  // B | C | x of 64 channels
 #pragma unroll
-                    for (int i = 0; i < 3; ++i) {
-                        const int chunk = 3 * tw.rank + i;
-                        const int per = kConvCh / kConvBoxRows;  // chunks per block
-                        rows[i] = (chunk / per) * H + h0 + (chunk % per) * kConvBoxRows;
+                        for (int i = 0; i < 3; ++i) rows[i] = i * H + h0;
                     }
                 });
     } else if (warp == 1) {
         if (lane == 0 && tw.rank == 0)
-            mma_tiles<kInStages, kConvN, CL>(tmem, stages, kConvStage, ps, nk, tw);
+            mma_tiles<kInStages, kConvN1, kConvN2, CL, kInBufs>(tmem, stages, kConvStage, ps, nk,
+                                                                 tw);
         __syncwarp();
     } else {
         // ---------------- epilogue: warps 2 .. 2 + kInEpiWarps - 1
@@ -429,53 +448,60 @@ __global__ void __launch_bounds__(kInThreads, 1)
             const int64_t t = (int64_t)mt * OUT - (K - 1) + r;  // global row (past T: no output)
             // This tile's taps (tap-major: wts[k * 64 + c]) and bias; the previous
             // tile is done with them.
+            // (With H % 128 == 64 the last column tile is half full: its upper 64
+            // channels are computed from other weight rows or zeros, never stored.)
             for (int e = et; e < kConvCh * K; e += kInEpiThreads)
-                wts[(e % K) * kConvCh + e / K] = __bfloat162float(w[(int64_t)h0 * K + e]);
+                wts[(e % K) * kConvCh + e / K] =
+                    h0 + e / K < H ? __bfloat162float(w[(int64_t)h0 * K + e]) : 0.f;
             if (bias != nullptr)
                 for (int e = et; e < kConvCh; e += kInEpiThreads)
-                    bsm[e] = __bfloat162float(bias[h0 + e]);
-            if (!epi_acquire(ps, it, kInEpiThreads)) break;
+                    bsm[e] = h0 + e < H ? __bfloat162float(bias[h0 + e]) : 0.f;
+            if (!epi_acquire<kInBufs>(ps, it, kInEpiThreads)) break;
             const uint32_t trow =
-                tmem + (uint32_t)(it % kAccBufs) * 256u + ((uint32_t)(q * 32) << 16) + cw;
+                tmem + (uint32_t)(it % kInBufs) * 256u + ((uint32_t)(q * 32) << 16) + cw;
 
-            // Phase A: this warp's channels of B, C and x, all loads in flight at
-            // once; u = round(round(B) round(x)) into u_tile; C kept rounded.
-            constexpr int NC = kChPerWarp / 16;  // 16-channel chunks of this warp
-            uint32_t rb[NC][16], rx[NC][16], rc[NC][16];
+            // Phase A: this warp's channels in passes of kChPass, each pass with
+            // its B, x and C loads in flight at once; u = round(round(B) round(x))
+            // into u_tile; C rounded to bf16 and kept packed in registers. Then
+            // the accumulator buffer goes back to the MMA lane.
+            uint32_t cvp[kChPerWarp / 2];  // rounded C, two channels a register
             __syncwarp();  // tcgen05.ld is warp-collective: lanes converge first
 #pragma unroll
-            for (int cc = 0; cc < NC; ++cc) {
-                tmem_ld16_nowait(trow + cc * 16, rb[cc]);
-                tmem_ld16_nowait(trow + 2 * kConvCh + cc * 16, rx[cc]);
-                tmem_ld16_nowait(trow + kConvCh + cc * 16, rc[cc]);
-            }
-            tmem_ld_wait();
+            for (int p0 = 0; p0 < kChPerWarp; p0 += kChPass) {
+                constexpr int NC = kChPass / 16;
+                uint32_t rb[NC][16], rx[NC][16], rc[NC][16];
 #pragma unroll
-            for (int cc = 0; cc < NC; ++cc) {
-                tmem_regs_ready(rb[cc]);
-                tmem_regs_ready(rx[cc]);
-                tmem_regs_ready(rc[cc]);
-            }
-            epi_release<CL>(ps, it, tw.rank);  // the accumulator buffer is read
-            float cv[NC][16];
-#pragma unroll
-            for (int cc = 0; cc < NC; ++cc) {
-                uint32_t pk[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float u0 = __fmul_rn(Dt<bf16>::round(__uint_as_float(rb[cc][2 * j])),
-                                               Dt<bf16>::round(__uint_as_float(rx[cc][2 * j])));
-                    const float u1 =
-                        __fmul_rn(Dt<bf16>::round(__uint_as_float(rb[cc][2 * j + 1])),
-                                  Dt<bf16>::round(__uint_as_float(rx[cc][2 * j + 1])));
-                    pk[j] = pack_bf16(u0, u1);
+                for (int cc = 0; cc < NC; ++cc) {
+                    const uint32_t col = trow + p0 + cc * 16;
+                    tmem_ld16_nowait(col, rb[cc]);
+                    tmem_ld16_nowait(col + 2 * kConvCh, rx[cc]);
+                    tmem_ld16_nowait(col + kConvCh, rc[cc]);
                 }
+                tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) cv[cc][j] = Dt<bf16>::round(__uint_as_float(rc[cc][j]));
-                uint4 *dst = reinterpret_cast<uint4 *>(urow + (cw + cc * 16) * 2);
-                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                for (int cc = 0; cc < NC; ++cc) {
+                    tmem_regs_ready(rb[cc]);
+                    tmem_regs_ready(rx[cc]);
+                    tmem_regs_ready(rc[cc]);
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float u0 =
+                            __fmul_rn(Dt<bf16>::round(__uint_as_float(rb[cc][2 * j])),
+                                      Dt<bf16>::round(__uint_as_float(rx[cc][2 * j])));
+                        const float u1 =
+                            __fmul_rn(Dt<bf16>::round(__uint_as_float(rb[cc][2 * j + 1])),
+                                      Dt<bf16>::round(__uint_as_float(rx[cc][2 * j + 1])));
+                        pk[j] = pack_bf16(u0, u1);
+                        cvp[(p0 + cc * 16) / 2 + j] = pack_bf16(__uint_as_float(rc[cc][2 * j]),
+                                                                __uint_as_float(rc[cc][2 * j + 1]));
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(urow + (cw + p0 + cc * 16) * 2);
+                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
             }
+            epi_release<CL, kInBufs>(ps, it, tw.rank);  // the accumulator buffer is read
             named_sync(1, kInEpiThreads);  // u_tile, taps and bias complete
 
             // Phase B: outputs of rows K-1 .. 127 of the tile, this warp's channels.
@@ -502,6 +528,7 @@ __global__ void __launch_bounds__(kInThreads, 1)
 #pragma unroll
                 for (int sc8 = 0; sc8 < kChPerWarp / 8; ++sc8) {  // 8-channel sub-chunks
                     const int c0 = cw + sc8 * 8;  // first channel of the sub-chunk in the tile
+                    if (h0 + c0 >= H) break;      // past the last channel (H % 64 == 0)
                     float win[K][8], wk[K][8], bv[8];
 #pragma unroll
                     for (int k = 0; k < K; ++k) {
@@ -546,7 +573,8 @@ __global__ void __launch_bounds__(kInThreads, 1)
 #pragma unroll
                             for (int k = 1; k < K; ++k) z = fmaf(wk[k][j + hh], win[k][j + hh], z);
                             if (bias != nullptr) z = z + bv[j + hh];
-                            o[hh] = cv[sc8 >> 1][(sc8 & 1) * 8 + j + hh] * z;
+                            const uint32_t cw2 = cvp[sc8 * 4 + (j + hh) / 2];
+                            o[hh] = (hh ? bf16_hi(cw2) : bf16_lo(cw2)) * z;
                         }
                         pk[j / 2] = pack_bf16(o[0], o[1]);
                     }
@@ -640,7 +668,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                 });
     } else if (warp == 1) {
         if (lane == 0 && tw.rank == 0)
-            mma_tiles<kOutStages, kOutN, CL>(tmem, stages, kOutStage, ps, nk, tw);
+            mma_tiles<kOutStages, kOutN, 0, CL, kOutBufs>(tmem, stages, kOutStage, ps, nk, tw);
         __syncwarp();
     } else {
         const int q = warp & 3;
@@ -650,9 +678,9 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             tw.at(grp, n_ntiles, mt, nt);
             const int64_t t = (int64_t)mt * kPBM + q * 32 + lane;  // past M_rows: no store
             const int col0 = nt * kOutN;
-            if (!epi_acquire(ps, it, 128)) break;
+            if (!epi_acquire<kOutBufs>(ps, it, 128)) break;
             const uint32_t trow =
-                tmem + (uint32_t)(it % kAccBufs) * 256u + ((uint32_t)(q * 32) << 16);
+                tmem + (uint32_t)(it % kOutBufs) * 256u + ((uint32_t)(q * 32) << 16);
             const bool store = t < M_rows;
 #pragma unroll 1
             for (int cc = 0; cc < kOutN / 16; ++cc) {
@@ -667,7 +695,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                 dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
-            epi_release<CL>(ps, it, tw.rank);
+            epi_release<CL, kOutBufs>(ps, it, tw.rank);
         }
     }
     pipe_finish<CL>(tmem);
@@ -776,7 +804,7 @@ static cudaError_t in_proj_inst(const CUtensorMap &mh, const CUtensorMap &mw, in
         int clusters = 0;
         e = max_clusters(kern, conv_smem_bytes(), kInThreads, sm_count, cache, &clusters);
         if (e != cudaSuccess) return e;
-        const int n_ctiles = H / kConvCh;
+        const int n_ctiles = (H + kConvCh - 1) / kConvCh;  // the last may be half full
         const int64_t n_mtiles = (T + OUT - 1) / OUT;
         const int64_t groups = (n_mtiles + kPCluster - 1) / kPCluster * n_ctiles;
         const int grid = kPCluster * (int)(groups < clusters ? groups : clusters);  // persistent
