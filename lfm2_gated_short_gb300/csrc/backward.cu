@@ -40,6 +40,9 @@ namespace sc {
 #ifndef SC_BWD_MIN_CTAS
 #define SC_BWD_MIN_CTAS 4
 #endif
+#ifndef SC_BWD_VARLEN_MIN_CTAS
+#define SC_BWD_VARLEN_MIN_CTAS 3  // the varlen kernel holds more state per thread
+#endif
 
 constexpr int kBwdCpt = 4;                         // channels per consumer thread
 constexpr int kBwdSlice = SC_BWD_SLICE;            // channels per CTA slice
@@ -338,7 +341,7 @@ constexpr size_t bwd_varlen_smem_bytes(int CW) {
 }
 
 template <typename T, int K, bool HB>
-__global__ void __launch_bounds__(kBwdConsumers + 32, 3)
+__global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_VARLEN_MIN_CTAS)
     k_backward_varlen(const T *__restrict__ bcx, int64_t T_rows, int H, const T *__restrict__ w,
                       const T *__restrict__ bias, const int32_t *__restrict__ cu, int N,
                       const T *__restrict__ init, const T *__restrict__ dy,

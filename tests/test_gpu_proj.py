@@ -259,3 +259,47 @@ def test_layer_chain_against_the_oracle():
     out_ref = layer.out_proj("bf16", y_ref, wo)
     # y may differ from the oracle's by one bf16 rounding; out inherits that
     assert_close("bf16", out, out_ref, "out")
+
+
+def test_graph_captured_projections_match_eager_calls():
+    """Two continued in_proj-fused prefills and an out_proj each, captured in one
+    CUDA graph (tensor maps are encoded on the host at capture time), give the
+    bits of eager calls."""
+    rng = np.random.default_rng(905)
+    c1 = make_case(rng, [100, 37], 128, 128, 3)
+    c2 = make_case(rng, [60, 5], 128, 128, 3)
+    wo = dyadic(rng, (256, 128), 8, -6)
+
+    def run(graph: bool):
+        pool = dev(c1["pool"], "bf16")
+        args = []
+        for c in (c1, c2):
+            args.append((dev(c["hidden"], "bf16"), dev(c1["w_in"], "bf16"), dev(c1["w"], "bf16"),
+                         dev(c["cu"], "i32"), dev(c1["slots"], "i32")))
+        ys = [torch.empty((a[0].shape[0], 128), dtype=torch.bfloat16, device="cuda") for a in args]
+        outs = [torch.empty((a[0].shape[0], 256), dtype=torch.bfloat16, device="cuda") for a in args]
+        ws = [torch.empty(sc.in_proj_workspace_bytes(128, 3, 2), dtype=torch.uint8, device="cuda")
+              for _ in args]
+        w_out = dev(wo, "bf16")
+
+        def body():
+            for a, y, o, wsp in zip(args, ys, outs, ws):
+                sc.in_proj_prefill(*a, pool, y=y, workspace=wsp)
+                sc.out_proj(y, w_out, out=o)
+
+        if graph:
+            side = torch.cuda.Stream()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g, stream=side):
+                    body()
+            g.replay()
+        else:
+            body()
+        torch.cuda.synchronize()
+        return [host(t) for t in ys + outs + [pool]]
+
+    eager, graphed = run(False), run(True)
+    for a, b in zip(eager, graphed):
+        assert_bits(b, a, "graph vs eager")
+    assert sc.get_error() == 0
