@@ -460,11 +460,12 @@ __global__ void __launch_bounds__(kInThreads, 1)
             const uint32_t trow =
                 tmem + (uint32_t)(it % kInBufs) * 256u + ((uint32_t)(q * 32) << 16) + cw;
 
-            // Phase A: this warp's channels in passes of kChPass, each pass with
-            // its B, x and C loads in flight at once; u = round(round(B) round(x))
-            // into u_tile; C rounded to bf16 and kept packed in registers. Then
-            // the accumulator buffer goes back to the MMA lane.
-            uint32_t cvp[kChPerWarp / 2];  // rounded C, two channels a register
+            // Phase A: this warp's channels in passes of kChPass, each pass with its
+            // B, x and C loads in flight at once. Each pass only packs: B and x to
+            // bf16 pairs, u = round(B x) by one bf16x2 multiply (the exact product
+            // rounded once), C to bf16 pairs. The accumulator buffer goes back to
+            // the MMA lane after the last pass; u then goes to u_tile.
+            uint32_t up[kChPerWarp / 2], cvp[kChPerWarp / 2];  // two channels a register
             __syncwarp();  // tcgen05.ld is warp-collective: lanes converge first
 #pragma unroll
             for (int p0 = 0; p0 < kChPerWarp; p0 += kChPass) {
@@ -483,25 +484,23 @@ __global__ void __launch_bounds__(kInThreads, 1)
                     tmem_regs_ready(rb[cc]);
                     tmem_regs_ready(rx[cc]);
                     tmem_regs_ready(rc[cc]);
-                    uint32_t pk[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const float u0 =
-                            __fmul_rn(Dt<bf16>::round(__uint_as_float(rb[cc][2 * j])),
-                                      Dt<bf16>::round(__uint_as_float(rx[cc][2 * j])));
-                        const float u1 =
-                            __fmul_rn(Dt<bf16>::round(__uint_as_float(rb[cc][2 * j + 1])),
-                                      Dt<bf16>::round(__uint_as_float(rx[cc][2 * j + 1])));
-                        pk[j] = pack_bf16(u0, u1);
-                        cvp[(p0 + cc * 16) / 2 + j] = pack_bf16(__uint_as_float(rc[cc][2 * j]),
-                                                                __uint_as_float(rc[cc][2 * j + 1]));
+                        const int e = (p0 + cc * 16) / 2 + j;
+                        up[e] = bf2_mul(pack_bf16(__uint_as_float(rb[cc][2 * j]),
+                                                  __uint_as_float(rb[cc][2 * j + 1])),
+                                        pack_bf16(__uint_as_float(rx[cc][2 * j]),
+                                                  __uint_as_float(rx[cc][2 * j + 1])));
+                        cvp[e] = pack_bf16(__uint_as_float(rc[cc][2 * j]),
+                                           __uint_as_float(rc[cc][2 * j + 1]));
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>(urow + (cw + p0 + cc * 16) * 2);
-                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                 }
             }
             epi_release<CL, kInBufs>(ps, it, tw.rank);  // the accumulator buffer is read
+#pragma unroll
+            for (int e = 0; e < kChPerWarp / 2; e += 4)
+                *reinterpret_cast<uint4 *>(urow + (cw + 2 * e) * 2) =
+                    make_uint4(up[e], up[e + 1], up[e + 2], up[e + 3]);
             named_sync(1, kInEpiThreads);  // u_tile, taps and bias complete
 
             // Phase B: outputs of rows K-1 .. 127 of the tile, this warp's channels.
