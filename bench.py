@@ -379,27 +379,36 @@ def verify_section(sc, device, flush, layers=10, batch=64, D=8, n_slots=1024, st
     win = torch.empty((layers, batch, D, H, K), dtype=torch.bfloat16, device=device)
     y = torch.empty((layers, batch * D, H), dtype=torch.bfloat16, device=device)
 
-    def one_step():
+    def one_step():  # verify layer by layer, then every layer's rollback in one launch
+        for l in range(layers):
+            sc.verify(bcx[l], w[l], slots, pools[l], D, win=win[l], y=y[l])
+        sc.rollback_layers(win, accepted, slots, pools)
+
+    def one_step_per_layer():  # the same with one rollback launch per layer
         for l in range(layers):
             sc.verify(bcx[l], w[l], slots, pools[l], D, win=win[l], y=y[l])
             sc.rollback(win[l], accepted, slots, pools[l])
 
-    one_step()
-    torch.cuda.synchronize()
-    side = torch.cuda.Stream(device)
-    gr = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(gr, stream=side):
-            one_step()
-    torch.cuda.synchronize()
-    es, ee = events(steps), events(steps)
-    for s in range(steps):
-        flush()
-        es[s].record()
-        gr.replay()
-        ee[s].record()
-    torch.cuda.synchronize()
-    step_us = [es[s].elapsed_time(ee[s]) * 1e3 for s in range(steps)]
+    def graph_us(body):
+        body()
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream(device)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(gr, stream=side):
+                body()
+        torch.cuda.synchronize()
+        es, ee = events(steps), events(steps)
+        for s in range(steps):
+            flush()
+            es[s].record()
+            gr.replay()
+            ee[s].record()
+        torch.cuda.synchronize()
+        return [es[s].elapsed_time(ee[s]) * 1e3 for s in range(steps)]
+
+    step_us = graph_us(one_step)
+    per_layer_us = graph_us(one_step_per_layer)
     les, lee = events(steps), events(steps)
     for s in range(steps):
         flush()
@@ -415,7 +424,8 @@ def verify_section(sc, device, flush, layers=10, batch=64, D=8, n_slots=1024, st
                 verify_bytes_per_layer=vb, rollback_bytes_per_layer=rb,
                 verify_layer_gbs=vb / (verify_us * 1e-6) / 1e9,
                 step_gbs=layers * (vb + rb) / (statistics.median(step_us) * 1e-6) / 1e9,
-                launches_per_step=2 * layers)
+                launches_per_step=layers + 1,
+                us_per_step_per_layer_rollback=statistics.median(per_layer_us))
 
 
 def varlen_section(sc, device, reps=20):

@@ -186,6 +186,23 @@ sc_status shortconv_rollback(sc_dtype dtype, int H, int K, int N, int D, const v
                              int n_slots, void *stream);
 
 /*
+ * shortconv_rollback for L layers in one launch. A sequence's accepted length
+ * is the same in every layer (acceptance is decided per sequence from the
+ * model's output), so a serving loop rolls back all layers' states at once
+ * after verify instead of one launch per layer. Layer l's verify tape is
+ * win + l * N*D*H*K elements and its pool pool + l * n_slots*H*K elements:
+ * stacked tapes and pools, each layer laid out as shortconv_rollback's.
+ *
+ *   win [L, N, D, H, K] read; accepted int32 [N] read; slot_ids int32 [N]
+ *   read; pool [L, n_slots, H, K] written. L >= 1; L = 1 is shortconv_rollback.
+ * Device errors: as shortconv_rollback (flagged once, for all layers).
+ */
+sc_status shortconv_rollback_layers(sc_dtype dtype, int H, int K, int L, int N, int D,
+                                   const void *win, const int32_t *accepted,
+                                   const int32_t *slot_ids, void *pool, int n_slots,
+                                   void *stream);
+
+/*
  * Bytes of device workspace shortconv_backward and shortconv_backward_varlen
  * need for these sizes (fp32 partial weight and bias gradients, one block per
  * row range). Host-only; no CUDA call; depends only on the arguments.

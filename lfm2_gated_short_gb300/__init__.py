@@ -58,6 +58,8 @@ def lib() -> ctypes.CDLL:
             L.shortconv_verify.argtypes = [i32, i32, i32, p, i32, i32, p, p, p, p, i32, p, p,
                                            p]
             L.shortconv_rollback.argtypes = [i32, i32, i32, i32, i32, p, p, p, p, i32, p]
+            L.shortconv_rollback_layers.argtypes = [i32, i32, i32, i32, i32, i32, p, p, p, p,
+                                                    i32, p]
             L.shortconv_backward_workspace_bytes.argtypes = [i32, i32, i64]
             L.shortconv_backward_workspace_bytes.restype = ctypes.c_size_t
             L.shortconv_backward.argtypes = [i32, i32, i32, p, i64, p, p, p, p, p, p, p,
@@ -75,7 +77,8 @@ def lib() -> ctypes.CDLL:
             L.shortconv_get_error.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
             L.shortconv_status_string.argtypes = [i32]
             L.shortconv_status_string.restype = ctypes.c_char_p
-            for f in ("prefill", "prefill_tiled", "decode", "verify", "rollback", "backward",
+            for f in ("prefill", "prefill_tiled", "decode", "verify", "rollback",
+                      "rollback_layers", "backward",
                       "backward_varlen", "in_proj_prefill", "out_proj", "slots_claim",
                       "slots_release", "pool_copy", "get_error"):
                 getattr(L, "shortconv_" + f).restype = i32
@@ -191,6 +194,21 @@ def rollback(win, accepted, slot_ids, pool, stream=None):
         _dev(accepted, "accepted", torch.int32, (N,)),
         _dev(slot_ids, "slot_ids", torch.int32, (N,)),
         _dev(pool, "pool", dt, (pool.shape[0], H, K)), pool.shape[0],
+        _stream(stream, win.device)))
+
+
+def rollback_layers(win, accepted, slot_ids, pool, stream=None):
+    """Roll back L layers at once: ``win [L, N, D, H, K]`` (stacked verify tapes),
+    ``pool [L, n_slots, H, K]`` (stacked pools, in place)."""
+    dt = win.dtype
+    L, N, D, H, K = win.shape
+    if pool.dim() != 4 or pool.shape[0] != L:
+        raise ValueError("pool must be [L, n_slots, H, K] for win [L, N, D, H, K]")
+    _raise_on("shortconv_rollback_layers", lib().shortconv_rollback_layers(
+        _dcode(win), H, K, L, N, D, _dev(win, "win", dt),
+        _dev(accepted, "accepted", torch.int32, (N,)),
+        _dev(slot_ids, "slot_ids", torch.int32, (N,)),
+        _dev(pool, "pool", dt, (L, pool.shape[1], H, K)), pool.shape[1],
         _stream(stream, win.device)))
 
 

@@ -159,21 +159,32 @@ sc_status shortconv_verify(sc_dtype dtype, int H, int K, const void *bcx, int N,
                                        win, y, (cudaStream_t)stream));
 }
 
-sc_status shortconv_rollback(sc_dtype dtype, int H, int K, int N, int D, const void *win,
-                             const int32_t *accepted, const int32_t *slot_ids, void *pool,
-                             int n_slots, void *stream) {
+sc_status shortconv_rollback_layers(sc_dtype dtype, int H, int K, int L, int N, int D,
+                                   const void *win, const int32_t *accepted,
+                                   const int32_t *slot_ids, void *pool, int n_slots,
+                                   void *stream) {
     sc_status st = check_shape(dtype, H, K);
     if (st != SC_OK) return st;
-    if (N < 0 || D <= 0 || n_slots <= 0) return SC_EINVAL;
+    if (L <= 0 || N < 0 || D <= 0 || n_slots <= 0) return SC_EINVAL;
     const size_t es = elem_size(dtype);
-    const size_t n_win = (size_t)N * D * H * K * es, n_pool = (size_t)n_slots * H * K * es;
+    const size_t n_win = (size_t)L * N * D * H * K * es;
+    const size_t n_pool = (size_t)L * n_slots * H * K * es;
     if (!ptr_ok(win, n_win, 16) || !ptr_ok(pool, n_pool, 16) ||
         !ptr_ok(accepted, (size_t)N * 4, 4) || !ptr_ok(slot_ids, (size_t)N * 4, 4))
         return SC_EINVAL;
-    if (overlaps(pool, n_pool, win, n_win)) return SC_EINVAL;
+    if (overlaps(pool, n_pool, win, n_win) || overlaps(pool, n_pool, accepted, (size_t)N * 4) ||
+        overlaps(pool, n_pool, slot_ids, (size_t)N * 4))
+        return SC_EINVAL;
     if (N == 0) return SC_OK;
-    return from_cuda(sc::launch_rollback(dtype, H, K, N, D, win, accepted, slot_ids, pool,
+    return from_cuda(sc::launch_rollback(dtype, H, K, L, N, D, win, accepted, slot_ids, pool,
                                          n_slots, (cudaStream_t)stream));
+}
+
+sc_status shortconv_rollback(sc_dtype dtype, int H, int K, int N, int D, const void *win,
+                             const int32_t *accepted, const int32_t *slot_ids, void *pool,
+                             int n_slots, void *stream) {
+    return shortconv_rollback_layers(dtype, H, K, 1, N, D, win, accepted, slot_ids, pool,
+                                     n_slots, stream);
 }
 
 size_t shortconv_backward_workspace_bytes(int H, int K, int64_t T) {

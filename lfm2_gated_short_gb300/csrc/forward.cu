@@ -497,37 +497,42 @@ cudaError_t launch_verify(int dtype, int H, int K, const void *bcx, int N, int D
 
 // ----------------------------------------------------------------- rollback
 //
-// A plain 16-byte copy of the accepted window record into the slot.
+// A plain 16-byte copy of the accepted window record into the slot, for L
+// layers at once: layer l's tape is win + l N D (H K) and its pool
+// pool + l n_slots (H K); every layer takes the same accepted lengths.
 __global__ void __launch_bounds__(kThreads)
-    k_rollback(int N, int D, int64_t q_per_seq, const uint4 *__restrict__ win,
+    k_rollback(int L, int N, int D, int64_t q_per_seq, const uint4 *__restrict__ win,
                const int32_t *__restrict__ accepted, const int32_t *__restrict__ slots,
                uint4 *__restrict__ pool, int n_slots) {
     pdl_wait();
     pdl_launch_dependents();
     const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (unit >= (int64_t)N * q_per_seq) return;
-    const int i = (int)(unit / q_per_seq);
-    const int64_t q = unit % q_per_seq;
+    const int64_t per_layer = (int64_t)N * q_per_seq;
+    if (unit >= (int64_t)L * per_layer) return;
+    const int64_t l = unit / per_layer, rem = unit % per_layer;
+    const int i = (int)(rem / q_per_seq);
+    const int64_t q = rem % q_per_seq;
     const int a = accepted[i], slot = slots[i];
     if (a < 0 || a > D) {
-        if (q == 0) raise_error(SC_DEV_BAD_ACCEPTED);
+        if (q == 0 && l == 0) raise_error(SC_DEV_BAD_ACCEPTED);
         return;
     }
     if (slot < 0 || slot >= n_slots) {
-        if (q == 0) raise_error(SC_DEV_BAD_SLOT);
+        if (q == 0 && l == 0) raise_error(SC_DEV_BAD_SLOT);
         return;
     }
     if (a == 0) return;
-    pool[(int64_t)slot * q_per_seq + q] = win[((int64_t)i * D + (a - 1)) * q_per_seq + q];
+    pool[(l * n_slots + slot) * q_per_seq + q] =
+        win[((l * N + i) * D + (a - 1)) * q_per_seq + q];
 }
 
-cudaError_t launch_rollback(int dtype, int H, int K, int N, int D, const void *win,
+cudaError_t launch_rollback(int dtype, int H, int K, int L, int N, int D, const void *win,
                             const int32_t *accepted, const int32_t *slots, void *pool,
                             int n_slots, cudaStream_t stream) {
     const int64_t elem = dtype == SC_BF16 ? 2 : 4;
     const int64_t q_per_seq = (int64_t)H * K * elem / 16;
-    const int64_t blocks = ((int64_t)N * q_per_seq + kThreads - 1) / kThreads;
-    return launch_pdl(k_rollback, dim3((unsigned)blocks), dim3(kThreads), 0, stream, N, D,
+    const int64_t blocks = ((int64_t)L * N * q_per_seq + kThreads - 1) / kThreads;
+    return launch_pdl(k_rollback, dim3((unsigned)blocks), dim3(kThreads), 0, stream, L, N, D,
                       q_per_seq, (const uint4 *)win, accepted, slots, (uint4 *)pool, n_slots);
 }
 

@@ -26,7 +26,8 @@ cudaError_t launch_verify(int dtype, int H, int K, const void *bcx, int N, int D
                           const void *pool, int n_slots, void *win, void *y,
                           cudaStream_t stream);
 
-cudaError_t launch_rollback(int dtype, int H, int K, int N, int D, const void *win,
+// L layers at once: win [L, N, D, H, K], pool [L, n_slots, H, K].
+cudaError_t launch_rollback(int dtype, int H, int K, int L, int N, int D, const void *win,
                             const int32_t *accepted, const int32_t *slot_ids, void *pool,
                             int n_slots, cudaStream_t stream);
 

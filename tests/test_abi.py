@@ -36,6 +36,7 @@ def L():
     lib.shortconv_decode.argtypes = [i32, i32, i32, p, i32, p, p, p, p, i32, p, p]
     lib.shortconv_verify.argtypes = [i32, i32, i32, p, i32, i32, p, p, p, p, i32, p, p, p]
     lib.shortconv_rollback.argtypes = [i32, i32, i32, i32, i32, p, p, p, p, i32, p]
+    lib.shortconv_rollback_layers.argtypes = [i32, i32, i32, i32, i32, i32, p, p, p, p, i32, p]
     lib.shortconv_backward_workspace_bytes.argtypes = [i32, i32, i64]
     lib.shortconv_backward_workspace_bytes.restype = ctypes.c_size_t
     lib.shortconv_backward.argtypes = [i32, i32, i32, p, i64, p, p, p, p, p, p, p,
@@ -126,6 +127,17 @@ def test_decode_verify_rollback_argument_errors(L):
                               None) == SC_EINVAL                       # y aliases bias
     assert L.shortconv_rollback(BF16, 256, 3, 4, 2, Fp, Cp, Dp, Fp, 4, None) == SC_EINVAL
     assert L.shortconv_rollback(F32, 256, 3, 0, 2, 0, 0, 0, Ep, 4, None) == SC_OK
+
+
+def test_rollback_layers_argument_errors(L):
+    # (dtype, H, K, L, N, D, win, accepted, slots, pool, n_slots, stream)
+    f = L.shortconv_rollback_layers
+    assert f(BF16, 256, 3, 0, 4, 2, Fp, Cp, Dp, Ep, 4, None) == SC_EINVAL       # no layers
+    assert f(BF16, 256, 3, 2, 4, 2, Fp, Cp, Dp, Fp + 64, 4, None) == SC_EINVAL  # pool in the tape
+    assert f(BF16, 256, 3, 2, 4, 2, Fp, Ep + 16, Dp, Ep, 4, None) == SC_EINVAL  # accepted in pool
+    assert f(BF16, 256, 3, 2, 4, 2, Fp, Cp, Ep + 32, Ep, 4, None) == SC_EINVAL  # slots in pool
+    assert f(BF16, 256, 3, 2, 4, 2, Fp + 8, Cp, Dp, Ep, 4, None) == SC_EINVAL   # misaligned tape
+    assert f(BF16, 256, 3, 2, 0, 2, Fp, Cp, Dp, Ep, 4, None) == SC_OK           # nothing to do
 
 
 def test_backward_workspace_and_errors(L):

@@ -304,3 +304,43 @@ def test_graph_captured_layers_match_eager_calls():
     for a, b in zip(eager, graphed):
         assert_bits(b, a, "graph vs eager")
     assert sc.get_error() == 0
+
+
+def test_rollback_layers_equals_per_layer_rollback_and_oracle():
+    """One launch for all layers' states gives each layer's rollback."""
+    L, N, D, H, K = 3, 21, 5, 256, 3
+    s = wl.verify_serving(layers=L, batch=N, D=D, H=H, K=K, n_slots=40, seed=130)
+    pools = torch.stack([dev(s.pools[l], "bf16") for l in range(L)])  # [L, n_slots, H, K]
+    wins = torch.empty((L, N, D, H, K), dtype=torch.bfloat16, device="cuda")
+    slots, acc = dev(s.slot_ids, "i32"), dev(s.accepted, "i32")
+    for l in range(L):
+        sc.verify(dev(s.bcx[l], "bf16"), dev(s.w[l], "bf16"), slots, pools[l], D, win=wins[l])
+    per_layer = pools.clone()
+    sc.rollback_layers(wins, acc, slots, pools)
+    for l in range(L):
+        sc.rollback(wins[l], acc, slots, per_layer[l])
+    torch.cuda.synchronize()
+    assert_bits(host(pools), host(per_layer), "stacked vs per-layer rollback")
+    for l in range(L):
+        pool_ref = s.pools[l].copy()
+        st, win_ref, _ = oracle.verify("bf16", s.bcx[l], s.w[l], s.slot_ids, pool_ref, D)
+        assert st == oracle.OK
+        assert oracle.rollback("bf16", win_ref, s.accepted, s.slot_ids, pool_ref) == oracle.OK
+        assert_bits(host(pools[l]), pool_ref, f"layer {l} vs oracle")
+    assert sc.get_error() == 0
+
+
+def test_rollback_layers_flags_bad_accepted_once_and_skips_it():
+    L, N, D, H, K = 2, 4, 3, 64, 3
+    s = wl.verify_serving(layers=L, batch=N, D=D, H=H, K=K, n_slots=8, seed=131)
+    pools = torch.stack([dev(s.pools[l], "bf16") for l in range(L)])
+    wins = torch.stack([dev(wl.normal(np.random.default_rng(l), (N, D, H, K), 1.0, "bf16"),
+                            "bf16") for l in range(L)])
+    acc = s.accepted.copy()
+    acc[2] = D + 1                                    # out of [0, D]
+    before = host(pools)
+    sc.rollback_layers(wins, dev(acc, "i32"), dev(s.slot_ids, "i32"), pools)
+    assert sc.get_error() == sc.DEV_BAD_ACCEPTED
+    after = host(pools)
+    bad_slot = s.slot_ids[2]
+    assert_bits(after[:, bad_slot], before[:, bad_slot], "skipped sequence's slots")
