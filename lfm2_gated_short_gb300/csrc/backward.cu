@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_VARLEN_MIN_CTAS)
         if constexpr (HB) load_bias_pairs<T, CPT>(bias, h0, bp);
     }
     const f32x2 one2 = f2_make(1.f, 1.f);
-    f32x2 uw[K][NP], dzw[K][NP], dzf[KH][NP], dfin[K][NP];
+    f32x2 uw[K][NP], dzw[K][NP], dfin[K][NP];
     Sec<T, CPT> rbq[KH], rxq[KH];
     int i = 0;
     int64_t s0 = 0, s1 = 0;
@@ -475,7 +475,6 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_VARLEN_MIN_CTAS)
         else
             zero(uw);
         zero(dzw);
-        zero(dzf);
         if (d_final != nullptr && s1 - K < cr1)  // needed only for the last K rows
             load_taps<float, CPT, K>(d_final + ((int64_t)i * H + h0) * K, dfin);
         else
@@ -525,6 +524,21 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_VARLEN_MIN_CTAS)
     };
     auto write_d_init = [&]() {
         const int64_t len = s1 - s0;
+        // dz of the sequence's first K-1 rows (zero past its end), read back
+        // from global memory: dy * C rounded once in fp32, as in the row loop.
+        f32x2 dzf[KH][NP];
+#pragma unroll
+        for (int k = 0; k < KH; ++k)
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                dzf[k][q] = 0ull;
+                if (K > 1 && k < len) {
+                    const T *cp = bcx + (s0 + k) * ld + H + h0 + 2 * q;
+                    const T *gp = dy + (s0 + k) * (int64_t)H + h0 + 2 * q;
+                    dzf[k][q] = f2_mul(f2_make(ld_elem(gp), ld_elem(gp + 1)),
+                                       f2_make(ld_elem(cp), ld_elem(cp + 1)));
+                }
+            }
         float *o = d_init + ((int64_t)i * H + h0) * K;
 #pragma unroll
         for (int q = 0; q < NP; ++q)
@@ -533,7 +547,10 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_VARLEN_MIN_CTAS)
                 f32x2 g = 0ull;
 #pragma unroll
                 for (int k = 0; k < m; ++k) g = f2_fma(wp[k][q], dzf[m - 1 - k][q], g);
-                if (m >= len) g = f2_fma(f2_make(1.f, 1.f), dfin[m - len][q], g);
+#pragma unroll
+                for (int e = 0; e < K; ++e)  // final-state tap m - len (no runtime index)
+                    if (m >= len && e == m - len)
+                        g = f2_fma(f2_make(1.f, 1.f), dfin[e][q], g);
                 float lo, hi;
                 f2_split(g, lo, hi);
                 o[(2 * q) * K + m] = lo;
@@ -602,12 +619,6 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_VARLEN_MIN_CTAS)
             for (int q = 0; q < NP; ++q) dz[q] = f2_mul(fg[q], fc[q]);
             slide(uw, u);
             slide(dzw, dz);
-            const int64_t r = t - s0;
-#pragma unroll
-            for (int k = 0; k < KH; ++k)
-                if (K > 1 && r == k)
-#pragma unroll
-                    for (int q = 0; q < NP; ++q) dzf[k][q] = dz[q];
             if (t >= cr0 && t < cr1) {
                 f32x2 dc[NP];
 #pragma unroll
