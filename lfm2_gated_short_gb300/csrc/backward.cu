@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_VARLEN_MIN_CTAS)
         }
     };
     // du for row s = t-K+1 of the current sequence, then dB_s, dx_s.
-    auto emit = [&](int64_t t, const Sec<T, CPT> &b_s, const Sec<T, CPT> &x_s) {
+    auto emit = [&](int64_t t, const Sec<T, CPT> &b_s, const Sec<T, CPT> &x_s, bool fin) {
         const int64_t s = t - (K - 1);
         if (s < s0 || s < cr0 || s >= cr1) return;
         f32x2 fb[NP], fx[NP], db[NP], dx[NP];
@@ -512,9 +512,10 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_VARLEN_MIN_CTAS)
             f32x2 du = f2_mul(wp[0][q], dzw[K - 1][q]);
 #pragma unroll
             for (int k = 1; k < K; ++k) du = f2_fma(wp[k][q], dzw[K - 1 - k][q], du);
+            if (fin)  // one of the sequence's last K rows may feed the final state
 #pragma unroll
-            for (int k = 0; k < K; ++k)
-                if (f == k) du = f2_fma(f2_make(1.f, 1.f), dfin[k][q], du);
+                for (int k = 0; k < K; ++k)
+                    if (f == k) du = f2_fma(f2_make(1.f, 1.f), dfin[k][q], du);
             db[q] = f2_mul(du, fx[q]);
             dx[q] = f2_mul(du, fb[q]);
         }
@@ -566,7 +567,7 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_VARLEN_MIN_CTAS)
 #pragma unroll
         for (int j = 0; j + 1 < K; ++j) {
             slide(dzw, zz);
-            emit(s1 + j, rbq[0], rxq[0]);
+            emit(s1 + j, rbq[0], rxq[0], true);
             push_bx(rbq[0], rxq[0]);
         }
         if (owner && d_init != nullptr) write_d_init();
@@ -635,10 +636,11 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_VARLEN_MIN_CTAS)
                 }
                 Pairs<T, CPT>::store(dbcx + t * ld + H + h0, dc);
             }
+            const bool fin = t + 1 == s1;  // the sequence's last row: its tap feeds the state
             if constexpr (K == 1)
-                emit(t, b, x);
+                emit(t, b, x, fin);
             else
-                emit(t, rbq[0], rxq[0]);
+                emit(t, rbq[0], rxq[0], fin);
             push_bx(b, x);
         }
         __syncwarp();
