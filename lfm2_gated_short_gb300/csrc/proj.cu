@@ -87,7 +87,7 @@ constexpr int kProjCuStaged = 512;
 #define SC_INPROJ_EPI_WARPS 8  // epilogue warps of the fused kernel: 4 or 8
 #endif
 // Epilogue warp w reads TMEM lanes 32 (w % 4) ..; with 8 warps two share each
-// lane quarter and each takes half of the tile's 64 channels.
+// lane quarter and each takes half of the tile's channels.
 constexpr int kInEpiWarps = SC_INPROJ_EPI_WARPS;
 constexpr int kInEpiThreads = 32 * kInEpiWarps;
 constexpr int kInThreads = 64 + kInEpiThreads;

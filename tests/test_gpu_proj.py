@@ -303,3 +303,16 @@ def test_graph_captured_projections_match_eager_calls():
     for a, b in zip(eager, graphed):
         assert_bits(b, a, "graph vs eager")
     assert sc.get_error() == 0
+
+
+def test_more_sequences_than_staged_in_shared_memory():
+    """600 sequences (more than the 512 cu_seqlens entries staged in shared
+    memory): the epilogue looks rows up in global memory."""
+    rng = np.random.default_rng(910)
+    lengths = rng.integers(0, 4, size=600)
+    c = make_case(rng, lengths, 64, 128, 3)
+    y, pool = run_gpu(c)
+    y_ref, pool_ref = run_oracle(c)
+    assert sc.get_error() == 0
+    assert_close("bf16", y, y_ref, "y")
+    assert_bits(pool, pool_ref, "pool")
