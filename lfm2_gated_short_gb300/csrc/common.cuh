@@ -26,6 +26,17 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Hints that may run before pdl_wait(). prefetch_l2() warms L2 with the line
+// holding p and returns nothing to the thread; L2 is the device's point of
+// coherence, so an early fetch cannot leave a stale value anywhere a later
+// load reads. slot_hint() reads a slot id through L2 only (no L1 line is
+// allocated) to choose what to prefetch: before the wait it may be stale, so
+// it only ever picks a bounds-checked address and is read again after it.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+__device__ __forceinline__ int slot_hint(const int32_t *p) { return __ldcg(p); }
+
 // ----------------------------------------------------------- raw 128-bit I/O
 
 __device__ __forceinline__ uint4 ld_stream(const void *p) {

@@ -326,12 +326,17 @@ __global__ void __launch_bounds__(kDecodeThreads)
     k_decode(const T *__restrict__ bcx, int N, int H, const T *__restrict__ w,
              const T *__restrict__ bias, const int32_t *__restrict__ slots,
              T *__restrict__ pool, int n_slots, T *__restrict__ y) {
-    pdl_wait();
-    pdl_launch_dependents();
     const int groups = H / kCh;
     const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (unit >= (int64_t)N * groups) return;
+    const bool live = unit < (int64_t)N * groups;
     const int i = (int)(unit / groups), cg = (int)(unit % groups), h0 = cg * kCh;
+    if (live) {  // warm L2 with the slot's state while earlier kernels finish
+        const int hint = slot_hint(slots + i);
+        if (hint >= 0 && hint < n_slots) prefetch_l2(pool + ((int64_t)hint * H + h0) * K);
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    if (!live) return;
     const T *p = bcx + (int64_t)i * 3 * H + h0;
     const Row<T> rb = load_row(p), rc = load_row(p + H), rx = load_row(p + 2 * H);
     const int slot = slots[i];
@@ -393,11 +398,14 @@ cudaError_t launch_decode(int dtype, int H, int K, const void *bcx, int N, const
 // ------------------------------------------------------------------- verify
 //
 // Unit = (sequence i, channel group); the D draft steps run in order in
-// registers. All draft rows (up to kVerifyRows at a time) are requested
+// registers. All draft rows (up to VerifyRows<T> at a time) are requested
 // before the slot-dependent state load, so a sequence costs two dependent
 // memory round trips. Small CTAs spread the few units over all SMs.
 constexpr int kVerifyThreads = 64;
-constexpr int kVerifyRows = 8;
+// Draft rows held in registers at once: 8 for bf16; 4 for fp32, whose rows
+// take twice the registers (8 spilled).
+template <typename T>
+constexpr int VerifyRows = sizeof(T) == 2 ? 8 : 4;
 
 template <typename T, int K>
 __global__ void __launch_bounds__(kVerifyThreads)
@@ -405,17 +413,23 @@ __global__ void __launch_bounds__(kVerifyThreads)
              const T *__restrict__ bias, const int32_t *__restrict__ slots,
              const T *__restrict__ pool, int n_slots, T *__restrict__ win_out,
              T *__restrict__ y) {
-    pdl_wait();
-    pdl_launch_dependents();
     const int groups = H / kCh;
     const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (unit >= (int64_t)N * groups) return;
+    const bool live = unit < (int64_t)N * groups;
     const int i = (int)(unit / groups), cg = (int)(unit % groups), h0 = cg * kCh;
+    if (live) {  // warm L2 with the slot's state while earlier kernels finish
+        const int hint = slot_hint(slots + i);
+        if (hint >= 0 && hint < n_slots) prefetch_l2(pool + ((int64_t)hint * H + h0) * K);
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    if (!live) return;
+    constexpr int VR = VerifyRows<T>;
     const int64_t ld = 3 * (int64_t)H;
     const int slot = slots[i];
-    Row<T> rb[kVerifyRows], rc[kVerifyRows], rx[kVerifyRows];
+    Row<T> rb[VR], rc[VR], rx[VR];
 #pragma unroll
-    for (int jj = 0; jj < kVerifyRows; ++jj) {
+    for (int jj = 0; jj < VR; ++jj) {
         if (jj < D) {
             const T *p = bcx + ((int64_t)i * D + jj) * ld + h0;
             rb[jj] = load_row(p);
@@ -431,10 +445,10 @@ __global__ void __launch_bounds__(kVerifyThreads)
         return;
     }
     load_block<T, K>(pool + ((int64_t)slot * H + h0) * K, win);
-    for (int j0 = 0; j0 < D; j0 += kVerifyRows) {
+    for (int j0 = 0; j0 < D; j0 += VR) {
         if (j0 > 0) {
 #pragma unroll
-            for (int jj = 0; jj < kVerifyRows; ++jj) {
+            for (int jj = 0; jj < VR; ++jj) {
                 if (j0 + jj < D) {
                     const T *p = bcx + ((int64_t)i * D + j0 + jj) * ld + h0;
                     rb[jj] = load_row(p);
@@ -444,7 +458,7 @@ __global__ void __launch_bounds__(kVerifyThreads)
             }
         }
 #pragma unroll
-        for (int jj = 0; jj < kVerifyRows; ++jj) {
+        for (int jj = 0; jj < VR; ++jj) {
             if (j0 + jj < D) {
                 const int64_t t = (int64_t)i * D + j0 + jj;
                 float b[kCh], c[kCh], x[kCh], out[kCh];
