@@ -112,6 +112,21 @@ __global__ void __launch_bounds__(kStreamSlice / kStreamCpt + 32, SC_STREAM_MIN_
         mbar_fence_init();
     }
     __syncthreads();
+    // Before the dependency wait: warm L2 with cu_seqlens, the slot ids and, in
+    // the first row range, the state of the slot the first row's sequence
+    // names. In a model these come from the host or an earlier step, not from
+    // the kernel just before, so the loads after the wait hit L2. Hints only:
+    // nothing read here is used as a value (see prefetch_l2, slot_hint).
+    if (!producer && N <= kStreamStaged) {
+        for (int j = tid * 32; j <= N; j += n_consumers * 32) {
+            prefetch_l2(cu + j);
+            if (j < N) prefetch_l2(slots + j);
+        }
+        if (cr0 == 0 && active && N > 0) {
+            const int hint = slot_hint(slots);
+            if (hint >= 0 && hint < n_slots) prefetch_l2(pool + ((int64_t)hint * H + h0) * K);
+        }
+    }
     pdl_wait();  // everything below may read what earlier kernels in the stream wrote
     pdl_launch_dependents();
 
