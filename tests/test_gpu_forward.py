@@ -208,6 +208,51 @@ def test_decode_serving_256_sequences_two_layers():
         assert_bits(host(pool), ref, f"pool layer {layer}")
 
 
+@pytest.mark.parametrize("op", ["decode", "verify"])
+def test_slot_ids_rewritten_by_the_kernel_just_before(op):
+    """Decode and verify read each slot id once before their dependency wait,
+    only to prefetch that slot's state into L2. Here the
+    kernel just before them in the stream, a device-side slot claim, rewrites
+    the slot-id buffer they read, so that early read can see the old ids. The
+    results must follow the claimed slots, and the old slots must stay as they
+    were."""
+    from oracle import slots as model
+    rng = np.random.default_rng(31)
+    n_slots, H, K, N, D = 96, 512, 3, 24, 4
+    for it in range(6):
+        bm = np.zeros(model.words(n_slots), np.uint32)
+        for s_ in rng.choice(n_slots, size=40, replace=False):
+            bm[s_ // 32] |= np.uint32(1 << (int(s_) % 32))
+        pool0 = oracle.round_bf16(rng.standard_normal((n_slots, H, K)))
+        w = oracle.round_bf16(rng.standard_normal((H, K)) * 0.6)
+        rows = N if op == "decode" else N * D
+        bcx = oracle.round_bf16(rng.standard_normal((rows, 3 * H)))
+        ref_bm, ref_pool = bm.copy(), pool0.copy()
+        st, claimed = model.claim(ref_bm, n_slots, N, pool=ref_pool)
+        assert st == model.OK
+        # the buffer first holds other valid ids: slots that the claim does not take
+        old = rng.permutation(np.setdiff1d(np.arange(n_slots), claimed))[:N].astype(np.int32)
+        slot_buf = dev(old, "i32")
+        pool = dev(pool0, "bf16")
+        d_bm = torch.from_numpy(bm.view(np.int32).copy()).cuda()
+        torch.cuda.synchronize()
+        sc.slots_claim(d_bm, n_slots, N, pool=pool, slots_out=slot_buf)
+        if op == "decode":
+            y = sc.decode(dev(bcx, "bf16"), dev(w, "bf16"), slot_buf, pool)
+            st, y_ref = oracle.decode("bf16", bcx, w, claimed, ref_pool)
+            assert st == oracle.OK
+            assert_close("bf16", host(y), y_ref, f"y, pass {it}")
+        else:
+            win, y = sc.verify(dev(bcx, "bf16"), dev(w, "bf16"), slot_buf, pool, D)
+            st, win_ref, y_ref = oracle.verify("bf16", bcx, w, claimed, ref_pool, D)
+            assert st == oracle.OK
+            assert_close("bf16", host(y), y_ref, f"y, pass {it}")
+            assert_bits(host(win), win_ref, f"win, pass {it}")
+        assert_bits(host(slot_buf), claimed, f"claimed ids, pass {it}")
+        assert_bits(host(pool), ref_pool, f"pool, pass {it}")
+        assert sc.get_error() == 0
+
+
 # ----------------------------------------------------------- verify/rollback
 
 @pytest.mark.parametrize("D", [1, 3, 4, 8])
