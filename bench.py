@@ -48,6 +48,7 @@ H, K, T = 2048, 3, 4096
 E = 2  # bf16 bytes
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal, for context beside the measured peak
 KERNEL_SOURCES = ["lfm2_gated_short_gb300/csrc/forward.cu",
                   "lfm2_gated_short_gb300/csrc/prefill_stream.cuh",
                   "lfm2_gated_short_gb300/csrc/common.cuh", "lfm2_gated_short_gb300/csrc/launch.h",
@@ -235,6 +236,23 @@ def headline(sc, device, steps, warmup, dist):
     total_ms = t0.elapsed_time(t1)
     assert sc.get_error() == 0
     return dict(total_ms=total_ms, bytes=nbytes, R=R, l2=l2, inputs=(p, w, cu, slots))
+
+
+def headline_warm(sc, device, inputs, reps=200):
+    """The headline prefill with one buffer set reused every call, so its
+    inputs stay resident in L2 (67 MB against a 126 MB L2): the warm-cache
+    counterpart of the headline, reported beside it, never as the value."""
+    p, w, cu, slots = inputs
+    b = to_dev(p.bcx, "bf16", device)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+    pool = torch.zeros((1, H, K), dtype=torch.bfloat16, device=device)
+    for _ in range(5):
+        sc.prefill(b, w, cu, slots, pool, y=y)
+    torch.cuda.synchronize()
+    us = time_loop(lambda i: sc.prefill(b, w, cu, slots, pool, y=y), reps)
+    assert sc.get_error() == 0
+    nb = prefill_bytes(T, H, K, 1)
+    return dict(us=us, gbs=nb / (us * 1e-6) / 1e9, note="inputs L2-resident (same buffers every call)")
 
 
 def e2e(sc, device, inputs, steps):
@@ -695,6 +713,7 @@ def main():
 
     extras = {}
     extras["e2e"] = e2e(sc, device, h["inputs"], min(args.steps, 50))
+    extras["prefill_warm"] = headline_warm(sc, device, h["inputs"])
     extras["decode"] = decode_section(sc, device, flush)
     extras["verify"] = verify_section(sc, device, flush)
     extras["varlen"] = varlen_section(sc, device)
@@ -726,7 +745,8 @@ def main():
                      "frac": achieved / peak, "traffic": profiled_traffic(),
                      "kernel": "k_prefill_stream<bf16,K=3>", "bytes_per_launch": h["bytes"],
                      "launch_us": launch_s * 1e6,
-                     "peak_source": f"{peak_kind} hbm_gbs (copy)"},
+                     "peak_source": f"{peak_kind} hbm_gbs (copy)",
+                     "nominal_gbs": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS},
         "cpu_baseline": cpu,
         "e2e": {"value": extras["e2e"]["value"], "unit": "GB/s",
                 "h2d_bytes_per_step": extras["e2e"]["h2d"],

@@ -155,6 +155,39 @@ def test_backward_varlen_one_fresh_sequence_matches_the_single_sequence_kernel()
     np.testing.assert_array_equal(dw, host(w2))
 
 
+@pytest.mark.parametrize("K", [2, 3, 4])
+def test_split_T_backward_summed_on_the_host_equals_the_full_backward(K):
+    """Sequence-parallel training emulated on one GPU: T rows split at T1.
+
+    The first chunk's prefill leaves the state the second chunk starts from.
+    The second chunk's backward starts from that state and returns d_init, the
+    gradient of the state; the first chunk's backward takes it as d_final. The
+    chunks' dB|dC|dx, and dW summed over them on the host, must equal the
+    full-sequence backward: the oracle's within the tolerances, and the GPU's
+    single-call backward within the dW tolerance."""
+    T, T1, H = 3001, 1234, 256
+    t = wl.training(T=T, H=H, K=K, seed=720 + K)
+    w = dev(t.w, "bf16")
+    pool = torch.zeros((1, H, K), dtype=torch.bfloat16, device="cuda")
+    sc.prefill(dev(t.bcx[:T1], "bf16"), w, dev(np.array([0, T1]), "i32"),
+               dev(np.array([0]), "i32"), pool)
+    d_b, dw_b, dinit_b = sc.backward_varlen(
+        dev(t.bcx[T1:], "bf16"), w, dev(np.array([0, T - T1]), "i32"), dev(t.dy[T1:], "bf16"),
+        init_states=pool)
+    d_a, dw_a, _ = sc.backward_varlen(
+        dev(t.bcx[:T1], "bf16"), w, dev(np.array([0, T1]), "i32"), dev(t.dy[:T1], "bf16"),
+        d_final=dinit_b)
+    assert sc.get_error() == 0
+    dbcx = np.concatenate([host(d_a), host(d_b)])
+    dw = host(dw_a).astype(np.float64) + host(dw_b)
+    st, d_ref, dw_ref = oracle.backward("bf16", t.bcx, t.w, t.dy)
+    assert st == oracle.OK
+    assert_close("bf16", dbcx, d_ref, "dB|dC|dx over both chunks")
+    assert_dw_close(dw, dw_ref, "dW summed over the chunks")
+    _, dw_full = sc.backward(dev(t.bcx, "bf16"), w, dev(t.dy, "bf16"))
+    assert_dw_close(dw, host(dw_full), "dW against the single-call backward")
+
+
 def test_backward_varlen_packed_lfm2_shapes_sampled_channels():
     """16 packed sequences, lengths U{64..2048}, H=2048, K=3, with states; 64 channels checked."""
     rng = np.random.default_rng(214)
