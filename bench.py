@@ -367,6 +367,16 @@ def decode_section(sc, device, flush, layers=10, steps=64, batch=256, n_slots=10
         ee[s].record()
     torch.cuda.synchronize()
     step_us = [es[s].elapsed_time(ee[s]) * 1e3 for s in range(steps)]
+    # the same steps as eager launches (no graph), enqueued ahead of the GPU
+    xs, xe = events(steps), events(steps)
+    run_ahead()
+    for s in range(steps):
+        flush()
+        xs[s].record()
+        one_step(s)
+        xe[s].record()
+    torch.cuda.synchronize()
+    eager_us = [xs[s].elapsed_time(xe[s]) * 1e3 for s in range(steps)]
     # one layer's kernel alone (cold L2), for the per-layer roofline
     les, lee = events(steps), events(steps)
     for s in range(steps):
@@ -379,6 +389,7 @@ def decode_section(sc, device, flush, layers=10, steps=64, batch=256, n_slots=10
     assert sc.get_error() == 0
     nb = decode_bytes_per_layer(batch, H, K)
     return dict(us_per_step=statistics.median(step_us), us_per_step_mean=statistics.mean(step_us),
+                us_per_step_eager=statistics.median(eager_us),
                 layer_us=statistics.median(layer_us), bytes_per_layer=nb,
                 layer_gbs=nb / (statistics.median(layer_us) * 1e-6) / 1e9,
                 step_gbs=layers * nb / (statistics.median(step_us) * 1e-6) / 1e9,
