@@ -374,6 +374,55 @@ def test_backward_f64_central_differences():
         assert abs((loss(bcx, a) - loss(bcx, b)) / (2 * h) - dw[idx]) < 1e-7
 
 
+def _fwd64(bcx, w):
+    """The oracle's float64 forward from a zero state: y [T, H]."""
+    T, H, K = bcx.shape[0], w.shape[0], w.shape[1]
+    st, y = oracle.prefill("f64", bcx, w, [0, T], [0], np.zeros((1, H, K)))
+    assert st == oracle.OK
+    return y
+
+
+@pytest.mark.parametrize("K", [1, 3, 4])
+def test_backward_f64_adjoint_identity(K):
+    """<dy, J v> = <J^T dy, v> for a random direction v = (vB, vC, vx).
+
+    y = C * conv(w, B * x) is linear in C and bilinear in (B, x), so the
+    directional derivative is a sum of three forward calls:
+    J v = F(B, vC, x) + F(vB, C, x) + F(B, C, vx). The right side is the
+    backward's dB|dC|dx dotted with v."""
+    rng = np.random.default_rng(60 + K)
+    H, T = 5, 23
+    bcx, v = rng.standard_normal((T, 3 * H)), rng.standard_normal((T, 3 * H))
+    w, dy = rng.standard_normal((H, K)), rng.standard_normal((T, H))
+    B, C, X = np.split(bcx, 3, axis=1)
+    vB, vC, vX = np.split(v, 3, axis=1)
+    jv = (_fwd64(np.hstack([B, vC, X]), w) + _fwd64(np.hstack([vB, C, X]), w)
+          + _fwd64(np.hstack([B, C, vX]), w))
+    st, dbcx, _ = oracle.backward("f64", bcx, w, dy)
+    assert st == oracle.OK
+    lhs, rhs = float((dy * jv).sum()), float((dbcx * v).sum())
+    assert abs(lhs - rhs) <= 1e-12 * max(1.0, abs(lhs))
+
+
+@pytest.mark.parametrize("K", [2, 3, 4])
+def test_backward_f64_weight_gradient_by_linearity_in_w(K):
+    """The forward is linear in w: y(w) = sum_k w_k y(e_k), per channel, where
+    e_k is the weight with tap k = 1 in every channel. So
+    dW[h, k] = sum_t dy[t, h] y(e_k)[t, h]."""
+    rng = np.random.default_rng(70 + K)
+    H, T = 4, 19
+    bcx, w, dy = (rng.standard_normal((T, 3 * H)), rng.standard_normal((H, K)),
+                  rng.standard_normal((T, H)))
+    basis = [_fwd64(bcx, np.eye(K)[None, k].repeat(H, 0)) for k in range(K)]
+    y = _fwd64(bcx, w)
+    np.testing.assert_allclose(y, sum(w[:, k] * basis[k] for k in range(K)),
+                               rtol=1e-12, atol=1e-12)
+    st, _, dw = oracle.backward("f64", bcx, w, dy)
+    assert st == oracle.OK
+    closed = np.stack([(dy * basis[k]).sum(axis=0) for k in range(K)], axis=1)
+    np.testing.assert_allclose(dw, closed, rtol=1e-12, atol=1e-12)
+
+
 def test_backward_bf16_matches_autograd_with_straight_through_rounding():
     rng = np.random.default_rng(51)
     H, K, T = 16, 3, 40
