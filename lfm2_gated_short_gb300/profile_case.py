@@ -4,6 +4,7 @@
     python -m lfm2_gated_short_gb300.profile_case decode   --N 256  --launches 6
     python -m lfm2_gated_short_gb300.profile_case verify   --N 64 --D 8 --launches 6
     python -m lfm2_gated_short_gb300.profile_case backward --T 65536 --launches 3
+    python -m lfm2_gated_short_gb300.profile_case backward_varlen --T 65536 --seqs 57 --launches 3
     python -m lfm2_gated_short_gb300.profile_case in_proj  --T 4096 --launches 3
     python -m lfm2_gated_short_gb300.profile_case out_proj --T 4096 --launches 3
 
@@ -24,7 +25,7 @@ import lfm2_gated_short_gb300 as sc
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("op", choices=["prefill", "prefill_tiled", "decode", "verify", "backward",
-                                   "in_proj", "out_proj"])
+                                   "backward_varlen", "in_proj", "out_proj"])
     ap.add_argument("--T", type=int, default=4096)
     ap.add_argument("--H", type=int, default=2048)
     ap.add_argument("--K", type=int, default=3)
@@ -32,6 +33,7 @@ def main() -> None:
     ap.add_argument("--D", type=int, default=8)
     ap.add_argument("--slots", type=int, default=1024)
     ap.add_argument("--tile", type=int, default=8)
+    ap.add_argument("--seqs", type=int, default=16, help="packed sequences (backward_varlen)")
     ap.add_argument("--launches", type=int, default=6)
     a = ap.parse_args()
     dev = torch.device("cuda", 0)
@@ -64,6 +66,11 @@ def main() -> None:
         else:
             sets.append(dict(bcx=rnd(a.T, 3 * H), dy=rnd(a.T, H)))
     cu = torch.tensor([0, a.T], dtype=torch.int32, device=dev)
+    if a.op == "backward_varlen":  # seeded cut points: a.seqs packed sequences of T rows
+        cuts = torch.randperm(a.T - 1, generator=torch.Generator().manual_seed(7))[:a.seqs - 1] + 1
+        cu = torch.cat([torch.tensor([0]), cuts.sort().values, torch.tensor([a.T])]).to(
+            torch.int32).to(dev)
+        init = rnd(a.seqs, H, K)
     slot0 = torch.zeros(1, dtype=torch.int32, device=dev)
     slots = torch.randperm(a.slots, generator=torch.Generator().manual_seed(7))[:a.N].to(
         torch.int32).to(dev)
@@ -81,6 +88,8 @@ def main() -> None:
             sc.in_proj_prefill(s["hidden"], w_in, w, cu, slot0, s["pool"], y=s["y"])
         elif a.op == "out_proj":
             sc.out_proj(s["y"], w_out)
+        elif a.op == "backward_varlen":
+            sc.backward_varlen(s["bcx"], w, cu, s["dy"], init_states=init)
         else:
             sc.backward(s["bcx"], w, s["dy"])
     torch.cuda.synchronize()
