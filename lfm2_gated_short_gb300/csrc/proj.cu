@@ -597,12 +597,21 @@ __global__ void __launch_bounds__(kInThreads, 1)
 
 // New state of sequence i = the last K entries of [old state; u of its rows]:
 // entry m is old[len + m] when len + m < K, else tail[i][h][m]. One thread per
-// (sequence, 8 channels); nothing for empty sequences.
+// (sequence, 8 channels); nothing for empty sequences. A thread's 8 channels x
+// K taps are 16 K contiguous bytes in the pool and in the tail, moved as
+// 16-byte words. Everything that does not depend on the slot id is requested
+// at once after the wait; the old state is read only for sequences shorter
+// than K, the only ones whose new state keeps part of it.
 template <int K>
 __global__ void __launch_bounds__(256)
     k_commit_states(const int32_t *__restrict__ cu, int N, int64_t T_rows,
                     const int32_t *__restrict__ slots, const uint16_t *__restrict__ tail,
                     uint16_t *__restrict__ pool, int n_slots, int H) {
+    constexpr int NQ = kCh * K * 2 / 16;  // 16-byte words in a thread's block
+    const int groups = H / kCh;
+    const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const bool live = unit < (int64_t)N * groups;
+    const int i = live ? (int)(unit / groups) : 0, h = (int)(unit % groups) * kCh;
     pdl_wait();
     pdl_launch_dependents();
     int bad = 0;
@@ -612,33 +621,49 @@ __global__ void __launch_bounds__(256)
         if (j == N && (int64_t)c != T_rows) bad = 1;
         if (j < N && cu[j + 1] < c) bad = 1;
     }
+    int64_t len = 0;
+    int slot = 0;
+    uint4 tq[NQ];
+    if (live) {
+        len = (int64_t)cu[i + 1] - cu[i];
+        slot = slots[i];
+        const uint4 *tp = reinterpret_cast<const uint4 *>(tail + ((int64_t)i * H + h) * K);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) tq[q] = tp[q];
+    }
     if (__syncthreads_or(bad)) {
         if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(SC_DEV_BAD_SEQLENS);
         return;
     }
-    const int groups = H / kCh;
-    const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (unit >= (int64_t)N * groups) return;
-    const int i = (int)(unit / groups), h = (int)(unit % groups) * kCh;
-    const int64_t len = (int64_t)cu[i + 1] - cu[i];
-    if (len == 0) return;
-    const int slot = slots[i];
+    if (!live || len == 0) return;
     if (slot < 0 || slot >= n_slots) {
         if (h == 0) raise_error(SC_DEV_BAD_SLOT);
         return;
     }
+    uint4 *sp = reinterpret_cast<uint4 *>(pool + ((int64_t)slot * H + h) * K);
+    if (len >= K) {  // the new state is the sequence's last K values of u
 #pragma unroll
-    for (int c = 0; c < kCh; ++c) {
-        uint16_t *st = pool + ((int64_t)slot * H + h + c) * K;
-        const uint16_t *tl = tail + ((int64_t)i * H + h + c) * K;
-        uint16_t old[K], nw[K];
-#pragma unroll
-        for (int k = 0; k < K; ++k) old[k] = st[k];
-#pragma unroll
-        for (int m = 0; m < K; ++m) nw[m] = len + m < K ? old[len + m] : tl[m];
-#pragma unroll
-        for (int m = 0; m < K; ++m) st[m] = nw[m];
+        for (int q = 0; q < NQ; ++q) sp[q] = tq[q];
+        return;
     }
+    uint4 oq[NQ], nq[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) oq[q] = sp[q];
+    const uint16_t *o = reinterpret_cast<const uint16_t *>(oq);
+    const uint16_t *tl = reinterpret_cast<const uint16_t *>(tq);
+    uint16_t *nw = reinterpret_cast<uint16_t *>(nq);
+#pragma unroll
+    for (int c = 0; c < kCh; ++c)
+#pragma unroll
+        for (int m = 0; m < K; ++m) {
+            uint16_t v = tl[c * K + m];
+#pragma unroll
+            for (int e = 0; e < K; ++e)  // old entry e = len + m, if it exists
+                if (len + m == e) v = o[c * K + e];
+            nw[c * K + m] = v;
+        }
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) sp[q] = nq[q];
 }
 
 // ------------------------------------------------------------ out_proj
