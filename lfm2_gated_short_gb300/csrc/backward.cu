@@ -673,7 +673,10 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_VARLEN_MIN_CTAS)
 
 // out[e] = sum over row ranges g = 0 .. G-1 of partial[g][e] for the P
 // entries of a partial (dW's HK first, then dbias's): 8 warps take interleaved
-// g for 32 consecutive e, then warp 0 adds the 8 sums in order.
+// g for 32 consecutive e, then warp 0 adds the 8 sums in order. A thread's
+// (at most kRedPerWarp) partials are all requested before the first add, so
+// the call costs one memory round trip, not one per partial.
+constexpr int kRedPerWarp = (kBwdRowCtas + 7) / 8;
 __global__ void __launch_bounds__(256)
     k_dw_reduce(const float *__restrict__ partial, int64_t G, int HK, int P,
                 float *__restrict__ dw, float *__restrict__ dbias) {
@@ -682,9 +685,16 @@ __global__ void __launch_bounds__(256)
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int e = blockIdx.x * 32 + lane;
+    float v[kRedPerWarp];
+#pragma unroll
+    for (int j = 0; j < kRedPerWarp; ++j) {
+        const int64_t g = warp + 8 * j;
+        v[j] = e < P && g < G ? partial[g * P + e] : 0.f;
+    }
     float s = 0.f;
-    if (e < P)
-        for (int64_t g = warp; g < G; g += 8) s += partial[g * P + e];
+#pragma unroll
+    for (int j = 0; j < kRedPerWarp; ++j)
+        if (warp + 8 * j < G) s += v[j];
     part[warp][lane] = s;
     __syncthreads();
     if (warp == 0 && e < P) {
