@@ -47,7 +47,10 @@ namespace sc {
 constexpr int kBwdCpt = 4;                         // channels per consumer thread
 constexpr int kBwdSlice = SC_BWD_SLICE;            // channels per CTA slice
 constexpr int kBwdConsumers = kBwdSlice / kBwdCpt;
-constexpr int kBwdStages = 4;
+#ifndef SC_BWD_STAGES
+#define SC_BWD_STAGES 4  // stage ring depth (the header holds up to 16 stages' barriers)
+#endif
+constexpr int kBwdStages = SC_BWD_STAGES;
 constexpr int kBwdMinRows = 16;                    // rows per CTA at least
 constexpr int kBwdRowCtas = 152;                   // row ranges per slice (GB300: one per SM)
 constexpr int kBwdHeader = 256;                    // mbarriers
