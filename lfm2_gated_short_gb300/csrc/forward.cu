@@ -400,7 +400,10 @@ cudaError_t launch_decode(int dtype, int H, int K, const void *bcx, int N, const
 // Unit = (sequence i, channel group); the D draft steps run in order in
 // registers. All draft rows (up to VerifyRows<T> at a time) are requested
 // before the slot-dependent state load, so a sequence costs two dependent
-// memory round trips. Small CTAs spread the few units over all SMs.
+// memory round trips. Small CTAs spread the few units over all SMs. The
+// default build runs k_verify_n with 2 channels a thread: at 64 sequences
+// the 8-channel k_verify leaves a few warps per SM, each with a long chain of
+// dependent steps.
 constexpr int kVerifyThreads = 64;
 // Draft rows held in registers at once: 8 for bf16; 4 for fp32, whose rows
 // take twice the registers (8 spilled).
@@ -478,15 +481,160 @@ __global__ void __launch_bounds__(kVerifyThreads)
     }
 }
 
+// NW consecutive 32-bit words at p with A-byte accesses (p aligned to A).
+template <int NW, int A>
+__device__ __forceinline__ void ld_words(const void *p, uint32_t (&w)[NW]) {
+    static_assert((NW * 4) % A == 0, "whole accesses");
+#pragma unroll
+    for (int i = 0; i < NW * 4 / A; ++i) {
+        if constexpr (A == 16) {
+            const uint4 v = reinterpret_cast<const uint4 *>(p)[i];
+            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        } else if constexpr (A == 8) {
+            const uint2 v = reinterpret_cast<const uint2 *>(p)[i];
+            w[2 * i] = v.x; w[2 * i + 1] = v.y;
+        } else {
+            w[i] = reinterpret_cast<const uint32_t *>(p)[i];
+        }
+    }
+}
+template <int NW, int A>
+__device__ __forceinline__ void st_words(void *p, const uint32_t (&w)[NW]) {
+#pragma unroll
+    for (int i = 0; i < NW * 4 / A; ++i) {
+        if constexpr (A == 16)
+            reinterpret_cast<uint4 *>(p)[i] =
+                make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        else if constexpr (A == 8)
+            reinterpret_cast<uint2 *>(p)[i] = make_uint2(w[2 * i], w[2 * i + 1]);
+        else
+            reinterpret_cast<uint32_t *>(p)[i] = w[i];
+    }
+}
+// Element e of raw words holding T values, as fp32; and the reverse (the value
+// is rounded to T, exactly when it is already representable).
+template <typename T, int NW>
+__device__ __forceinline__ float word_elem(const uint32_t (&w)[NW], int e) {
+    if constexpr (sizeof(T) == 2)
+        return (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
+    else
+        return __uint_as_float(w[e]);
+}
+template <typename T, int NE, int NW>
+__device__ __forceinline__ void pack_words(const float (&v)[NE], uint32_t (&w)[NW]) {
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+        for (int m = 0; m < NW; ++m) w[m] = pack_bf16(v[2 * m], v[2 * m + 1]);
+    } else {
+#pragma unroll
+        for (int m = 0; m < NW; ++m) w[m] = __float_as_uint(v[m]);
+    }
+}
+
+// k_verify with CH (2 or 4) channels per thread instead of 8: 2 or 4 times the
+// threads, each with a shorter chain of draft steps and fewer registers, for
+// more warps per SM to hide the steps' latency. Same arithmetic and order.
+template <typename T, int K, int CH>
+__global__ void __launch_bounds__(kVerifyThreads)
+    k_verify_n(const T *__restrict__ bcx, int N, int D, int H, const T *__restrict__ w,
+               const T *__restrict__ bias, const int32_t *__restrict__ slots,
+               const T *__restrict__ pool, int n_slots, T *__restrict__ win_out,
+               T *__restrict__ y) {
+    constexpr int NWR = CH * (int)sizeof(T) / 4;          // words of a row section
+    constexpr int AR = NWR * 4 >= 16 ? 16 : NWR * 4;
+    constexpr int SB = CH * K * (int)sizeof(T);           // bytes of a [CH][K] block
+    constexpr int NWS = SB / 4;
+    constexpr int AS = SB % 16 == 0 ? 16 : (SB % 8 == 0 ? 8 : 4);
+    constexpr int VR = VerifyRows<T>;
+    const int groups = H / CH;
+    const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const bool live = unit < (int64_t)N * groups;
+    const int i = (int)(unit / groups), cg = (int)(unit % groups), h0 = cg * CH;
+    if (live) {  // warm L2 with the slot's state while earlier kernels finish
+        const int hint = slot_hint(slots + i);
+        if (hint >= 0 && hint < n_slots) prefetch_l2(pool + ((int64_t)hint * H + h0) * K);
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    if (!live) return;
+    const int64_t ld = 3 * (int64_t)H;
+    const int slot = slots[i];
+    uint32_t rb[VR][NWR], rc[VR][NWR], rx[VR][NWR];
+    auto load_rows = [&](int j0) {
+#pragma unroll
+        for (int jj = 0; jj < VR; ++jj) {
+            if (j0 + jj < D) {
+                const T *p = bcx + ((int64_t)i * D + j0 + jj) * ld + h0;
+                ld_words<NWR, AR>(p, rb[jj]);
+                ld_words<NWR, AR>(p + H, rc[jj]);
+                ld_words<NWR, AR>(p + 2 * H, rx[jj]);
+            }
+        }
+    };
+    load_rows(0);
+    uint32_t ww[NWS], sw[NWS], bw[NWR];
+    ld_words<NWS, AS>(w + (int64_t)h0 * K, ww);
+    if (bias != nullptr) ld_words<NWR, AR>(bias + h0, bw);
+    if (slot < 0 || slot >= n_slots) {
+        if (cg == 0) raise_error(SC_DEV_BAD_SLOT);
+        return;
+    }
+    ld_words<NWS, AS>(pool + ((int64_t)slot * H + h0) * K, sw);
+    float wt[CH][K], win[CH][K], bh[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        bh[c] = bias != nullptr ? word_elem<T>(bw, c) : 0.f;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            wt[c][k] = word_elem<T>(ww, c * K + k);
+            win[c][k] = word_elem<T>(sw, c * K + k);
+        }
+    }
+    for (int j0 = 0; j0 < D; j0 += VR) {
+        if (j0 > 0) load_rows(j0);
+#pragma unroll
+        for (int jj = 0; jj < VR; ++jj) {
+            if (j0 + jj < D) {
+                const int64_t t = (int64_t)i * D + j0 + jj;
+                float out[CH], st[CH * K];
+#pragma unroll
+                for (int c = 0; c < CH; ++c) {
+                    const float u = gate_in<T>(word_elem<T>(rb[jj], c), word_elem<T>(rx[jj], c));
+                    float z = slide_dot<K>(win[c], wt[c], u);
+                    if (bias != nullptr) z = z + bh[c];
+                    out[c] = word_elem<T>(rc[jj], c) * z;
+#pragma unroll
+                    for (int k = 0; k < K; ++k) st[c * K + k] = win[c][k];
+                }
+                uint32_t yw[NWR], stw[NWS];
+                pack_words<T>(out, yw);
+                pack_words<T>(st, stw);
+                st_words<NWR, AR>(y + t * H + h0, yw);
+                st_words<NWS, AS>(win_out + (t * H + h0) * K, stw);
+            }
+        }
+    }
+}
+
+#ifndef SC_VERIFY_CH
+#define SC_VERIFY_CH 2  // channels per verify thread: 2 or 4 (k_verify_n), 8 (k_verify)
+#endif
+
 template <typename T, int K>
 static cudaError_t verify_inst(const void *bcx, int N, int D, int H, const void *w,
                                const void *bias, const int32_t *slots, const void *pool,
                                int n_slots, void *win, void *y, cudaStream_t stream) {
-    const int64_t units = (int64_t)N * (H / kCh);
+    constexpr int CH = SC_VERIFY_CH;
+    const int64_t units = (int64_t)N * (H / CH);
     const int64_t blocks = (units + kVerifyThreads - 1) / kVerifyThreads;
-    return launch_pdl(k_verify<T, K>, dim3((unsigned)blocks), dim3(kVerifyThreads), 0, stream,
-                      (const T *)bcx, N, D, H, (const T *)w, (const T *)bias, slots,
-                      (const T *)pool, n_slots, (T *)win, (T *)y);
+    if constexpr (CH == 8)
+        return launch_pdl(k_verify<T, K>, dim3((unsigned)blocks), dim3(kVerifyThreads), 0,
+                          stream, (const T *)bcx, N, D, H, (const T *)w, (const T *)bias, slots,
+                          (const T *)pool, n_slots, (T *)win, (T *)y);
+    else
+        return launch_pdl(k_verify_n<T, K, CH>, dim3((unsigned)blocks), dim3(kVerifyThreads),
+                          0, stream, (const T *)bcx, N, D, H, (const T *)w, (const T *)bias,
+                          slots, (const T *)pool, n_slots, (T *)win, (T *)y);
 }
 
 template <typename T>
