@@ -312,6 +312,56 @@ cudaError_t launch_prefill(int dtype, int H, int K, const void *bcx, int64_t row
     return prefill_K<float>(K, L, bcx, rows, H, w, bias, cu, N, slots, pool, n_slots, y, s);
 }
 
+// NW consecutive 32-bit words at p with A-byte accesses (p aligned to A).
+template <int NW, int A>
+__device__ __forceinline__ void ld_words(const void *p, uint32_t (&w)[NW]) {
+    static_assert((NW * 4) % A == 0, "whole accesses");
+#pragma unroll
+    for (int i = 0; i < NW * 4 / A; ++i) {
+        if constexpr (A == 16) {
+            const uint4 v = reinterpret_cast<const uint4 *>(p)[i];
+            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        } else if constexpr (A == 8) {
+            const uint2 v = reinterpret_cast<const uint2 *>(p)[i];
+            w[2 * i] = v.x; w[2 * i + 1] = v.y;
+        } else {
+            w[i] = reinterpret_cast<const uint32_t *>(p)[i];
+        }
+    }
+}
+template <int NW, int A>
+__device__ __forceinline__ void st_words(void *p, const uint32_t (&w)[NW]) {
+#pragma unroll
+    for (int i = 0; i < NW * 4 / A; ++i) {
+        if constexpr (A == 16)
+            reinterpret_cast<uint4 *>(p)[i] =
+                make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        else if constexpr (A == 8)
+            reinterpret_cast<uint2 *>(p)[i] = make_uint2(w[2 * i], w[2 * i + 1]);
+        else
+            reinterpret_cast<uint32_t *>(p)[i] = w[i];
+    }
+}
+// Element e of raw words holding T values, as fp32; and the reverse (the value
+// is rounded to T, exactly when it is already representable).
+template <typename T, int NW>
+__device__ __forceinline__ float word_elem(const uint32_t (&w)[NW], int e) {
+    if constexpr (sizeof(T) == 2)
+        return (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
+    else
+        return __uint_as_float(w[e]);
+}
+template <typename T, int NE, int NW>
+__device__ __forceinline__ void pack_words(const float (&v)[NE], uint32_t (&w)[NW]) {
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+        for (int m = 0; m < NW; ++m) w[m] = pack_bf16(v[2 * m], v[2 * m + 1]);
+    } else {
+#pragma unroll
+        for (int m = 0; m < NW; ++m) w[m] = __float_as_uint(v[m]);
+    }
+}
+
 // ------------------------------------------------------------------- decode
 //
 #ifndef SC_DECODE_THREADS
@@ -364,15 +414,83 @@ __global__ void __launch_bounds__(kDecodeThreads)
     store_block<T, K>(st, win);
 }
 
+// k_decode with CH (2 or 4) channels per thread instead of 8.
+template <typename T, int K, int CH>
+__global__ void __launch_bounds__(kDecodeThreads)
+    k_decode_n(const T *__restrict__ bcx, int N, int H, const T *__restrict__ w,
+               const T *__restrict__ bias, const int32_t *__restrict__ slots,
+               T *__restrict__ pool, int n_slots, T *__restrict__ y) {
+    constexpr int NWR = CH * (int)sizeof(T) / 4;
+    constexpr int AR = NWR * 4 >= 16 ? 16 : NWR * 4;
+    constexpr int SB = CH * K * (int)sizeof(T);
+    constexpr int NWS = SB / 4;
+    constexpr int AS = SB % 16 == 0 ? 16 : (SB % 8 == 0 ? 8 : 4);
+    const int groups = H / CH;
+    const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const bool live = unit < (int64_t)N * groups;
+    const int i = (int)(unit / groups), cg = (int)(unit % groups), h0 = cg * CH;
+    if (live) {  // warm L2 with the slot's state while earlier kernels finish
+        const int hint = slot_hint(slots + i);
+        if (hint >= 0 && hint < n_slots) prefetch_l2(pool + ((int64_t)hint * H + h0) * K);
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    if (!live) return;
+    const T *p = bcx + (int64_t)i * 3 * H + h0;
+    uint32_t rb[NWR], rc[NWR], rx[NWR], ww[NWS], sw[NWS], bw[NWR];
+    ld_words<NWR, AR>(p, rb);
+    ld_words<NWR, AR>(p + H, rc);
+    ld_words<NWR, AR>(p + 2 * H, rx);
+    const int slot = slots[i];
+    ld_words<NWS, AS>(w + (int64_t)h0 * K, ww);
+    if (bias != nullptr) ld_words<NWR, AR>(bias + h0, bw);
+    if (slot < 0 || slot >= n_slots) {
+        if (cg == 0) raise_error(SC_DEV_BAD_SLOT);
+        return;
+    }
+    T *st = pool + ((int64_t)slot * H + h0) * K;
+    ld_words<NWS, AS>(st, sw);
+    float out[CH], nst[CH * K];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        float win[K], wt[K];
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            win[k] = word_elem<T>(sw, c * K + k);
+            wt[k] = word_elem<T>(ww, c * K + k);
+        }
+        float z = slide_dot<K>(win, wt, gate_in<T>(word_elem<T>(rb, c), word_elem<T>(rx, c)));
+        if (bias != nullptr) z = z + word_elem<T>(bw, c);
+        out[c] = word_elem<T>(rc, c) * z;
+#pragma unroll
+        for (int k = 0; k < K; ++k) nst[c * K + k] = win[k];
+    }
+    uint32_t yw[NWR], stw[NWS];
+    pack_words<T>(out, yw);
+    pack_words<T>(nst, stw);
+    st_words<NWR, AR>(y + (int64_t)i * H + h0, yw);
+    st_words<NWS, AS>(st, stw);
+}
+
+#ifndef SC_DECODE_CH
+#define SC_DECODE_CH 4  // channels per decode thread: 4 or 2 (k_decode_n), 8 (k_decode)
+#endif
+
 template <typename T, int K>
 static cudaError_t decode_inst(const void *bcx, int N, int H, const void *w, const void *bias,
                                const int32_t *slots, void *pool, int n_slots, void *y,
                                cudaStream_t stream) {
-    const int64_t units = (int64_t)N * (H / kCh);
+    constexpr int CH = SC_DECODE_CH;
+    const int64_t units = (int64_t)N * (H / CH);
     const int64_t blocks = (units + kDecodeThreads - 1) / kDecodeThreads;
-    return launch_pdl(k_decode<T, K>, dim3((unsigned)blocks), dim3(kDecodeThreads), 0, stream,
-                      (const T *)bcx, N, H, (const T *)w, (const T *)bias, slots, (T *)pool,
-                      n_slots, (T *)y);
+    if constexpr (CH == 8)
+        return launch_pdl(k_decode<T, K>, dim3((unsigned)blocks), dim3(kDecodeThreads), 0,
+                          stream, (const T *)bcx, N, H, (const T *)w, (const T *)bias, slots,
+                          (T *)pool, n_slots, (T *)y);
+    else
+        return launch_pdl(k_decode_n<T, K, CH>, dim3((unsigned)blocks), dim3(kDecodeThreads),
+                          0, stream, (const T *)bcx, N, H, (const T *)w, (const T *)bias, slots,
+                          (T *)pool, n_slots, (T *)y);
 }
 
 template <typename T>
@@ -478,56 +596,6 @@ __global__ void __launch_bounds__(kVerifyThreads)
                 store_block<T, K>(win_out + (t * H + h0) * K, win);
             }
         }
-    }
-}
-
-// NW consecutive 32-bit words at p with A-byte accesses (p aligned to A).
-template <int NW, int A>
-__device__ __forceinline__ void ld_words(const void *p, uint32_t (&w)[NW]) {
-    static_assert((NW * 4) % A == 0, "whole accesses");
-#pragma unroll
-    for (int i = 0; i < NW * 4 / A; ++i) {
-        if constexpr (A == 16) {
-            const uint4 v = reinterpret_cast<const uint4 *>(p)[i];
-            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-        } else if constexpr (A == 8) {
-            const uint2 v = reinterpret_cast<const uint2 *>(p)[i];
-            w[2 * i] = v.x; w[2 * i + 1] = v.y;
-        } else {
-            w[i] = reinterpret_cast<const uint32_t *>(p)[i];
-        }
-    }
-}
-template <int NW, int A>
-__device__ __forceinline__ void st_words(void *p, const uint32_t (&w)[NW]) {
-#pragma unroll
-    for (int i = 0; i < NW * 4 / A; ++i) {
-        if constexpr (A == 16)
-            reinterpret_cast<uint4 *>(p)[i] =
-                make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-        else if constexpr (A == 8)
-            reinterpret_cast<uint2 *>(p)[i] = make_uint2(w[2 * i], w[2 * i + 1]);
-        else
-            reinterpret_cast<uint32_t *>(p)[i] = w[i];
-    }
-}
-// Element e of raw words holding T values, as fp32; and the reverse (the value
-// is rounded to T, exactly when it is already representable).
-template <typename T, int NW>
-__device__ __forceinline__ float word_elem(const uint32_t (&w)[NW], int e) {
-    if constexpr (sizeof(T) == 2)
-        return (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
-    else
-        return __uint_as_float(w[e]);
-}
-template <typename T, int NE, int NW>
-__device__ __forceinline__ void pack_words(const float (&v)[NE], uint32_t (&w)[NW]) {
-    if constexpr (sizeof(T) == 2) {
-#pragma unroll
-        for (int m = 0; m < NW; ++m) w[m] = pack_bf16(v[2 * m], v[2 * m + 1]);
-    } else {
-#pragma unroll
-        for (int m = 0; m < NW; ++m) w[m] = __float_as_uint(v[m]);
     }
 }
 
