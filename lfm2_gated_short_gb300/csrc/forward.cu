@@ -522,7 +522,10 @@ cudaError_t launch_decode(int dtype, int H, int K, const void *bcx, int N, const
 // default build runs k_verify_n with 2 channels a thread: at 64 sequences
 // the 8-channel k_verify leaves a few warps per SM, each with a long chain of
 // dependent steps.
-constexpr int kVerifyThreads = 64;
+#ifndef SC_VERIFY_THREADS
+#define SC_VERIFY_THREADS 64  // threads per verify CTA (build-time knob)
+#endif
+constexpr int kVerifyThreads = SC_VERIFY_THREADS;
 // Draft rows held in registers at once: 8 for bf16; 4 for fp32, whose rows
 // take twice the registers (8 spilled).
 template <typename T>
