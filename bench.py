@@ -721,6 +721,15 @@ def reference_arm(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def with_fracs(section, peak):
+    """The section with each GB/s figure also given as a fraction of the HBM peak."""
+    out = dict(section)
+    for k, v in section.items():
+        if k.endswith("gbs") and isinstance(v, (int, float)):
+            out[k[:-3] + "frac"] = v / peak
+    return out
+
+
 def config_dict(h):
     d = {"workload": WORKLOAD, "H": H, "K": K, "T": T, "n_seqs": 1,
          "parallelism": "independent replicas, one per GPU"}
@@ -817,7 +826,7 @@ def main():
                 "serial_value": extras["e2e"]["value_serial"]},
         "clocks": clk,
         "gpu_launches": args.steps,
-        "sections": {k: v for k, v in extras.items() if k != "e2e"},
+        "sections": {k: with_fracs(v, peak) for k, v in extras.items() if k != "e2e"},
     }
     log(json.dumps(line, indent=1))
     print(json.dumps(line), flush=True)
