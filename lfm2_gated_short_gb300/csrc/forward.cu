@@ -369,57 +369,15 @@ __device__ __forceinline__ void pack_words(const float (&v)[NE], uint32_t (&w)[N
 #endif
 constexpr int kDecodeThreads = SC_DECODE_THREADS;
 //
-// Unit = (sequence i, channel group). The token's B, C, x loads do not depend
+// Unit = (sequence i, CH channels). The token's B, C, x loads do not depend
 // on the slot id, so they are issued before the slot-dependent state load.
-template <typename T, int K>
+// CH = 4 by default: at 256 sequences both 8 channels a thread (fewer
+// threads to hide the two round trips) and 2 measured slower.
+template <typename T, int K, int CH>
 __global__ void __launch_bounds__(kDecodeThreads)
     k_decode(const T *__restrict__ bcx, int N, int H, const T *__restrict__ w,
              const T *__restrict__ bias, const int32_t *__restrict__ slots,
              T *__restrict__ pool, int n_slots, T *__restrict__ y) {
-    const int groups = H / kCh;
-    const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const bool live = unit < (int64_t)N * groups;
-    const int i = (int)(unit / groups), cg = (int)(unit % groups), h0 = cg * kCh;
-    if (live) {  // warm L2 with the slot's state while earlier kernels finish
-        const int hint = slot_hint(slots + i);
-        if (hint >= 0 && hint < n_slots) prefetch_l2(pool + ((int64_t)hint * H + h0) * K);
-    }
-    pdl_wait();
-    pdl_launch_dependents();
-    if (!live) return;
-    const T *p = bcx + (int64_t)i * 3 * H + h0;
-    const Row<T> rb = load_row(p), rc = load_row(p + H), rx = load_row(p + 2 * H);
-    const int slot = slots[i];
-    float wt[kCh][K], bh[kCh];
-    load_block<T, K>(w + (int64_t)h0 * K, wt);
-    load_bias8<T>(bias, h0, bh);
-    if (slot < 0 || slot >= n_slots) {
-        if (cg == 0) raise_error(SC_DEV_BAD_SLOT);
-        return;
-    }
-    T *st = pool + ((int64_t)slot * H + h0) * K;
-    float win[kCh][K];
-    load_block<T, K>(st, win);
-    float b[kCh], c[kCh], x[kCh], out[kCh];
-    unpack_row(rb, b);
-    unpack_row(rc, c);
-    unpack_row(rx, x);
-#pragma unroll
-    for (int ch = 0; ch < kCh; ++ch) {
-        float z = slide_dot<K>(win[ch], wt[ch], gate_in<T>(b[ch], x[ch]));
-        if (bias != nullptr) z = z + bh[ch];
-        out[ch] = c[ch] * z;
-    }
-    store_row(y + (int64_t)i * H + h0, out);
-    store_block<T, K>(st, win);
-}
-
-// k_decode with CH (2 or 4) channels per thread instead of 8.
-template <typename T, int K, int CH>
-__global__ void __launch_bounds__(kDecodeThreads)
-    k_decode_n(const T *__restrict__ bcx, int N, int H, const T *__restrict__ w,
-               const T *__restrict__ bias, const int32_t *__restrict__ slots,
-               T *__restrict__ pool, int n_slots, T *__restrict__ y) {
     constexpr int NWR = CH * (int)sizeof(T) / 4;
     constexpr int AR = NWR * 4 >= 16 ? 16 : NWR * 4;
     constexpr int SB = CH * K * (int)sizeof(T);
@@ -473,7 +431,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
 }
 
 #ifndef SC_DECODE_CH
-#define SC_DECODE_CH 4  // channels per decode thread: 4 or 2 (k_decode_n), 8 (k_decode)
+#define SC_DECODE_CH 4  // channels per decode thread: 2, 4 or 8
 #endif
 
 template <typename T, int K>
@@ -481,16 +439,12 @@ static cudaError_t decode_inst(const void *bcx, int N, int H, const void *w, con
                                const int32_t *slots, void *pool, int n_slots, void *y,
                                cudaStream_t stream) {
     constexpr int CH = SC_DECODE_CH;
+    static_assert(CH == 2 || CH == 4 || CH == 8, "H is a multiple of 8");
     const int64_t units = (int64_t)N * (H / CH);
     const int64_t blocks = (units + kDecodeThreads - 1) / kDecodeThreads;
-    if constexpr (CH == 8)
-        return launch_pdl(k_decode<T, K>, dim3((unsigned)blocks), dim3(kDecodeThreads), 0,
-                          stream, (const T *)bcx, N, H, (const T *)w, (const T *)bias, slots,
-                          (T *)pool, n_slots, (T *)y);
-    else
-        return launch_pdl(k_decode_n<T, K, CH>, dim3((unsigned)blocks), dim3(kDecodeThreads),
-                          0, stream, (const T *)bcx, N, H, (const T *)w, (const T *)bias, slots,
-                          (T *)pool, n_slots, (T *)y);
+    return launch_pdl(k_decode<T, K, CH>, dim3((unsigned)blocks), dim3(kDecodeThreads), 0,
+                      stream, (const T *)bcx, N, H, (const T *)w, (const T *)bias, slots,
+                      (T *)pool, n_slots, (T *)y);
 }
 
 template <typename T>
@@ -515,13 +469,12 @@ cudaError_t launch_decode(int dtype, int H, int K, const void *bcx, int N, const
 
 // ------------------------------------------------------------------- verify
 //
-// Unit = (sequence i, channel group); the D draft steps run in order in
+// Unit = (sequence i, CH channels); the D draft steps run in order in
 // registers. All draft rows (up to VerifyRows<T> at a time) are requested
 // before the slot-dependent state load, so a sequence costs two dependent
-// memory round trips. Small CTAs spread the few units over all SMs. The
-// default build runs k_verify_n with 2 channels a thread: at 64 sequences
-// the 8-channel k_verify leaves a few warps per SM, each with a long chain of
-// dependent steps.
+// memory round trips. Small CTAs spread the few units over all SMs. CH = 2
+// channels a thread by default: at 64 sequences, 8 channels a thread leave
+// a few warps per SM, each with a long chain of dependent steps.
 #ifndef SC_VERIFY_THREADS
 #define SC_VERIFY_THREADS 64  // threads per verify CTA (build-time knob)
 #endif
@@ -531,86 +484,12 @@ constexpr int kVerifyThreads = SC_VERIFY_THREADS;
 template <typename T>
 constexpr int VerifyRows = sizeof(T) == 2 ? 8 : 4;
 
-template <typename T, int K>
+template <typename T, int K, int CH>
 __global__ void __launch_bounds__(kVerifyThreads)
     k_verify(const T *__restrict__ bcx, int N, int D, int H, const T *__restrict__ w,
              const T *__restrict__ bias, const int32_t *__restrict__ slots,
              const T *__restrict__ pool, int n_slots, T *__restrict__ win_out,
              T *__restrict__ y) {
-    const int groups = H / kCh;
-    const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const bool live = unit < (int64_t)N * groups;
-    const int i = (int)(unit / groups), cg = (int)(unit % groups), h0 = cg * kCh;
-    if (live) {  // warm L2 with the slot's state while earlier kernels finish
-        const int hint = slot_hint(slots + i);
-        if (hint >= 0 && hint < n_slots) prefetch_l2(pool + ((int64_t)hint * H + h0) * K);
-    }
-    pdl_wait();
-    pdl_launch_dependents();
-    if (!live) return;
-    constexpr int VR = VerifyRows<T>;
-    const int64_t ld = 3 * (int64_t)H;
-    const int slot = slots[i];
-    Row<T> rb[VR], rc[VR], rx[VR];
-#pragma unroll
-    for (int jj = 0; jj < VR; ++jj) {
-        if (jj < D) {
-            const T *p = bcx + ((int64_t)i * D + jj) * ld + h0;
-            rb[jj] = load_row(p);
-            rc[jj] = load_row(p + H);
-            rx[jj] = load_row(p + 2 * H);
-        }
-    }
-    float wt[kCh][K], win[kCh][K], bh[kCh];
-    load_block<T, K>(w + (int64_t)h0 * K, wt);
-    load_bias8<T>(bias, h0, bh);
-    if (slot < 0 || slot >= n_slots) {
-        if (cg == 0) raise_error(SC_DEV_BAD_SLOT);
-        return;
-    }
-    load_block<T, K>(pool + ((int64_t)slot * H + h0) * K, win);
-    for (int j0 = 0; j0 < D; j0 += VR) {
-        if (j0 > 0) {
-#pragma unroll
-            for (int jj = 0; jj < VR; ++jj) {
-                if (j0 + jj < D) {
-                    const T *p = bcx + ((int64_t)i * D + j0 + jj) * ld + h0;
-                    rb[jj] = load_row(p);
-                    rc[jj] = load_row(p + H);
-                    rx[jj] = load_row(p + 2 * H);
-                }
-            }
-        }
-#pragma unroll
-        for (int jj = 0; jj < VR; ++jj) {
-            if (j0 + jj < D) {
-                const int64_t t = (int64_t)i * D + j0 + jj;
-                float b[kCh], c[kCh], x[kCh], out[kCh];
-                unpack_row(rb[jj], b);
-                unpack_row(rc[jj], c);
-                unpack_row(rx[jj], x);
-#pragma unroll
-                for (int ch = 0; ch < kCh; ++ch) {
-                    float z = slide_dot<K>(win[ch], wt[ch], gate_in<T>(b[ch], x[ch]));
-                    if (bias != nullptr) z = z + bh[ch];
-                    out[ch] = c[ch] * z;
-                }
-                store_row(y + t * H + h0, out);
-                store_block<T, K>(win_out + (t * H + h0) * K, win);
-            }
-        }
-    }
-}
-
-// k_verify with CH (2 or 4) channels per thread instead of 8: 2 or 4 times the
-// threads, each with a shorter chain of draft steps and fewer registers, for
-// more warps per SM to hide the steps' latency. Same arithmetic and order.
-template <typename T, int K, int CH>
-__global__ void __launch_bounds__(kVerifyThreads)
-    k_verify_n(const T *__restrict__ bcx, int N, int D, int H, const T *__restrict__ w,
-               const T *__restrict__ bias, const int32_t *__restrict__ slots,
-               const T *__restrict__ pool, int n_slots, T *__restrict__ win_out,
-               T *__restrict__ y) {
     constexpr int NWR = CH * (int)sizeof(T) / 4;          // words of a row section
     constexpr int AR = NWR * 4 >= 16 ? 16 : NWR * 4;
     constexpr int SB = CH * K * (int)sizeof(T);           // bytes of a [CH][K] block
@@ -688,7 +567,7 @@ __global__ void __launch_bounds__(kVerifyThreads)
 }
 
 #ifndef SC_VERIFY_CH
-#define SC_VERIFY_CH 2  // channels per verify thread: 2 or 4 (k_verify_n), 8 (k_verify)
+#define SC_VERIFY_CH 2  // channels per verify thread: 2, 4 or 8
 #endif
 
 template <typename T, int K>
@@ -696,16 +575,12 @@ static cudaError_t verify_inst(const void *bcx, int N, int D, int H, const void 
                                const void *bias, const int32_t *slots, const void *pool,
                                int n_slots, void *win, void *y, cudaStream_t stream) {
     constexpr int CH = SC_VERIFY_CH;
+    static_assert(CH == 2 || CH == 4 || CH == 8, "H is a multiple of 8");
     const int64_t units = (int64_t)N * (H / CH);
     const int64_t blocks = (units + kVerifyThreads - 1) / kVerifyThreads;
-    if constexpr (CH == 8)
-        return launch_pdl(k_verify<T, K>, dim3((unsigned)blocks), dim3(kVerifyThreads), 0,
-                          stream, (const T *)bcx, N, D, H, (const T *)w, (const T *)bias, slots,
-                          (const T *)pool, n_slots, (T *)win, (T *)y);
-    else
-        return launch_pdl(k_verify_n<T, K, CH>, dim3((unsigned)blocks), dim3(kVerifyThreads),
-                          0, stream, (const T *)bcx, N, D, H, (const T *)w, (const T *)bias,
-                          slots, (const T *)pool, n_slots, (T *)win, (T *)y);
+    return launch_pdl(k_verify<T, K, CH>, dim3((unsigned)blocks), dim3(kVerifyThreads), 0,
+                      stream, (const T *)bcx, N, D, H, (const T *)w, (const T *)bias, slots,
+                      (const T *)pool, n_slots, (T *)win, (T *)y);
 }
 
 template <typename T>
