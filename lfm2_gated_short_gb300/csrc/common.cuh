@@ -1,8 +1,9 @@
 // common.cuh -- device helpers shared by the ShortConv kernels.
 //
-// Every kernel maps one thread to 8 consecutive channels of a row. For bf16
-// that is one 128-bit access per array and row (a warp covers 256 channels
-// = 512 contiguous bytes); for fp32 it is two 128-bit accesses.
+// A thread owns a few consecutive channels of a row: 8 in the register-tiled
+// prefill (the Row / block helpers below: one 128-bit access per array and
+// row in bf16, two in fp32, so a warp covers 512 contiguous bytes), 4 in the
+// streamed kernels and decode, 2 in verify (packed pairs and word helpers).
 #pragma once
 
 #include <cuda_bf16.h>
