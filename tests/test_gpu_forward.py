@@ -255,7 +255,7 @@ def test_slot_ids_rewritten_by_the_kernel_just_before(op):
 
 # ----------------------------------------------------------- verify/rollback
 
-@pytest.mark.parametrize("D", [1, 3, 4, 8])
+@pytest.mark.parametrize("D", [1, 3, 4, 8, 12])
 @pytest.mark.parametrize("K", [1, 3, 4])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_verify_and_rollback_small(dtype, K, D):
