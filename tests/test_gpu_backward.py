@@ -147,6 +147,15 @@ def test_backward_varlen_many_sequences_across_row_ranges():
     _check_varlen(c, *_run_varlen(c))
 
 
+def test_backward_varlen_more_sequences_than_staged_in_shared_memory():
+    """900 sequences: past the 512 cu_seqlens entries staged in shared memory,
+    so the kernel reads the offsets from global memory."""
+    rng = np.random.default_rng(217)
+    lengths = rng.integers(0, 12, size=900)
+    c = _varlen_case(lengths, 128, 3, 218)
+    _check_varlen(c, *_run_varlen(c))
+
+
 def test_backward_varlen_one_fresh_sequence_matches_the_single_sequence_kernel():
     c = _varlen_case([3001], 512, 3, 213, with_init=False, with_final=False)
     dbcx, dw, _ = _run_varlen(c)
