@@ -386,6 +386,18 @@ sc_status shortconv_pool_copy(sc_dtype dtype, int H, int K, void *pool, int n_sl
                               void *stream);
 
 /*
+ * shortconv_check_wait_limit: a health check of the device-side timeout path,
+ * which a working call never reaches. Every waiting kernel of this library
+ * bounds each wait on an asynchronous copy or on the tensor cores (about 2 s),
+ * then sets SC_DEV_TIMEOUT and returns instead of hanging. This call enqueues
+ * a one-thread kernel that waits, with that same bounded wait, on a device
+ * barrier that nothing ever completes: about 2 s later it sets SC_DEV_TIMEOUT
+ * and returns, and shortconv_get_error reports it. The device stays usable.
+ * Not part of the pages' interface. Errors: SC_ECUDA if the launch fails.
+ */
+sc_status shortconv_check_wait_limit(void *stream);
+
+/*
  * Synchronize `stream`, then read and clear the current device's error word.
  * *device_code receives the SC_DEV_* bits seen since the last clear (0 if
  * none). Returns SC_OK if the word was 0, SC_EDEVICE if not, SC_ECUDA if a

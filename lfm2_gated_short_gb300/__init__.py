@@ -75,12 +75,13 @@ def lib() -> ctypes.CDLL:
             L.shortconv_slots_release.argtypes = [p, i32, p, i32, p]
             L.shortconv_pool_copy.argtypes = [i32, i32, i32, p, i32, p, p, i32, p]
             L.shortconv_get_error.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
+            L.shortconv_check_wait_limit.argtypes = [p]
             L.shortconv_status_string.argtypes = [i32]
             L.shortconv_status_string.restype = ctypes.c_char_p
             for f in ("prefill", "prefill_tiled", "decode", "verify", "rollback",
                       "rollback_layers", "backward",
                       "backward_varlen", "in_proj_prefill", "out_proj", "slots_claim",
-                      "slots_release", "pool_copy", "get_error"):
+                      "slots_release", "pool_copy", "get_error", "check_wait_limit"):
                 getattr(L, "shortconv_" + f).restype = i32
             _lib = L
     return _lib
@@ -366,6 +367,13 @@ def pool_copy(pool, src_slots, dst_slots, stream=None):
         _dcode(pool), H, K, _dev(pool, "pool", pool.dtype, (n_slots, H, K)), n_slots,
         _dev(src_slots, "src_slots", torch.int32, (n,)),
         _dev(dst_slots, "dst_slots", torch.int32, (n,)), n, _stream(stream, pool.device)))
+
+
+def check_wait_limit(stream=None, device=None) -> None:
+    """Enqueue the device-side timeout check: a kernel whose bounded wait runs
+    out (about 2 s) and sets DEV_TIMEOUT, which get_error() then returns."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    _raise_on("shortconv_check_wait_limit", lib().shortconv_check_wait_limit(_stream(stream, dev)))
 
 
 def get_error(stream=None, device=None) -> int:

@@ -396,6 +396,10 @@ sc_status shortconv_pool_copy(sc_dtype dtype, int H, int K, void *pool, int n_sl
                                           (cudaStream_t)stream));
 }
 
+sc_status shortconv_check_wait_limit(void *stream) {
+    return from_cuda(sc::launch_wait_limit_check((cudaStream_t)stream));
+}
+
 sc_status shortconv_get_error(void *stream, int *device_code) {
     if (device_code == nullptr) return SC_EINVAL;
     unsigned int code = 0;

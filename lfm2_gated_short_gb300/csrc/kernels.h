@@ -85,6 +85,8 @@ cudaError_t launch_slots_release(uint32_t *in_use, int n_slots, const int32_t *s
 cudaError_t launch_pool_copy(const int32_t *src, const int32_t *dst, int n, int64_t state_bytes,
                              void *pool, int n_slots, cudaStream_t stream);
 cudaError_t take_error_slots(cudaStream_t stream, unsigned int *code);
+// A one-thread kernel whose bounded wait must run out and set SC_DEV_TIMEOUT.
+cudaError_t launch_wait_limit_check(cudaStream_t stream);
 
 // Read and clear the device error word of the current device (synchronous
 // with respect to `stream`).

@@ -12,6 +12,7 @@
 #include "kernels.h"
 #include "launch.h"
 #include "shortconv.h"
+#include "tma.cuh"
 
 namespace sc {
 
@@ -134,6 +135,27 @@ cudaError_t launch_pool_copy(const int32_t *src, const int32_t *dst, int n, int6
     const int64_t blocks = ((int64_t)n * q + 255) / 256;
     return launch_pdl(k_pool_copy, dim3((unsigned)blocks), dim3(256), 0, stream, src, dst, n, q,
                       (uint4 *)pool, n_slots);
+}
+
+// ------------------------------------------------------- wait-limit check
+//
+// Every kernel here that waits on an mbarrier (the streamed prefill and
+// backwards, the projections) gives up after kWaitLimitNs, sets
+// SC_DEV_TIMEOUT and returns instead of hanging. This one-thread kernel waits
+// with that same bounded wait on a barrier that nothing ever completes, so
+// the give-up and the report can be checked on a device without any copy
+// failing.
+__global__ void k_wait_limit_check() {
+    __shared__ uint64_t bar;
+    pdl_wait();
+    pdl_launch_dependents();
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+    if (!mbar_wait_bounded(&bar, 0u)) raise_error(SC_DEV_TIMEOUT);
+}
+
+cudaError_t launch_wait_limit_check(cudaStream_t stream) {
+    return launch_pdl(k_wait_limit_check, dim3(1), dim3(1), 0, stream);
 }
 
 cudaError_t take_error_slots(cudaStream_t stream, unsigned int *code) {

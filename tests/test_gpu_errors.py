@@ -87,3 +87,29 @@ def test_rollback_bad_accepted_and_slot():
     assert_bits(got[s.slot_ids[1]], w[1, 1], "accepted sequence")
     for i in (0, 2, 3):
         assert_bits(got[s.slot_ids[i]], s.pools[0][s.slot_ids[i]], f"skipped sequence {i}")
+
+
+def test_bounded_wait_gives_up_reports_a_timeout_and_leaves_the_device_usable():
+    """The device-side timeout path, without any copy failing: a kernel waits,
+    with the bounded wait every waiting kernel uses, on a barrier that
+    nothing completes. It must give up after about the wait limit (2 s), set
+    DEV_TIMEOUT, and leave the device computing correctly afterwards."""
+    import time
+    assert sc.get_error() == 0
+    t0 = time.perf_counter()
+    sc.check_wait_limit()
+    code = sc.get_error()
+    elapsed = time.perf_counter() - t0
+    assert code == sc.DEV_TIMEOUT
+    assert 1.5 < elapsed < 60, elapsed
+    assert sc.get_error() == 0
+    p = wl.varlen_prefill(n_seqs=3, H=64, K=3, n_slots=4, seed=102, lengths=[7, 1, 12])
+    pool = dev(p.pool, "bf16")
+    y = sc.prefill(dev(p.bcx, "bf16"), dev(p.w, "bf16"), dev(p.cu_seqlens, "i32"),
+                   dev(p.slot_ids, "i32"), pool)
+    ref = p.pool.copy()
+    st, y_ref = oracle.prefill("bf16", p.bcx, p.w, p.cu_seqlens, p.slot_ids, ref)
+    assert st == oracle.OK
+    assert_close("bf16", host(y), y_ref, "prefill after the timeout check")
+    assert_bits(host(pool), ref, "pool after the timeout check")
+    assert sc.get_error() == 0
