@@ -7,9 +7,11 @@
  * the in_proj output of a token is split into B, C and x; u = B * x; a
  * per-sequence window of the last K values of u slides by one per token
  * (oldest dropped, u appended); z = sum_k w[h,k] * window[k]; y = C * z.
- * Tap k = K-1 multiplies the newest value. There is no bias and no
- * activation (the released LFM2 configurations are bias-free: Liger-Kernel
- * PR #1317, "Kernel changes / Gated short convolution").
+ * Tap k = K-1 multiplies the newest value. There is no activation. The
+ * per-channel conv bias is optional: NULL for the released LFM2
+ * configurations, which are bias-free (Liger-Kernel PR #1317, "Kernel
+ * changes / Gated short convolution"); when given, z = sum + b before the C
+ * gate.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
