@@ -1,0 +1,80 @@
+"""Calls on several streams at once, each on its own buffers.
+
+The library keeps no per-call state on the device besides the shared error
+word, so work enqueued on different streams may overlap freely. Four streams
+each run a different call (prefill, decode, verify + rollback, backward),
+enqueued interleaved and repeated; every result must match the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import lfm2_gated_short_gb300 as sc
+from lfm2_gated_short_gb300 import workloads as wl
+from gpu_util import assert_bits, assert_close, assert_dw_close, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+def test_four_streams_interleaved():
+    H, K, reps = 512, 3, 3
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    p = wl.varlen_prefill(n_seqs=6, lo=20, hi=300, H=H, K=K, n_slots=10, seed=1100)
+    d = wl.decode_serving(layers=1, steps=reps, batch=40, H=H, K=K, n_slots=64, seed=1101)
+    v = wl.verify_serving(layers=1, batch=12, D=6, H=H, K=K, n_slots=20, seed=1102)
+    t = wl.training(T=2000, H=H, K=K, seed=1103)
+    # device inputs, made before any stream runs
+    p_in = (dev(p.bcx, "bf16"), dev(p.w, "bf16"), dev(p.cu_seqlens, "i32"), dev(p.slot_ids, "i32"))
+    p_pools = [dev(p.pool, "bf16") for _ in range(reps)]
+    d_w, d_slots, d_pool = dev(d.w[0], "bf16"), dev(d.slot_ids, "i32"), dev(d.pools[0], "bf16")
+    d_rows = [dev(d.bcx[0, s], "bf16") for s in range(reps)]
+    v_in = (dev(v.bcx[0], "bf16"), dev(v.w[0], "bf16"), dev(v.slot_ids, "i32"))
+    v_pools = [dev(v.pools[0], "bf16") for _ in range(reps)]
+    v_acc = dev(v.accepted, "i32")
+    t_in = (dev(t.bcx, "bf16"), dev(t.w, "bf16"), dev(t.dy, "bf16"))
+    torch.cuda.synchronize()
+    outs = {"p": [], "d": [], "v": [], "t": []}
+    for r in range(reps):
+        with torch.cuda.stream(streams[0]):
+            outs["p"].append(sc.prefill(*p_in, p_pools[r]))
+        with torch.cuda.stream(streams[1]):
+            outs["d"].append(sc.decode(d_rows[r], d_w, d_slots, d_pool))
+        with torch.cuda.stream(streams[2]):
+            win, y = sc.verify(*v_in, v_pools[r], v.D)
+            sc.rollback(win, v_acc, v_in[2], v_pools[r])
+            outs["v"].append((win, y))
+        with torch.cuda.stream(streams[3]):
+            outs["t"].append(sc.backward(*t_in))
+    torch.cuda.synchronize()
+    assert sc.get_error() == 0
+    # prefill: every repetition from the same initial pool
+    ref = p.pool.copy()
+    st, y_ref = oracle.prefill("bf16", p.bcx, p.w, p.cu_seqlens, p.slot_ids, ref)
+    assert st == oracle.OK
+    for r in range(reps):
+        assert_close("bf16", host(outs["p"][r]), y_ref, f"prefill y, rep {r}")
+        assert_bits(host(p_pools[r]), ref, f"prefill pool, rep {r}")
+    # decode: consecutive steps on one pool, in stream order
+    ref = d.pools[0].copy()
+    for r in range(reps):
+        st, y_ref = oracle.decode("bf16", d.bcx[0, r], d.w[0], d.slot_ids, ref)
+        assert st == oracle.OK
+        assert_close("bf16", host(outs["d"][r]), y_ref, f"decode y, step {r}")
+    assert_bits(host(d_pool), ref, "decode pool")
+    # verify + rollback: every repetition from the same initial pool
+    st, win_ref, y_ref = oracle.verify("bf16", v.bcx[0], v.w[0], v.slot_ids, v.pools[0], v.D)
+    assert st == oracle.OK
+    ref = v.pools[0].copy()
+    assert oracle.rollback("bf16", win_ref, v.accepted, v.slot_ids, ref) == oracle.OK
+    for r in range(reps):
+        assert_bits(host(outs["v"][r][0]), win_ref, f"verify windows, rep {r}")
+        assert_close("bf16", host(outs["v"][r][1]), y_ref, f"verify y, rep {r}")
+        assert_bits(host(v_pools[r]), ref, f"pool after rollback, rep {r}")
+    # backward: deterministic, so every repetition has the same bits
+    st, d_ref, dw_ref = oracle.backward("bf16", t.bcx, t.w, t.dy)
+    assert st == oracle.OK
+    for r in range(reps):
+        assert_close("bf16", host(outs["t"][r][0]), d_ref, f"dB|dC|dx, rep {r}")
+        assert_dw_close(host(outs["t"][r][1]), dw_ref)
+        assert np.array_equal(host(outs["t"][r][1]), host(outs["t"][0][1])), "dW bits"
