@@ -78,3 +78,50 @@ def test_four_streams_interleaved():
         assert_close("bf16", host(outs["t"][r][0]), d_ref, f"dB|dC|dx, rep {r}")
         assert_dw_close(host(outs["t"][r][1]), dw_ref)
         assert np.array_equal(host(outs["t"][r][1]), host(outs["t"][0][1])), "dW bits"
+
+
+def test_host_threads_calling_at_once():
+    """Four host threads, each with its own stream and buffers, call the
+    library concurrently (the binding's C calls release the GIL). Results
+    must match single-threaded calls bit for bit."""
+    import threading
+    H, K, n_iter = 256, 3, 15
+    cases = []
+    for j in range(4):
+        p = wl.varlen_prefill(n_seqs=3 + j, lo=10, hi=200, H=H, K=K, n_slots=8, seed=1200 + j)
+        cases.append(p)
+    inputs = [(dev(p.bcx, "bf16"), dev(p.w, "bf16"), dev(p.cu_seqlens, "i32"),
+               dev(p.slot_ids, "i32")) for p in cases]
+    expect = []
+    for j, p in enumerate(cases):  # single-threaded results first
+        pool = dev(p.pool, "bf16")
+        y = sc.prefill(*inputs[j], pool)
+        dbcx, dw = sc.backward(inputs[j][0], inputs[j][1], y.repeat(1, 1))
+        torch.cuda.synchronize()
+        expect.append((host(y), host(pool), host(dbcx), host(dw)))
+    results = [None] * 4
+    errors = []
+
+    def worker(j):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(n_iter):
+                    pool = dev(cases[j].pool, "bf16")
+                    y = sc.prefill(*inputs[j], pool)
+                    dbcx, dw = sc.backward(inputs[j][0], inputs[j][1], y.repeat(1, 1))
+            s.synchronize()
+            results[j] = (host(y), host(pool), host(dbcx), host(dw))
+        except Exception as e:  # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(j,)) for j in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    assert sc.get_error() == 0
+    for j in range(4):
+        for got, want, what in zip(results[j], expect[j], ("y", "pool", "dbcx", "dw")):
+            assert np.array_equal(got, want), f"thread {j}: {what}"
