@@ -65,7 +65,17 @@ constexpr size_t bwd_smem_bytes(int CW) {
     return (size_t)kBwdHeader + (size_t)kBwdStages * BwdShape<T>::R * 4 * CW * sizeof(T);
 }
 
-// Row ranges per channel slice; fixed by T alone so the workspace size is.
+// CTAs per SM each kernel's registers are budgeted for. K = 4 keeps a fourth
+// window tap per channel pair and spilled at the K <= 3 budgets (backward
+// 550 us against 313 us at T = 65536), so it is budgeted one CTA fewer.
+// fp32 holds twice the bytes per section and takes one CTA fewer again at K = 4.
+template <typename T, int K>
+constexpr int kBwdCtas = K == 4 ? SC_BWD_MIN_CTAS - (sizeof(T) == 4 ? 2 : 1) : SC_BWD_MIN_CTAS;
+template <int K>
+constexpr int kBwdVarlenCtas = K == 4 ? SC_BWD_VARLEN_MIN_CTAS - 1 : SC_BWD_VARLEN_MIN_CTAS;
+
+// Row ranges per channel slice at most; fixed by T alone so the workspace
+// size is. A launch may use fewer (bwd_launch_rows).
 static int64_t bwd_row_ctas(int64_t T) {
     const int64_t n = (T + kBwdMinRows - 1) / kBwdMinRows;
     return n < 1 ? 1 : (n > kBwdRowCtas ? kBwdRowCtas : n);
@@ -118,7 +128,7 @@ __device__ __forceinline__ void store_partial(float *__restrict__ part, int H, i
 // HB: a conv bias is given or dbias is wanted. The instance without carries
 // no bias registers or branches; with_dbias then is false.
 template <typename T, int K, bool HB>
-__global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_MIN_CTAS)
+__global__ void __launch_bounds__(kBwdConsumers + 32, kBwdCtas<T, K>)
     k_backward(const T *__restrict__ bcx, int64_t T_rows, int H, const T *__restrict__ w,
                const T *__restrict__ bias, const T *__restrict__ dy, T *__restrict__ dbcx,
                float *__restrict__ partial, bool with_dbias, int n_slices, int n_row_ctas) {
@@ -344,7 +354,7 @@ constexpr size_t bwd_varlen_smem_bytes(int CW) {
 }
 
 template <typename T, int K, bool HB>
-__global__ void __launch_bounds__(kBwdConsumers + 32, SC_BWD_VARLEN_MIN_CTAS)
+__global__ void __launch_bounds__(kBwdConsumers + 32, kBwdVarlenCtas<K>)
     k_backward_varlen(const T *__restrict__ bcx, int64_t T_rows, int H, const T *__restrict__ w,
                       const T *__restrict__ bias, const int32_t *__restrict__ cu, int N,
                       const T *__restrict__ init, const T *__restrict__ dy,
@@ -711,6 +721,38 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Row ranges per slice for one launch: one wave of CTAs at the kernel's
+// occupancy on this device (n_slices slices share the SMs), capped by what
+// the workspace holds. The row split, and so dW's summation order, depends
+// only on T, H and the device.
+// The caller's cache (one per kernel instance) keeps the wave per device.
+struct WaveCache {
+    std::atomic<int> key{-1}, wave{0};
+};
+template <typename Kern>
+static cudaError_t bwd_launch_rows(Kern kern, int threads, size_t smem, int n_slices, int64_t T,
+                                   WaveCache &cache, int64_t *n_row) {
+    std::atomic<int> &cached_key = cache.key, &cached_wave = cache.wave;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int key = dev * 65536 + n_slices;
+    int wave = cached_key.load() == key ? cached_wave.load() : 0;
+    if (wave <= 0) {
+        int sms = 0, occ = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+        if (e != cudaSuccess) return e;
+        wave = sms * (occ > 0 ? occ : 1) / n_slices;
+        cached_wave.store(wave);
+        cached_key.store(key);
+    }
+    const int64_t cap = bwd_row_ctas(T);
+    *n_row = wave < 1 ? 1 : (wave < cap ? wave : cap);
+    return cudaSuccess;
+}
+
 static cudaError_t launch_reduce(const void *ws, int64_t n_row, int H, int K, float *dw,
                                  float *dbias, cudaStream_t stream) {
     const int HK = H * K, P = HK + (dbias != nullptr ? H : 0);
@@ -726,7 +768,6 @@ static cudaError_t backward_inst(const void *bcx, int64_t rows, int H, const voi
     const int n_slices = (H + kBwdSlice - 1) / kBwdSlice;
     const int threads = (CW / kBwdCpt + 31) / 32 * 32 + 32;  // consumers + one producer warp
     const size_t smem = bwd_smem_bytes<T>(CW);
-    const int64_t n_row = bwd_row_ctas(rows);
     auto kern = k_backward<T, K, HB>;
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
@@ -738,6 +779,10 @@ static cudaError_t backward_inst(const void *bcx, int64_t rows, int H, const voi
         if (e != cudaSuccess) return e;
         configured.fetch_or(1ull << dev);
     }
+    static WaveCache waves;
+    int64_t n_row = 1;
+    e = bwd_launch_rows(kern, threads, smem, n_slices, rows, waves, &n_row);
+    if (e != cudaSuccess) return e;
     e = launch_pdl(kern, dim3((unsigned)(n_row * n_slices)), dim3(threads), smem, stream,
                    (const T *)bcx, rows, H, (const T *)w, (const T *)bias, (const T *)dy,
                    (T *)dbcx, (float *)ws, dbias != nullptr, n_slices, (int)n_row);
@@ -755,7 +800,6 @@ static cudaError_t backward_varlen_inst(const void *bcx, int64_t rows, int H, co
     const int n_slices = (H + kBwdSlice - 1) / kBwdSlice;
     const int threads = (CW / kBwdCpt + 31) / 32 * 32 + 32;
     const size_t smem = bwd_varlen_smem_bytes<T>(CW);
-    const int64_t n_row = bwd_row_ctas(rows);
     auto kern = k_backward_varlen<T, K, HB>;
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
@@ -767,6 +811,10 @@ static cudaError_t backward_varlen_inst(const void *bcx, int64_t rows, int H, co
         if (e != cudaSuccess) return e;
         configured.fetch_or(1ull << dev);
     }
+    static WaveCache waves;
+    int64_t n_row = 1;
+    e = bwd_launch_rows(kern, threads, smem, n_slices, rows, waves, &n_row);
+    if (e != cudaSuccess) return e;
     e = launch_pdl(kern, dim3((unsigned)(n_row * n_slices)), dim3(threads), smem, stream,
                    (const T *)bcx, rows, H, (const T *)w, (const T *)bias, cu, N,
                    (const T *)init, (const T *)dy, d_final, (T *)dbcx, (float *)ws,
