@@ -725,19 +725,24 @@ __global__ void __launch_bounds__(256)
 // occupancy on this device (n_slices slices share the SMs), capped by what
 // the workspace holds. The row split, and so dW's summation order, depends
 // only on T, H and the device.
-// The caller's cache (one per kernel instance) keeps the wave per device.
+//
+// The caller's cache (one per kernel instance) keeps the last (device, slice
+// count, slice width) and its wave in one 64-bit word, so concurrent callers
+// never pair a key with another key's wave.
 struct WaveCache {
-    std::atomic<int> key{-1}, wave{0};
+    std::atomic<unsigned long long> packed{0};  // key << 20 | wave; 0 = empty
 };
 template <typename Kern>
-static cudaError_t bwd_launch_rows(Kern kern, int threads, size_t smem, int n_slices, int64_t T,
-                                   WaveCache &cache, int64_t *n_row) {
-    std::atomic<int> &cached_key = cache.key, &cached_wave = cache.wave;
+static cudaError_t bwd_launch_rows(Kern kern, int threads, size_t smem, int n_slices, int CW,
+                                   int64_t T, WaveCache &cache, int64_t *n_row) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const int key = dev * 65536 + n_slices;
-    int wave = cached_key.load() == key ? cached_wave.load() : 0;
+    const unsigned long long key = ((unsigned long long)(dev & 0xFF) << 36) |
+                                   ((unsigned long long)(n_slices & 0xFFFFFF) << 12) |
+                                   (unsigned long long)((CW / 8) & 0xFFF);
+    const unsigned long long got = cache.packed.load();
+    int wave = got != 0 && (got >> 20) == key ? (int)(got & 0xFFFFF) : 0;
     if (wave <= 0) {
         int sms = 0, occ = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -745,11 +750,12 @@ static cudaError_t bwd_launch_rows(Kern kern, int threads, size_t smem, int n_sl
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
         if (e != cudaSuccess) return e;
         wave = sms * (occ > 0 ? occ : 1) / n_slices;
-        cached_wave.store(wave);
-        cached_key.store(key);
+        if (wave < 1) wave = 1;
+        if (wave > 0xFFFFF) wave = 0xFFFFF;
+        cache.packed.store(key << 20 | (unsigned long long)wave);
     }
     const int64_t cap = bwd_row_ctas(T);
-    *n_row = wave < 1 ? 1 : (wave < cap ? wave : cap);
+    *n_row = wave < cap ? wave : cap;
     return cudaSuccess;
 }
 
@@ -781,7 +787,7 @@ static cudaError_t backward_inst(const void *bcx, int64_t rows, int H, const voi
     }
     static WaveCache waves;
     int64_t n_row = 1;
-    e = bwd_launch_rows(kern, threads, smem, n_slices, rows, waves, &n_row);
+    e = bwd_launch_rows(kern, threads, smem, n_slices, CW, rows, waves, &n_row);
     if (e != cudaSuccess) return e;
     e = launch_pdl(kern, dim3((unsigned)(n_row * n_slices)), dim3(threads), smem, stream,
                    (const T *)bcx, rows, H, (const T *)w, (const T *)bias, (const T *)dy,
@@ -813,7 +819,7 @@ static cudaError_t backward_varlen_inst(const void *bcx, int64_t rows, int H, co
     }
     static WaveCache waves;
     int64_t n_row = 1;
-    e = bwd_launch_rows(kern, threads, smem, n_slices, rows, waves, &n_row);
+    e = bwd_launch_rows(kern, threads, smem, n_slices, CW, rows, waves, &n_row);
     if (e != cudaSuccess) return e;
     e = launch_pdl(kern, dim3((unsigned)(n_row * n_slices)), dim3(threads), smem, stream,
                    (const T *)bcx, rows, H, (const T *)w, (const T *)bias, cu, N,

@@ -147,6 +147,31 @@ def test_backward_varlen_many_sequences_across_row_ranges():
     _check_varlen(c, *_run_varlen(c))
 
 
+def test_dw_bits_do_not_depend_on_the_calls_in_between():
+    """The launch picks its row split from the device and the shapes; calls
+    with other widths in between (a different occupancy, the same slice
+    count) must not change it, so dW and d_init keep their bits."""
+    a = wl.training(T=3001, H=512, K=3, seed=740)
+    b = wl.training(T=3001, H=64, K=3, seed=741)
+    cu = np.array([0, 1000, 3001], np.int32)
+
+    def run(t, varlen):
+        args = (dev(t.bcx, "bf16"), dev(t.w, "bf16"))
+        if varlen:
+            out = sc.backward_varlen(args[0], args[1], dev(cu, "i32"), dev(t.dy, "bf16"))
+            return host(out[1]), host(out[2])
+        return host(sc.backward(args[0], args[1], dev(t.dy, "bf16"))[1]), None
+
+    for varlen in (False, True):
+        first = run(a, varlen)
+        run(b, varlen)
+        again = run(a, varlen)
+        assert np.array_equal(first[0], again[0]), "dW bits"
+        if varlen:
+            assert np.array_equal(first[1], again[1]), "d_init bits"
+    assert sc.get_error() == 0
+
+
 def test_backward_varlen_more_sequences_than_staged_in_shared_memory():
     """900 sequences: past the 512 cu_seqlens entries staged in shared memory,
     so the kernel reads the offsets from global memory."""
