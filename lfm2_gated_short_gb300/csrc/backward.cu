@@ -17,7 +17,8 @@
 // mbarriers; the consumer warps, 4 channels per thread, walk the rows. Each
 // thread holds its channels' dW (and dbias) over the whole range in registers
 // and writes one fp32 partial per CTA; a second kernel adds the partials of
-// all CTAs in a fixed order, so dW and dbias have the same bits on every call.
+// all CTAs in a fixed order, so dW and dbias have the same bits on every call
+// with the same T, H and device (the row split depends on those alone).
 // Partial layout per row range: H*K dW entries, then H dbias entries when the
 // caller asked for dbias.
 #include <atomic>
