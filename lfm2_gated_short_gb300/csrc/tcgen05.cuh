@@ -34,18 +34,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// The same copy into the shared memory of every CTA of the cluster named in
-// cta_mask (same CTA-relative offsets for the data and the mbarrier).
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *map,
-                                               uint64_t *bar, int x, int y, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y),
-        "h"(cta_mask)
-        : "memory");
-}
-
 // A CTA pair's tile copy (cta_group::2): the data land in this CTA's shared
 // memory, the transaction bytes count on the mbarrier at shared::cluster
 // address bar_cluster, which may be in the peer CTA (the pair's leader).
@@ -154,16 +142,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_addr(bar))
-        : "memory");
-}
-
-// mma_commit arriving on the mbarrier at the same offset in every CTA of
-// the cluster named in cta_mask.
-__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_addr(bar)),
-        "h"(cta_mask)
         : "memory");
 }
 
