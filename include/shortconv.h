@@ -114,7 +114,8 @@ typedef enum { SC_F32 = 0, SC_BF16 = 1 } sc_dtype;
  * (that sequence's rows of y and its slot are not written), SC_DEV_TIMEOUT
  * (an asynchronous row copy did not complete within 2 s; output incomplete).
  *
- * Implementation: one CTA per SM streams a balanced range of rows through
+ * Implementation: persistent CTAs (as many per SM as fit, 4 or 5 at bf16)
+ * each stream a balanced range of rows of a 512-channel slice through
  * shared memory with bulk asynchronous copies (see shortconv_prefill_tiled
  * for the register-tiled alternative; both give identical bits).
  */
@@ -295,8 +296,11 @@ sc_status shortconv_backward_varlen(sc_dtype dtype, int H, int K, const void *bc
  *     for H * K <= 13,797 (every T for H = 2048 or H = 4096 with K = 3);
  *     for H = 8192, K = 4 rows above T = 1024 are.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture on that device.
+ *     (cudaGetSymbolAddress, with that device current) and caches it for
+ *     the life of the process; make that first call before any stream
+ *     capture on that device. A device reset (cudaDeviceReset) or a context
+ *     torn down and created again after that first call is not supported:
+ *     the cached address would no longer be the array's.
  *   - All calls on a device share the one array and each overwrites it
  *     before reading it, so no clearing is needed; calls that overlap on the
  *     GPU (for instance on two streams) race on it and must be serialized

@@ -7,7 +7,8 @@
 // after it (the sequence-owner extension) -- through NS shared-memory stages
 // with 1-D bulk asynchronous copies (cp.async.bulk). Each stage has a "full"
 // mbarrier (the copies' byte count) and an "empty" one (one arrival per
-// consumer warp), so the 8 consumer warps, 8 channels per thread, run ahead
+// consumer warp), so the consumer warps (4 channels per thread by default:
+// 4 warps for a 512-channel slice) run ahead
 // or behind each other freely while up to NS stages of copies are in flight:
 // bytes in flight per SM do not depend on registers or occupancy. The
 // consumers use packed arithmetic (bf16x2 products, f32x2 multiply-adds) in

@@ -6,9 +6,10 @@ mid-step). It keeps its scratch in a fixed array inside the library instead
 of a caller workspace.
 
 This file is collected last on purpose. It calls the entry point through the
-C ABI and checks it against shortconv_backward, which takes a caller
-workspace, on two calls in a row. It must pass alone in a fresh process and
-after the other tests.
+C ABI and checks it, on two calls in a row, bit for bit against
+shortconv_backward (which takes a caller workspace: the row split and the
+fixed-order dW sum are the same, so the bits are too) and against the CPU
+oracle. It must pass alone in a fresh process and after the other tests.
 """
 import ctypes
 
@@ -19,7 +20,8 @@ import torch
 import lfm2_gated_short_gb300 as sc
 from lfm2_gated_short_gb300 import build as sc_build
 from lfm2_gated_short_gb300 import workloads as wl
-from gpu_util import assert_close, assert_dw_close, dev, host
+import oracle
+from gpu_util import assert_bits, assert_close, assert_dw_close, dev, host
 
 SCRATCH_LIMIT = 8 << 20  # bytes of fixed device scratch behind the call
 
@@ -50,30 +52,51 @@ def call_noalloc(bcx, w, dy):
     return dbcx, dw
 
 
+def check_against_oracle(p, dbcx, dw, channels=None):
+    """The oracle on a subset of channels (all of them when None): channels are
+    independent, so its run on their columns is the full run restricted to them."""
+    H = p.H
+    ch = np.arange(H) if channels is None else np.asarray(channels)
+    cols = np.concatenate([ch, H + ch, 2 * H + ch])
+    st, d_ref, dw_ref = oracle.backward(p.dtype, p.bcx[:, cols], p.w[ch], p.dy[:, ch])
+    assert st == oracle.OK
+    assert_close(p.dtype, dbcx[:, cols], d_ref, "dB|dC|dx vs oracle")
+    assert_dw_close(dw[ch], dw_ref, "dW vs oracle")
+
+
 @pytest.mark.gpu
-def test_two_calls_in_a_row_match_the_workspace_entry_point():
-    cases = [wl.training(T=5003, H=512, K=3, seed=301),
-             wl.training(T=65536, H=2048, K=3, seed=302)]
-    for p in cases:
+def test_two_calls_in_a_row_match_the_workspace_entry_point_and_the_oracle():
+    rng = np.random.default_rng(0)
+    sampled = np.sort(np.concatenate([[0, 7, 8, 255, 256, 2047],
+                                      rng.choice(np.arange(9, 2040), 58, replace=False)]))
+    cases = [(wl.training(T=5003, H=512, K=3, seed=301), None),
+             (wl.training(T=65536, H=2048, K=3, seed=302), sampled)]
+    for p, channels in cases:
         bcx, w, dy = dev(p.bcx, p.dtype), dev(p.w, p.dtype), dev(p.dy, p.dtype)
         assert partial_bytes(p.H, p.K, p.bcx.shape[0]) <= SCRATCH_LIMIT
         ref_dbcx, ref_dw = sc.backward(bcx, w, dy)
-        got_dbcx, got_dw = call_noalloc(bcx, w, dy)
-        torch.cuda.synchronize()
-        assert_close(p.dtype, host(got_dbcx), host(ref_dbcx), "dB|dC|dx")
-        assert_dw_close(host(got_dw), host(ref_dw).astype(np.float64))
+        ref_dbcx, ref_dw = host(ref_dbcx), host(ref_dw)
+        for call in range(2):
+            got_dbcx, got_dw = call_noalloc(bcx, w, dy)
+            torch.cuda.synchronize()
+            got_dbcx, got_dw = host(got_dbcx), host(got_dw)
+            assert_bits(got_dbcx, ref_dbcx, f"dB|dC|dx, call {call}")
+            assert_bits(got_dw, ref_dw, f"dW, call {call}")
+            check_against_oracle(p, got_dbcx, got_dw, channels)
     assert sc.get_error() == 0
 
 
 @pytest.mark.gpu
-def test_fp32_call_matches_the_workspace_entry_point():
+def test_fp32_call_matches_the_workspace_entry_point_and_the_oracle():
     p = wl.training(T=777, H=64, K=4, seed=303, dtype="f32")
     bcx, w, dy = dev(p.bcx, "f32"), dev(p.w, "f32"), dev(p.dy, "f32")
     ref_dbcx, ref_dw = sc.backward(bcx, w, dy)
-    got_dbcx, got_dw = call_noalloc(bcx, w, dy)
-    torch.cuda.synchronize()
-    assert_close("f32", host(got_dbcx), host(ref_dbcx), "dB|dC|dx")
-    assert_dw_close(host(got_dw), host(ref_dw).astype(np.float64))
+    for call in range(2):
+        got_dbcx, got_dw = call_noalloc(bcx, w, dy)
+        torch.cuda.synchronize()
+        assert_bits(host(got_dbcx), host(ref_dbcx), f"dB|dC|dx, call {call}")
+        assert_bits(host(got_dw), host(ref_dw), f"dW, call {call}")
+        check_against_oracle(p, host(got_dbcx), host(got_dw))
 
 
 def test_sizes_beyond_the_scratch_are_rejected_before_any_work():
