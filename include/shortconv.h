@@ -73,6 +73,8 @@ typedef enum { SC_F32 = 0, SC_BF16 = 1 } sc_dtype;
 #define SC_DEV_BAD_ACCEPTED 0x4u  /* an accepted length outside [0, D]: that sequence skipped */
 #define SC_DEV_TIMEOUT 0x8u       /* a bounded wait on an asynchronous copy gave up: output incomplete */
 #define SC_DEV_NO_SLOT 0x10u      /* a claim asked for more slots than were free: nothing claimed */
+#define SC_DEV_OUT_OF_BOUNDS 0x20u /* bounds-checked build only: an access outside the call's
+                                      buffers was refused (see shortconv_bounds_checked) */
 
 /*
  * The optional conv bias. Every forward and backward call below takes
@@ -414,6 +416,40 @@ sc_status shortconv_get_error(void *stream, int *device_code);
 
 /* Static, never-NULL description of a status code. */
 const char *shortconv_status_string(sc_status status);
+
+/*
+ * The bounds-checked build. The library can also be built with
+ * -DSC_BOUNDS_CHECK (python -m lfm2_gated_short_gb300.build --bounds-check,
+ * into _build/bounds/). In that build every entry point first records the
+ * buffers the call may read and write (its arguments, with the sizes the
+ * call implies), and every global load and store the kernels make through
+ * their memory helpers checks that its whole byte range lies in one of them
+ * (stores: in a writable one). A refused access is skipped -- a load reads
+ * zeros, a store writes nothing, a bulk copy is not issued -- and sets
+ * SC_DEV_OUT_OF_BOUNDS in the error word; nothing traps. Tiled tensor copies
+ * (the projections' operand loads) are bounded by their tensor maps instead.
+ * The records are per library instance, so calls that overlap on the GPU
+ * must not be made in this build. It is slower and meant for tests; the
+ * pages have no counterpart to it.
+ *
+ * shortconv_bounds_checked: 1 in the bounds-checked build, 0 otherwise.
+ *
+ * shortconv_bounds_trim_next: shorten, by `bytes`, buffer number `region`
+ * of the next call's record (buffers are numbered in the order each entry
+ * point lists them: for shortconv_prefill bcx 0, w 1, bias 2, cu_seqlens 3,
+ * slot_ids 4, pool 5, y 6), so that its last bytes count as outside the
+ * call. This shows the checks at work without any real out-of-bounds
+ * access: the memory is still there, only the record is shorter.
+ * SC_EINVAL for a region number outside [0, 16); SC_EUNSUPPORTED in the
+ * standard build.
+ *
+ * shortconv_bounds_take_first_bad: synchronize `stream` and return in
+ * *addr the first device address refused since the last take (0 if none),
+ * clearing it. SC_EUNSUPPORTED in the standard build.
+ */
+int shortconv_bounds_checked(void);
+sc_status shortconv_bounds_trim_next(int region, uint64_t bytes);
+sc_status shortconv_bounds_take_first_bad(void *stream, uint64_t *addr);
 
 #ifdef __cplusplus
 }

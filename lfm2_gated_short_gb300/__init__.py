@@ -22,7 +22,10 @@ import threading
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libshortconv.so")
+# SHORTCONV_LIBRARY selects another build of this library (the tests use it to
+# load the bounds-checked build, _build/bounds/libshortconv.so).
+LIB_PATH = os.environ.get("SHORTCONV_LIBRARY") or os.path.join(_HERE, "_build", "libshortconv.so")
+DEV_OUT_OF_BOUNDS = 0x20
 
 SC_OK, SC_EINVAL, SC_EUNSUPPORTED, SC_ECUDA, SC_EDEVICE = 0, 1, 2, 3, 4
 SC_F32, SC_BF16 = 0, 1
@@ -76,12 +79,17 @@ def lib() -> ctypes.CDLL:
             L.shortconv_pool_copy.argtypes = [i32, i32, i32, p, i32, p, p, i32, p]
             L.shortconv_get_error.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
             L.shortconv_check_wait_limit.argtypes = [p]
+            L.shortconv_bounds_checked.argtypes = []
+            L.shortconv_bounds_checked.restype = i32
+            L.shortconv_bounds_trim_next.argtypes = [i32, ctypes.c_uint64]
+            L.shortconv_bounds_take_first_bad.argtypes = [p, ctypes.POINTER(ctypes.c_uint64)]
             L.shortconv_status_string.argtypes = [i32]
             L.shortconv_status_string.restype = ctypes.c_char_p
             for f in ("prefill", "prefill_tiled", "decode", "verify", "rollback",
                       "rollback_layers", "backward",
                       "backward_varlen", "in_proj_prefill", "out_proj", "slots_claim",
-                      "slots_release", "pool_copy", "get_error", "check_wait_limit"):
+                      "slots_release", "pool_copy", "get_error", "check_wait_limit",
+                      "bounds_trim_next", "bounds_take_first_bad"):
                 getattr(L, "shortconv_" + f).restype = i32
             _lib = L
     return _lib
@@ -384,3 +392,22 @@ def get_error(stream=None, device=None) -> int:
     if st not in (SC_OK, SC_EDEVICE):
         _raise_on("shortconv_get_error", st)
     return code.value
+
+
+def bounds_checked() -> bool:
+    """True when the loaded library is the bounds-checked build."""
+    return bool(lib().shortconv_bounds_checked())
+
+
+def bounds_trim_next(region: int, nbytes: int) -> None:
+    """Bounds-checked build: shorten buffer ``region`` of the next call's record."""
+    _raise_on("shortconv_bounds_trim_next", lib().shortconv_bounds_trim_next(region, nbytes))
+
+
+def bounds_take_first_bad(stream=None, device=None) -> int:
+    """Bounds-checked build: the first refused device address since the last take (0: none)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    addr = ctypes.c_uint64(0)
+    _raise_on("shortconv_bounds_take_first_bad",
+              lib().shortconv_bounds_take_first_bad(_stream(stream, dev), ctypes.byref(addr)))
+    return addr.value

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <initializer_list>
 #include <mutex>
 
 #include "kernels.h"
@@ -58,6 +59,51 @@ int sm_count_of_current_device() {
 
 sc_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SC_OK : SC_ECUDA; }
 
+#ifdef SC_BOUNDS_CHECK
+// The bounds-checked build: before its launches, each entry point installs
+// the buffers the call may read (RO) and write (RW), in the order listed at
+// the call, in the table of the translation unit it launches into.
+// shortconv_bounds_trim_next shortens one listed buffer of the next call.
+std::mutex g_trim_mu;
+int g_trim_index = -1;
+uint64_t g_trim_bytes = 0;
+
+sc::BoundsRegion RO(const void *p, size_t bytes) {
+    return sc::BoundsRegion{reinterpret_cast<uint64_t>(p), p ? (uint64_t)bytes : 0, 0, 0};
+}
+sc::BoundsRegion RW(void *p, size_t bytes) {
+    return sc::BoundsRegion{reinterpret_cast<uint64_t>(p), p ? (uint64_t)bytes : 0, 1, 0};
+}
+sc_status bounds_install(int unit, std::initializer_list<sc::BoundsRegion> regions,
+                         void *stream) {
+    sc::BoundsRegion r[sc::kMaxBoundsRegions];
+    int n = 0;
+    for (const sc::BoundsRegion &x : regions) {
+        if (n == sc::kMaxBoundsRegions) return SC_EUNSUPPORTED;
+        r[n++] = x;
+    }
+    {
+        std::lock_guard<std::mutex> lock(g_trim_mu);
+        if (g_trim_index >= 0 && g_trim_index < n) {
+            uint64_t &b = r[g_trim_index].bytes;
+            b = b > g_trim_bytes ? b - g_trim_bytes : 0;
+        }
+        g_trim_index = -1;
+        g_trim_bytes = 0;
+    }
+    return from_cuda(sc::bounds_install(unit, r, n, (cudaStream_t)stream));
+}
+#define SC_BOUNDS_INSTALL(unit, ...)                                           \
+    do {                                                                      \
+        const sc_status bst = bounds_install(sc::unit, {__VA_ARGS__}, stream); \
+        if (bst != SC_OK) return bst;                                         \
+    } while (0)
+#else
+#define SC_BOUNDS_INSTALL(unit, ...) \
+    do {                             \
+    } while (0)
+#endif
+
 sc_status prefill_impl(sc_dtype dtype, int H, int K, const void *bcx, int64_t T, const void *w,
                        const void *bias, const int32_t *cu_seqlens, int N,
                        const int32_t *slot_ids, void *pool, int n_slots, void *y,
@@ -85,6 +131,9 @@ sc_status prefill_impl(sc_dtype dtype, int H, int K, const void *bcx, int64_t T,
     if (N == 0) return SC_OK;
     const int sms = sm_count_of_current_device();
     if (sms <= 0) return SC_ECUDA;
+    SC_BOUNDS_INSTALL(kUnitForward, RO(bcx, n_bcx), RO(w, n_w), RO(bias, n_b),
+                      RO(cu_seqlens, (size_t)(N + 1) * 4), RO(slot_ids, (size_t)N * 4),
+                      RW(pool, n_pool), RW(y, n_y));
     return from_cuda(sc::launch_prefill(dtype, H, K, bcx, T, w, bias, cu_seqlens, N, slot_ids,
                                         pool, n_slots, y, rows_per_thread, sms,
                                         (cudaStream_t)stream));
@@ -129,6 +178,8 @@ sc_status shortconv_decode(sc_dtype dtype, int H, int K, const void *bcx, int N,
         overlaps(pool, n_pool, bias, n_b))
         return SC_EINVAL;
     if (N == 0) return SC_OK;
+    SC_BOUNDS_INSTALL(kUnitForward, RO(bcx, n_bcx), RO(w, n_w), RO(bias, n_b),
+                      RO(slot_ids, (size_t)N * 4), RW(pool, n_pool), RW(y, n_y));
     return from_cuda(sc::launch_decode(dtype, H, K, bcx, N, w, bias, slot_ids, pool, n_slots, y,
                                        (cudaStream_t)stream));
 }
@@ -155,6 +206,8 @@ sc_status shortconv_verify(sc_dtype dtype, int H, int K, const void *bcx, int N,
             return SC_EINVAL;
     if (overlaps(y, n_y, win, n_win)) return SC_EINVAL;
     if (N == 0) return SC_OK;
+    SC_BOUNDS_INSTALL(kUnitForward, RO(bcx, n_bcx), RO(w, n_w), RO(bias, nins[3]),
+                      RO(slot_ids, (size_t)N * 4), RO(pool, n_pool), RW(win, n_win), RW(y, n_y));
     return from_cuda(sc::launch_verify(dtype, H, K, bcx, N, D, w, bias, slot_ids, pool, n_slots,
                                        win, y, (cudaStream_t)stream));
 }
@@ -176,6 +229,8 @@ sc_status shortconv_rollback_layers(sc_dtype dtype, int H, int K, int L, int N, 
         overlaps(pool, n_pool, slot_ids, (size_t)N * 4))
         return SC_EINVAL;
     if (N == 0) return SC_OK;
+    SC_BOUNDS_INSTALL(kUnitForward, RO(win, n_win), RO(accepted, (size_t)N * 4),
+                      RO(slot_ids, (size_t)N * 4), RW(pool, n_pool));
     return from_cuda(sc::launch_rollback(dtype, H, K, L, N, D, win, accepted, slot_ids, pool,
                                          n_slots, (cudaStream_t)stream));
 }
@@ -218,6 +273,9 @@ sc_status shortconv_backward(sc_dtype dtype, int H, int K, const void *bcx, int6
         for (int p = o + 1; p < 4; ++p)
             if (overlaps(outs[o], nouts[o], outs[p], nouts[p])) return SC_EINVAL;
     }
+    SC_BOUNDS_INSTALL(kUnitBackward, RO(bcx, n_bcx), RO(w, n_w), RO(bias, nins[3]),
+                      RO(dy, n_dy), RW(dbcx, n_bcx), RW(dw, n_dw), RW(dbias, nouts[2]),
+                      RW(workspace, need));
     return from_cuda(sc::launch_backward(dtype, H, K, bcx, T, w, bias, dy, dbcx, dw, dbias,
                                          workspace, (cudaStream_t)stream));
 }
@@ -256,6 +314,10 @@ sc_status shortconv_backward_varlen(sc_dtype dtype, int H, int K, const void *bc
         for (int p = o + 1; p < 5; ++p)
             if (overlaps(outs[o], nouts[o], outs[p], nouts[p])) return SC_EINVAL;
     }
+    SC_BOUNDS_INSTALL(kUnitBackward, RO(bcx, n_bcx), RO(w, n_w), RO(bias, nins[6]),
+                      RO(cu_seqlens, nins[5]), RO(init_states, nins[3]), RO(dy, n_dy),
+                      RO(d_final, nins[4]), RW(dbcx, n_bcx), RW(dw, n_dw), RW(dbias, nouts[4]),
+                      RW(d_init, nouts[2]), RW(workspace, need));
     return from_cuda(sc::launch_backward_varlen(dtype, H, K, bcx, T, w, bias, cu_seqlens, N,
                                                 init_states, dy, d_final, dbcx, dw, dbias,
                                                 d_init, workspace, (cudaStream_t)stream));
@@ -281,6 +343,8 @@ sc_status shortconv_backward_noalloc(sc_dtype dtype, int H, int K, const void *b
         if (overlaps(dbcx, n_bcx, ins[i], nins[i]) || overlaps(dw, n_dw, ins[i], nins[i]))
             return SC_EINVAL;
     if (overlaps(dbcx, n_bcx, dw, n_dw)) return SC_EINVAL;
+    SC_BOUNDS_INSTALL(kUnitBackward, RO(bcx, n_bcx), RO(w, n_w), RO(dy, n_dy), RW(dbcx, n_bcx),
+                      RW(dw, n_dw));  // the launcher adds the fixed scratch array
     return from_cuda(sc::launch_backward_noalloc(dtype, H, K, bcx, T, w, dy, dbcx, dw,
                                                  (cudaStream_t)stream));
 }
@@ -324,6 +388,9 @@ sc_status shortconv_in_proj_prefill(sc_dtype dtype, int D, int H, int K, const v
     if (N == 0) return SC_OK;
     const int sms = sm_count_of_current_device();
     if (sms <= 0) return SC_ECUDA;
+    SC_BOUNDS_INSTALL(kUnitProj, RO(hidden, n_h), RO(w_in, n_win), RO(w, n_w), RO(bias, nins[3]),
+                      RO(cu_seqlens, nins[4]), RO(slot_ids, nins[5]), RW(pool, n_pool),
+                      RW(y, n_y), RW(workspace, need));
     return from_cuda(sc::launch_in_proj_prefill(D, H, K, hidden, T, w_in, w, bias, cu_seqlens, N,
                                                 slot_ids, pool, n_slots, y, workspace, sms,
                                                 (cudaStream_t)stream));
@@ -343,6 +410,7 @@ sc_status shortconv_out_proj(sc_dtype dtype, int H, int D, const void *y, int64_
     if (T == 0) return SC_OK;
     const int sms = sm_count_of_current_device();
     if (sms <= 0) return SC_ECUDA;
+    SC_BOUNDS_INSTALL(kUnitProj, RO(y, n_y), RO(w_out, n_wo), RW(out, n_out));
     return from_cuda(sc::launch_out_proj(H, D, y, T, w_out, out, sms, (cudaStream_t)stream));
 }
 
@@ -363,6 +431,8 @@ sc_status shortconv_slots_claim(uint32_t *in_use, int n_slots, int n_claim, int3
     if (overlaps(in_use, n_bm, slots_out, (size_t)n_claim * 4) ||
         overlaps(in_use, n_bm, pool, n_pool) || overlaps(slots_out, (size_t)n_claim * 4, pool, n_pool))
         return SC_EINVAL;
+    SC_BOUNDS_INSTALL(kUnitSlots, RW(in_use, n_bm), RW(slots_out, (size_t)n_claim * 4),
+                      RW(pool, n_pool));
     return from_cuda(sc::launch_slots_claim(in_use, n_slots, n_claim, slots_out, pool,
                                             state_bytes, (cudaStream_t)stream));
 }
@@ -374,6 +444,7 @@ sc_status shortconv_slots_release(uint32_t *in_use, int n_slots, const int32_t *
     if (!ptr_ok(in_use, n_bm, 4) || !ptr_ok(slot_ids, (size_t)n * 4, 4)) return SC_EINVAL;
     if (overlaps(in_use, n_bm, slot_ids, (size_t)n * 4)) return SC_EINVAL;
     if (n == 0) return SC_OK;
+    SC_BOUNDS_INSTALL(kUnitSlots, RW(in_use, n_bm), RO(slot_ids, (size_t)n * 4));
     return from_cuda(sc::launch_slots_release(in_use, n_slots, slot_ids, n, (cudaStream_t)stream));
 }
 
@@ -392,6 +463,8 @@ sc_status shortconv_pool_copy(sc_dtype dtype, int H, int K, void *pool, int n_sl
         overlaps(pool, n_pool, dst_slots, (size_t)n * 4))
         return SC_EINVAL;
     if (n == 0) return SC_OK;
+    SC_BOUNDS_INSTALL(kUnitSlots, RW(pool, n_pool), RO(src_slots, (size_t)n * 4),
+                      RO(dst_slots, (size_t)n * 4));
     return from_cuda(sc::launch_pool_copy(src_slots, dst_slots, n, state_bytes, pool, n_slots,
                                           (cudaStream_t)stream));
 }
@@ -407,6 +480,43 @@ sc_status shortconv_get_error(void *stream, int *device_code) {
     if (e != cudaSuccess) return SC_ECUDA;
     *device_code = (int)code;
     return code == 0 ? SC_OK : SC_EDEVICE;
+}
+
+int shortconv_bounds_checked(void) {
+#ifdef SC_BOUNDS_CHECK
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+sc_status shortconv_bounds_trim_next(int region, uint64_t bytes) {
+#ifdef SC_BOUNDS_CHECK
+    if (region < 0 || region >= sc::kMaxBoundsRegions) return SC_EINVAL;
+    std::lock_guard<std::mutex> lock(g_trim_mu);
+    g_trim_index = region;
+    g_trim_bytes = bytes;
+    return SC_OK;
+#else
+    (void)region;
+    (void)bytes;
+    return SC_EUNSUPPORTED;
+#endif
+}
+
+sc_status shortconv_bounds_take_first_bad(void *stream, uint64_t *addr) {
+#ifdef SC_BOUNDS_CHECK
+    if (addr == nullptr) return SC_EINVAL;
+    unsigned long long a = 0;
+    const cudaError_t e = sc::bounds_take_first_bad((cudaStream_t)stream, &a);
+    if (e != cudaSuccess) return SC_ECUDA;
+    *addr = (uint64_t)a;
+    return SC_OK;
+#else
+    (void)stream;
+    (void)addr;
+    return SC_EUNSUPPORTED;
+#endif
 }
 
 const char *shortconv_status_string(sc_status status) {

@@ -114,14 +114,14 @@ __device__ __forceinline__ void store_partial(float *__restrict__ part, int H, i
         for (int k = 0; k < K; ++k) {
             float lo, hi;
             f2_split(acc[k][q], lo, hi);
-            pp[(2 * q) * K + k] = lo;
-            pp[(2 * q + 1) * K + k] = hi;
+            gst(pp + (2 * q) * K + k, lo);
+            gst(pp + (2 * q + 1) * K + k, hi);
         }
         if (with_dbias) {
             float lo, hi;
             f2_split(accb[q], lo, hi);
-            part[(int64_t)H * K + h0 + 2 * q] = lo;
-            part[(int64_t)H * K + h0 + 2 * q + 1] = hi;
+            gst(part + (int64_t)H * K + h0 + 2 * q, lo);
+            gst(part + (int64_t)H * K + h0 + 2 * q + 1, hi);
         }
     }
 }
@@ -429,11 +429,11 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, kBwdVarlenCtas<K>)
     const bool staged = N <= kBwdStaged;
     int bad = 0;
     for (int j = tid; j <= N; j += blockDim.x) {
-        const int32_t c = cu[j];
+        const int32_t c = gld(cu + j);
         if (staged) s_cu[j] = c;
         if (j == 0 && c != 0) bad = 1;
         if (j == N && (int64_t)c != T_rows) bad = 1;
-        if (j < N && cu[j + 1] < c) bad = 1;
+        if (j < N && gld(cu + j + 1) < c) bad = 1;
     }
     f32x2 acc[K][NP], accb[NP];
 #pragma unroll
@@ -464,7 +464,7 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, kBwdVarlenCtas<K>)
         return;
     }
 
-    auto CU = [&](int j) -> int64_t { return staged ? s_cu[j] : cu[j]; };
+    auto CU = [&](int j) -> int64_t { return staged ? s_cu[j] : gld(cu + j); };
     f32x2 wp[K][NP], bp[NP];
     if (active) {
         load_taps<T, CPT, K>(w + (int64_t)h0 * K, wp);
@@ -568,8 +568,8 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, kBwdVarlenCtas<K>)
                         g = f2_fma(f2_make(1.f, 1.f), dfin[e][q], g);
                 float lo, hi;
                 f2_split(g, lo, hi);
-                o[(2 * q) * K + m] = lo;
-                o[(2 * q + 1) * K + m] = hi;
+                gst(o + (2 * q) * K + m, lo);
+                gst(o + (2 * q + 1) * K + m, hi);
             }
     };
     // The sequence ended at s1 inside the stream: K-1 rows with dz = 0 finish
@@ -679,7 +679,7 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, kBwdVarlenCtas<K>)
             if (CU(j + 1) != CU(j)) continue;
             float *o = d_init + ((int64_t)j * H + h0) * K;
             for (int e = 0; e < CPT * K; ++e)
-                o[e] = d_final != nullptr ? d_final[((int64_t)j * H + h0) * K + e] : 0.f;
+                gst(o + e, d_final != nullptr ? gld(d_final + ((int64_t)j * H + h0) * K + e) : 0.f);
         }
     }
     store_partial<K, CPT>(part, H, h0, HB && with_dbias, acc, accb);
@@ -703,7 +703,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int j = 0; j < kRedPerWarp; ++j) {
         const int64_t g = warp + 8 * j;
-        v[j] = e < P && g < G ? partial[g * P + e] : 0.f;
+        v[j] = e < P && g < G ? gld(partial + g * P + e) : 0.f;
     }
     float s = 0.f;
 #pragma unroll
@@ -716,9 +716,9 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int j = 0; j < 8; ++j) t += part[j][lane];
         if (e < HK)
-            dw[e] = t;
+            gst(dw + e, t);
         else
-            dbias[e - HK] = t;
+            gst(dbias + (e - HK), t);
     }
 }
 
@@ -893,6 +893,15 @@ cudaError_t take_error_backward(cudaStream_t stream, unsigned int *code) {
     return take_error_here(stream, code);
 }
 
+#ifdef SC_BOUNDS_CHECK
+cudaError_t bounds_install_backward(const BoundsRegion *r, int n, cudaStream_t stream) {
+    return bounds_install_here(r, n, stream);
+}
+cudaError_t bounds_take_backward(cudaStream_t stream, unsigned long long *addr) {
+    return bounds_take_first_bad_here(stream, addr);
+}
+#endif
+
 // ------------------------------------------------ no-allocation entry point
 //
 // shortconv_backward_noalloc runs the kernels above (without a conv bias) with
@@ -929,8 +938,13 @@ cudaError_t launch_backward_noalloc(int dtype, int H, int K, const void *bcx, in
                                     const void *w, const void *dy, void *dbcx, float *dw,
                                     cudaStream_t s) {
     void *ws = nullptr;
-    const cudaError_t e = noalloc_scratch(&ws);
+    cudaError_t e = noalloc_scratch(&ws);
     if (e != cudaSuccess) return e;
+#ifdef SC_BOUNDS_CHECK
+    e = bounds_append_here(BoundsRegion{reinterpret_cast<uint64_t>(ws), kNoAllocScratchBytes, 1, 0},
+                           s);
+    if (e != cudaSuccess) return e;
+#endif
     if (dtype == SC_BF16)
         return backward_K<__nv_bfloat16>(K, bcx, T, H, w, nullptr, dy, dbcx, dw, nullptr, ws, s);
     return backward_K<float>(K, bcx, T, H, w, nullptr, dy, dbcx, dw, nullptr, ws, s);

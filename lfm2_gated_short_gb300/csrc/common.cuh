@@ -10,6 +10,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "bounds.cuh"
+
 namespace sc {
 
 constexpr int kCh = 8;  // channels per thread
@@ -36,12 +38,16 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 __device__ __forceinline__ void prefetch_l2(const void *p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
-__device__ __forceinline__ int slot_hint(const int32_t *p) { return __ldcg(p); }
+__device__ __forceinline__ int slot_hint(const int32_t *p) {
+    if (!SC_RD_OK(p, 4)) return -1;
+    return __ldcg(p);
+}
 
 // ----------------------------------------------------------- raw 128-bit I/O
 
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
     // Read-only data touched once by this thread: bypass L1, keep L2 default.
+    if (!SC_RD_OK(p, 16)) return make_uint4(0u, 0u, 0u, 0u);
     uint4 r;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
@@ -50,15 +56,16 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
 }
 
 __device__ __forceinline__ uint4 ld_plain(const void *p) {
-    return *reinterpret_cast<const uint4 *>(p);
+    return gld(reinterpret_cast<const uint4 *>(p));
 }
 
 __device__ __forceinline__ void st_plain(void *p, uint4 v) {
-    *reinterpret_cast<uint4 *>(p) = v;
+    gst(reinterpret_cast<uint4 *>(p), v);
 }
 
 __device__ __forceinline__ void st_stream(void *p, uint4 v) {
     // Output written once and not re-read by this kernel: evict-first in L2.
+    if (!SC_WR_OK(p, 16)) return;
     asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
                  :
                  : "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
@@ -280,6 +287,7 @@ __device__ __forceinline__ void lds_words(uint32_t addr, uint32_t *w, int nw) {
 }
 
 __device__ __forceinline__ void stg_words(void *p, const uint32_t *w, int nw) {
+    if (!SC_WR_OK(p, 4 * nw)) return;
     if (nw == 1) {
         asm volatile("st.global.cs.b32 [%0], %1;" ::"l"(p), "r"(w[0]) : "memory");
     } else if (nw == 2) {
@@ -356,16 +364,16 @@ struct Pairs<float, CPT> {
 template <typename T>
 __device__ __forceinline__ float ld_elem(const T *p) {
     if constexpr (sizeof(T) == 2)
-        return __uint_as_float((uint32_t)(*reinterpret_cast<const unsigned short *>(p)) << 16);
+        return __uint_as_float((uint32_t)gld(reinterpret_cast<const unsigned short *>(p)) << 16);
     else
-        return *p;
+        return gld(p);
 }
 template <typename T>
 __device__ __forceinline__ void st_elem(T *p, float v) {  // v representable in T
     if constexpr (sizeof(T) == 2)
-        *reinterpret_cast<unsigned short *>(p) = (unsigned short)(__float_as_uint(v) >> 16);
+        gst(reinterpret_cast<unsigned short *>(p), (unsigned short)(__float_as_uint(v) >> 16));
     else
-        *p = v;
+        gst(p, v);
 }
 template <typename T, int CPT, int K>
 __device__ __forceinline__ void load_taps(const T *p, f32x2 (&f)[K][CPT / 2]) {

@@ -116,11 +116,11 @@ __global__ void __launch_bounds__(kThreads)
     // The whole call is skipped unless cu_seqlens is 0 = c0 <= ... <= cN = T.
     int bad = 0;
     for (int j = threadIdx.x; j <= N; j += blockDim.x) {
-        const int32_t c = cu[j];
+        const int32_t c = gld(cu + j);
         if (staged) s_cu[j] = c;
         if (j == 0 && c != 0) bad = 1;
         if (j == N && (int64_t)c != T_rows) bad = 1;
-        if (j < N && cu[j + 1] < c) bad = 1;
+        if (j < N && gld(cu + j + 1) < c) bad = 1;
     }
     if (__syncthreads_or(bad)) {
         if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(SC_DEV_BAD_SEQLENS);
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kThreads)
     const int h0 = cg * kCh;
     const int64_t r0 = (unit / groups) * L;
     const int64_t r1 = min(r0 + (int64_t)L, T_rows);
-    auto CU = [&](int j) -> int64_t { return staged ? s_cu[j] : cu[j]; };
+    auto CU = [&](int j) -> int64_t { return staged ? s_cu[j] : gld(cu + j); };
 
     // Largest i with cu[i] <= r0: the sequence holding row r0.
     int lo = 0, hi = N - 1;
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads)
             e = min(s1, r1);
             if (a >= e) continue;
         }
-        const int slot = slots[i];
+        const int slot = gld(slots + i);
         if (slot < 0 || slot >= n_slots) {
             if (owner && cg == 0) raise_error(SC_DEV_BAD_SLOT);
             continue;
@@ -316,6 +316,11 @@ cudaError_t launch_prefill(int dtype, int H, int K, const void *bcx, int64_t row
 template <int NW, int A>
 __device__ __forceinline__ void ld_words(const void *p, uint32_t (&w)[NW]) {
     static_assert((NW * 4) % A == 0, "whole accesses");
+    if (!SC_RD_OK(p, NW * 4)) {
+#pragma unroll
+        for (int i = 0; i < NW; ++i) w[i] = 0u;
+        return;
+    }
 #pragma unroll
     for (int i = 0; i < NW * 4 / A; ++i) {
         if constexpr (A == 16) {
@@ -331,6 +336,7 @@ __device__ __forceinline__ void ld_words(const void *p, uint32_t (&w)[NW]) {
 }
 template <int NW, int A>
 __device__ __forceinline__ void st_words(void *p, const uint32_t (&w)[NW]) {
+    if (!SC_WR_OK(p, NW * 4)) return;
 #pragma unroll
     for (int i = 0; i < NW * 4 / A; ++i) {
         if constexpr (A == 16)
@@ -399,7 +405,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
     ld_words<NWR, AR>(p, rb);
     ld_words<NWR, AR>(p + H, rc);
     ld_words<NWR, AR>(p + 2 * H, rx);
-    const int slot = slots[i];
+    const int slot = gld(slots + i);
     ld_words<NWS, AS>(w + (int64_t)h0 * K, ww);
     if (bias != nullptr) ld_words<NWR, AR>(bias + h0, bw);
     if (slot < 0 || slot >= n_slots) {
@@ -508,7 +514,7 @@ __global__ void __launch_bounds__(kVerifyThreads)
     pdl_launch_dependents();
     if (!live) return;
     const int64_t ld = 3 * (int64_t)H;
-    const int slot = slots[i];
+    const int slot = gld(slots + i);
     uint32_t rb[VR][NWR], rc[VR][NWR], rx[VR][NWR];
     auto load_rows = [&](int j0) {
 #pragma unroll
@@ -620,7 +626,7 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t l = unit / per_layer, rem = unit % per_layer;
     const int i = (int)(rem / q_per_seq);
     const int64_t q = rem % q_per_seq;
-    const int a = accepted[i], slot = slots[i];
+    const int a = gld(accepted + i), slot = gld(slots + i);
     if (a < 0 || a > D) {
         if (q == 0 && l == 0) raise_error(SC_DEV_BAD_ACCEPTED);
         return;
@@ -630,8 +636,8 @@ __global__ void __launch_bounds__(kThreads)
         return;
     }
     if (a == 0) return;
-    pool[(l * n_slots + slot) * q_per_seq + q] =
-        win[((l * N + i) * D + (a - 1)) * q_per_seq + q];
+    gst(pool + (l * n_slots + slot) * q_per_seq + q,
+        gld(win + ((l * N + i) * D + (a - 1)) * q_per_seq + q));
 }
 
 cudaError_t launch_rollback(int dtype, int H, int K, int L, int N, int D, const void *win,
@@ -659,5 +665,30 @@ cudaError_t read_and_clear_error(cudaStream_t stream, unsigned int *code) {
     *code = a | b | c | d;
     return cudaSuccess;
 }
+
+#ifdef SC_BOUNDS_CHECK
+// ------------------------------------------------- bounds-checked build only
+
+cudaError_t bounds_install(int unit, const BoundsRegion *r, int n, cudaStream_t s) {
+    switch (unit) {
+        case kUnitForward: return bounds_install_here(r, n, s);
+        case kUnitBackward: return bounds_install_backward(r, n, s);
+        case kUnitProj: return bounds_install_proj(r, n, s);
+        default: return bounds_install_slots(r, n, s);
+    }
+}
+
+cudaError_t bounds_take_first_bad(cudaStream_t s, unsigned long long *addr) {
+    unsigned long long a[4] = {0, 0, 0, 0};
+    cudaError_t e = bounds_take_first_bad_here(s, &a[0]);
+    if (e == cudaSuccess) e = bounds_take_backward(s, &a[1]);
+    if (e == cudaSuccess) e = bounds_take_proj(s, &a[2]);
+    if (e == cudaSuccess) e = bounds_take_slots(s, &a[3]);
+    if (e != cudaSuccess) return e;
+    *addr = 0;
+    for (int i = 0; i < 4 && *addr == 0; ++i) *addr = a[i] & ~1ull;  // bit 0 marks "set"
+    return cudaSuccess;
+}
+#endif
 
 }  // namespace sc

@@ -92,4 +92,27 @@ cudaError_t launch_wait_limit_check(cudaStream_t stream);
 // with respect to `stream`).
 cudaError_t read_and_clear_error(cudaStream_t stream, unsigned int *code);
 
+// The bounds-checked build (-DSC_BOUNDS_CHECK): a buffer a call may touch,
+// [base, base + bytes), writable or read only. The entry points install the
+// call's buffers in the table of each translation unit they launch into.
+struct BoundsRegion {
+    uint64_t base;
+    uint64_t bytes;
+    uint32_t writable;
+    uint32_t pad;
+};
+constexpr int kMaxBoundsRegions = 16;
+#ifdef SC_BOUNDS_CHECK
+enum BoundsUnit { kUnitForward = 0, kUnitBackward = 1, kUnitProj = 2, kUnitSlots = 3 };
+cudaError_t bounds_install(int unit, const BoundsRegion *r, int n, cudaStream_t stream);
+// The first address any unit refused since the last call (0 when none), cleared.
+cudaError_t bounds_take_first_bad(cudaStream_t stream, unsigned long long *addr);
+cudaError_t bounds_install_backward(const BoundsRegion *r, int n, cudaStream_t stream);
+cudaError_t bounds_install_proj(const BoundsRegion *r, int n, cudaStream_t stream);
+cudaError_t bounds_install_slots(const BoundsRegion *r, int n, cudaStream_t stream);
+cudaError_t bounds_take_backward(cudaStream_t stream, unsigned long long *addr);
+cudaError_t bounds_take_proj(cudaStream_t stream, unsigned long long *addr);
+cudaError_t bounds_take_slots(cudaStream_t stream, unsigned long long *addr);
+#endif
+
 }  // namespace sc

@@ -166,14 +166,14 @@ __global__ void __launch_bounds__(kStreamSlice / kStreamCpt + 32, SC_STREAM_MIN_
     const bool staged = N <= kStreamStaged;
     int bad = 0;
     for (int j = tid; j <= N; j += blockDim.x) {
-        const int32_t c = cu[j];
+        const int32_t c = gld(cu + j);
         if (staged) {
             s_cu[j] = c;
-            if (j < N) s_slot[j] = slots[j];
+            if (j < N) s_slot[j] = gld(slots + j);
         }
         if (j == 0 && c != 0) bad = 1;
         if (j == N && (int64_t)c != T_rows) bad = 1;
-        if (j < N && cu[j + 1] < c) bad = 1;
+        if (j < N && gld(cu + j + 1) < c) bad = 1;
     }
     if (__syncthreads_or(bad)) {
         if (blockIdx.x == 0 && tid == 0) raise_error(SC_DEV_BAD_SEQLENS);
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kStreamSlice / kStreamCpt + 32, SC_STREAM_MIN_
         return;
     }
 
-    auto CU = [&](int j) -> int64_t { return staged ? s_cu[j] : cu[j]; };
+    auto CU = [&](int j) -> int64_t { return staged ? s_cu[j] : gld(cu + j); };
     int lo = 0, hi = N - 1;  // largest i with cu[i] <= sr0: the sequence holding row sr0
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kStreamSlice / kStreamCpt + 32, SC_STREAM_MIN_
         }
         ok = false;
         if (oa < oe) {
-            const int slot = staged ? s_slot[i] : slots[i];
+            const int slot = staged ? s_slot[i] : gld(slots + i);
             ok = slot >= 0 && slot < n_slots;
             if (!ok && owner && slice == 0 && tid == 0) raise_error(SC_DEV_BAD_SLOT);
             if (ok && owner) st = pool + ((int64_t)slot * H + h0) * K;

@@ -429,15 +429,15 @@ __global__ void __launch_bounds__(kInThreads, 1)
         const bool staged = N <= kProjCuStaged;
         bool bad = false;
         for (int j = et; j <= N; j += kInEpiThreads) {
-            const int32_t c = cu[j];
+            const int32_t c = gld(cu + j);
             if (staged) s_cu[j] = c;
             if (j == 0 && c != 0) bad = true;
             if (j == N && (int64_t)c != T_rows) bad = true;
-            if (j < N && cu[j + 1] < c) bad = true;
+            if (j < N && gld(cu + j + 1) < c) bad = true;
         }
         bad = named_or(1, kInEpiThreads, bad);  // also orders the staging above
         if (bad && blockIdx.x == 0 && et == 0) raise_error(SC_DEV_BAD_SEQLENS);
-        auto CU = [&](int j) -> int64_t { return staged ? s_cu[j] : cu[j]; };
+        auto CU = [&](int j) -> int64_t { return staged ? s_cu[j] : gld(cu + j); };
         unsigned char *urow = u_tile + r * kUStride;
 
         int it = 0;
@@ -452,10 +452,10 @@ __global__ void __launch_bounds__(kInThreads, 1)
             // channels are computed from other weight rows or zeros, never stored.)
             for (int e = et; e < kConvCh * K; e += kInEpiThreads)
                 wts[(e % K) * kConvCh + e / K] =
-                    h0 + e / K < H ? __bfloat162float(w[(int64_t)h0 * K + e]) : 0.f;
+                    h0 + e / K < H ? __bfloat162float(gld(w + (int64_t)h0 * K + e)) : 0.f;
             if (bias != nullptr)
                 for (int e = et; e < kConvCh; e += kInEpiThreads)
-                    bsm[e] = h0 + e < H ? __bfloat162float(bias[h0 + e]) : 0.f;
+                    bsm[e] = h0 + e < H ? __bfloat162float(gld(bias + h0 + e)) : 0.f;
             if (!epi_acquire<kInBufs>(ps, it, kInEpiThreads)) break;
             const uint32_t trow =
                 tmem + (uint32_t)(it % kInBufs) * 256u + ((uint32_t)(q * 32) << 16) + cw;
@@ -516,7 +516,7 @@ __global__ void __launch_bounds__(kInThreads, 1)
                 i = lo;
                 s0 = CU(i);
                 s1 = CU(i + 1);
-                slot = slots[i];
+                slot = gld(slots + i);
                 if (slot < 0 || slot >= n_slots) {
                     raise_error(SC_DEV_BAD_SLOT);
                     out_row = false;
@@ -559,7 +559,7 @@ __global__ void __launch_bounds__(kInThreads, 1)
 #pragma unroll
                                 for (int j = 0; j < 8; ++j)
                                     win[k][j] = __bfloat162float(
-                                        pool[((int64_t)slot * H + h0 + c0 + j) * K + e]);
+                                        gld(pool + ((int64_t)slot * H + h0 + c0 + j) * K + e));
                         }
                     }
                     uint32_t pk[4];
@@ -577,15 +577,15 @@ __global__ void __launch_bounds__(kInThreads, 1)
                         }
                         pk[j / 2] = pack_bf16(o[0], o[1]);
                     }
-                    *reinterpret_cast<uint4 *>(y + t * (int64_t)H + h0 + c0) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    gst(reinterpret_cast<uint4 *>(y + t * (int64_t)H + h0 + c0),
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]));
                     if (t >= s1 - K) {  // one of the sequence's last K rows: its u to the tail
                         const int m = (int)(K - (s1 - t));
                         const uint16_t *ur = reinterpret_cast<const uint16_t *>(urow + c0 * 2);
                         uint16_t *tl = reinterpret_cast<uint16_t *>(tail);
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            tl[((int64_t)i * H + h0 + c0 + j) * K + m] = ur[j];
+                            gst(tl + ((int64_t)i * H + h0 + c0 + j) * K + m, ur[j]);
                     }
                 }
             }
@@ -616,20 +616,20 @@ __global__ void __launch_bounds__(256)
     pdl_launch_dependents();
     int bad = 0;
     for (int j = threadIdx.x; j <= N; j += blockDim.x) {
-        const int32_t c = cu[j];
+        const int32_t c = gld(cu + j);
         if (j == 0 && c != 0) bad = 1;
         if (j == N && (int64_t)c != T_rows) bad = 1;
-        if (j < N && cu[j + 1] < c) bad = 1;
+        if (j < N && gld(cu + j + 1) < c) bad = 1;
     }
     int64_t len = 0;
     int slot = 0;
     uint4 tq[NQ];
     if (live) {
-        len = (int64_t)cu[i + 1] - cu[i];
-        slot = slots[i];
+        len = (int64_t)gld(cu + i + 1) - gld(cu + i);
+        slot = gld(slots + i);
         const uint4 *tp = reinterpret_cast<const uint4 *>(tail + ((int64_t)i * H + h) * K);
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) tq[q] = tp[q];
+        for (int q = 0; q < NQ; ++q) tq[q] = gld(tp + q);
     }
     if (__syncthreads_or(bad)) {
         if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(SC_DEV_BAD_SEQLENS);
@@ -643,12 +643,12 @@ __global__ void __launch_bounds__(256)
     uint4 *sp = reinterpret_cast<uint4 *>(pool + ((int64_t)slot * H + h) * K);
     if (len >= K) {  // the new state is the sequence's last K values of u
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) sp[q] = tq[q];
+        for (int q = 0; q < NQ; ++q) gst(sp + q, tq[q]);
         return;
     }
     uint4 oq[NQ], nq[NQ];
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) oq[q] = sp[q];
+    for (int q = 0; q < NQ; ++q) oq[q] = gld(sp + q);
     const uint16_t *o = reinterpret_cast<const uint16_t *>(oq);
     const uint16_t *tl = reinterpret_cast<const uint16_t *>(tq);
     uint16_t *nw = reinterpret_cast<uint16_t *>(nq);
@@ -663,7 +663,7 @@ __global__ void __launch_bounds__(256)
             nw[c * K + m] = v;
         }
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) sp[q] = nq[q];
+    for (int q = 0; q < NQ; ++q) gst(sp + q, nq[q]);
 }
 
 // ------------------------------------------------------------ out_proj
@@ -716,8 +716,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) pk[j] = pack_bf16(v[2 * j], v[2 * j + 1]);
                 uint4 *dst = reinterpret_cast<uint4 *>(out + t * (int64_t)N_cols + col0 + cc * 16);
-                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                gst(dst, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+                gst(dst + 1, make_uint4(pk[4], pk[5], pk[6], pk[7]));
             }
             epi_release<CL, kOutBufs>(ps, it, tw.rank);
         }
@@ -893,5 +893,14 @@ cudaError_t launch_out_proj(int H, int D, const void *y, int64_t T, const void *
 cudaError_t take_error_proj(cudaStream_t stream, unsigned int *code) {
     return take_error_here(stream, code);
 }
+
+#ifdef SC_BOUNDS_CHECK
+cudaError_t bounds_install_proj(const BoundsRegion *r, int n, cudaStream_t stream) {
+    return bounds_install_here(r, n, stream);
+}
+cudaError_t bounds_take_proj(cudaStream_t stream, unsigned long long *addr) {
+    return bounds_take_first_bad_here(stream, addr);
+}
+#endif
 
 }  // namespace sc

@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(kClaimThreads)
         return rem >= 32 ? 0xFFFFFFFFu : ((1u << rem) - 1u);
     };
     int mine = 0;
-    for (int wi = w0; wi < w1; ++wi) mine += __popc(~in_use[wi] & valid(wi));
+    for (int wi = w0; wi < w1; ++wi) mine += __popc(~gld(in_use + wi) & valid(wi));
     s_scan[tid] = mine;
     __syncthreads();
     for (int off = 1; off < kClaimThreads; off <<= 1) {  // inclusive scan (Hillis-Steele)
@@ -47,21 +47,21 @@ __global__ void __launch_bounds__(kClaimThreads)
     }
     const int total = s_scan[kClaimThreads - 1];
     if (total < n_claim) {
-        for (int i = tid; i < n_claim; i += kClaimThreads) out[i] = -1;
+        for (int i = tid; i < n_claim; i += kClaimThreads) gst(out + i, -1);
         if (tid == 0) raise_error(SC_DEV_NO_SLOT);
         return;
     }
     int rank = s_scan[tid] - mine;  // free slots before this thread's words
     for (int wi = w0; wi < w1 && rank < n_claim; ++wi) {
-        uint32_t word = in_use[wi];
+        uint32_t word = gld(in_use + wi);
         uint32_t fr = ~word & valid(wi);
         while (fr != 0u && rank < n_claim) {
             const int b = __ffs(fr) - 1;
             fr &= fr - 1u;
             word |= 1u << b;
-            out[rank++] = wi * 32 + b;
+            gst(out + rank++, wi * 32 + b);
         }
-        in_use[wi] = word;
+        gst(in_use + wi, word);
     }
 }
 
@@ -73,9 +73,9 @@ __global__ void __launch_bounds__(256)
     pdl_launch_dependents();
     const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (unit >= (int64_t)n * q_per_slot) return;
-    const int s = slots[unit / q_per_slot];
+    const int s = gld(slots + unit / q_per_slot);
     if (s < 0 || s >= n_slots) return;  // nothing was claimed
-    pool[(int64_t)s * q_per_slot + unit % q_per_slot] = make_uint4(0u, 0u, 0u, 0u);
+    gst(pool + (int64_t)s * q_per_slot + unit % q_per_slot, make_uint4(0u, 0u, 0u, 0u));
 }
 
 __global__ void __launch_bounds__(256)
@@ -85,12 +85,13 @@ __global__ void __launch_bounds__(256)
     pdl_launch_dependents();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
-    const int s = slots[i];
+    const int s = gld(slots + i);
     if (s < 0 || s >= n_slots) {
         raise_error(SC_DEV_BAD_SLOT);
         return;
     }
     const uint32_t bit = 1u << (s & 31);
+    if (!SC_WR_OK(in_use + (s >> 5), 4)) return;
     const uint32_t old = atomicAnd(&in_use[s >> 5], ~bit);
     if (!(old & bit)) raise_error(SC_DEV_BAD_SLOT);  // it was not in use
 }
@@ -104,12 +105,12 @@ __global__ void __launch_bounds__(256)
     if (unit >= (int64_t)n * q_per_slot) return;
     const int i = (int)(unit / q_per_slot);
     const int64_t q = unit % q_per_slot;
-    const int s = src[i], d = dst[i];
+    const int s = gld(src + i), d = gld(dst + i);
     if (s < 0 || s >= n_slots || d < 0 || d >= n_slots) {
         if (q == 0) raise_error(SC_DEV_BAD_SLOT);
         return;
     }
-    pool[(int64_t)d * q_per_slot + q] = pool[(int64_t)s * q_per_slot + q];
+    gst(pool + (int64_t)d * q_per_slot + q, gld(pool + (int64_t)s * q_per_slot + q));
 }
 
 cudaError_t launch_slots_claim(uint32_t *in_use, int n_slots, int n_claim, int32_t *out,
@@ -161,5 +162,14 @@ cudaError_t launch_wait_limit_check(cudaStream_t stream) {
 cudaError_t take_error_slots(cudaStream_t stream, unsigned int *code) {
     return take_error_here(stream, code);
 }
+
+#ifdef SC_BOUNDS_CHECK
+cudaError_t bounds_install_slots(const BoundsRegion *r, int n, cudaStream_t stream) {
+    return bounds_install_here(r, n, stream);
+}
+cudaError_t bounds_take_slots(cudaStream_t stream, unsigned long long *addr) {
+    return bounds_take_first_bad_here(stream, addr);
+}
+#endif
 
 }  // namespace sc

@@ -3,6 +3,8 @@
 
 #include <stdint.h>
 
+#include "bounds.cuh"
+
 namespace sc {
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
@@ -66,6 +68,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 
 __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes,
                                               uint64_t *bar) {
+#ifdef SC_BOUNDS_CHECK
+    if (!SC_RD_OK(src, bytes)) {  // refused: count the bytes anyway so no wait hangs
+        asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(
+                         smem_addr(bar)),
+                     "r"(bytes)
+                     : "memory");
+        return;
+    }
+#endif
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
             "r"(smem_addr(dst)),

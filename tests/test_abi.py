@@ -225,3 +225,29 @@ def test_status_strings_and_get_error_null(L):
     for s in range(6):
         assert L.shortconv_status_string(s)
     assert L.shortconv_get_error(None, None) == SC_EINVAL
+
+
+def test_standard_build_has_no_bounds_checks(L):
+    L.shortconv_bounds_checked.restype = ctypes.c_int
+    L.shortconv_bounds_trim_next.argtypes = [ctypes.c_int, ctypes.c_uint64]
+    assert L.shortconv_bounds_checked() == 0
+    assert L.shortconv_bounds_trim_next(6, 16) == SC_EUNSUPPORTED
+    addr = ctypes.c_uint64(0)
+    L.shortconv_bounds_take_first_bad.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    assert L.shortconv_bounds_take_first_bad(None, ctypes.byref(addr)) == SC_EUNSUPPORTED
+
+
+def test_bounds_checked_build_loads_and_exports_every_declared_function():
+    B = ctypes.CDLL(sc_build.build(bounds_check=True))
+    for name in declared_functions():
+        assert hasattr(B, name), f"{name} declared in include/ but not exported"
+    B.shortconv_bounds_checked.restype = ctypes.c_int
+    B.shortconv_bounds_trim_next.argtypes = [ctypes.c_int, ctypes.c_uint64]
+    assert B.shortconv_bounds_checked() == 1
+    assert B.shortconv_bounds_trim_next(16, 1) == SC_EINVAL
+    assert B.shortconv_bounds_trim_next(-1, 1) == SC_EINVAL
+    # host validation answers before any record is installed or CUDA call made
+    p, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    B.shortconv_prefill.argtypes = [i32, i32, i32, p, i64, p, p, p, i32, p, p, i32, p, p]
+    assert B.shortconv_prefill(7, 256, 3, A, 64, Bp, None, Cp, 1, Dp, Ep, 4, Fp,
+                               None) == SC_EUNSUPPORTED
