@@ -617,6 +617,68 @@ def layer_section(sc, device, T_, reps=20):
                 peak_source=f"{src} bf16_tflops")
 
 
+def decode_layer_section(sc, device, flush, layers=10, batch=256, n_slots=1024, steps=16):
+    """A decode step with each layer's input projection: bs=256 sequences of
+    one token, D = H = 2048. ``fused``: shortconv_in_proj_prefill (in_proj on
+    the tensor cores with the conv decode in its epilogue, one-token
+    sequences); ``unfused``: a cuBLAS in_proj (torch.matmul, comparison only),
+    then shortconv_decode. Per layer (one call, L2 flushed before) and per
+    10-layer step (CUDA-graph replay, L2 flushed between steps)."""
+    D = H
+    g = torch.Generator(device=device).manual_seed(10)
+    rng = np.random.default_rng(10)
+    slots = torch.tensor(rng.permutation(n_slots)[:batch].astype(np.int32), device=device)
+    cu = torch.arange(batch + 1, dtype=torch.int32, device=device)
+    hidden = randn_bf16((layers, batch, D), g, device)
+    w_in = randn_bf16((layers, 3 * H, D), g, device, D ** -0.5)
+    w = randn_bf16((layers, H, K), g, device, wl.WEIGHT_STD)
+    pools = randn_bf16((layers, n_slots, H, K), g, device)
+    y = torch.empty((layers, batch, H), dtype=torch.bfloat16, device=device)
+    bcx = torch.empty((layers, batch, 3 * H), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(max(16, sc.in_proj_workspace_bytes(H, K, batch)), dtype=torch.uint8,
+                     device=device)
+
+    def fused(l):
+        sc.in_proj_prefill(hidden[l], w_in[l], w[l], cu, slots, pools[l], y=y[l], workspace=ws)
+
+    def unfused(l):
+        torch.matmul(hidden[l], w_in[l].t(), out=bcx[l])
+        sc.decode(bcx[l], w[l], slots, pools[l], y=y[l])
+
+    res = {}
+    for f in (fused, unfused):
+        for l in range(layers):
+            f(l)
+        torch.cuda.synchronize()
+        es, ee = events(steps), events(steps)
+        for s in range(steps):
+            flush()
+            es[s].record()
+            f(s % layers)
+            ee[s].record()
+        torch.cuda.synchronize()
+        res[f.__name__ + "_layer_us"] = statistics.median(
+            es[s].elapsed_time(ee[s]) * 1e3 for s in range(steps))
+        side = torch.cuda.Stream(device)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(gr, stream=side):
+                for l in range(layers):
+                    f(l)
+        torch.cuda.synchronize()
+        es, ee = events(steps), events(steps)
+        for s in range(steps):
+            flush()
+            es[s].record()
+            gr.replay()
+            ee[s].record()
+        torch.cuda.synchronize()
+        res[f.__name__ + "_step_us"] = statistics.median(
+            es[s].elapsed_time(ee[s]) * 1e3 for s in range(steps))
+    assert sc.get_error() == 0
+    return dict(batch=batch, D=D, H=H, layers=layers, **res)
+
+
 _HOST_PROBLEM = []
 
 
@@ -756,6 +818,8 @@ def compact_sections(ex, peak):
         "fwd_T65536_frac": r(tr64["fwd_gbs"] / peak), "bwd_T65536_us": r(tr64["bwd_us"], 1),
         "bwd_T65536_frac": r(tr64["bwd_gbs"] / peak),
         "bwd_packed_T65536_frac": r(ex["train_packed_T65536"]["bwd_gbs"] / peak),
+        "decode_in_proj_fused_step_us": r(ex["decode_layer"]["fused_step_us"], 1),
+        "decode_in_proj_unfused_step_us": r(ex["decode_layer"]["unfused_step_us"], 1),
         "in_proj_conv_T4096_us": r(l4["fused_in_proj_conv_us"], 2),
         "unfused_T4096_us": r(l4["unfused_matmul_plus_conv_us"], 2),
         "out_proj_T4096_us": r(l4["out_proj_us"], 2),
@@ -818,6 +882,7 @@ def main():
     extras["train_T4096_bias"] = training_section(sc, device, 4096, 20, 4, bias=True)
     extras["train_T65536_bias"] = training_section(sc, device, 65536, 10, 1, bias=True)
     extras["train_packed_T65536"] = packed_training_section(sc, device)
+    extras["decode_layer"] = decode_layer_section(sc, device, flush)
     extras["layer_T4096"] = layer_section(sc, device, 4096)
     extras["layer_T16384"] = layer_section(sc, device, 16384, reps=10)
     clk = clocks.stop()

@@ -144,34 +144,38 @@ def _ambiguous(exact, bound):
     return oracle.round_bf16(exact - bound) != oracle.round_bf16(exact + bound)
 
 
-def test_normal_inputs_outside_rounding_ambiguity():
-    """Normal inputs: outputs whose projection values are all farther than the
-    accumulation bound from a bf16 rounding boundary meet the tolerance; their
-    states match bit for bit."""
-    rng = np.random.default_rng(860)
-    D, H, K = 128, 128, 3
-    c = make_case(rng, [200, 0, 3, 333, 64], D, H, K, exact=False)
-    y, pool = run_gpu(c)
-    y_ref, pool_ref = run_oracle(c)
+def _check_unambiguous(c, y, pool, ch=None, min_keep=0.5):
+    """Outputs whose projection values all lie farther than the accumulation
+    bound from a bf16 rounding boundary meet the tolerance, and their states
+    match bit for bit; on the channel subset ``ch`` (all when None). Returns
+    the share of outputs kept."""
+    D, H, K = c["D"], c["H"], c["K"]
+    ch = np.arange(H) if ch is None else np.asarray(ch)
+    rows = np.concatenate([ch, H + ch, 2 * H + ch])
+    sub = dict(c, w_in=c["w_in"][rows], w=np.ascontiguousarray(c["w"][ch]),
+               pool=np.ascontiguousarray(c["pool"][:, ch]), H=len(ch))
+    y_ref, pool_ref = run_oracle(sub)
+    y, pool = y[:, ch], pool[:, ch]
+    Hs = len(ch)
     h = oracle.bf16_to_f64(c["hidden"])
-    wi = oracle.bf16_to_f64(c["w_in"])
+    wi = oracle.bf16_to_f64(sub["w_in"])
     exact = h @ wi.T
     # fp32 accumulation of D products: |error| <= lam sqrt(D) 2^-24 sum|terms| except
     # with probability below 2 exp(-lam^2 / 2) (Higham and Mary's probabilistic
     # rounding-error bound); lam = 8 puts that below 1e-13 per sum. The worst-case
-    # bound (D in place of lam sqrt(D)) spans a quarter of a bf16 step here and
-    # would exclude nearly every output. The ambiguous share grows with D.
+    # bound (D in place of lam sqrt(D)) spans a quarter of a bf16 step at D = 128
+    # and would exclude nearly every output. The ambiguous share grows with D.
     bound = 8 * np.sqrt(D) * 2.0 ** -24 * (np.abs(h) @ np.abs(wi).T)
     amb = _ambiguous(exact, bound)
-    amb_b, amb_c, amb_x = amb[:, :H], amb[:, H:2 * H], amb[:, 2 * H:]
+    amb_b, amb_c, amb_x = amb[:, :Hs], amb[:, Hs:2 * Hs], amb[:, 2 * Hs:]
     u_amb = amb_b | amb_x
     T = y.shape[0]
-    bad_in = np.zeros((T, H), bool)  # output (t, h) uses C_t and u of rows t-K+1 .. t
+    bad_in = np.zeros((T, Hs), bool)  # output (t, h) uses C_t and u of rows t-K+1 .. t
     for k in range(K):
         bad_in[k:] |= u_amb[:T - k] if k else u_amb
     bad_in |= amb_c
     keep = ~bad_in
-    assert keep.mean() > 0.5, keep.mean()  # each output uses 2K + 1 projection values
+    assert keep.mean() > min_keep, keep.mean()  # each output uses 2K + 1 projection values
     g, r = oracle.bf16_to_f64(y), oracle.bf16_to_f64(y_ref)
     ok = np.abs(g - r) <= 1e-2 + 2.0 ** -7 * np.abs(r)
     assert ok[keep].all(), f"{int((~ok[keep]).sum())} unambiguous outputs out of tolerance"
@@ -185,6 +189,92 @@ def test_normal_inputs_outside_rounding_ambiguity():
                 continue
             sel = ~u_amb[t]
             np.testing.assert_array_equal(pool[s, sel, m], pool_ref[s, sel, m])
+    return float(keep.mean())
+
+
+def test_normal_inputs_outside_rounding_ambiguity():
+    """Normal inputs at D = 128, every channel."""
+    rng = np.random.default_rng(860)
+    c = make_case(rng, [200, 0, 3, 333, 64], 128, 128, 3, exact=False)
+    y, pool = run_gpu(c)
+    _check_unambiguous(c, y, pool)
+
+
+def _check_intervals(c, y, pool, ch):
+    """Every output against the range the fp32 accumulation allows.
+
+    Each projection value the GPU rounds is within the accumulation bound of
+    the exact value (Higham-Mary, lam = 8, as above), and bf16 rounding is
+    monotone, so the GPU's bf16 value is round(exact - bound) or
+    round(exact + bound). Carried through u = round(B x), the K-tap window and
+    y = C z by interval arithmetic, this gives for every output a range that
+    holds the GPU's value up to its own fp32 rounding; y must lie within the
+    usual tolerance of that range, and every state value within its range
+    (bit-exact where the range is one value). No output is excluded."""
+    D, H, K = c["D"], c["H"], c["K"]
+    ch = np.asarray(ch)
+    Hs = len(ch)
+    rows = np.concatenate([ch, H + ch, 2 * H + ch])
+    h = oracle.bf16_to_f64(c["hidden"])
+    wi = oracle.bf16_to_f64(c["w_in"][rows])
+    exact = h @ wi.T
+    bound = 8 * np.sqrt(D) * 2.0 ** -24 * (np.abs(h) @ np.abs(wi).T)
+    lo = oracle.bf16_to_f64(oracle.round_bf16(exact - bound))
+    hi = oracle.bf16_to_f64(oracle.round_bf16(exact + bound))
+    B, C, X = [(lo[:, j * Hs:(j + 1) * Hs], hi[:, j * Hs:(j + 1) * Hs]) for j in range(3)]
+    uc = [oracle.bf16_to_f64(oracle.round_bf16(b * x)) for b in B for x in X]
+    u_lo, u_hi = np.minimum.reduce(uc), np.maximum.reduce(uc)
+    w = oracle.bf16_to_f64(c["w"][ch])  # [Hs, K]
+    g = oracle.bf16_to_f64(y[:, ch])
+    gp = oracle.bf16_to_f64(pool[:, ch])
+    cu = c["cu"]
+    for i, slot in enumerate(c["slots"]):
+        s0, s1 = int(cu[i]), int(cu[i + 1])
+        n = s1 - s0
+        st = oracle.bf16_to_f64(c["pool"][slot][ch]).T  # [K, Hs]
+        e_lo = np.concatenate([st, u_lo[s0:s1]])       # [state; u] of the sequence
+        e_hi = np.concatenate([st, u_hi[s0:s1]])
+        z_lo = np.zeros((n, Hs))
+        z_hi = np.zeros((n, Hs))
+        for k in range(K):  # row j's window is ext[j + 1 .. j + K]
+            a, b = w[:, k] * e_lo[1 + k:1 + k + n], w[:, k] * e_hi[1 + k:1 + k + n]
+            z_lo += np.minimum(a, b)
+            z_hi += np.maximum(a, b)
+        yc = [cc[s0:s1] * z for cc in C for z in (z_lo, z_hi)]
+        y_lo, y_hi = np.minimum.reduce(yc), np.maximum.reduce(yc)
+        tol = lambda v: 1e-2 + 2.0 ** -7 * np.abs(v)  # noqa: E731
+        gi = g[s0:s1]
+        ok = (gi >= y_lo - tol(y_lo)) & (gi <= y_hi + tol(y_hi))
+        assert ok.all(), f"sequence {i}: {int((~ok).sum())} outputs outside their range"
+        f_lo, f_hi = e_lo[n:n + K].T, e_hi[n:n + K].T   # final state [Hs, K]
+        gs = gp[slot]
+        assert np.all((gs >= f_lo) & (gs <= f_hi)), f"sequence {i}: state outside its range"
+        one = f_lo == f_hi
+        np.testing.assert_array_equal(gs[one], f_lo[one])
+    untouched = np.setdiff1d(np.arange(c["pool"].shape[0]), c["slots"])
+    assert_bits(pool[untouched], c["pool"][untouched], "untouched slots")
+
+
+def test_normal_inputs_within_accumulation_ranges_lfm2_width():
+    """Normal inputs at LFM2-1.2B's width (D = H = 2048): four sequences that
+    continue from N(0, 1) states, 4,099 rows, oracle ranges on 64 sampled
+    channels, every row. At this depth the accumulation bound puts about 46%
+    of the projection values within reach of a bf16 rounding boundary, so
+    excluding the outputs that touch one (as at D = 128) would keep only 1.3%
+    of them; the ranges keep all."""
+    rng = np.random.default_rng(861)
+    c = make_case(rng, [1000, 7, 2048, 1044], 2048, 2048, 3, exact=False)
+    y, pool = run_gpu(c)
+    ch = np.sort(np.concatenate([[0, 63, 64, 127, 128, 1023, 1024, 2047],
+                                 rng.choice(np.arange(129, 2040), 56, replace=False)]))
+    _check_intervals(c, y, pool, ch)
+
+
+def test_normal_inputs_within_accumulation_ranges_small():
+    rng = np.random.default_rng(862)
+    c = make_case(rng, [200, 0, 3, 333, 64, 1, 2], 128, 192, 4, exact=False)
+    y, pool = run_gpu(c)
+    _check_intervals(c, y, pool, np.arange(192))
 
 
 def test_errors_write_nothing():
