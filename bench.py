@@ -52,7 +52,8 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal, for context beside the measured
 KERNEL_SOURCES = ["lfm2_gated_short_gb300/csrc/forward.cu",
                   "lfm2_gated_short_gb300/csrc/prefill_stream.cuh",
                   "lfm2_gated_short_gb300/csrc/common.cuh", "lfm2_gated_short_gb300/csrc/launch.h",
-                  "lfm2_gated_short_gb300/csrc/tma.cuh", "lfm2_gated_short_gb300/csrc/errors.cuh"]
+                  "lfm2_gated_short_gb300/csrc/tma.cuh", "lfm2_gated_short_gb300/csrc/errors.cuh",
+                  "lfm2_gated_short_gb300/csrc/bounds.cuh"]
 PROFILE = "profiles/prefill_T4096_H2048.txt"
 
 
@@ -619,11 +620,12 @@ def layer_section(sc, device, T_, reps=20):
 
 def decode_layer_section(sc, device, flush, layers=10, batch=256, n_slots=1024, steps=16):
     """A decode step with each layer's input projection: bs=256 sequences of
-    one token, D = H = 2048. ``fused``: shortconv_in_proj_prefill (in_proj on
-    the tensor cores with the conv decode in its epilogue, one-token
-    sequences); ``unfused``: a cuBLAS in_proj (torch.matmul, comparison only),
-    then shortconv_decode. Per layer (one call, L2 flushed before) and per
-    10-layer step (CUDA-graph replay, L2 flushed between steps)."""
+    one token, D = H = 2048. ``fused``: shortconv_in_proj_decode (in_proj on
+    the tensor cores with the conv decode in its epilogue, one launch);
+    ``prefill_path``: shortconv_in_proj_prefill on one-token sequences;
+    ``unfused``: a cuBLAS in_proj (torch.matmul, comparison only), then
+    shortconv_decode. Per layer (one call, L2 flushed before) and per 10-layer
+    step (CUDA-graph replay, L2 flushed between steps)."""
     D = H
     g = torch.Generator(device=device).manual_seed(10)
     rng = np.random.default_rng(10)
@@ -638,7 +640,10 @@ def decode_layer_section(sc, device, flush, layers=10, batch=256, n_slots=1024, 
     ws = torch.empty(max(16, sc.in_proj_workspace_bytes(H, K, batch)), dtype=torch.uint8,
                      device=device)
 
-    def fused(l):
+    def fused(l):  # the decode kernel fused into in_proj: one launch
+        sc.in_proj_decode(hidden[l], w_in[l], w[l], slots, pools[l], y=y[l])
+
+    def prefill_path(l):  # the fused prefill call on one-token sequences
         sc.in_proj_prefill(hidden[l], w_in[l], w[l], cu, slots, pools[l], y=y[l], workspace=ws)
 
     def unfused(l):
@@ -646,7 +651,7 @@ def decode_layer_section(sc, device, flush, layers=10, batch=256, n_slots=1024, 
         sc.decode(bcx[l], w[l], slots, pools[l], y=y[l])
 
     res = {}
-    for f in (fused, unfused):
+    for f in (fused, prefill_path, unfused):
         for l in range(layers):
             f(l)
         torch.cuda.synchronize()

@@ -351,6 +351,35 @@ sc_status shortconv_in_proj_prefill(sc_dtype dtype, int D, int H, int K, const v
                                     size_t workspace_bytes, void *stream);
 
 /*
+ * shortconv_in_proj_decode: in_proj fused with shortconv_decode, for the
+ * serving decode step (one token per sequence). The MAX LFM2 article
+ * (section "短卷积实现（LFM2ShortConv）") gives the per-token step: gather
+ * the sequence's conv state, slide in bx = b * xv, take the weighted sum,
+ * gate by c, scatter the state back. Here row i of `hidden` is the one
+ * token of sequence i: its [B | C | x] projection is accumulated in fp32 on
+ * the tensor cores, rounded to bf16 and consumed in the GEMM's epilogue
+ * (never stored), and the conv state of slot slot_ids[i] is read and written
+ * in the same pass. One launch, no workspace. Results are those of
+ * shortconv_decode on that bf16 projection.
+ *
+ *   D, H, K      model width (D % 64 == 0), channels (H % 64 == 0), taps
+ *   hidden       device [N, D] bf16            read
+ *   N            sequences (rows), >= 0
+ *   w_in         device [3H, D] bf16           read (rows b | c | xv)
+ *   w, bias      device [H, K] bf16; bias [H] bf16 or NULL
+ *   slot_ids     device int32 [N]              read; distinct
+ *   pool         device [n_slots, H, K] bf16   read and written in place
+ *   y            device [N, H] bf16            written
+ * Device errors: SC_DEV_BAD_SLOT (that sequence's y row and slot are not
+ * written), SC_DEV_TIMEOUT (a bounded wait on a tensor copy or on the tensor
+ * cores gave up; output incomplete).
+ */
+sc_status shortconv_in_proj_decode(sc_dtype dtype, int D, int H, int K, const void *hidden,
+                                   int N, const void *w_in, const void *w, const void *bias,
+                                   const int32_t *slot_ids, void *pool, int n_slots, void *y,
+                                   void *stream);
+
+/*
  * out_proj: out = y w_out^T, fp32 accumulation, rounded once to bf16.
  *   y [T, H] bf16 read (H % 64 == 0); w_out [D, H] bf16 read
  *   (D % 256 == 0); out [T, D] bf16 written.

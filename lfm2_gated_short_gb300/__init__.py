@@ -74,6 +74,8 @@ def lib() -> ctypes.CDLL:
             L.shortconv_in_proj_prefill.argtypes = [i32, i32, i32, i32, p, i64, p, p, p, p, i32,
                                                     p, p, i32, p, p, ctypes.c_size_t, p]
             L.shortconv_out_proj.argtypes = [i32, i32, i32, p, i64, p, p, p]
+            L.shortconv_in_proj_decode.argtypes = [i32, i32, i32, i32, p, i32, p, p, p, p, p,
+                                                   i32, p, p]
             L.shortconv_slots_claim.argtypes = [p, i32, i32, p, i32, i32, i32, p, p]
             L.shortconv_slots_release.argtypes = [p, i32, p, i32, p]
             L.shortconv_pool_copy.argtypes = [i32, i32, i32, p, i32, p, p, i32, p]
@@ -87,7 +89,8 @@ def lib() -> ctypes.CDLL:
             L.shortconv_status_string.restype = ctypes.c_char_p
             for f in ("prefill", "prefill_tiled", "decode", "verify", "rollback",
                       "rollback_layers", "backward",
-                      "backward_varlen", "in_proj_prefill", "out_proj", "slots_claim",
+                      "backward_varlen", "in_proj_prefill", "in_proj_decode", "out_proj",
+                      "slots_claim",
                       "slots_release", "pool_copy", "get_error", "check_wait_limit",
                       "bounds_trim_next", "bounds_take_first_bad"):
                 getattr(L, "shortconv_" + f).restype = i32
@@ -322,6 +325,23 @@ def in_proj_prefill(hidden, w_in, w, cu_seqlens, slot_ids, pool, y=None, bias=No
         _dev(slot_ids, "slot_ids", torch.int32, (N,)),
         _dev(pool, "pool", dt, (pool.shape[0], H, K)), pool.shape[0], _dev(y, "y", dt, (T, H)),
         _dev(workspace, "workspace"), workspace.numel(), _stream(stream, hidden.device)))
+    return y
+
+
+def in_proj_decode(hidden, w_in, w, slot_ids, pool, y=None, bias=None, stream=None):
+    """in_proj fused with the decode of one token per sequence (bf16): row i of
+    ``hidden [N, D]`` is sequence i; updates ``pool`` and returns ``y [N, H]``."""
+    dt = torch.bfloat16
+    N, D = hidden.shape
+    H, K = w.shape
+    if y is None:
+        y = torch.empty((N, H), dtype=dt, device=hidden.device)
+    _raise_on("shortconv_in_proj_decode", lib().shortconv_in_proj_decode(
+        _dcode(hidden), D, H, K, _dev(hidden, "hidden", dt), N,
+        _dev(w_in, "w_in", dt, (3 * H, D)), _dev(w, "w", dt), _bias(bias, dt, H),
+        _dev(slot_ids, "slot_ids", torch.int32, (N,)),
+        _dev(pool, "pool", dt, (pool.shape[0], H, K)), pool.shape[0], _dev(y, "y", dt, (N, H)),
+        _stream(stream, hidden.device)))
     return y
 
 

@@ -396,6 +396,39 @@ sc_status shortconv_in_proj_prefill(sc_dtype dtype, int D, int H, int K, const v
                                                 (cudaStream_t)stream));
 }
 
+sc_status shortconv_in_proj_decode(sc_dtype dtype, int D, int H, int K, const void *hidden,
+                                   int N, const void *w_in, const void *w, const void *bias,
+                                   const int32_t *slot_ids, void *pool, int n_slots, void *y,
+                                   void *stream) {
+    if (dtype != SC_BF16 && dtype != SC_F32) return SC_EUNSUPPORTED;
+    if (D <= 0 || H <= 0 || K <= 0) return SC_EINVAL;
+    if (dtype != SC_BF16 || D % 64 != 0 || H % 64 != 0 || K > 4) return SC_EUNSUPPORTED;
+    if ((int64_t)H * 3 > INT32_MAX / 2 || D > INT32_MAX / 2) return SC_EUNSUPPORTED;
+    if (N < 0 || n_slots <= 0) return SC_EINVAL;
+    const size_t n_h = (size_t)N * D * 2, n_win = (size_t)3 * H * D * 2, n_w = (size_t)H * K * 2;
+    const size_t n_y = (size_t)N * H * 2, n_pool = (size_t)n_slots * H * K * 2;
+    const size_t n_b = bias ? (size_t)H * 2 : 0;
+    if (!ptr_ok(hidden, n_h, 16) || !ptr_ok(w_in, n_win, 16) || !ptr_ok(w, n_w, 16) ||
+        !ptr_ok(y, n_y, 16) || !ptr_ok(pool, n_pool, 16) || !ptr_ok(slot_ids, (size_t)N * 4, 4) ||
+        !opt_ok(bias, 16))
+        return SC_EINVAL;
+    const void *ins[5] = {hidden, w_in, w, bias, slot_ids};
+    const size_t nins[5] = {n_h, n_win, n_w, n_b, (size_t)N * 4};
+    const void *outs[2] = {y, pool};
+    const size_t nouts[2] = {n_y, n_pool};
+    for (int o = 0; o < 2; ++o)
+        for (int i = 0; i < 5; ++i)
+            if (overlaps(outs[o], nouts[o], ins[i], nins[i])) return SC_EINVAL;
+    if (overlaps(y, n_y, pool, n_pool)) return SC_EINVAL;
+    if (N == 0) return SC_OK;
+    const int sms = sm_count_of_current_device();
+    if (sms <= 0) return SC_ECUDA;
+    SC_BOUNDS_INSTALL(kUnitProj, RO(hidden, n_h), RO(w_in, n_win), RO(w, n_w), RO(bias, n_b),
+                      RO(slot_ids, (size_t)N * 4), RW(pool, n_pool), RW(y, n_y));
+    return from_cuda(sc::launch_in_proj_decode(D, H, K, hidden, N, w_in, w, bias, slot_ids, pool,
+                                               n_slots, y, sms, (cudaStream_t)stream));
+}
+
 sc_status shortconv_out_proj(sc_dtype dtype, int H, int D, const void *y, int64_t T,
                              const void *w_out, void *out, void *stream) {
     if (dtype != SC_BF16 && dtype != SC_F32) return SC_EUNSUPPORTED;

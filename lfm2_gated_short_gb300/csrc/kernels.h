@@ -71,6 +71,12 @@ cudaError_t launch_in_proj_prefill(int D, int H, int K, const void *hidden, int6
                                    int sm_count, cudaStream_t stream);
 cudaError_t launch_out_proj(int H, int D, const void *y, int64_t T, const void *w_out, void *out,
                             int sm_count, cudaStream_t stream);
+// in_proj fused with the decode of N one-token sequences (bf16): y [N, H] and
+// the slots' new states, in one launch.
+cudaError_t launch_in_proj_decode(int D, int H, int K, const void *hidden, int N,
+                                  const void *w_in, const void *w, const void *bias,
+                                  const int32_t *slot_ids, void *pool, int n_slots, void *y,
+                                  int sm_count, cudaStream_t stream);
 cudaError_t take_error_proj(cudaStream_t stream, unsigned int *code);
 
 // Take (read and clear) the backward translation unit's error word.

@@ -230,13 +230,15 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap *ma, const CUten
 // Warp 1, one lane of the (leader) CTA: per 16-deep K step one MMA of N1
 // columns (B rows 0 .. N1/CL - 1 of the CTA's stage) into the buffer's
 // columns 0.., and, if N2 > 0, one of N2 columns (the next N2/CL B rows)
-// into columns 256..; into accumulator buffer it % NBUF (it = the CTA's tile
-// count, buffers 256 columns apart). A stage is released when its MMAs
+// into columns C2..; into accumulator buffer it % NBUF (it = the CTA's tile
+// count, buffers BS columns apart). A stage is released when its MMAs
 // complete, a buffer is announced full when all of the tile's have.
-template <int S, int N1, int N2, int CL, int NBUF>
+template <int S, int N1, int N2, int CL, int NBUF, int C2 = 256, int BS = 256>
 __device__ __forceinline__ void mma_tiles(uint32_t tmem, uint32_t stages, uint32_t stage_bytes,
                                           PipeState *ps, int nk, const TileWalk &tw) {
-    static_assert(N2 == 0 || NBUF == 1, "a second MMA uses the second 256 columns");
+    static_assert(C2 >= N1 && (N2 == 0 || C2 + N2 <= BS || NBUF == 1),
+                  "the MMAs of one buffer do not overlap each other or the next buffer");
+    static_assert((NBUF - 1) * BS + (N2 > 0 ? C2 + N2 : N1) <= (int)kPTmemCols, "fits TMEM");
     constexpr uint32_t idesc1 = idesc_bf16_f32(kPBM * CL, N1);
     constexpr uint32_t idesc2 = idesc_bf16_f32(kPBM * CL, N2 > 0 ? N2 : 16);
     constexpr uint32_t b2_off = (uint32_t)(N1 / CL) * kPBK * 2;  // bytes to the second B part
@@ -252,7 +254,7 @@ __device__ __forceinline__ void mma_tiles(uint32_t tmem, uint32_t stages, uint32
             break;
         }
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)b * 256u;  // NBUF == 1: b == 0
+        const uint32_t d = tmem + (uint32_t)b * (uint32_t)BS;  // NBUF == 1: b == 0
         for (int kb = 0; kb < nk; ++kb, ++g) {
             const uint32_t s = g % S;
             if (!mbar_wait_bounded(&ps->full[s], (g / S) & 1u)) {
@@ -270,11 +272,11 @@ __device__ __forceinline__ void mma_tiles(uint32_t tmem, uint32_t stages, uint32
                 const uint32_t acc = (kb | j) != 0;
                 if constexpr (CL == 1) {
                     mma_bf16(d, da + 2 * j, db + 2 * j, idesc1, acc);
-                    if constexpr (N2 > 0) mma_bf16(d + 256u, da + 2 * j, db2 + 2 * j, idesc2, acc);
+                    if constexpr (N2 > 0) mma_bf16(d + C2, da + 2 * j, db2 + 2 * j, idesc2, acc);
                 } else {
                     mma_bf16_pair(d, da + 2 * j, db + 2 * j, idesc1, acc);
                     if constexpr (N2 > 0)
-                        mma_bf16_pair(d + 256u, da + 2 * j, db2 + 2 * j, idesc2, acc);
+                        mma_bf16_pair(d + C2, da + 2 * j, db2 + 2 * j, idesc2, acc);
                 }
             }
             if constexpr (CL == 1)
@@ -666,6 +668,187 @@ __global__ void __launch_bounds__(256)
     for (int q = 0; q < NQ; ++q) gst(sp + q, nq[q]);
 }
 
+// ------------------------------------------------------------ fused in_proj + decode
+//
+// One token per sequence (serving decode): row i of the hidden state is
+// sequence i, its conv history is the K - 1 newest values of its slot, and
+// its new state is [history; u]. A CTA pair computes the B | C | x product
+// block of kDecCh channels for 2 x 128 sequences: one N = 2 kDecCh MMA (rank
+// 0 stages the B rows of w_in, rank 1 the C rows) into TMEM columns 0.., one
+// N = kDecCh MMA (x, half the rows from each CTA) into columns 2 kDecCh..;
+// two accumulator buffers 128 columns apart, so a CTA's next tile's MMAs
+// overlap this tile's epilogue. Narrow tiles put every SM to work at a
+// serving batch (256 sequences, H = 2048: 64 tile pairs).
+//
+// Epilogue thread = (sequence, 16 channels): the slot id, the 16 x K state
+// block and the taps are loaded while the MMAs run; then u = round(B x),
+// z = sum_k w_k window_k (+ bias), y = round(C z), and the new state block is
+// written back. A (sequence, channel) pair belongs to exactly one thread of
+// one tile, so the slot is read and written by the same thread: no commit
+// pass is needed. The arithmetic and its order are those of k_decode, so the
+// results are shortconv_decode's on the bf16 projection.
+constexpr int kDecCh = 32;                          // channels per tile
+constexpr int kDecN1 = 2 * kDecCh;                  // B | C
+constexpr int kDecN2 = kDecCh;                      // x
+constexpr int kDecC2 = 2 * kDecCh;                  // x's first TMEM column
+constexpr int kDecBufStride = 128;                  // TMEM columns between buffers
+constexpr int kDecBufs = 2;
+constexpr int kDecBoxRows = 16;
+constexpr uint32_t kDecBox = kDecBoxRows * kPBK * 2;         // 2 KB
+constexpr uint32_t kDecStage = kPABytes + 3 * kDecBox;       // 22 KB
+#ifndef SC_DECPROJ_STAGES
+#define SC_DECPROJ_STAGES 8
+#endif
+constexpr int kDecStages = SC_DECPROJ_STAGES;
+constexpr int kDecEpiWarps = 8;                     // two per TMEM lane quarter
+constexpr int kDecEpiThreads = 32 * kDecEpiWarps;
+constexpr int kDecThreads = 64 + kDecEpiThreads;
+constexpr int kDecChPerThread = kDecCh * 4 / kDecEpiWarps;  // 16
+static_assert(kDecChPerThread == 16, "one 16-column TMEM read per part");
+static_assert(kDecStages <= kMaxStages, "too many stages");
+static_assert(kDecStage % 1024 == 0, "stages stay 1024-byte aligned");
+constexpr size_t dec_smem_bytes() { return 1024 + (size_t)kDecStages * kDecStage + sizeof(PipeState); }
+static_assert(dec_smem_bytes() <= 232448, "stage ring larger than a CTA's shared memory");
+
+template <int K>
+__global__ void __launch_bounds__(kDecThreads, 1)
+    k_in_proj_decode(const __grid_constant__ CUtensorMap map_h,
+                     const __grid_constant__ CUtensorMap map_w, int N, int D, int H,
+                     const bf16 *__restrict__ w, const bf16 *__restrict__ bias,
+                     const int32_t *__restrict__ slots, bf16 *__restrict__ pool, int n_slots,
+                     bf16 *__restrict__ y, int n_ctiles, int n_mtiles) {
+    constexpr int CL = 2;
+    constexpr int CPT = kDecChPerThread;
+    constexpr int SQ = CPT * K * 2 / 16;  // 16-byte words of a thread's state block
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *base = align1024(smem_raw);
+    PipeState *ps = reinterpret_cast<PipeState *>(base + (size_t)kDecStages * kDecStage);
+    const uint32_t stages = smem_addr(base);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nk = D / kPBK;
+    const uint32_t tmem = pipe_start<CL>(ps, &map_h, &map_w, kDecEpiWarps);
+    const TileWalk tw = tile_walk<CL>(n_mtiles, n_ctiles);
+
+    if (warp == 0) {
+        if (lane == 0)
+            produce_tiles<kDecStages, 3, CL>(
+                &map_h, &map_w, stages, kDecStage, ps, nk, tw, n_ctiles, kDecBox,
+                [&](int mt, int ct, int &a_row, int (&rows)[3]) {
+                    const int h0 = ct * kDecCh;
+                    a_row = mt * kPBM;
+                    rows[0] = tw.rank * H + h0;  // rank 0: B rows, rank 1: C rows
+                    rows[1] = rows[0] + kDecBoxRows;
+                    rows[2] = 2 * H + h0 + kDecBoxRows * tw.rank;  // half of the x rows
+                });
+    } else if (warp == 1) {
+        if (lane == 0 && tw.rank == 0)
+            mma_tiles<kDecStages, kDecN1, kDecN2, CL, kDecBufs, kDecC2, kDecBufStride>(
+                tmem, stages, kDecStage, ps, nk, tw);
+        __syncwarp();
+    } else {
+        const int q = warp & 3;                          // TMEM lane quarter
+        const int r = q * 32 + lane;                     // tile row = TMEM lane
+        const int cpart = ((warp - 2) >> 2) * CPT;       // this thread's first channel
+        int it = 0;
+        for (int grp = tw.first; grp < tw.n_groups; grp += tw.step, ++it) {
+            int mt, ct;
+            tw.at(grp, n_ctiles, mt, ct);
+            const int h = ct * kDecCh + cpart;           // first channel of the thread
+            const int64_t i = (int64_t)mt * kPBM + r;    // sequence
+            // Everything that does not depend on the product, while the MMAs run.
+            bool live = i < N;
+            int slot = 0;
+            uint4 sq[SQ];
+            uint32_t wq[CPT * K / 2], bq[CPT / 2];
+            if (live) {
+                slot = gld(slots + i);
+                if (slot < 0 || slot >= n_slots) {
+                    if (h == 0) raise_error(SC_DEV_BAD_SLOT);
+                    live = false;
+                }
+            }
+            if (live) {
+                const uint4 *sp = reinterpret_cast<const uint4 *>(pool + ((int64_t)slot * H + h) * K);
+#pragma unroll
+                for (int e = 0; e < SQ; ++e) sq[e] = gld(sp + e);
+                const uint32_t *wp = reinterpret_cast<const uint32_t *>(w + (int64_t)h * K);
+#pragma unroll
+                for (int e = 0; e < CPT * K / 2; ++e) wq[e] = gld(wp + e);
+                if (bias != nullptr) {
+                    const uint32_t *bp = reinterpret_cast<const uint32_t *>(bias + h);
+#pragma unroll
+                    for (int e = 0; e < CPT / 2; ++e) bq[e] = gld(bp + e);
+                }
+            }
+            if (!epi_acquire<kDecBufs>(ps, it, kDecEpiThreads)) break;
+            const uint32_t trow = tmem + (uint32_t)(it % kDecBufs) * (uint32_t)kDecBufStride +
+                                  ((uint32_t)(q * 32) << 16) + (uint32_t)cpart;
+            uint32_t rb[16], rc[16], rx[16];
+            __syncwarp();  // tcgen05.ld is warp-collective
+            tmem_ld16_nowait(trow, rb);
+            tmem_ld16_nowait(trow + kDecCh, rc);
+            tmem_ld16_nowait(trow + kDecC2, rx);
+            tmem_ld_wait();
+            tmem_regs_ready(rb);
+            tmem_regs_ready(rc);
+            tmem_regs_ready(rx);
+            epi_release<CL, kDecBufs>(ps, it, tw.rank);  // the accumulator buffer is read
+            if (!live) continue;
+            uint32_t sw[4 * SQ];  // the state block as words: element e in half e % 2 of word e / 2
+#pragma unroll
+            for (int e = 0; e < SQ; ++e) {
+                sw[4 * e] = sq[e].x;
+                sw[4 * e + 1] = sq[e].y;
+                sw[4 * e + 2] = sq[e].z;
+                sw[4 * e + 3] = sq[e].w;
+            }
+            auto elem = [](const uint32_t *wd, int e) {
+                return (e & 1) ? bf16_hi(wd[e >> 1]) : bf16_lo(wd[e >> 1]);
+            };
+            uint32_t yw[CPT / 2];
+            float ns[CPT * K];  // the new state block, bf16 values
+#pragma unroll
+            for (int c = 0; c < CPT; c += 2) {
+                // B, x and C rounded to bf16 (the values a separate in_proj stores);
+                // u = round(B x), the exact product rounded once
+                const uint32_t bx = bf2_mul(pack_bf16(__uint_as_float(rb[c]), __uint_as_float(rb[c + 1])),
+                                            pack_bf16(__uint_as_float(rx[c]), __uint_as_float(rx[c + 1])));
+                const uint32_t cc = pack_bf16(__uint_as_float(rc[c]), __uint_as_float(rc[c + 1]));
+                float o[2];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int ch = c + hh;
+                    float win[K], wk[K];
+#pragma unroll
+                    for (int k = 0; k < K; ++k) {
+                        win[k] = elem(sw, ch * K + k);
+                        wk[k] = elem(wq, ch * K + k);
+                    }
+                    const float u = hh ? bf16_hi(bx) : bf16_lo(bx);
+                    float z = slide_dot<K>(win, wk, u);
+                    if (bias != nullptr) z = z + elem(bq, ch);
+                    o[hh] = (hh ? bf16_hi(cc) : bf16_lo(cc)) * z;
+#pragma unroll
+                    for (int k = 0; k < K; ++k) ns[ch * K + k] = win[k];
+                }
+                yw[c / 2] = pack_bf16(o[0], o[1]);
+            }
+            uint4 *yp = reinterpret_cast<uint4 *>(y + i * (int64_t)H + h);
+            gst(yp, make_uint4(yw[0], yw[1], yw[2], yw[3]));
+            gst(yp + 1, make_uint4(yw[4], yw[5], yw[6], yw[7]));
+            uint32_t nw[4 * SQ];  // exact: every value is a bf16 already
+#pragma unroll
+            for (int m = 0; m < 4 * SQ; ++m)
+                nw[m] = (__float_as_uint(ns[2 * m]) >> 16) | (__float_as_uint(ns[2 * m + 1]) & 0xFFFF0000u);
+            uint4 *sp = reinterpret_cast<uint4 *>(pool + ((int64_t)slot * H + h) * K);
+#pragma unroll
+            for (int e = 0; e < SQ; ++e)
+                gst(sp + e, make_uint4(nw[4 * e], nw[4 * e + 1], nw[4 * e + 2], nw[4 * e + 3]));
+        }
+    }
+    pipe_finish<CL>(tmem);
+}
+
 // ------------------------------------------------------------ out_proj
 
 template <int CL>
@@ -862,6 +1045,46 @@ cudaError_t launch_in_proj_prefill(int D, int H, int K, const void *hidden, int6
         case 2: return in_proj_inst<2>(mh, mw, T, D, H, w, bias, cu, N, slots, pool, n_slots, y, workspace, sm_count, stream);
         case 3: return in_proj_inst<3>(mh, mw, T, D, H, w, bias, cu, N, slots, pool, n_slots, y, workspace, sm_count, stream);
         default: return in_proj_inst<4>(mh, mw, T, D, H, w, bias, cu, N, slots, pool, n_slots, y, workspace, sm_count, stream);
+    }
+}
+
+template <int K>
+static cudaError_t in_proj_decode_inst(const CUtensorMap &mh, const CUtensorMap &mw, int N, int D,
+                                       int H, const void *w, const void *bias,
+                                       const int32_t *slots, void *pool, int n_slots, void *y,
+                                       int sm_count, cudaStream_t stream) {
+    auto kern = k_in_proj_decode<K>;
+    static std::atomic<unsigned long long> done{0};
+    cudaError_t e = smem_opt_in(kern, dec_smem_bytes(), done);
+    if (e != cudaSuccess) return e;
+    static std::atomic<int> cache[64];
+    int clusters = 0;
+    e = max_clusters(kern, dec_smem_bytes(), kDecThreads, sm_count, cache, &clusters);
+    if (e != cudaSuccess) return e;
+    const int n_ctiles = H / kDecCh;
+    const int n_mtiles = (N + kPBM - 1) / kPBM;
+    const int64_t groups = (int64_t)(n_mtiles + 1) / 2 * n_ctiles;
+    const int grid = 2 * (int)(groups < clusters ? groups : clusters);  // persistent pairs
+    return launch_pdl_cluster(kern, dim3((unsigned)grid), dim3(kDecThreads), dec_smem_bytes(),
+                              stream, 2u, mh, mw, N, D, H, (const bf16 *)w, (const bf16 *)bias,
+                              slots, (bf16 *)pool, n_slots, (bf16 *)y, n_ctiles, n_mtiles);
+}
+
+cudaError_t launch_in_proj_decode(int D, int H, int K, const void *hidden, int N,
+                                  const void *w_in, const void *w, const void *bias,
+                                  const int32_t *slots, void *pool, int n_slots, void *y,
+                                  int sm_count, cudaStream_t stream) {
+    if (N == 0) return cudaSuccess;
+    CUtensorMap mh, mw;
+    cudaError_t e = map_2d(&mh, hidden, (uint64_t)D, (uint64_t)N, kPBM);
+    if (e != cudaSuccess) return e;
+    e = map_2d(&mw, w_in, (uint64_t)D, (uint64_t)3 * H, kDecBoxRows);
+    if (e != cudaSuccess) return e;
+    switch (K) {
+        case 1: return in_proj_decode_inst<1>(mh, mw, N, D, H, w, bias, slots, pool, n_slots, y, sm_count, stream);
+        case 2: return in_proj_decode_inst<2>(mh, mw, N, D, H, w, bias, slots, pool, n_slots, y, sm_count, stream);
+        case 3: return in_proj_decode_inst<3>(mh, mw, N, D, H, w, bias, slots, pool, n_slots, y, sm_count, stream);
+        default: return in_proj_decode_inst<4>(mh, mw, N, D, H, w, bias, slots, pool, n_slots, y, sm_count, stream);
     }
 }
 

@@ -3,9 +3,10 @@
     python -m lfm2_gated_short_gb300.profile_case prefill  --T 4096 --launches 6
     python -m lfm2_gated_short_gb300.profile_case decode   --N 256  --launches 6
     python -m lfm2_gated_short_gb300.profile_case verify   --N 64 --D 8 --launches 6
+    python -m lfm2_gated_short_gb300.profile_case rollback --N 64 --D 8 --layers 10 --launches 3
     python -m lfm2_gated_short_gb300.profile_case backward --T 65536 --launches 3
     python -m lfm2_gated_short_gb300.profile_case backward_varlen --T 65536 --seqs 57 --launches 3
-    python -m lfm2_gated_short_gb300.profile_case in_proj  --T 4096 --launches 3
+    python -m lfm2_gated_short_gb300.profile_case in_proj  --T 4096 --seqs 16 --launches 3
     python -m lfm2_gated_short_gb300.profile_case out_proj --T 4096 --launches 3
 
 Inputs are drawn on the device with a seeded generator (bf16, N(0,1) data,
@@ -24,8 +25,8 @@ import lfm2_gated_short_gb300 as sc
 
 def main() -> None:
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["prefill", "prefill_tiled", "decode", "verify", "backward",
-                                   "backward_varlen", "in_proj", "out_proj"])
+    ap.add_argument("op", choices=["prefill", "prefill_tiled", "decode", "verify", "rollback",
+                                   "backward", "backward_varlen", "in_proj", "out_proj"])
     ap.add_argument("--T", type=int, default=4096)
     ap.add_argument("--H", type=int, default=2048)
     ap.add_argument("--K", type=int, default=3)
@@ -33,9 +34,13 @@ def main() -> None:
     ap.add_argument("--D", type=int, default=8)
     ap.add_argument("--slots", type=int, default=1024)
     ap.add_argument("--tile", type=int, default=8)
-    ap.add_argument("--seqs", type=int, default=16, help="packed sequences (backward_varlen)")
+    ap.add_argument("--seqs", type=int, default=None,
+                    help="packed sequences: backward_varlen (default 16), in_proj (default 1)")
+    ap.add_argument("--layers", type=int, default=10, help="stacked layers (rollback)")
     ap.add_argument("--launches", type=int, default=6)
     a = ap.parse_args()
+    if a.seqs is None:
+        a.seqs = 16 if a.op == "backward_varlen" else 1
     dev = torch.device("cuda", 0)
     g = torch.Generator(device=dev).manual_seed(7)
 
@@ -57,23 +62,30 @@ def main() -> None:
             sets.append(dict(bcx=rnd(a.N, 3 * H), pool=rnd(a.slots, H, K)))
         elif a.op == "verify":
             sets.append(dict(bcx=rnd(a.N * a.D, 3 * H), pool=rnd(a.slots, H, K)))
+        elif a.op == "rollback":  # every layer's verify tape, then one stacked rollback
+            sets.append(dict(win=rnd(a.layers, a.N, a.D, H, K),
+                             pools=rnd(a.layers, a.slots, H, K)))
         elif a.op == "in_proj":
             sets.append(dict(hidden=rnd(a.T, Dm), y=torch.empty(a.T, H, dtype=torch.bfloat16,
                                                                  device=dev),
-                             pool=torch.zeros(1, H, K, dtype=torch.bfloat16, device=dev)))
+                             pool=rnd(a.slots, H, K)))
         elif a.op == "out_proj":
             sets.append(dict(y=rnd(a.T, H)))
         else:
             sets.append(dict(bcx=rnd(a.T, 3 * H), dy=rnd(a.T, H)))
     cu = torch.tensor([0, a.T], dtype=torch.int32, device=dev)
-    if a.op == "backward_varlen":  # seeded cut points: a.seqs packed sequences of T rows
+    if a.op in ("backward_varlen", "in_proj"):  # seeded cut points: a.seqs packed sequences
         cuts = torch.randperm(a.T - 1, generator=torch.Generator().manual_seed(7))[:a.seqs - 1] + 1
         cu = torch.cat([torch.tensor([0]), cuts.sort().values, torch.tensor([a.T])]).to(
             torch.int32).to(dev)
         init = rnd(a.seqs, H, K)
     slot0 = torch.zeros(1, dtype=torch.int32, device=dev)
+    seq_slots = torch.randperm(a.slots, generator=torch.Generator().manual_seed(8))[:a.seqs].to(
+        torch.int32).to(dev)
     slots = torch.randperm(a.slots, generator=torch.Generator().manual_seed(7))[:a.N].to(
         torch.int32).to(dev)
+    accepted = torch.randint(0, a.D + 1, (a.N,), generator=torch.Generator().manual_seed(7),
+                             dtype=torch.int32).to(dev)
     for i in range(a.launches):
         s = sets[i % 3]
         if a.op == "prefill":
@@ -84,8 +96,10 @@ def main() -> None:
             sc.decode(s["bcx"], w, slots, s["pool"])
         elif a.op == "verify":
             sc.verify(s["bcx"], w, slots, s["pool"], a.D)
+        elif a.op == "rollback":
+            sc.rollback_layers(s["win"], accepted, slots, s["pools"])
         elif a.op == "in_proj":
-            sc.in_proj_prefill(s["hidden"], w_in, w, cu, slot0, s["pool"], y=s["y"])
+            sc.in_proj_prefill(s["hidden"], w_in, w, cu, seq_slots, s["pool"], y=s["y"])
         elif a.op == "out_proj":
             sc.out_proj(s["y"], w_out)
         elif a.op == "backward_varlen":

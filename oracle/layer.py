@@ -20,7 +20,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import DTYPES, prefill, round_bf16, to_f64
+from . import DTYPES, decode, prefill, round_bf16, to_f64
 
 
 def round_to(dtype: str, values: np.ndarray) -> np.ndarray:
@@ -58,3 +58,10 @@ def in_proj_prefill(dtype, hidden, w_in, w, cu_seqlens, slot_ids, pool, bias=Non
     """``in_proj`` then the packed varlen prefill; ``pool`` in place; returns ``(status, y)``."""
     bcx = in_proj(dtype, hidden, w_in)
     return prefill(dtype, bcx, w, cu_seqlens, slot_ids, pool, bias=bias)
+
+
+def in_proj_decode(dtype, hidden, w_in, w, slot_ids, pool, bias=None):
+    """``in_proj`` then the decode of one token per sequence (row i of ``hidden``
+    is sequence i's token); ``pool`` in place; returns ``(status, y)``."""
+    bcx = in_proj(dtype, hidden, w_in)
+    return decode(dtype, bcx, w, slot_ids, pool, bias=bias)

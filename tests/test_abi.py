@@ -251,3 +251,28 @@ def test_bounds_checked_build_loads_and_exports_every_declared_function():
     B.shortconv_prefill.argtypes = [i32, i32, i32, p, i64, p, p, p, i32, p, p, i32, p, p]
     assert B.shortconv_prefill(7, 256, 3, A, 64, Bp, None, Cp, 1, Dp, Ep, 4, Fp,
                                None) == SC_EUNSUPPORTED
+
+
+def test_in_proj_decode_argument_errors(L):
+    p, i32 = ctypes.c_void_p, ctypes.c_int
+    f = L.shortconv_in_proj_decode
+    f.argtypes = [i32, i32, i32, i32, p, i32, p, p, p, p, p, i32, p, p]
+    ok = dict(dtype=BF16, D=128, H=64, K=3, hidden=A, N=4, w_in=Bp, w=Cp, bias=None, slots=Dp,
+              pool=Ep, n_slots=8, y=Fp)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["dtype"], a["D"], a["H"], a["K"], a["hidden"], a["N"], a["w_in"], a["w"],
+                 a["bias"], a["slots"], a["pool"], a["n_slots"], a["y"], None)
+
+    assert call(dtype=F32) == SC_EUNSUPPORTED
+    assert call(D=96) == SC_EUNSUPPORTED
+    assert call(H=96) == SC_EUNSUPPORTED
+    assert call(K=5) == SC_EUNSUPPORTED
+    assert call(N=-1) == SC_EINVAL
+    assert call(n_slots=0) == SC_EINVAL
+    assert call(hidden=A + 8) == SC_EINVAL        # not 16-byte aligned
+    assert call(y=A + 64) == SC_EINVAL            # y overlaps hidden
+    assert call(pool=Bp) == SC_EINVAL             # pool overlaps w_in
+    assert call(slots=Dp + 2) == SC_EINVAL        # int32 array not 4-byte aligned
+    assert call(N=0, hidden=0, y=0) == SC_OK      # nothing to do, no device needed

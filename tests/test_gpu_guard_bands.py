@@ -276,6 +276,31 @@ def test_in_proj_prefill_and_out_proj(D, H, K):
     assert sc.get_error() == 0
 
 
+@pytest.mark.parametrize("N,D,H,K", [(1, 64, 64, 3), (130, 64, 192, 4), (300, 128, 64, 1)])
+def test_in_proj_decode(N, D, H, K):
+    rng = np.random.default_rng(1850 + N)
+    hidden = _dyadic(rng, (N, D), 8, -3)
+    w_in = _dyadic(rng, (3 * H, D), 8, -6)
+    w = oracle.round_bf16(rng.standard_normal((H, K)) * np.sqrt(1 / 3))
+    n_slots = N + 5
+    slots = rng.permutation(n_slots)[:N].astype(np.int32)
+    pool0 = np.full((n_slots, H, K), 0xDEAD, np.uint16)
+    for s_ in slots:
+        pool0[s_] = oracle.round_bf16(rng.standard_normal((H, K)))
+    pool = banded_from(pool0, "bf16")
+    y = banded_empty((N, H), "bf16")
+    sc.in_proj_decode(dev(hidden, "bf16"), dev(w_in, "bf16"), dev(w, "bf16"), dev(slots, "i32"),
+                      pool.t, y=y.t)
+    pool.check("pool")
+    y.check("y")
+    ref = pool0.copy()
+    st, y_ref = layer.in_proj_decode("bf16", hidden, w_in, w, slots, ref)
+    assert st == oracle.OK
+    assert_close("bf16", host(y.t), y_ref, "y")
+    assert_bits(host(pool.t), ref, "pool")
+    assert sc.get_error() == 0
+
+
 # ------------------------------------------------------------ slot pool
 
 def test_slots_claim_release_copy():

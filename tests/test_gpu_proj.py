@@ -406,3 +406,126 @@ def test_more_sequences_than_staged_in_shared_memory():
     assert sc.get_error() == 0
     assert_close("bf16", y, y_ref, "y")
     assert_bits(pool, pool_ref, "pool")
+
+
+# ------------------------------------------------ in_proj fused with decode
+
+def make_decode_case(rng, N, D, H, K, extra_slots=7, exact=True, with_bias=False):
+    if exact:
+        hidden = dyadic(rng, (N, D), 8, -3)
+        w_in = dyadic(rng, (3 * H, D), 8, -6)
+    else:
+        hidden = oracle.round_bf16(rng.standard_normal((N, D)))
+        w_in = oracle.round_bf16(rng.standard_normal((3 * H, D)) / np.sqrt(D))
+    w = oracle.round_bf16(rng.standard_normal((H, K)) * np.sqrt(1 / 3))
+    bias = oracle.round_bf16(rng.standard_normal(H) * 0.5) if with_bias else None
+    n_slots = N + extra_slots
+    slots = rng.permutation(n_slots)[:N].astype(np.int32)
+    pool = np.full((n_slots, H, K), 0xDEAD, np.uint16)  # untouched slots keep this
+    for s in slots:
+        pool[s] = oracle.round_bf16(rng.standard_normal((H, K)))
+    return dict(hidden=hidden, w_in=w_in, w=w, bias=bias, slots=slots, pool=pool,
+                cu=np.arange(N + 1, dtype=np.int32), D=D, H=H, K=K)
+
+
+def run_decode_gpu(c):
+    pool = dev(c["pool"], "bf16")
+    y = sc.in_proj_decode(dev(c["hidden"], "bf16"), dev(c["w_in"], "bf16"), dev(c["w"], "bf16"),
+                          dev(c["slots"], "i32"), pool,
+                          bias=None if c["bias"] is None else dev(c["bias"], "bf16"))
+    torch.cuda.synchronize()
+    return host(y), host(pool)
+
+
+@pytest.mark.parametrize("N,D,H,K", [(1, 64, 64, 3), (5, 128, 64, 1), (37, 64, 192, 2),
+                                     (129, 128, 64, 3), (300, 64, 128, 4),
+                                     (256, 2048, 2048, 3)])
+def test_in_proj_decode_exact_inputs(N, D, H, K):
+    """Exact projections: y within the bf16 tolerance of the oracle, states bit
+    for bit, untouched slots kept, and the same bits as shortconv_decode on
+    the projection."""
+    rng = np.random.default_rng(880 + N + K)
+    c = make_decode_case(rng, N, D, H, K)
+    y, pool = run_decode_gpu(c)
+    assert sc.get_error() == 0
+    ref = c["pool"].copy()
+    st, y_ref = layer.in_proj_decode("bf16", c["hidden"], c["w_in"], c["w"], c["slots"], ref)
+    assert st == oracle.OK
+    assert_close("bf16", y, y_ref, "y")
+    assert_bits(pool, ref, "pool")
+    bcx = layer.in_proj("bf16", c["hidden"], c["w_in"])
+    pool2 = dev(c["pool"], "bf16")
+    y2 = sc.decode(dev(bcx, "bf16"), dev(c["w"], "bf16"), dev(c["slots"], "i32"), pool2)
+    torch.cuda.synchronize()
+    assert_bits(y, host(y2), "y against shortconv_decode")
+    assert_bits(pool, host(pool2), "pool against shortconv_decode")
+
+
+def test_in_proj_decode_with_bias():
+    rng = np.random.default_rng(890)
+    c = make_decode_case(rng, 77, 128, 128, 3, with_bias=True)
+    y, pool = run_decode_gpu(c)
+    assert sc.get_error() == 0
+    ref = c["pool"].copy()
+    st, y_ref = layer.in_proj_decode("bf16", c["hidden"], c["w_in"], c["w"], c["slots"], ref,
+                                     bias=c["bias"])
+    assert st == oracle.OK
+    assert_close("bf16", y, y_ref, "y")
+    assert_bits(pool, ref, "pool")
+
+
+def test_in_proj_decode_normal_inputs_lfm2_shape():
+    """Serving shape: 256 sequences, D = H = 2048, normal inputs; every output
+    within its accumulation range (see _check_intervals), 64 sampled channels."""
+    rng = np.random.default_rng(891)
+    c = make_decode_case(rng, 256, 2048, 2048, 3, exact=False)
+    y, pool = run_decode_gpu(c)
+    assert sc.get_error() == 0
+    ch = np.sort(np.concatenate([[0, 15, 16, 31, 32, 1023, 1024, 2047],
+                                 rng.choice(np.arange(33, 2040), 56, replace=False)]))
+    _check_intervals(c, y, pool, ch)
+
+
+def test_in_proj_decode_continues_a_prefill_token_by_token():
+    """A fused prefill of a sequence's first rows, then fused decode steps,
+    equal the fused prefill of the whole sequence (exact projections)."""
+    rng = np.random.default_rng(892)
+    D, H, K, T = 128, 192, 3, 9
+    hs = dyadic(rng, (T, D), 8, -3)
+    w_in = dyadic(rng, (3 * H, D), 8, -6)
+    w = oracle.round_bf16(rng.standard_normal((H, K)) * np.sqrt(1 / 3))
+    pa = dev(np.zeros((2, H, K), np.uint16), "bf16")
+    ya = sc.in_proj_prefill(dev(hs, "bf16"), dev(w_in, "bf16"), dev(w, "bf16"),
+                            dev(np.array([0, T], np.int32), "i32"), dev(np.array([1], np.int32), "i32"),
+                            pa)
+    pb = dev(np.zeros((2, H, K), np.uint16), "bf16")
+    yb = [sc.in_proj_prefill(dev(hs[:3], "bf16"), dev(w_in, "bf16"), dev(w, "bf16"),
+                             dev(np.array([0, 3], np.int32), "i32"),
+                             dev(np.array([1], np.int32), "i32"), pb)]
+    for t in range(3, T):
+        yb.append(sc.in_proj_decode(dev(hs[t:t + 1], "bf16"), dev(w_in, "bf16"), dev(w, "bf16"),
+                                    dev(np.array([1], np.int32), "i32"), pb))
+    torch.cuda.synchronize()
+    assert_bits(np.concatenate([host(v) for v in yb]), host(ya), "y")
+    assert_bits(host(pb), host(pa), "pool")
+    assert sc.get_error() == 0
+
+
+def test_in_proj_decode_bad_slot_skips_that_sequence():
+    rng = np.random.default_rng(893)
+    c = make_decode_case(rng, 40, 64, 64, 3)
+    slots = c["slots"].copy()
+    slots[7] = 10 ** 6
+    pool = dev(c["pool"], "bf16")
+    y = torch.full((40, 64), 3.0, dtype=torch.bfloat16, device="cuda")
+    sc.in_proj_decode(dev(c["hidden"], "bf16"), dev(c["w_in"], "bf16"), dev(c["w"], "bf16"),
+                      dev(slots, "i32"), pool, y=y)
+    assert sc.get_error() == sc.DEV_BAD_SLOT
+    ref = c["pool"].copy()
+    keep = np.arange(40) != 7
+    st, y_ref = layer.in_proj_decode("bf16", c["hidden"][keep], c["w_in"], c["w"],
+                                     c["slots"][keep], ref)
+    g = host(y)
+    assert np.all(g[7] == np.uint16(0x4040)), "the skipped row was written"
+    assert_close("bf16", g[keep], y_ref, "y")
+    assert_bits(host(pool), ref, "pool")

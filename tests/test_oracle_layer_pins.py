@@ -105,3 +105,36 @@ def test_out_proj_matches_brute_force_and_orientation():
     assert got.shape == (T, D)
     exact = (yi.astype(object) @ wi.T.astype(object)).astype(np.float64) * 2.0 ** -6
     np.testing.assert_array_equal(got, exact)
+
+
+def test_in_proj_decode_is_the_layer_prefill_of_one_token_sequences():
+    """Decoding N one-token sequences equals the layer prefill of N sequences
+    of length one (the per-token step of the page's definition); token by
+    token it continues a longer prefill exactly."""
+    rng = np.random.default_rng(706)
+    N, H, D, K = 9, 8, 16, 3
+    hidden = oracle.round_bf16(rng.standard_normal((N, D)))
+    w_in = oracle.round_bf16(rng.standard_normal((3 * H, D)) / 4)
+    w = oracle.round_bf16(rng.standard_normal((H, K)) / 2)
+    b = oracle.round_bf16(rng.standard_normal(H) / 2)
+    slots = rng.permutation(12)[:N].astype(np.int32)
+    pool0 = oracle.round_bf16(rng.standard_normal((12, H, K)))
+    p1 = pool0.copy()
+    st, y1 = layer.in_proj_decode("bf16", hidden, w_in, w, slots, p1, bias=b)
+    assert st == oracle.OK
+    p2 = pool0.copy()
+    st, y2 = layer.in_proj_prefill("bf16", hidden, w_in, w, np.arange(N + 1), slots, p2, bias=b)
+    assert st == oracle.OK
+    np.testing.assert_array_equal(y1, y2)
+    np.testing.assert_array_equal(p1, p2)
+    # one sequence, token by token, continues a prefill of its first rows
+    T = 6
+    hs = oracle.round_bf16(rng.standard_normal((T, D)))
+    pa = np.zeros((1, H, K), np.uint16)
+    ya = layer.in_proj_prefill("bf16", hs, w_in, w, [0, T], [0], pa)[1]
+    pb = np.zeros((1, H, K), np.uint16)
+    yb = [layer.in_proj_prefill("bf16", hs[:2], w_in, w, [0, 2], [0], pb)[1]]
+    for t in range(2, T):
+        yb.append(layer.in_proj_decode("bf16", hs[t:t + 1], w_in, w, [0], pb)[1])
+    np.testing.assert_array_equal(np.concatenate(yb), ya)
+    np.testing.assert_array_equal(pb, pa)
