@@ -57,6 +57,12 @@ constexpr uint32_t kPABytes = kPBM * kPBK * 2;  // 16 KB
 #ifndef SC_INPROJ_STAGES
 #define SC_INPROJ_STAGES 4  // stage ring depth of the fused in_proj (40 KB a stage)
 #endif
+#ifndef SC_INPROJ_ROT
+#define SC_INPROJ_ROT 0  // 1: rotated K-block order in the fused in_proj (see produce_tiles)
+#endif
+#ifndef SC_OUTPROJ_ROT
+#define SC_OUTPROJ_ROT 0  // 1: rotated K-block order in out_proj
+#endif
 #ifndef SC_OUTPROJ_STAGES
 #define SC_OUTPROJ_STAGES (SC_PROJ_CLUSTER == 2 ? 6 : 4)  // stage ring depth, out_proj
 #endif
@@ -176,8 +182,11 @@ __device__ __forceinline__ void pipe_init(PipeState *ps, int CL, int epi_warps) 
 
 // Warp 0, one lane. coords(mt, ct, a_row, rows) gives the tile's A row and the
 // first rows of this CTA's NB boxes of B (box_bytes each); a stage holds A,
-// then the boxes.
-template <int S, int NB, int CL, typename Coords>
+// then the boxes. With ROT, tile group grp walks its K blocks starting at
+// block grp % nk (wrapping): the pairs running at the same time then read
+// different A columns, where many tiles share the same A rows (the MMA lane
+// counts blocks, not positions, so the sum only changes order).
+template <int S, int NB, int CL, typename Coords, bool ROT = false>
 __device__ __forceinline__ void produce_tiles(const CUtensorMap *ma, const CUtensorMap *mb,
                                               uint32_t stages, uint32_t stage_bytes,
                                               PipeState *ps, int nk, const TileWalk &tw,
@@ -190,7 +199,8 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap *ma, const CUten
         int mt, ct, a_row, rows[NB];
         tw.at(grp, n_col_tiles, mt, ct);
         coords(mt, ct, a_row, rows);
-        for (int kb = 0; kb < nk; ++kb, ++g) {
+        for (int kb_i = 0; kb_i < nk; ++kb_i, ++g) {
+            const int kb = ROT ? (kb_i + grp % nk) % nk : kb_i;
             const uint32_t s = g % S;
             if (g >= S && !mbar_wait_bounded(&ps->empty[s], (g / S - 1) & 1u)) {
                 raise_error(SC_DEV_TIMEOUT);
@@ -399,23 +409,23 @@ __global__ void __launch_bounds__(kInThreads, 1)
     const TileWalk tw = tile_walk<CL>(n_mtiles, n_ctiles);
 
     if (warp == 0) {
-        if (lane == 0)
-            produce_tiles<kInStages, 3, CL>(
-                &map_h, &map_w, stages, kConvStage, ps, nk, tw, n_ctiles, kConvBox,
-                [&](int mt, int ct, int &a_row, int (&rows)[3]) {
-                    const int h0 = ct * kConvCh;
-                    a_row = mt * OUT - (K - 1);
-                    if constexpr (CL == 2) {
-                        // First MMA's B rows (B | C of 128 channels): rank 0 holds the
-                        // 128 of B, rank 1 the 128 of C; second MMA's (x): 64 each.
-                        rows[0] = tw.rank * H + h0;
-                        rows[1] = tw.rank * H + h0 + 64;
-                        rows[2] = 2 * H + h0 + 64 * tw.rank;
-                    } else {  // B | C | x of 64 channels
+        auto conv_coords = [&](int mt, int ct, int &a_row, int (&rows)[3]) {
+            const int h0 = ct * kConvCh;
+            a_row = mt * OUT - (K - 1);
+            if constexpr (CL == 2) {
+                // First MMA's B rows (B | C of 128 channels): rank 0 holds the
+                // 128 of B, rank 1 the 128 of C; second MMA's (x): 64 each.
+                rows[0] = tw.rank * H + h0;
+                rows[1] = tw.rank * H + h0 + 64;
+                rows[2] = 2 * H + h0 + 64 * tw.rank;
+            } else {  // B | C | x of 64 channels
 #pragma unroll
-                        for (int i = 0; i < 3; ++i) rows[i] = i * H + h0;
-                    }
-                });
+                for (int i = 0; i < 3; ++i) rows[i] = i * H + h0;
+            }
+        };
+        if (lane == 0)
+            produce_tiles<kInStages, 3, CL, decltype(conv_coords), SC_INPROJ_ROT != 0>(
+                &map_h, &map_w, stages, kConvStage, ps, nk, tw, n_ctiles, kConvBox, conv_coords);
     } else if (warp == 1) {
         if (lane == 0 && tw.rank == 0)
             mma_tiles<kInStages, kConvN1, kConvN2, CL, kInBufs>(tmem, stages, kConvStage, ps, nk,
@@ -730,16 +740,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const TileWalk tw = tile_walk<CL>(n_mtiles, n_ctiles);
 
     if (warp == 0) {
+        auto dec_coords = [&](int mt, int ct, int &a_row, int (&rows)[3]) {
+            const int h0 = ct * kDecCh;
+            a_row = mt * kPBM;
+            rows[0] = tw.rank * H + h0;  // rank 0: B rows, rank 1: C rows
+            rows[1] = rows[0] + kDecBoxRows;
+            rows[2] = 2 * H + h0 + kDecBoxRows * tw.rank;  // half of the x rows
+        };
+        // 64 column tiles share each 256 rows of A: rotated K order (ROT)
         if (lane == 0)
-            produce_tiles<kDecStages, 3, CL>(
-                &map_h, &map_w, stages, kDecStage, ps, nk, tw, n_ctiles, kDecBox,
-                [&](int mt, int ct, int &a_row, int (&rows)[3]) {
-                    const int h0 = ct * kDecCh;
-                    a_row = mt * kPBM;
-                    rows[0] = tw.rank * H + h0;  // rank 0: B rows, rank 1: C rows
-                    rows[1] = rows[0] + kDecBoxRows;
-                    rows[2] = 2 * H + h0 + kDecBoxRows * tw.rank;  // half of the x rows
-                });
+            produce_tiles<kDecStages, 3, CL, decltype(dec_coords), true>(
+                &map_h, &map_w, stages, kDecStage, ps, nk, tw, n_ctiles, kDecBox, dec_coords);
     } else if (warp == 1) {
         if (lane == 0 && tw.rank == 0)
             mma_tiles<kDecStages, kDecN1, kDecN2, CL, kDecBufs, kDecC2, kDecBufStride>(
@@ -866,13 +877,13 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     const TileWalk tw = tile_walk<CL>(n_mtiles, n_ntiles);
 
     if (warp == 0) {
+        auto out_coords = [&](int mt, int nt, int &a_row, int (&rows)[1]) {
+            a_row = mt * kPBM;
+            rows[0] = nt * kOutN + tw.rank * kOutBoxRows;
+        };
         if (lane == 0)
-            produce_tiles<kOutStages, 1, CL>(
-                &map_a, &map_b, stages, kOutStage, ps, nk, tw, n_ntiles, kOutBox,
-                [&](int mt, int nt, int &a_row, int (&rows)[1]) {
-                    a_row = mt * kPBM;
-                    rows[0] = nt * kOutN + tw.rank * kOutBoxRows;
-                });
+            produce_tiles<kOutStages, 1, CL, decltype(out_coords), SC_OUTPROJ_ROT != 0>(
+                &map_a, &map_b, stages, kOutStage, ps, nk, tw, n_ntiles, kOutBox, out_coords);
     } else if (warp == 1) {
         if (lane == 0 && tw.rank == 0)
             mma_tiles<kOutStages, kOutN, 0, CL, kOutBufs>(tmem, stages, kOutStage, ps, nk, tw);

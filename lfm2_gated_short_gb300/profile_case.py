@@ -8,6 +8,7 @@
     python -m lfm2_gated_short_gb300.profile_case backward_varlen --T 65536 --seqs 57 --launches 3
     python -m lfm2_gated_short_gb300.profile_case in_proj  --T 4096 --seqs 16 --launches 3
     python -m lfm2_gated_short_gb300.profile_case out_proj --T 4096 --launches 3
+    python -m lfm2_gated_short_gb300.profile_case in_proj_decode --N 256 --launches 6
 
 Inputs are drawn on the device with a seeded generator (bf16, N(0,1) data,
 N(0,1/3) weights, N(0,1) pools). Consecutive launches rotate over three input
@@ -26,7 +27,8 @@ import lfm2_gated_short_gb300 as sc
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("op", choices=["prefill", "prefill_tiled", "decode", "verify", "rollback",
-                                   "backward", "backward_varlen", "in_proj", "out_proj"])
+                                   "backward", "backward_varlen", "in_proj", "out_proj",
+                                   "in_proj_decode"])
     ap.add_argument("--T", type=int, default=4096)
     ap.add_argument("--H", type=int, default=2048)
     ap.add_argument("--K", type=int, default=3)
@@ -50,7 +52,7 @@ def main() -> None:
     H, K = a.H, a.K
     w = rnd(H, K, std=(1 / 3) ** 0.5)
     Dm = H  # model width of the projections (LFM2-1.2B: D = H)
-    w_in = rnd(3 * H, Dm, std=Dm ** -0.5) if a.op == "in_proj" else None
+    w_in = rnd(3 * H, Dm, std=Dm ** -0.5) if a.op in ("in_proj", "in_proj_decode") else None
     w_out = rnd(Dm, H, std=H ** -0.5) if a.op == "out_proj" else None
     sets = []
     for _ in range(3):
@@ -71,6 +73,8 @@ def main() -> None:
                              pool=rnd(a.slots, H, K)))
         elif a.op == "out_proj":
             sets.append(dict(y=rnd(a.T, H)))
+        elif a.op == "in_proj_decode":  # one token for each of N sequences
+            sets.append(dict(hidden=rnd(a.N, Dm), pool=rnd(a.slots, H, K)))
         else:
             sets.append(dict(bcx=rnd(a.T, 3 * H), dy=rnd(a.T, H)))
     cu = torch.tensor([0, a.T], dtype=torch.int32, device=dev)
@@ -102,6 +106,8 @@ def main() -> None:
             sc.in_proj_prefill(s["hidden"], w_in, w, cu, seq_slots, s["pool"], y=s["y"])
         elif a.op == "out_proj":
             sc.out_proj(s["y"], w_out)
+        elif a.op == "in_proj_decode":
+            sc.in_proj_decode(s["hidden"], w_in, w, slots, s["pool"])
         elif a.op == "backward_varlen":
             sc.backward_varlen(s["bcx"], w, cu, s["dy"], init_states=init)
         else:
