@@ -48,6 +48,9 @@ namespace sc {
 constexpr int kBwdCpt = 4;                         // channels per consumer thread
 constexpr int kBwdSlice = SC_BWD_SLICE;            // channels per CTA slice
 constexpr int kBwdConsumers = kBwdSlice / kBwdCpt;
+#ifndef SC_BWD_HALO_HINT
+#define SC_BWD_HALO_HINT 0  // 1: evict-last L2 policy on the rows a neighbouring CTA reads again
+#endif
 #ifndef SC_BWD_STAGES
 #define SC_BWD_STAGES 4  // stage ring depth (the header holds up to 16 stages' barriers)
 #endif
@@ -174,6 +177,10 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, kBwdCtas<T, K>)
     pdl_launch_dependents();
 
     // Stage layout per row: B | C | x | dy sections of CW channels.
+    // The 2 (K-1) rows around the range's start are read again by the CTA of
+    // the range before, at its end: with SC_BWD_HALO_HINT they are fetched
+    // with an evict-last L2 policy so that second read finds them in L2.
+    const uint64_t keep = SC_BWD_HALO_HINT ? l2_policy_evict_last() : 0;
     auto issue = [&](int c) {
         const int s = c % NS;
         const int64_t rb = sr0 + (int64_t)c * R;
@@ -182,6 +189,15 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, kBwdCtas<T, K>)
         for (int rr = 0; rr < rows; ++rr) {
             const T *src = bcx + (rb + rr) * ld + c0;
             T *dst = stage + (size_t)(s * R + rr) * 4 * CW;
+            if (SC_BWD_HALO_HINT && rc > 0 && rb + rr < cr0 + (K - 1)) {
+#pragma unroll
+                for (int q = 0; q < 3; ++q)
+                    bulk_copy_g2s_hint(dst + (size_t)q * CW, src + (int64_t)q * H, sec_bytes,
+                                       &full[s], keep);
+                bulk_copy_g2s_hint(dst + (size_t)3 * CW, dy + (rb + rr) * (int64_t)H + c0,
+                                   sec_bytes, &full[s], keep);
+                continue;
+            }
 #pragma unroll
             for (int q = 0; q < 3; ++q)
                 bulk_copy_g2s(dst + (size_t)q * CW, src + (int64_t)q * H, sec_bytes, &full[s]);

@@ -60,6 +60,9 @@ constexpr uint32_t kPABytes = kPBM * kPBK * 2;  // 16 KB
 #ifndef SC_INPROJ_ROT
 #define SC_INPROJ_ROT 0  // 1: rotated K-block order in the fused in_proj (see produce_tiles)
 #endif
+#ifndef SC_DECPROJ_ROT
+#define SC_DECPROJ_ROT 0  // 1: rotated K-block order in the fused in_proj decode
+#endif
 #ifndef SC_OUTPROJ_ROT
 #define SC_OUTPROJ_ROT 0  // 1: rotated K-block order in out_proj
 #endif
@@ -683,38 +686,40 @@ __global__ void __launch_bounds__(256)
 // One token per sequence (serving decode): row i of the hidden state is
 // sequence i, its conv history is the K - 1 newest values of its slot, and
 // its new state is [history; u]. A CTA pair computes the B | C | x product
-// block of kDecCh channels for 2 x 128 sequences: one N = 2 kDecCh MMA (rank
-// 0 stages the B rows of w_in, rank 1 the C rows) into TMEM columns 0.., one
-// N = kDecCh MMA (x, half the rows from each CTA) into columns 2 kDecCh..;
-// two accumulator buffers 128 columns apart, so a CTA's next tile's MMAs
-// overlap this tile's epilogue. Narrow tiles put every SM to work at a
-// serving batch (256 sequences, H = 2048: 64 tile pairs).
+// block of kDecCh channels for 2 x 128 sequences with one N = 3 kDecCh MMA
+// per 16-deep K step: rank 0 stages the kDecCh B rows of w_in and the first
+// half of the x rows, rank 1 the C rows and the second half, so TMEM columns
+// hold [B | x_lo | C | x_hi]. Two accumulator buffers let a CTA's next tile's
+// MMAs overlap this tile's epilogue. Narrow tiles put every SM to work at a
+// serving batch (256 sequences, H = 2048, 32 channels: 64 tile pairs).
 //
-// Epilogue thread = (sequence, 16 channels): the slot id, the 16 x K state
+// Epilogue thread = (sequence, kDecCh / 2 channels): the slot id, the state
 // block and the taps are loaded while the MMAs run; then u = round(B x),
 // z = sum_k w_k window_k (+ bias), y = round(C z), and the new state block is
 // written back. A (sequence, channel) pair belongs to exactly one thread of
 // one tile, so the slot is read and written by the same thread: no commit
 // pass is needed. The arithmetic and its order are those of k_decode, so the
 // results are shortconv_decode's on the bf16 projection.
-constexpr int kDecCh = 32;                          // channels per tile
-constexpr int kDecN1 = 2 * kDecCh;                  // B | C
-constexpr int kDecN2 = kDecCh;                      // x
-constexpr int kDecC2 = 2 * kDecCh;                  // x's first TMEM column
-constexpr int kDecBufStride = 128;                  // TMEM columns between buffers
+#ifndef SC_DECPROJ_CH
+#define SC_DECPROJ_CH 32  // channels per tile: 32 or 64
+#endif
+constexpr int kDecCh = SC_DECPROJ_CH;
+static_assert(kDecCh == 32 || kDecCh == 64, "32 or 64 channels per decode tile");
+constexpr int kDecN = 3 * kDecCh;                   // B | x_lo | C | x_hi
+constexpr int kDecHalf = kDecCh / 2;
+constexpr int kDecBufStride = kDecN <= 128 ? 128 : 256;  // TMEM columns between buffers
 constexpr int kDecBufs = 2;
-constexpr int kDecBoxRows = 16;
-constexpr uint32_t kDecBox = kDecBoxRows * kPBK * 2;         // 2 KB
-constexpr uint32_t kDecStage = kPABytes + 3 * kDecBox;       // 22 KB
+constexpr int kDecBoxRows = kDecHalf;               // B or C: two boxes; x: one
+constexpr uint32_t kDecBox = kDecBoxRows * kPBK * 2;
+constexpr uint32_t kDecStage = kPABytes + 3 * kDecBox;
 #ifndef SC_DECPROJ_STAGES
-#define SC_DECPROJ_STAGES 8
+#define SC_DECPROJ_STAGES (kDecCh == 32 ? 8 : 7)
 #endif
 constexpr int kDecStages = SC_DECPROJ_STAGES;
 constexpr int kDecEpiWarps = 8;                     // two per TMEM lane quarter
 constexpr int kDecEpiThreads = 32 * kDecEpiWarps;
 constexpr int kDecThreads = 64 + kDecEpiThreads;
-constexpr int kDecChPerThread = kDecCh * 4 / kDecEpiWarps;  // 16
-static_assert(kDecChPerThread == 16, "one 16-column TMEM read per part");
+constexpr int kDecChPerThread = kDecHalf;           // 16 or 32
 static_assert(kDecStages <= kMaxStages, "too many stages");
 static_assert(kDecStage % 1024 == 0, "stages stay 1024-byte aligned");
 constexpr size_t dec_smem_bytes() { return 1024 + (size_t)kDecStages * kDecStage + sizeof(PipeState); }
@@ -729,6 +734,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                      bf16 *__restrict__ y, int n_ctiles, int n_mtiles) {
     constexpr int CL = 2;
     constexpr int CPT = kDecChPerThread;
+    constexpr int NL = CPT / 16;          // 16-column TMEM reads per part
     constexpr int SQ = CPT * K * 2 / 16;  // 16-byte words of a thread's state block
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = align1024(smem_raw);
@@ -745,21 +751,25 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             a_row = mt * kPBM;
             rows[0] = tw.rank * H + h0;  // rank 0: B rows, rank 1: C rows
             rows[1] = rows[0] + kDecBoxRows;
-            rows[2] = 2 * H + h0 + kDecBoxRows * tw.rank;  // half of the x rows
+            rows[2] = 2 * H + h0 + kDecHalf * tw.rank;  // half of the x rows
         };
-        // 64 column tiles share each 256 rows of A: rotated K order (ROT)
         if (lane == 0)
-            produce_tiles<kDecStages, 3, CL, decltype(dec_coords), true>(
+            produce_tiles<kDecStages, 3, CL, decltype(dec_coords), SC_DECPROJ_ROT != 0>(
                 &map_h, &map_w, stages, kDecStage, ps, nk, tw, n_ctiles, kDecBox, dec_coords);
     } else if (warp == 1) {
         if (lane == 0 && tw.rank == 0)
-            mma_tiles<kDecStages, kDecN1, kDecN2, CL, kDecBufs, kDecC2, kDecBufStride>(
+            mma_tiles<kDecStages, kDecN, 0, CL, kDecBufs, kDecN, kDecBufStride>(
                 tmem, stages, kDecStage, ps, nk, tw);
         __syncwarp();
     } else {
         const int q = warp & 3;                          // TMEM lane quarter
         const int r = q * 32 + lane;                     // tile row = TMEM lane
-        const int cpart = ((warp - 2) >> 2) * CPT;       // this thread's first channel
+        const int half = (warp - 2) >> 2;                // this thread's half of the channels
+        const int cpart = half * CPT;                    // its first channel in the tile
+        // TMEM columns of its B, C and x values: [B | x_lo | C | x_hi]
+        const uint32_t col_b = (uint32_t)cpart;
+        const uint32_t col_c = (uint32_t)(kDecCh + kDecHalf + cpart);
+        const uint32_t col_x = half == 0 ? (uint32_t)kDecCh : (uint32_t)(2 * kDecCh + kDecHalf);
         int it = 0;
         for (int grp = tw.first; grp < tw.n_groups; grp += tw.step, ++it) {
             int mt, ct;
@@ -793,16 +803,22 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             }
             if (!epi_acquire<kDecBufs>(ps, it, kDecEpiThreads)) break;
             const uint32_t trow = tmem + (uint32_t)(it % kDecBufs) * (uint32_t)kDecBufStride +
-                                  ((uint32_t)(q * 32) << 16) + (uint32_t)cpart;
-            uint32_t rb[16], rc[16], rx[16];
+                                  ((uint32_t)(q * 32) << 16);
+            uint32_t rb[NL][16], rc[NL][16], rx[NL][16];
             __syncwarp();  // tcgen05.ld is warp-collective
-            tmem_ld16_nowait(trow, rb);
-            tmem_ld16_nowait(trow + kDecCh, rc);
-            tmem_ld16_nowait(trow + kDecC2, rx);
+#pragma unroll
+            for (int l = 0; l < NL; ++l) {
+                tmem_ld16_nowait(trow + col_b + 16 * l, rb[l]);
+                tmem_ld16_nowait(trow + col_c + 16 * l, rc[l]);
+                tmem_ld16_nowait(trow + col_x + 16 * l, rx[l]);
+            }
             tmem_ld_wait();
-            tmem_regs_ready(rb);
-            tmem_regs_ready(rc);
-            tmem_regs_ready(rx);
+#pragma unroll
+            for (int l = 0; l < NL; ++l) {
+                tmem_regs_ready(rb[l]);
+                tmem_regs_ready(rc[l]);
+                tmem_regs_ready(rx[l]);
+            }
             epi_release<CL, kDecBufs>(ps, it, tw.rank);  // the accumulator buffer is read
             if (!live) continue;
             uint32_t sw[4 * SQ];  // the state block as words: element e in half e % 2 of word e / 2
@@ -820,11 +836,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             float ns[CPT * K];  // the new state block, bf16 values
 #pragma unroll
             for (int c = 0; c < CPT; c += 2) {
+                const int l = c / 16, j = c % 16;
                 // B, x and C rounded to bf16 (the values a separate in_proj stores);
                 // u = round(B x), the exact product rounded once
-                const uint32_t bx = bf2_mul(pack_bf16(__uint_as_float(rb[c]), __uint_as_float(rb[c + 1])),
-                                            pack_bf16(__uint_as_float(rx[c]), __uint_as_float(rx[c + 1])));
-                const uint32_t cc = pack_bf16(__uint_as_float(rc[c]), __uint_as_float(rc[c + 1]));
+                const uint32_t bx =
+                    bf2_mul(pack_bf16(__uint_as_float(rb[l][j]), __uint_as_float(rb[l][j + 1])),
+                            pack_bf16(__uint_as_float(rx[l][j]), __uint_as_float(rx[l][j + 1])));
+                const uint32_t cc =
+                    pack_bf16(__uint_as_float(rc[l][j]), __uint_as_float(rc[l][j + 1]));
                 float o[2];
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
@@ -845,8 +864,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 yw[c / 2] = pack_bf16(o[0], o[1]);
             }
             uint4 *yp = reinterpret_cast<uint4 *>(y + i * (int64_t)H + h);
-            gst(yp, make_uint4(yw[0], yw[1], yw[2], yw[3]));
-            gst(yp + 1, make_uint4(yw[4], yw[5], yw[6], yw[7]));
+#pragma unroll
+            for (int e = 0; e < CPT / 8; ++e)
+                gst(yp + e, make_uint4(yw[4 * e], yw[4 * e + 1], yw[4 * e + 2], yw[4 * e + 3]));
             uint32_t nw[4 * SQ];  // exact: every value is a bf16 already
 #pragma unroll
             for (int m = 0; m < 4 * SQ; ++m)

@@ -66,6 +66,33 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
+// An L2 cache policy that keeps the lines it is given in L2 ahead of others
+// (evict last), for data a second reader fetches later.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// bulk_copy_g2s with an L2 cache policy for the source lines.
+__device__ __forceinline__ void bulk_copy_g2s_hint(void *dst, const void *src, uint32_t bytes,
+                                                   uint64_t *bar, uint64_t policy) {
+#ifdef SC_BOUNDS_CHECK
+    if (!SC_RD_OK(src, bytes)) {  // refused: count the bytes anyway so no wait hangs
+        asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(
+                         smem_addr(bar)),
+                     "r"(bytes)
+                     : "memory");
+        return;
+    }
+#endif
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes,
                                               uint64_t *bar) {
 #ifdef SC_BOUNDS_CHECK
