@@ -49,8 +49,14 @@ constexpr int kBwdCpt = 4;                         // channels per consumer thre
 constexpr int kBwdSlice = SC_BWD_SLICE;            // channels per CTA slice
 constexpr int kBwdConsumers = kBwdSlice / kBwdCpt;
 #ifndef SC_BWD_HALO_HINT
-#define SC_BWD_HALO_HINT 0  // 1: evict-last L2 policy on the rows a neighbouring CTA reads again
+#define SC_BWD_HALO_HINT 1  // 1: evict-last L2 policy on the rows a neighbouring CTA reads again
 #endif
+// Row ranges up to this many rows take the hint. There the K-1 rows before
+// and after a range are a sizeable share of its reads (4 of 31 rows at
+// T = 4096, H = 2048), and without the hint the second read of them missed
+// L2 (T = 4096: 70.6-73.4 MB read per launch for 67.1 MB of inputs; with
+// it 65.0-67.2 MB). Longer ranges (T = 65536: 431 rows) do without it.
+constexpr int64_t kBwdHintRows = 256;
 #ifndef SC_BWD_STAGES
 #define SC_BWD_STAGES 4  // stage ring depth (the header holds up to 16 stages' barriers)
 #endif
@@ -180,7 +186,8 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, kBwdCtas<T, K>)
     // The 2 (K-1) rows around the range's start are read again by the CTA of
     // the range before, at its end: with SC_BWD_HALO_HINT they are fetched
     // with an evict-last L2 policy so that second read finds them in L2.
-    const uint64_t keep = SC_BWD_HALO_HINT ? l2_policy_evict_last() : 0;
+    const bool hint = SC_BWD_HALO_HINT && rc > 0 && cr1 - cr0 <= kBwdHintRows;
+    const uint64_t keep = hint ? l2_policy_evict_last() : 0;
     auto issue = [&](int c) {
         const int s = c % NS;
         const int64_t rb = sr0 + (int64_t)c * R;
@@ -189,7 +196,7 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, kBwdCtas<T, K>)
         for (int rr = 0; rr < rows; ++rr) {
             const T *src = bcx + (rb + rr) * ld + c0;
             T *dst = stage + (size_t)(s * R + rr) * 4 * CW;
-            if (SC_BWD_HALO_HINT && rc > 0 && rb + rr < cr0 + (K - 1)) {
+            if (hint && rb + rr < cr0 + (K - 1)) {
 #pragma unroll
                 for (int q = 0; q < 3; ++q)
                     bulk_copy_g2s_hint(dst + (size_t)q * CW, src + (int64_t)q * H, sec_bytes,
@@ -420,6 +427,10 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, kBwdVarlenCtas<K>)
     pdl_wait();
     pdl_launch_dependents();
 
+    // Evict-last L2 policy on the rows around the range's start, which the
+    // CTA before reads again at its end (as in k_backward).
+    const bool hint = SC_BWD_HALO_HINT && rc > 0 && cr1 - cr0 <= kBwdHintRows;
+    const uint64_t keep = hint ? l2_policy_evict_last() : 0;
     auto issue = [&](int c) {
         const int s = c % NS;
         const int64_t rb = sr0 + (int64_t)c * R;
@@ -428,6 +439,15 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, kBwdVarlenCtas<K>)
         for (int rr = 0; rr < rows; ++rr) {
             const T *src = bcx + (rb + rr) * ld + c0;
             T *dst = stage + (size_t)(s * R + rr) * 4 * CW;
+            if (hint && rb + rr < cr0 + (K - 1)) {
+#pragma unroll
+                for (int q = 0; q < 3; ++q)
+                    bulk_copy_g2s_hint(dst + (size_t)q * CW, src + (int64_t)q * H, sec_bytes,
+                                       &full[s], keep);
+                bulk_copy_g2s_hint(dst + (size_t)3 * CW, dy + (rb + rr) * (int64_t)H + c0,
+                                   sec_bytes, &full[s], keep);
+                continue;
+            }
 #pragma unroll
             for (int q = 0; q < 3; ++q)
                 bulk_copy_g2s(dst + (size_t)q * CW, src + (int64_t)q * H, sec_bytes, &full[s]);
