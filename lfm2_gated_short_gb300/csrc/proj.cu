@@ -57,15 +57,6 @@ constexpr uint32_t kPABytes = kPBM * kPBK * 2;  // 16 KB
 #ifndef SC_INPROJ_STAGES
 #define SC_INPROJ_STAGES 4  // stage ring depth of the fused in_proj (40 KB a stage)
 #endif
-#ifndef SC_INPROJ_ROT
-#define SC_INPROJ_ROT 0  // 1: rotated K-block order in the fused in_proj (see produce_tiles)
-#endif
-#ifndef SC_DECPROJ_ROT
-#define SC_DECPROJ_ROT 0  // 1: rotated K-block order in the fused in_proj decode
-#endif
-#ifndef SC_OUTPROJ_ROT
-#define SC_OUTPROJ_ROT 0  // 1: rotated K-block order in out_proj
-#endif
 #ifndef SC_OUTPROJ_STAGES
 #define SC_OUTPROJ_STAGES (SC_PROJ_CLUSTER == 2 ? 6 : 4)  // stage ring depth, out_proj
 #endif
@@ -185,11 +176,8 @@ __device__ __forceinline__ void pipe_init(PipeState *ps, int CL, int epi_warps) 
 
 // Warp 0, one lane. coords(mt, ct, a_row, rows) gives the tile's A row and the
 // first rows of this CTA's NB boxes of B (box_bytes each); a stage holds A,
-// then the boxes. With ROT, tile group grp walks its K blocks starting at
-// block grp % nk (wrapping): the pairs running at the same time then read
-// different A columns, where many tiles share the same A rows (the MMA lane
-// counts blocks, not positions, so the sum only changes order).
-template <int S, int NB, int CL, typename Coords, bool ROT = false>
+// then the boxes.
+template <int S, int NB, int CL, typename Coords>
 __device__ __forceinline__ void produce_tiles(const CUtensorMap *ma, const CUtensorMap *mb,
                                               uint32_t stages, uint32_t stage_bytes,
                                               PipeState *ps, int nk, const TileWalk &tw,
@@ -202,8 +190,7 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap *ma, const CUten
         int mt, ct, a_row, rows[NB];
         tw.at(grp, n_col_tiles, mt, ct);
         coords(mt, ct, a_row, rows);
-        for (int kb_i = 0; kb_i < nk; ++kb_i, ++g) {
-            const int kb = ROT ? (kb_i + grp % nk) % nk : kb_i;
+        for (int kb = 0; kb < nk; ++kb, ++g) {
             const uint32_t s = g % S;
             if (g >= S && !mbar_wait_bounded(&ps->empty[s], (g / S - 1) & 1u)) {
                 raise_error(SC_DEV_TIMEOUT);
@@ -427,7 +414,7 @@ __global__ void __launch_bounds__(kInThreads, 1)
             }
         };
         if (lane == 0)
-            produce_tiles<kInStages, 3, CL, decltype(conv_coords), SC_INPROJ_ROT != 0>(
+            produce_tiles<kInStages, 3, CL>(
                 &map_h, &map_w, stages, kConvStage, ps, nk, tw, n_ctiles, kConvBox, conv_coords);
     } else if (warp == 1) {
         if (lane == 0 && tw.rank == 0)
@@ -687,9 +674,11 @@ __global__ void __launch_bounds__(256)
 // sequence i, its conv history is the K - 1 newest values of its slot, and
 // its new state is [history; u]. A CTA pair computes the B | C | x product
 // block of kDecCh channels for 2 x 128 sequences with one N = 3 kDecCh MMA
-// per 16-deep K step: rank 0 stages the kDecCh B rows of w_in and the first
-// half of the x rows, rank 1 the C rows and the second half, so TMEM columns
-// hold [B | x_lo | C | x_hi]. Two accumulator buffers let a CTA's next tile's
+// per 16-deep K step. With w_in seen as [3][H][D] (a 3-D tensor map), each
+// CTA stages the B, C and x rows of its half of the channels with one copy:
+// rank 0 channels h0 .. h0 + kDecCh/2 - 1, rank 1 the rest, so TMEM columns
+// hold [B | C | x of the first half | B | C | x of the second half]. Two
+// accumulator buffers let a CTA's next tile's
 // MMAs overlap this tile's epilogue. Narrow tiles put every SM to work at a
 // serving batch (256 sequences, H = 2048, 32 channels: 64 tile pairs).
 //
@@ -709,9 +698,7 @@ constexpr int kDecN = 3 * kDecCh;                   // B | x_lo | C | x_hi
 constexpr int kDecHalf = kDecCh / 2;
 constexpr int kDecBufStride = kDecN <= 128 ? 128 : 256;  // TMEM columns between buffers
 constexpr int kDecBufs = 2;
-constexpr int kDecBoxRows = kDecHalf;               // B or C: two boxes; x: one
-constexpr uint32_t kDecBox = kDecBoxRows * kPBK * 2;
-constexpr uint32_t kDecStage = kPABytes + 3 * kDecBox;
+constexpr uint32_t kDecStage = kPABytes + 3 * kDecHalf * kPBK * 2;  // A; B, C, x of a half
 #ifndef SC_DECPROJ_STAGES
 #define SC_DECPROJ_STAGES (kDecCh == 32 ? 8 : 7)
 #endif
@@ -728,7 +715,7 @@ static_assert(dec_smem_bytes() <= 232448, "stage ring larger than a CTA's shared
 template <int K>
 __global__ void __launch_bounds__(kDecThreads, 1)
     k_in_proj_decode(const __grid_constant__ CUtensorMap map_h,
-                     const __grid_constant__ CUtensorMap map_w, int N, int D, int H,
+                     const __grid_constant__ CUtensorMap map_w3, int N, int D, int H,
                      const bf16 *__restrict__ w, const bf16 *__restrict__ bias,
                      const int32_t *__restrict__ slots, bf16 *__restrict__ pool, int n_slots,
                      bf16 *__restrict__ y, int n_ctiles, int n_mtiles) {
@@ -742,20 +729,42 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const uint32_t stages = smem_addr(base);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = D / kPBK;
-    const uint32_t tmem = pipe_start<CL>(ps, &map_h, &map_w, kDecEpiWarps);
+    const uint32_t tmem = pipe_start<CL>(ps, &map_h, &map_w3, kDecEpiWarps);
     const TileWalk tw = tile_walk<CL>(n_mtiles, n_ctiles);
 
     if (warp == 0) {
-        auto dec_coords = [&](int mt, int ct, int &a_row, int (&rows)[3]) {
-            const int h0 = ct * kDecCh;
-            a_row = mt * kPBM;
-            rows[0] = tw.rank * H + h0;  // rank 0: B rows, rank 1: C rows
-            rows[1] = rows[0] + kDecBoxRows;
-            rows[2] = 2 * H + h0 + kDecHalf * tw.rank;  // half of the x rows
-        };
-        if (lane == 0)
-            produce_tiles<kDecStages, 3, CL, decltype(dec_coords), SC_DECPROJ_ROT != 0>(
-                &map_h, &map_w, stages, kDecStage, ps, nk, tw, n_ctiles, kDecBox, dec_coords);
+        // One A box and one [3 sections][kDecHalf channels][64 K] box per stage.
+        if (lane == 0) {
+            const bool leader = tw.rank == 0;
+            uint32_t g = 0;
+            bool ok = true;
+            for (int grp = tw.first; grp < tw.n_groups && ok; grp += tw.step) {
+                int mt, ct;
+                tw.at(grp, n_ctiles, mt, ct);
+                const int a_row = mt * kPBM, ch = ct * kDecCh + kDecHalf * tw.rank;
+                for (int kb = 0; kb < nk; ++kb, ++g) {
+                    const uint32_t s = g % kDecStages;
+                    if (g >= kDecStages &&
+                        !mbar_wait_bounded(&ps->empty[s], (g / kDecStages - 1) & 1u)) {
+                        raise_error(SC_DEV_TIMEOUT);
+                        ps->abort = 1;
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = stages + s * kDecStage;
+                    const uint32_t bar = cluster_map(smem_addr(&ps->full[s]), 0);
+                    if (leader) mbar_arrive_expect_tx(&ps->full[s], 2 * kDecStage);
+                    tma_load_2d_pair(st, &map_h, bar, kb * kPBK, a_row);
+                    tma_load_3d_pair(st + kPABytes, &map_w3, bar, kb * kPBK, ch, 0);
+                }
+            }
+            if (leader)
+                for (uint32_t c = g > kDecStages ? g - kDecStages : 0; c < g; ++c)
+                    mbar_wait_bounded(&ps->full[c % kDecStages], (c / kDecStages) & 1u);
+            if (ok)
+                for (uint32_t c = g > kDecStages ? g - kDecStages : 0; c < g; ++c)
+                    mbar_wait_bounded(&ps->empty[c % kDecStages], (c / kDecStages) & 1u);
+        }
     } else if (warp == 1) {
         if (lane == 0 && tw.rank == 0)
             mma_tiles<kDecStages, kDecN, 0, CL, kDecBufs, kDecN, kDecBufStride>(
@@ -766,10 +775,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const int r = q * 32 + lane;                     // tile row = TMEM lane
         const int half = (warp - 2) >> 2;                // this thread's half of the channels
         const int cpart = half * CPT;                    // its first channel in the tile
-        // TMEM columns of its B, C and x values: [B | x_lo | C | x_hi]
-        const uint32_t col_b = (uint32_t)cpart;
-        const uint32_t col_c = (uint32_t)(kDecCh + kDecHalf + cpart);
-        const uint32_t col_x = half == 0 ? (uint32_t)kDecCh : (uint32_t)(2 * kDecCh + kDecHalf);
+        // TMEM columns of its B, C and x values: [B | C | x] of its half
+        const uint32_t col_b = (uint32_t)(3 * cpart);
+        const uint32_t col_c = col_b + kDecHalf;
+        const uint32_t col_x = col_b + 2 * kDecHalf;
         int it = 0;
         for (int grp = tw.first; grp < tw.n_groups; grp += tw.step, ++it) {
             int mt, ct;
@@ -902,7 +911,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             rows[0] = nt * kOutN + tw.rank * kOutBoxRows;
         };
         if (lane == 0)
-            produce_tiles<kOutStages, 1, CL, decltype(out_coords), SC_OUTPROJ_ROT != 0>(
+            produce_tiles<kOutStages, 1, CL>(
                 &map_a, &map_b, stages, kOutStage, ps, nk, tw, n_ntiles, kOutBox, out_coords);
     } else if (warp == 1) {
         if (lane == 0 && tw.rank == 0)
@@ -971,6 +980,24 @@ static cudaError_t map_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint6
     const cuuint32_t box[2] = {(cuuint32_t)kPBK, box_rows};
     const cuuint32_t es[2] = {1, 1};
     const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims,
+                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// w_in [3H, D] seen as [3][H][D]: a box covers 64 K values of `box_rows`
+// channels in each of the three sections (B, C, x), written to shared memory
+// section after section (3 box_rows rows of 128 bytes, 128-byte swizzle).
+static cudaError_t map_3d_sections(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t H,
+                                   uint32_t box_rows) {
+    EncodeTiledFn fn = encode_tiled();
+    if (fn == nullptr) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {inner, H, 3};
+    const cuuint64_t strides[2] = {inner * 2, H * inner * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)kPBK, box_rows, 3};
+    const cuuint32_t es[3] = {1, 1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims,
                           strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1080,7 +1107,8 @@ cudaError_t launch_in_proj_prefill(int D, int H, int K, const void *hidden, int6
 }
 
 template <int K>
-static cudaError_t in_proj_decode_inst(const CUtensorMap &mh, const CUtensorMap &mw, int N, int D,
+static cudaError_t in_proj_decode_inst(const CUtensorMap &mh, const CUtensorMap &mw3, int N,
+                                       int D,
                                        int H, const void *w, const void *bias,
                                        const int32_t *slots, void *pool, int n_slots, void *y,
                                        int sm_count, cudaStream_t stream) {
@@ -1097,7 +1125,7 @@ static cudaError_t in_proj_decode_inst(const CUtensorMap &mh, const CUtensorMap 
     const int64_t groups = (int64_t)(n_mtiles + 1) / 2 * n_ctiles;
     const int grid = 2 * (int)(groups < clusters ? groups : clusters);  // persistent pairs
     return launch_pdl_cluster(kern, dim3((unsigned)grid), dim3(kDecThreads), dec_smem_bytes(),
-                              stream, 2u, mh, mw, N, D, H, (const bf16 *)w, (const bf16 *)bias,
+                              stream, 2u, mh, mw3, N, D, H, (const bf16 *)w, (const bf16 *)bias,
                               slots, (bf16 *)pool, n_slots, (bf16 *)y, n_ctiles, n_mtiles);
 }
 
@@ -1106,16 +1134,17 @@ cudaError_t launch_in_proj_decode(int D, int H, int K, const void *hidden, int N
                                   const int32_t *slots, void *pool, int n_slots, void *y,
                                   int sm_count, cudaStream_t stream) {
     if (N == 0) return cudaSuccess;
-    CUtensorMap mh, mw;
+    CUtensorMap mh;
     cudaError_t e = map_2d(&mh, hidden, (uint64_t)D, (uint64_t)N, kPBM);
     if (e != cudaSuccess) return e;
-    e = map_2d(&mw, w_in, (uint64_t)D, (uint64_t)3 * H, kDecBoxRows);
+    CUtensorMap mw3;  // w_in as [3 sections][H channels][D]: boxes of all three sections
+    e = map_3d_sections(&mw3, w_in, (uint64_t)D, (uint64_t)H, (uint32_t)kDecHalf);
     if (e != cudaSuccess) return e;
     switch (K) {
-        case 1: return in_proj_decode_inst<1>(mh, mw, N, D, H, w, bias, slots, pool, n_slots, y, sm_count, stream);
-        case 2: return in_proj_decode_inst<2>(mh, mw, N, D, H, w, bias, slots, pool, n_slots, y, sm_count, stream);
-        case 3: return in_proj_decode_inst<3>(mh, mw, N, D, H, w, bias, slots, pool, n_slots, y, sm_count, stream);
-        default: return in_proj_decode_inst<4>(mh, mw, N, D, H, w, bias, slots, pool, n_slots, y, sm_count, stream);
+        case 1: return in_proj_decode_inst<1>(mh, mw3, N, D, H, w, bias, slots, pool, n_slots, y, sm_count, stream);
+        case 2: return in_proj_decode_inst<2>(mh, mw3, N, D, H, w, bias, slots, pool, n_slots, y, sm_count, stream);
+        case 3: return in_proj_decode_inst<3>(mh, mw3, N, D, H, w, bias, slots, pool, n_slots, y, sm_count, stream);
+        default: return in_proj_decode_inst<4>(mh, mw3, N, D, H, w, bias, slots, pool, n_slots, y, sm_count, stream);
     }
 }
 

@@ -336,6 +336,20 @@ def test_out_proj_lfm2_shape_sampled_columns():
     assert_bits(out[:, cols], layer.out_proj("bf16", y, wo[cols]), "out")
 
 
+@pytest.mark.parametrize("T,H,D", [(1000, 64, 768), (513, 128, 256), (4133, 2048, 2048)])
+def test_out_proj_every_column_on_sampled_rows(T, H, D):
+    """Every output column (the balanced schedule cuts the columns into
+    ranges and pieces of any multiple of 16), on sampled rows including the
+    first and the last ones."""
+    rng = np.random.default_rng(896 + T)
+    y = dyadic(rng, (T, H), 8, -3)
+    wo = dyadic(rng, (D, H), 8, -6)
+    out = host(sc.out_proj(dev(y, "bf16"), dev(wo, "bf16")))
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, T - 2, T - 1],
+                                     rng.choice(T, min(T, 56), replace=False)]))
+    assert_bits(out[rows], layer.out_proj("bf16", y[rows], wo), "out")
+
+
 def test_layer_chain_against_the_oracle():
     """in_proj + conv, then out_proj: the whole ShortConv layer."""
     rng = np.random.default_rng(899)
