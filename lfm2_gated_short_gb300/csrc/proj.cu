@@ -692,13 +692,19 @@ __global__ void __launch_bounds__(256)
 #ifndef SC_DECPROJ_CH
 #define SC_DECPROJ_CH 32  // channels per tile: 32 or 64
 #endif
+#ifndef SC_DECPROJ_CL
+#define SC_DECPROJ_CL 1  // 1: single CTAs issue their own MMAs (M = 128); 2: CTA pairs (M = 256)
+#endif
+constexpr int kDecCL = SC_DECPROJ_CL;
+static_assert(kDecCL == 1 || kDecCL == 2, "single CTAs or pairs");
 constexpr int kDecCh = SC_DECPROJ_CH;
 static_assert(kDecCh == 32 || kDecCh == 64, "32 or 64 channels per decode tile");
-constexpr int kDecN = 3 * kDecCh;                   // B | x_lo | C | x_hi
+constexpr int kDecN = 3 * kDecCh;                   // B | C | x per staged channel group
 constexpr int kDecHalf = kDecCh / 2;
+constexpr int kDecBoxCh = kDecCh / kDecCL;          // channels a CTA stages
 constexpr int kDecBufStride = kDecN <= 128 ? 128 : 256;  // TMEM columns between buffers
 constexpr int kDecBufs = 2;
-constexpr uint32_t kDecStage = kPABytes + 3 * kDecHalf * kPBK * 2;  // A; B, C, x of a half
+constexpr uint32_t kDecStage = kPABytes + 3 * kDecBoxCh * kPBK * 2;  // A; B, C, x rows
 #ifndef SC_DECPROJ_STAGES
 #define SC_DECPROJ_STAGES (kDecCh == 32 ? 8 : 7)
 #endif
@@ -719,7 +725,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                      const bf16 *__restrict__ w, const bf16 *__restrict__ bias,
                      const int32_t *__restrict__ slots, bf16 *__restrict__ pool, int n_slots,
                      bf16 *__restrict__ y, int n_ctiles, int n_mtiles) {
-    constexpr int CL = 2;
+    constexpr int CL = kDecCL;
     constexpr int CPT = kDecChPerThread;
     constexpr int NL = CPT / 16;          // 16-column TMEM reads per part
     constexpr int SQ = CPT * K * 2 / 16;  // 16-byte words of a thread's state block
@@ -733,7 +739,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const TileWalk tw = tile_walk<CL>(n_mtiles, n_ctiles);
 
     if (warp == 0) {
-        // One A box and one [3 sections][kDecHalf channels][64 K] box per stage.
+        // One A box and one [3 sections][kDecBoxCh channels][64 K] box per stage.
         if (lane == 0) {
             const bool leader = tw.rank == 0;
             uint32_t g = 0;
@@ -741,7 +747,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             for (int grp = tw.first; grp < tw.n_groups && ok; grp += tw.step) {
                 int mt, ct;
                 tw.at(grp, n_ctiles, mt, ct);
-                const int a_row = mt * kPBM, ch = ct * kDecCh + kDecHalf * tw.rank;
+                const int a_row = mt * kPBM, ch = ct * kDecCh + kDecBoxCh * tw.rank;
                 for (int kb = 0; kb < nk; ++kb, ++g) {
                     const uint32_t s = g % kDecStages;
                     if (g >= kDecStages &&
@@ -752,13 +758,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                         break;
                     }
                     const uint32_t st = stages + s * kDecStage;
-                    const uint32_t bar = cluster_map(smem_addr(&ps->full[s]), 0);
-                    if (leader) mbar_arrive_expect_tx(&ps->full[s], 2 * kDecStage);
-                    tma_load_2d_pair(st, &map_h, bar, kb * kPBK, a_row);
-                    tma_load_3d_pair(st + kPABytes, &map_w3, bar, kb * kPBK, ch, 0);
+                    if constexpr (CL == 1) {
+                        mbar_arrive_expect_tx(&ps->full[s], kDecStage);
+                        tma_load_2d(st, &map_h, &ps->full[s], kb * kPBK, a_row);
+                        tma_load_3d(st + kPABytes, &map_w3, &ps->full[s], kb * kPBK, ch, 0);
+                    } else {
+                        const uint32_t bar = cluster_map(smem_addr(&ps->full[s]), 0);
+                        if (leader) mbar_arrive_expect_tx(&ps->full[s], 2 * kDecStage);
+                        tma_load_2d_pair(st, &map_h, bar, kb * kPBK, a_row);
+                        tma_load_3d_pair(st + kPABytes, &map_w3, bar, kb * kPBK, ch, 0);
+                    }
                 }
             }
-            if (leader)
+            if (CL == 1 || leader)
                 for (uint32_t c = g > kDecStages ? g - kDecStages : 0; c < g; ++c)
                     mbar_wait_bounded(&ps->full[c % kDecStages], (c / kDecStages) & 1u);
             if (ok)
@@ -775,10 +787,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const int r = q * 32 + lane;                     // tile row = TMEM lane
         const int half = (warp - 2) >> 2;                // this thread's half of the channels
         const int cpart = half * CPT;                    // its first channel in the tile
-        // TMEM columns of its B, C and x values: [B | C | x] of its half
-        const uint32_t col_b = (uint32_t)(3 * cpart);
-        const uint32_t col_c = col_b + kDecHalf;
-        const uint32_t col_x = col_b + 2 * kDecHalf;
+        // TMEM columns of its B, C and x values. Pairs: [B | C | x] of each
+        // CTA's half of the channels in turn; single CTAs: [B | C | x] of all.
+        const uint32_t col_b = CL == 2 ? (uint32_t)(3 * cpart) : (uint32_t)cpart;
+        const uint32_t col_c = col_b + kDecBoxCh;
+        const uint32_t col_x = col_b + 2 * kDecBoxCh;
         int it = 0;
         for (int grp = tw.first; grp < tw.n_groups; grp += tw.step, ++it) {
             int mt, ct;
@@ -1116,16 +1129,19 @@ static cudaError_t in_proj_decode_inst(const CUtensorMap &mh, const CUtensorMap 
     static std::atomic<unsigned long long> done{0};
     cudaError_t e = smem_opt_in(kern, dec_smem_bytes(), done);
     if (e != cudaSuccess) return e;
-    static std::atomic<int> cache[64];
-    int clusters = 0;
-    e = max_clusters(kern, dec_smem_bytes(), kDecThreads, sm_count, cache, &clusters);
-    if (e != cudaSuccess) return e;
+    int clusters = sm_count;  // single CTAs: one per SM (the stage ring fills its shared memory)
+    if (kDecCL == 2) {
+        static std::atomic<int> cache[64];
+        e = max_clusters(kern, dec_smem_bytes(), kDecThreads, sm_count, cache, &clusters);
+        if (e != cudaSuccess) return e;
+    }
     const int n_ctiles = H / kDecCh;
     const int n_mtiles = (N + kPBM - 1) / kPBM;
-    const int64_t groups = (int64_t)(n_mtiles + 1) / 2 * n_ctiles;
-    const int grid = 2 * (int)(groups < clusters ? groups : clusters);  // persistent pairs
+    const int64_t groups = (int64_t)(n_mtiles + kDecCL - 1) / kDecCL * n_ctiles;
+    const int grid = kDecCL * (int)(groups < clusters ? groups : clusters);  // persistent
     return launch_pdl_cluster(kern, dim3((unsigned)grid), dim3(kDecThreads), dec_smem_bytes(),
-                              stream, 2u, mh, mw3, N, D, H, (const bf16 *)w, (const bf16 *)bias,
+                              stream, (unsigned)kDecCL, mh, mw3, N, D, H, (const bf16 *)w,
+                              (const bf16 *)bias,
                               slots, (bf16 *)pool, n_slots, (bf16 *)y, n_ctiles, n_mtiles);
 }
 
@@ -1138,7 +1154,7 @@ cudaError_t launch_in_proj_decode(int D, int H, int K, const void *hidden, int N
     cudaError_t e = map_2d(&mh, hidden, (uint64_t)D, (uint64_t)N, kPBM);
     if (e != cudaSuccess) return e;
     CUtensorMap mw3;  // w_in as [3 sections][H channels][D]: boxes of all three sections
-    e = map_3d_sections(&mw3, w_in, (uint64_t)D, (uint64_t)H, (uint32_t)kDecHalf);
+    e = map_3d_sections(&mw3, w_in, (uint64_t)D, (uint64_t)H, (uint32_t)kDecBoxCh);
     if (e != cudaSuccess) return e;
     switch (K) {
         case 1: return in_proj_decode_inst<1>(mh, mw3, N, D, H, w, bias, slots, pool, n_slots, y, sm_count, stream);
