@@ -55,7 +55,9 @@ constexpr int kBwdConsumers = kBwdSlice / kBwdCpt;
 // and after a range are a sizeable share of its reads (4 of 31 rows at
 // T = 4096, H = 2048), and without the hint the second read of them missed
 // L2 (T = 4096: 70.6-73.4 MB read per launch for 67.1 MB of inputs; with
-// it 65.0-67.2 MB). Longer ranges (T = 65536: 431 rows) do without it.
+// it 65.0-67.2 MB). Longer ranges (T = 65536: 431 rows) do without it: in
+// k_backward they run an instance without the hint's code, which measured
+// 1% faster there than the same code with the hint switched off at run time.
 constexpr int64_t kBwdHintRows = 256;
 #ifndef SC_BWD_STAGES
 #define SC_BWD_STAGES 4  // stage ring depth (the header holds up to 16 stages' barriers)
@@ -137,7 +139,7 @@ __device__ __forceinline__ void store_partial(float *__restrict__ part, int H, i
 
 // HB: a conv bias is given or dbias is wanted. The instance without carries
 // no bias registers or branches; with_dbias then is false.
-template <typename T, int K, bool HB>
+template <typename T, int K, bool HB, bool HINT>
 __global__ void __launch_bounds__(kBwdConsumers + 32, kBwdCtas<T, K>)
     k_backward(const T *__restrict__ bcx, int64_t T_rows, int H, const T *__restrict__ w,
                const T *__restrict__ bias, const T *__restrict__ dy, T *__restrict__ dbcx,
@@ -184,9 +186,10 @@ __global__ void __launch_bounds__(kBwdConsumers + 32, kBwdCtas<T, K>)
 
     // Stage layout per row: B | C | x | dy sections of CW channels.
     // The 2 (K-1) rows around the range's start are read again by the CTA of
-    // the range before, at its end: with SC_BWD_HALO_HINT they are fetched
-    // with an evict-last L2 policy so that second read finds them in L2.
-    const bool hint = SC_BWD_HALO_HINT && rc > 0 && cr1 - cr0 <= kBwdHintRows;
+    // the range before, at its end: in the HINT instance (short ranges) they
+    // are fetched with an evict-last L2 policy so that second read finds
+    // them in L2. Long ranges run the instance without the hint's code.
+    const bool hint = HINT && rc > 0;
     const uint64_t keep = hint ? l2_policy_evict_last() : 0;
     auto issue = [&](int c) {
         const int s = c % NS;
@@ -811,22 +814,28 @@ static cudaError_t backward_inst(const void *bcx, int64_t rows, int H, const voi
     const int n_slices = (H + kBwdSlice - 1) / kBwdSlice;
     const int threads = (CW / kBwdCpt + 31) / 32 * 32 + 32;  // consumers + one producer warp
     const size_t smem = bwd_smem_bytes<T>(CW);
-    auto kern = k_backward<T, K, HB>;
+    auto kern = k_backward<T, K, HB, false>;
+    auto kern_hint = k_backward<T, K, HB, SC_BWD_HALO_HINT != 0>;
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !(configured.load() & (1ull << dev))) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)bwd_smem_bytes<T>(kBwdSlice));
-        if (e != cudaSuccess) return e;
+        for (auto kr : {kern, kern_hint}) {
+            e = cudaFuncSetAttribute(kr, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)bwd_smem_bytes<T>(kBwdSlice));
+            if (e != cudaSuccess) return e;
+        }
         configured.fetch_or(1ull << dev);
     }
     static WaveCache waves;
     int64_t n_row = 1;
     e = bwd_launch_rows(kern, threads, smem, n_slices, CW, rows, waves, &n_row);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(kern, dim3((unsigned)(n_row * n_slices)), dim3(threads), smem, stream,
+    // Both instances have the same register budget and shared memory, so the
+    // same row split (and so the same dW bits).
+    const bool short_ranges = (rows + n_row - 1) / n_row <= kBwdHintRows;
+    e = launch_pdl(short_ranges ? kern_hint : kern, dim3((unsigned)(n_row * n_slices)), dim3(threads), smem, stream,
                    (const T *)bcx, rows, H, (const T *)w, (const T *)bias, (const T *)dy,
                    (T *)dbcx, (float *)ws, dbias != nullptr, n_slices, (int)n_row);
     if (e != cudaSuccess) return e;

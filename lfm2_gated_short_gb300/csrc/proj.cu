@@ -672,15 +672,16 @@ __global__ void __launch_bounds__(256)
 //
 // One token per sequence (serving decode): row i of the hidden state is
 // sequence i, its conv history is the K - 1 newest values of its slot, and
-// its new state is [history; u]. A CTA pair computes the B | C | x product
-// block of kDecCh channels for 2 x 128 sequences with one N = 3 kDecCh MMA
-// per 16-deep K step. With w_in seen as [3][H][D] (a 3-D tensor map), each
-// CTA stages the B, C and x rows of its half of the channels with one copy:
-// rank 0 channels h0 .. h0 + kDecCh/2 - 1, rank 1 the rest, so TMEM columns
-// hold [B | C | x of the first half | B | C | x of the second half]. Two
-// accumulator buffers let a CTA's next tile's
-// MMAs overlap this tile's epilogue. Narrow tiles put every SM to work at a
-// serving batch (256 sequences, H = 2048, 32 channels: 64 tile pairs).
+// its new state is [history; u]. A CTA computes the B | C | x product block
+// of kDecCh channels for 128 sequences with one N = 3 kDecCh MMA per 16-deep
+// K step. With w_in seen as [3][H][D] (a 3-D tensor map), the B, C and x rows
+// of the tile's channels come with one copy per stage, so TMEM columns hold
+// [B | C | x]. Two accumulator buffers let a CTA's next tile's MMAs overlap
+// this tile's epilogue. Narrow tiles put every SM to work at a serving batch
+// (256 sequences, H = 2048, 32 channels: 128 tiles). Each MMA carries a
+// fixed cost, so single CTAs, each issuing its own MMAs, beat CTA pairs
+// (one MMA stream per two SMs) here; pairs (M = 256, each CTA staging its
+// half of the channels) remain a build knob.
 //
 // Epilogue thread = (sequence, kDecCh / 2 channels): the slot id, the state
 // block and the taps are loaded while the MMAs run; then u = round(B x),

@@ -543,3 +543,25 @@ def test_in_proj_decode_bad_slot_skips_that_sequence():
     assert np.all(g[7] == np.uint16(0x4040)), "the skipped row was written"
     assert_close("bf16", g[keep], y_ref, "y")
     assert_bits(host(pool), ref, "pool")
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_in_proj_decode_seeded_shapes(seed):
+    """Seeded shapes: N in 1..600 (ragged last tile), H a multiple of 64 up to
+    320, D a multiple of 64 up to 384, K in 1..4, with or without a bias;
+    exact projections, against the oracle."""
+    rng = np.random.default_rng(7700 + seed)
+    N = int(rng.integers(1, 601))
+    D = 64 * int(rng.integers(1, 7))
+    H = 64 * int(rng.integers(1, 6))
+    K = int(rng.integers(1, 5))
+    c = make_decode_case(rng, N, D, H, K, extra_slots=int(rng.integers(0, 9)),
+                         with_bias=bool(rng.integers(0, 2)))
+    y, pool = run_decode_gpu(c)
+    assert sc.get_error() == 0
+    ref = c["pool"].copy()
+    st, y_ref = layer.in_proj_decode("bf16", c["hidden"], c["w_in"], c["w"], c["slots"], ref,
+                                     bias=c["bias"])
+    assert st == oracle.OK
+    assert_close("bf16", y, y_ref, "y")
+    assert_bits(pool, ref, "pool")
