@@ -705,9 +705,15 @@ constexpr int kDecHalf = kDecCh / 2;
 constexpr int kDecBoxCh = kDecCh / kDecCL;          // channels a CTA stages
 constexpr int kDecBufStride = kDecN <= 128 ? 128 : 256;  // TMEM columns between buffers
 constexpr int kDecBufs = 2;
-constexpr uint32_t kDecStage = kPABytes + 3 * kDecBoxCh * kPBK * 2;  // A; B, C, x rows
+#ifndef SC_DECPROJ_KB
+#define SC_DECPROJ_KB 2  // 64-deep K blocks per stage (each MMA lane wait covers this many)
+#endif
+constexpr int kDecKB = SC_DECPROJ_KB;
+static_assert(kDecKB == 1 || kDecKB == 2 || kDecKB == 4, "1, 2 or 4 K blocks per stage");
+constexpr uint32_t kDecBSub = 3 * kDecBoxCh * kPBK * 2;               // B, C, x rows of a block
+constexpr uint32_t kDecStage = kDecKB * (kPABytes + kDecBSub);      // [A blocks][B blocks]
 #ifndef SC_DECPROJ_STAGES
-#define SC_DECPROJ_STAGES (kDecCh == 32 ? 8 : 7)
+#define SC_DECPROJ_STAGES ((232448 - 2048) / (int)kDecStage < 8 ? (232448 - 2048) / (int)kDecStage : 8)
 #endif
 constexpr int kDecStages = SC_DECPROJ_STAGES;
 constexpr int kDecEpiWarps = 8;                     // two per TMEM lane quarter
@@ -735,12 +741,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     PipeState *ps = reinterpret_cast<PipeState *>(base + (size_t)kDecStages * kDecStage);
     const uint32_t stages = smem_addr(base);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nk = D / kPBK;
+    const int nk = D / kPBK;                        // 64-deep K blocks
+    const int ns = (nk + kDecKB - 1) / kDecKB;      // stages per tile
     const uint32_t tmem = pipe_start<CL>(ps, &map_h, &map_w3, kDecEpiWarps);
     const TileWalk tw = tile_walk<CL>(n_mtiles, n_ctiles);
 
     if (warp == 0) {
-        // One A box and one [3 sections][kDecBoxCh channels][64 K] box per stage.
+        // Per K block one A box and one [3 sections][kDecBoxCh channels][64 K]
+        // box; a stage holds kDecKB blocks (fewer in the last stage when nk is odd).
         if (lane == 0) {
             const bool leader = tw.rank == 0;
             uint32_t g = 0;
@@ -749,7 +757,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 int mt, ct;
                 tw.at(grp, n_ctiles, mt, ct);
                 const int a_row = mt * kPBM, ch = ct * kDecCh + kDecBoxCh * tw.rank;
-                for (int kb = 0; kb < nk; ++kb, ++g) {
+                for (int si = 0; si < ns; ++si, ++g) {
                     const uint32_t s = g % kDecStages;
                     if (g >= kDecStages &&
                         !mbar_wait_bounded(&ps->empty[s], (g / kDecStages - 1) & 1u)) {
@@ -759,15 +767,25 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                         break;
                     }
                     const uint32_t st = stages + s * kDecStage;
+                    const int nb = min(kDecKB, nk - si * kDecKB);  // K blocks in this stage
+                    const uint32_t bytes = (uint32_t)nb * (kPABytes + kDecBSub);
                     if constexpr (CL == 1) {
-                        mbar_arrive_expect_tx(&ps->full[s], kDecStage);
-                        tma_load_2d(st, &map_h, &ps->full[s], kb * kPBK, a_row);
-                        tma_load_3d(st + kPABytes, &map_w3, &ps->full[s], kb * kPBK, ch, 0);
+                        mbar_arrive_expect_tx(&ps->full[s], bytes);
+                        for (int b = 0; b < nb; ++b) {
+                            const int kx = (si * kDecKB + b) * kPBK;
+                            tma_load_2d(st + b * kPABytes, &map_h, &ps->full[s], kx, a_row);
+                            tma_load_3d(st + kDecKB * kPABytes + b * kDecBSub, &map_w3,
+                                        &ps->full[s], kx, ch, 0);
+                        }
                     } else {
                         const uint32_t bar = cluster_map(smem_addr(&ps->full[s]), 0);
-                        if (leader) mbar_arrive_expect_tx(&ps->full[s], 2 * kDecStage);
-                        tma_load_2d_pair(st, &map_h, bar, kb * kPBK, a_row);
-                        tma_load_3d_pair(st + kPABytes, &map_w3, bar, kb * kPBK, ch, 0);
+                        if (leader) mbar_arrive_expect_tx(&ps->full[s], 2 * bytes);
+                        for (int b = 0; b < nb; ++b) {
+                            const int kx = (si * kDecKB + b) * kPBK;
+                            tma_load_2d_pair(st + b * kPABytes, &map_h, bar, kx, a_row);
+                            tma_load_3d_pair(st + kDecKB * kPABytes + b * kDecBSub, &map_w3, bar,
+                                             kx, ch, 0);
+                        }
                     }
                 }
             }
@@ -779,9 +797,63 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     mbar_wait_bounded(&ps->empty[c % kDecStages], (c / kDecStages) & 1u);
         }
     } else if (warp == 1) {
-        if (lane == 0 && tw.rank == 0)
-            mma_tiles<kDecStages, kDecN, 0, CL, kDecBufs, kDecN, kDecBufStride>(
-                tmem, stages, kDecStage, ps, nk, tw);
+        // One lane of the (leader) CTA: per stage, per K block, 4 MMAs of N = kDecN
+        // into accumulator buffer it % 2 (as mma_tiles, with kDecKB blocks a stage).
+        if (lane == 0 && tw.rank == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kPBM * CL, kDecN);
+            uint32_t g = 0;
+            int it = 0;
+            bool ok = true;
+            for (int grp = tw.first; grp < tw.n_groups && ok; grp += tw.step, ++it) {
+                const int b = it % kDecBufs, use = it / kDecBufs;
+                if (use >= 1 && !mbar_wait_bounded(&ps->tempty[b], (uint32_t)(use - 1) & 1u)) {
+                    raise_error(SC_DEV_TIMEOUT);
+                    ps->abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)b * (uint32_t)kDecBufStride;
+                for (int si = 0; si < ns; ++si, ++g) {
+                    const uint32_t s = g % kDecStages;
+                    if (!mbar_wait_bounded(&ps->full[s], (g / kDecStages) & 1u)) {
+                        raise_error(SC_DEV_TIMEOUT);
+                        ps->abort = 1;
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = stages + s * kDecStage;
+                    const int nb = min(kDecKB, nk - si * kDecKB);
+                    for (int kb = 0; kb < nb; ++kb) {
+                        const uint64_t da = sdesc_k128(st + kb * kPABytes);
+                        const uint64_t db = sdesc_k128(st + kDecKB * kPABytes + kb * kDecBSub);
+#pragma unroll
+                        for (int j = 0; j < kPBK / 16; ++j) {
+                            const uint32_t acc = (si | kb | j) != 0;
+                            if constexpr (CL == 1)
+                                mma_bf16(d, da + 2 * j, db + 2 * j, idesc, acc);
+                            else
+                                mma_bf16_pair(d, da + 2 * j, db + 2 * j, idesc, acc);
+                        }
+                    }
+                    if constexpr (CL == 1)
+                        mma_commit(&ps->empty[s]);
+                    else
+                        mma_commit_pair(&ps->empty[s], 3);
+                }
+                if (ok) {
+                    if constexpr (CL == 1)
+                        mma_commit(&ps->tfull[b]);
+                    else
+                        mma_commit_pair(&ps->tfull[b], 3);
+                }
+            }
+            if constexpr (CL == 1)
+                mma_commit(&ps->mma_done);
+            else
+                mma_commit_pair(&ps->mma_done, 1);
+            mbar_wait_bounded(&ps->mma_done, 0);
+        }
         __syncwarp();
     } else {
         const int q = warp & 3;                          // TMEM lane quarter
