@@ -676,8 +676,9 @@ __global__ void __launch_bounds__(256)
 // of kDecCh channels for 128 sequences with one N = 3 kDecCh MMA per 16-deep
 // K step. With w_in seen as [3][H][D] (a 3-D tensor map), the B, C and x rows
 // of the tile's channels come with one copy per stage, so TMEM columns hold
-// [B | C | x]. Two accumulator buffers let a CTA's next tile's MMAs overlap
-// this tile's epilogue. Narrow tiles put every SM to work at a serving batch
+// [B | C | x]. A stage holds kDecKB such K blocks, so the MMA lane waits and
+// commits once per 4 kDecKB MMAs. Two accumulator buffers let a CTA's next
+// tile's MMAs overlap this tile's epilogue. Narrow tiles put every SM to work at a serving batch
 // (256 sequences, H = 2048, 32 channels: 128 tiles). Each MMA carries a
 // fixed cost, so single CTAs, each issuing its own MMAs, beat CTA pairs
 // (one MMA stream per two SMs) here; pairs (M = 256, each CTA staging its
