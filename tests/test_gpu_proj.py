@@ -409,6 +409,48 @@ def test_graph_captured_projections_match_eager_calls():
     assert sc.get_error() == 0
 
 
+def test_graph_captured_decode_steps_match_eager_calls():
+    """Three fused decode steps (in_proj + decode, one token per sequence)
+    captured in one CUDA graph give the bits of eager calls."""
+    rng = np.random.default_rng(906)
+    c = make_decode_case(rng, 200, 256, 128, 3)
+    tokens = [dyadic(rng, (200, 256), 8, -3) for _ in range(3)]
+
+    def run(graph: bool):
+        pool = dev(c["pool"], "bf16")
+        w_in, w, slots = dev(c["w_in"], "bf16"), dev(c["w"], "bf16"), dev(c["slots"], "i32")
+        hs = [dev(t, "bf16") for t in tokens]
+        ys = [torch.empty((200, 128), dtype=torch.bfloat16, device="cuda") for _ in hs]
+
+        def body():
+            for h, y in zip(hs, ys):
+                sc.in_proj_decode(h, w_in, w, slots, pool, y=y)
+
+        if graph:
+            side = torch.cuda.Stream()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g, stream=side):
+                    body()
+            g.replay()
+        else:
+            body()
+        torch.cuda.synchronize()
+        return [host(t) for t in ys + [pool]]
+
+    eager, graphed = run(False), run(True)
+    for a, b in zip(eager, graphed):
+        assert_bits(b, a, "graph vs eager")
+    # and the three steps against the oracle, token by token
+    ref = c["pool"].copy()
+    for t, got in zip(tokens, eager[:3]):
+        st, y_ref = layer.in_proj_decode("bf16", t, c["w_in"], c["w"], c["slots"], ref)
+        assert st == oracle.OK
+        assert_close("bf16", got, y_ref, "y")
+    assert_bits(eager[3], ref, "pool")
+    assert sc.get_error() == 0
+
+
 def test_more_sequences_than_staged_in_shared_memory():
     """600 sequences (more than the 512 cu_seqlens entries staged in shared
     memory): the epilogue looks rows up in global memory."""
