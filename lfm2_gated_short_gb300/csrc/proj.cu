@@ -19,8 +19,9 @@
 // each sequence to a workspace, and k_commit_states (next in the stream)
 // writes the new states: no tile writes a slot another tile reads.
 //
-// k_out_proj is the plain out_proj GEMM (128 x 256 tiles) on the same
-// mainloop, with a store epilogue.
+// k_out_proj is the plain out_proj GEMM (256 x 256 tiles a pair) on the same
+// mainloop; its epilogue rounds to bf16 into swizzled shared-memory boxes
+// that TMA copies store.
 //
 // Warp roles: warp 0 issues the TMA copies, warp 1 owns the TMEM allocation
 // and one of its lanes issues the MMAs, the other warps run the epilogue
@@ -99,7 +100,13 @@ constexpr int kOutN = 256;                    // out_proj N per tile
 constexpr int kOutBoxRows = kOutN / kPCluster;
 constexpr uint32_t kOutBox = kOutBoxRows * kPBK * 2;
 constexpr uint32_t kOutStage = kPABytes + kOutBox;  // 48 KB single, 32 KB a pair CTA
-
+// out_proj's store staging: per epilogue warp two boxes of 32 rows x 64
+// columns (128-byte swizzle), filled from TMEM and written by TMA stores.
+constexpr uint32_t kOutStgBox = 32 * kPBK * 2;  // 4 KB
+constexpr uint32_t kOutStg = 4 * 2 * kOutStgBox;  // 32 KB
+constexpr int kOutBoxes = kOutN / kPBK;           // boxes of a warp's tile rows
+static_assert(4u * kOutBoxes * kOutStgBox <= (uint32_t)kOutStages * kOutStage,
+              "the stage ring holds a whole tile's boxes");
 // Shared memory after the stage ring: barriers and flags. The accumulator
 // is double-buffered in TMEM (columns 0.. and 256..): the MMA lane fills one
 // buffer while the epilogue warps drain the other.
@@ -121,7 +128,7 @@ constexpr size_t conv_smem_bytes() {
     return 1024 + (size_t)kInStages * kConvStage + kConvExtra + sizeof(PipeState);
 }
 constexpr size_t out_smem_bytes() {
-    return 1024 + (size_t)kOutStages * kOutStage + sizeof(PipeState);
+    return 1024 + (size_t)kOutStages * kOutStage + kOutStg + sizeof(PipeState);
 }
 static_assert(conv_smem_bytes() <= 232448 && out_smem_bytes() <= 232448,
               "stage ring larger than a CTA's shared memory");
@@ -981,11 +988,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 template <int CL>
 __global__ void __launch_bounds__(kOutThreads, 1)
     k_out_proj(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-               int64_t M_rows, int Kdim, int N_cols, bf16 *__restrict__ out, int n_ntiles,
-               int n_mtiles) {
+               const __grid_constant__ CUtensorMap map_o, int Kdim, int n_ntiles, int n_mtiles) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = align1024(smem_raw);
-    PipeState *ps = reinterpret_cast<PipeState *>(base + (size_t)kOutStages * kOutStage);
+    unsigned char *stg_all = base + (size_t)kOutStages * kOutStage;
+    PipeState *ps = reinterpret_cast<PipeState *>(stg_all + kOutStg);
     const uint32_t stages = smem_addr(base);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = Kdim / kPBK;
@@ -1005,32 +1012,67 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             mma_tiles<kOutStages, kOutN, 0, CL, kOutBufs>(tmem, stages, kOutStage, ps, nk, tw);
         __syncwarp();
     } else {
+        // Warp q drains TMEM lanes 32q .. 32q + 31 (tile rows) in boxes of 64
+        // columns: rounded to bf16 into a staging box and stored by lane 0
+        // with a TMA copy (rows past the end are not written). Boxes alternate
+        // between the warp's two staging boxes, except in the CTA's last tile:
+        // its MMAs have consumed every stage and no load follows, so the
+        // stage ring holds all of its boxes and no store waits for another.
+        if (lane == 0) tma_prefetch_map(&map_o);
         const int q = warp & 3;
+        unsigned char *stg = stg_all + (size_t)q * 2 * kOutStgBox;
+        unsigned char *ring = base + (size_t)q * kOutBoxes * kOutStgBox;
+        uint32_t nbox = 0;  // staging boxes this warp has filled
         int it = 0;
         for (int grp = tw.first; grp < tw.n_groups; grp += tw.step, ++it) {
             int mt, nt;
             tw.at(grp, n_ntiles, mt, nt);
-            const int64_t t = (int64_t)mt * kPBM + q * 32 + lane;  // past M_rows: no store
+            const int row0 = mt * kPBM + q * 32;
             const int col0 = nt * kOutN;
+            const bool last = grp + tw.step >= tw.n_groups;
             if (!epi_acquire<kOutBufs>(ps, it, 128)) break;
             const uint32_t trow =
                 tmem + (uint32_t)(it % kOutBufs) * 256u + ((uint32_t)(q * 32) << 16);
-            const bool store = t < M_rows;
 #pragma unroll 1
-            for (int cc = 0; cc < kOutN / 16; ++cc) {
+            for (int bx = 0; bx < kOutBoxes; ++bx) {
+                uint32_t r[4][16];
                 __syncwarp();
-                float v[16];
-                tmem_ld16(trow + cc * 16, v);
-                if (!store) continue;
-                uint32_t pk[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) pk[j] = pack_bf16(v[2 * j], v[2 * j + 1]);
-                uint4 *dst = reinterpret_cast<uint4 *>(out + t * (int64_t)N_cols + col0 + cc * 16);
-                gst(dst, make_uint4(pk[0], pk[1], pk[2], pk[3]));
-                gst(dst + 1, make_uint4(pk[4], pk[5], pk[6], pk[7]));
+                for (int i = 0; i < 4; ++i) tmem_ld16_nowait(trow + bx * kPBK + i * 16, r[i]);
+                unsigned char *buf;
+                if (last) {
+                    buf = ring + (size_t)bx * kOutStgBox;
+                } else {
+                    buf = stg + (nbox++ & 1u) * kOutStgBox;
+                    if (lane == 0) bulk_wait_read<1>();  // the store that last read buf is done
+                }
+                __syncwarp();
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) tmem_regs_ready(r[i]);
+                // Row `lane` of the box: 16-byte chunk j (columns 8j .. 8j + 7)
+                // goes to chunk position j ^ (row % 8) of the row's 128 bytes.
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t *v = &r[j >> 1][(j & 1) * 8];
+                    uint4 pk;
+                    pk.x = pack_bf16(__uint_as_float(v[0]), __uint_as_float(v[1]));
+                    pk.y = pack_bf16(__uint_as_float(v[2]), __uint_as_float(v[3]));
+                    pk.z = pack_bf16(__uint_as_float(v[4]), __uint_as_float(v[5]));
+                    pk.w = pack_bf16(__uint_as_float(v[6]), __uint_as_float(v[7]));
+                    *reinterpret_cast<uint4 *>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = pk;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&map_o, smem_addr(buf), col0 + bx * kPBK, row0);
+                    bulk_commit();
+                }
             }
             epi_release<CL, kOutBufs>(ps, it, tw.rank);
         }
+        if (lane == 0) bulk_wait_read<0>();  // staging stays valid until every store has read it
+        __syncwarp();
     }
     pipe_finish<CL>(tmem);
 }
@@ -1056,8 +1098,9 @@ static EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-// A row-major bf16 matrix [outer, inner] read in {64, box_rows} boxes with
-// the 128-byte swizzle; rows past the end (or before row 0) read as zeros.
+// A row-major bf16 matrix [outer, inner] copied in {64, box_rows} boxes with
+// the 128-byte swizzle; a load reads rows past the end (or before row 0) as
+// zeros, a store leaves them unwritten.
 static cudaError_t map_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer,
                           uint32_t box_rows) {
     EncodeTiledFn fn = encode_tiled();
@@ -1241,10 +1284,12 @@ cudaError_t launch_in_proj_decode(int D, int H, int K, const void *hidden, int N
 cudaError_t launch_out_proj(int H, int D, const void *y, int64_t T, const void *w_out, void *out,
                             int sm_count, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mo;
     cudaError_t e = map_2d(&ma, y, (uint64_t)H, (uint64_t)T, kPBM);
     if (e != cudaSuccess) return e;
     e = map_2d(&mb, w_out, (uint64_t)H, (uint64_t)D, kOutBoxRows);
+    if (e != cudaSuccess) return e;
+    e = map_2d(&mo, out, (uint64_t)D, (uint64_t)T, 32);
     if (e != cudaSuccess) return e;
     auto kern = k_out_proj<kPCluster>;
     static std::atomic<unsigned long long> done{0};
@@ -1259,8 +1304,7 @@ cudaError_t launch_out_proj(int H, int D, const void *y, int64_t T, const void *
     const int64_t groups = (n_mtiles + kPCluster - 1) / kPCluster * n_ntiles;
     const int grid = kPCluster * (int)(groups < clusters ? groups : clusters);  // persistent
     return launch_pdl_cluster(kern, dim3((unsigned)grid), dim3(kOutThreads), out_smem_bytes(),
-                              stream, kPCluster, ma, mb, T, H, D, (bf16 *)out, n_ntiles,
-                              (int)n_mtiles);
+                              stream, kPCluster, ma, mb, mo, H, n_ntiles, (int)n_mtiles);
 }
 
 cudaError_t take_error_proj(cudaStream_t stream, unsigned int *code) {

@@ -338,9 +338,8 @@ def test_out_proj_lfm2_shape_sampled_columns():
 
 @pytest.mark.parametrize("T,H,D", [(1000, 64, 768), (513, 128, 256), (4133, 2048, 2048)])
 def test_out_proj_every_column_on_sampled_rows(T, H, D):
-    """Every output column (the balanced schedule cuts the columns into
-    ranges and pieces of any multiple of 16), on sampled rows including the
-    first and the last ones."""
+    """Every output column, on sampled rows including the first and the last
+    ones."""
     rng = np.random.default_rng(896 + T)
     y = dyadic(rng, (T, H), 8, -3)
     wo = dyadic(rng, (D, H), 8, -6)
