@@ -338,8 +338,10 @@ sc_status shortconv_backward_noalloc(sc_dtype dtype, int H, int K, const void *b
  *   workspace    device scratch of at least
  *                shortconv_in_proj_workspace_bytes(H, K, N) bytes, 16-byte
  *                aligned, owned by the caller (the last K values of u per
- *                sequence, from which the slots' new states are written
- *                after all rows are done)
+ *                sequence, from which a second pass writes the slots' new
+ *                states after all rows are done; a call with one sequence
+ *                usually writes its state in the fused pass and leaves the
+ *                workspace untouched)
  * Device errors: as shortconv_prefill, plus SC_DEV_TIMEOUT (a bounded wait
  * on a tensor copy or on the tensor cores gave up; output incomplete).
  */

@@ -17,7 +17,10 @@
 // A tile holding a sequence's first rows reads the slot; another tile may
 // hold its last rows. So the fused kernel writes the last K values of u of
 // each sequence to a workspace, and k_commit_states (next in the stream)
-// writes the new states: no tile writes a slot another tile reads.
+// writes the new states: no tile writes a slot another tile reads. A call
+// with one sequence skips that pass: its walk gives each column's first and
+// last row tiles to one cluster, and the CTA with the last one writes the
+// new state after the cluster's final barrier (see TileWalk::group).
 //
 // k_out_proj is the plain out_proj GEMM (256 x 256 tiles a pair) on the same
 // mainloop; its epilogue rounds to bf16 into swizzled shared-memory boxes
@@ -147,21 +150,46 @@ static_assert(kInStages <= kMaxStages && kOutStages <= kMaxStages, "too many sta
 
 struct TileWalk {
     int first, step, n_groups, rank, CL;
-    // Row tile and column tile of the group's tile for this CTA.
-    __device__ __forceinline__ void at(int grp, int n_col_tiles, int &mt, int &ct) const {
+    int single_cols, pairs;  // single-sequence schedule: column tiles (0: off), row-tile pairs
+
+    // Single-sequence schedule of the fused prefill (one sequence over several
+    // row-tile pairs): walk position i -> tile group. Positions 0 .. C-1 take
+    // each column's first pair, and the last position of each of those
+    // clusters takes the same column's last pair: the cluster that reads a
+    // column's old state (its first rows) also writes the new one (its last
+    // rows), after all of its other tiles. The other positions take the
+    // middle pairs in order. Needs C <= clusters and n_groups >= clusters + C.
+    __device__ __forceinline__ int group(int i) const {
+        const int C = single_cols;
+        if (i < C) return i;
+        const int L0 = (n_groups - 1) / step, r0 = (n_groups - 1) % step;
+        auto last_of = [&](int c) { return c + step * (c <= r0 ? L0 : L0 - 1); };
+        const int c = i % step;
+        if (c < C && i == last_of(c)) return (pairs - 1) * C + c;
+        int below = C;  // special positions before i
+        for (int k = 0; k < C; ++k) below += last_of(k) < i ? 1 : 0;
+        return C + (i - below);
+    }
+    // Row tile and column tile of the tile at walk position pos for this CTA.
+    __device__ __forceinline__ void at(int pos, int n_col_tiles, int &mt, int &ct) const {
+        const int grp = single_cols ? group(pos) : pos;
         ct = grp % n_col_tiles;
         mt = (grp / n_col_tiles) * CL + rank;
     }
 };
 
 template <int CL>
-__device__ __forceinline__ TileWalk tile_walk(int n_row_tiles, int n_col_tiles) {
+__device__ __forceinline__ TileWalk tile_walk(int n_row_tiles, int n_col_tiles,
+                                              bool single = false) {
     TileWalk w;
     w.CL = CL;
     w.rank = CL > 1 ? (int)cluster_ctarank() : 0;
     w.first = blockIdx.x / CL;
     w.step = gridDim.x / CL;
-    w.n_groups = (n_row_tiles + CL - 1) / CL * n_col_tiles;
+    w.pairs = (n_row_tiles + CL - 1) / CL;
+    w.n_groups = w.pairs * n_col_tiles;
+    // With one pair every group is its column's first and last: no reordering.
+    w.single_cols = single && w.pairs > 1 ? n_col_tiles : 0;
     return w;
 }
 
@@ -389,8 +417,9 @@ __global__ void __launch_bounds__(kInThreads, 1)
     k_in_proj_conv(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
                    int64_t T_rows, int D, int H, const bf16 *__restrict__ w,
                    const bf16 *__restrict__ bias, const int32_t *__restrict__ cu, int N,
-                   const int32_t *__restrict__ slots, const bf16 *__restrict__ pool, int n_slots,
-                   bf16 *__restrict__ y, bf16 *__restrict__ tail, int n_ctiles, int n_mtiles) {
+                   const int32_t *__restrict__ slots, bf16 *__restrict__ pool, int n_slots,
+                   bf16 *__restrict__ y, bf16 *__restrict__ tail, int n_ctiles, int n_mtiles,
+                   int single) {
     constexpr int OUT = kPBM - (K - 1);  // output rows per tile
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = align1024(smem_raw);
@@ -403,7 +432,10 @@ __global__ void __launch_bounds__(kInThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = D / kPBK;
     const uint32_t tmem = pipe_start<CL>(ps, &map_h, &map_w, kInEpiWarps);
-    const TileWalk tw = tile_walk<CL>(n_mtiles, n_ctiles);
+    const TileWalk tw = tile_walk<CL>(n_mtiles, n_ctiles, single != 0);
+    // Single-sequence schedule: the CTA's last tile, and whether every tile ran.
+    int fin_mt = -1, fin_ct = 0;
+    bool fin_ok = false;
 
     if (warp == 0) {
         auto conv_coords = [&](int mt, int ct, int &a_row, int (&rows)[3]) {
@@ -450,9 +482,12 @@ __global__ void __launch_bounds__(kInThreads, 1)
         unsigned char *urow = u_tile + r * kUStride;
 
         int it = 0;
+        bool all = true;
         for (int grp = tw.first; grp < tw.n_groups; grp += tw.step, ++it) {
             int mt, ct;
             tw.at(grp, n_ctiles, mt, ct);
+            fin_mt = mt;
+            fin_ct = ct;
             const int h0 = ct * kConvCh;
             const int64_t t = (int64_t)mt * OUT - (K - 1) + r;  // global row (past T: no output)
             // This tile's taps (tap-major: wts[k * 64 + c]) and bias; the previous
@@ -465,7 +500,10 @@ __global__ void __launch_bounds__(kInThreads, 1)
             if (bias != nullptr)
                 for (int e = et; e < kConvCh; e += kInEpiThreads)
                     bsm[e] = h0 + e < H ? __bfloat162float(gld(bias + h0 + e)) : 0.f;
-            if (!epi_acquire<kInBufs>(ps, it, kInEpiThreads)) break;
+            if (!epi_acquire<kInBufs>(ps, it, kInEpiThreads)) {
+                all = false;
+                break;
+            }
             const uint32_t trow =
                 tmem + (uint32_t)(it % kInBufs) * 256u + ((uint32_t)(q * 32) << 16) + cw;
 
@@ -588,7 +626,7 @@ __global__ void __launch_bounds__(kInThreads, 1)
                     }
                     gst(reinterpret_cast<uint4 *>(y + t * (int64_t)H + h0 + c0),
                         make_uint4(pk[0], pk[1], pk[2], pk[3]));
-                    if (t >= s1 - K) {  // one of the sequence's last K rows: its u to the tail
+                    if (!single && t >= s1 - K) {  // one of the sequence's last K rows: its u to the tail
                         const int m = (int)(K - (s1 - t));
                         const uint16_t *ur = reinterpret_cast<const uint16_t *>(urow + c0 * 2);
                         uint16_t *tl = reinterpret_cast<uint16_t *>(tail);
@@ -600,8 +638,38 @@ __global__ void __launch_bounds__(kInThreads, 1)
             }
             named_sync(1, kInEpiThreads);  // u_tile, taps and bias free for the next tile
         }
+        fin_ok = all && !bad;
     }
     pipe_finish<CL>(tmem);
+
+    // Single-sequence schedule: the CTA that ran the sequence's last row tile
+    // (its last tile, so u_tile still holds it) writes the new state of the
+    // tile's channels: the last K entries of [old state; u]. The cluster
+    // barrier in pipe_finish ordered every read of the old state (the
+    // column's first row tile, in this cluster) before these writes.
+    if (single && warp >= 2 && fin_ok && fin_mt == n_mtiles - 1) {
+        const int et = threadIdx.x - 64;
+        const int h0 = fin_ct * kConvCh;
+        const int32_t slot = gld(slots);
+        const int64_t row0 = (int64_t)fin_mt * OUT - (K - 1);  // global row of tile row 0
+        if (slot < 0 || slot >= n_slots) {
+            if (et == 0) raise_error(SC_DEV_BAD_SLOT);
+        } else {
+            for (int c = et; c < kConvCh && h0 + c < H; c += kInEpiThreads) {
+                bf16 *dst = pool + ((int64_t)slot * H + h0 + c) * K;
+                bf16 nv[K];
+#pragma unroll
+                for (int m = 0; m < K; ++m) {
+                    const int64_t e = T_rows + m;  // index into [old state; u_0 .. u_{T-1}]
+                    nv[m] = e < K ? gld(dst + e)
+                                  : *reinterpret_cast<const bf16 *>(
+                                        u_tile + (e - K - row0) * kUStride + c * 2);
+                }
+#pragma unroll
+                for (int m = 0; m < K; ++m) gst(dst + m, nv[m]);
+            }
+        }
+    }
 }
 
 // New state of sequence i = the last K entries of [old state; u of its rows]:
@@ -1190,6 +1258,7 @@ static cudaError_t in_proj_inst(const CUtensorMap &mh, const CUtensorMap &mw, in
                                 void *tail, int sm_count, cudaStream_t stream) {
     constexpr int OUT = kPBM - (K - 1);
     cudaError_t e;
+    bool single = false;  // one sequence: the fused kernel writes its new state itself
     if (T > 0) {
         auto kern = k_in_proj_conv<K, kPCluster>;
         static std::atomic<unsigned long long> done{0};
@@ -1201,14 +1270,20 @@ static cudaError_t in_proj_inst(const CUtensorMap &mh, const CUtensorMap &mw, in
         if (e != cudaSuccess) return e;
         const int n_ctiles = (H + kConvCh - 1) / kConvCh;  // the last may be half full
         const int64_t n_mtiles = (T + OUT - 1) / OUT;
-        const int64_t groups = (n_mtiles + kPCluster - 1) / kPCluster * n_ctiles;
+        const int64_t pairs = (n_mtiles + kPCluster - 1) / kPCluster;
+        const int64_t groups = pairs * n_ctiles;
         const int grid = kPCluster * (int)(groups < clusters ? groups : clusters);  // persistent
+        // The single-sequence walk needs every column's first and last pair in
+        // one cluster, the last one being that cluster's last tile.
+        single = N == 1 && n_ctiles <= clusters &&
+                 (pairs == 1 || groups >= (int64_t)clusters + n_ctiles);
         e = launch_pdl_cluster(kern, dim3((unsigned)grid), dim3(kInThreads), conv_smem_bytes(),
                                stream, kPCluster, mh, mw, T, D, H, (const bf16 *)w,
-                               (const bf16 *)bias, cu, N, slots, (const bf16 *)pool, n_slots,
-                               (bf16 *)y, (bf16 *)tail, n_ctiles, (int)n_mtiles);
+                               (const bf16 *)bias, cu, N, slots, (bf16 *)pool, n_slots,
+                               (bf16 *)y, (bf16 *)tail, n_ctiles, (int)n_mtiles, single ? 1 : 0);
         if (e != cudaSuccess) return e;
     }
+    if (single) return cudaSuccess;  // no commit pass
     const int64_t units = (int64_t)N * (H / kCh);
     if (units == 0) return cudaSuccess;
     return launch_pdl(k_commit_states<K>, dim3((unsigned)((units + 255) / 256)), dim3(256), 0,

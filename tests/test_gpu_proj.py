@@ -138,6 +138,107 @@ def test_lfm2_shape_T4096_D2048_H2048_sampled_channels():
     assert_bits(pool[:, ch], pool_ref, "pool")
 
 
+# One sequence per call: when the tile groups allow it (every column's first
+# and last row-tile pairs in one cluster, on the 76 pairs of this device), the
+# fused kernel writes the new state itself after its cluster's last tile and
+# no commit pass runs; otherwise the workspace and the commit pass do it.
+# (T, D, H, K): one row tile; two row tiles on the two CTAs of one pair;
+# T < K; T = K; two pairs and one column (too few groups: commit pass); many
+# pairs of one column; of two columns, the second half full; LFM2's width.
+SINGLE_CASES = [(50, 64, 64, 3), (200, 128, 128, 3), (1, 64, 128, 3), (2, 64, 64, 4),
+                (3, 64, 64, 3), (300, 64, 128, 3), (20000, 64, 128, 3), (12000, 128, 192, 2),
+                (12000, 64, 192, 1), (9000, 64, 128, 4), (4096, 2048, 2048, 3)]
+
+
+@pytest.mark.parametrize("T,D,H,K", SINGLE_CASES)
+def test_single_sequence_from_a_random_state(T, D, H, K):
+    rng = np.random.default_rng(860 + T + D + H + K)
+    c = make_case(rng, [T], D, H, K, extra_slots=3)
+    bias = oracle.round_bf16(rng.standard_normal(H) * 0.5) if T % 2 == 0 else None
+    y, pool = run_gpu(c, bias)
+    assert sc.get_error() == 0
+    if H > 256:  # the oracle on 64 channels (channels are independent)
+        ch = np.sort(np.concatenate([[0, 127, 128, H - 1], rng.choice(np.arange(1, H - 1), 60,
+                                                                      replace=False)]))
+        rows = np.concatenate([ch, H + ch, 2 * H + ch])
+        sub = dict(c, w_in=c["w_in"][rows], w=np.ascontiguousarray(c["w"][ch]),
+                   pool=np.ascontiguousarray(c["pool"][:, ch]), H=len(ch))
+        y_ref, pool_ref = run_oracle(sub, None if bias is None else bias[ch])
+        y, pool = y[:, ch], pool[:, ch]
+    else:
+        y_ref, pool_ref = run_oracle(c, bias)
+    assert_bits(pool, pool_ref, "pool (new state bit-exact, other slots unchanged)")
+    assert_close("bf16", y, y_ref, "y")
+
+
+@pytest.mark.parametrize("H,splits", [(128, [7000, 1, 2, 13000]), (192, [5000, 11000])])
+def test_single_sequence_continued_over_calls(H, splits):
+    """A sequence prefilled in pieces, one call per piece (each call carries
+    its state to the next through the slot), equals the oracle on the whole
+    sequence: y piece by piece, and the final state."""
+    rng = np.random.default_rng(870 + H)
+    D, K = 64, 3
+    T = sum(splits)
+    c = make_case(rng, [T], D, H, K, extra_slots=2)
+    pool = dev(c["pool"], "bf16")
+    w_in, w, slot = dev(c["w_in"], "bf16"), dev(c["w"], "bf16"), dev(c["slots"], "i32")
+    ys, t0 = [], 0
+    for n in splits:
+        cu = dev(np.array([0, n], np.int32), "i32")
+        ys.append(host(sc.in_proj_prefill(dev(c["hidden"][t0:t0 + n], "bf16"), w_in, w, cu,
+                                          slot, pool)))
+        t0 += n
+    torch.cuda.synchronize()
+    assert sc.get_error() == 0
+    y_ref, pool_ref = run_oracle(c)
+    assert_bits(host(pool), pool_ref, "pool after the last piece")
+    assert_close("bf16", np.concatenate(ys), y_ref, "y")
+
+
+def test_single_sequence_calls_in_a_cuda_graph():
+    """Two single-sequence fused prefills of one slot, captured in a CUDA
+    graph and replayed twice, give the bits of the same calls made eagerly."""
+    rng = np.random.default_rng(875)
+    D, H, K = 64, 128, 3
+    c1 = make_case(rng, [20000], D, H, K, extra_slots=1)
+    h2 = dyadic(rng, (9000, D), 8, -3)
+
+    def run(graph: bool):
+        pool = dev(c1["pool"], "bf16")
+        w_in, w, slot = dev(c1["w_in"], "bf16"), dev(c1["w"], "bf16"), dev(c1["slots"], "i32")
+        hs = [dev(c1["hidden"], "bf16"), dev(h2, "bf16")]
+        cus = [dev(np.array([0, len(h)], np.int32), "i32") for h in (c1["hidden"], h2)]
+        ys = [torch.empty((h.shape[0], H), dtype=torch.bfloat16, device="cuda") for h in hs]
+        ws = torch.empty(max(16, sc.in_proj_workspace_bytes(H, K, 1)), dtype=torch.uint8,
+                         device="cuda")
+
+        def body():
+            for h, cu, y in zip(hs, cus, ys):
+                sc.in_proj_prefill(h, w_in, w, cu, slot, pool, y=y, workspace=ws)
+
+        if graph:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g, stream=side):
+                    body()
+            g.replay()
+            g.replay()
+        else:
+            body()
+            body()
+        torch.cuda.synchronize()
+        return [host(y) for y in ys], host(pool)
+
+    ys_e, pool_e = run(False)
+    ys_g, pool_g = run(True)
+    for a, b in zip(ys_g, ys_e):
+        assert_bits(a, b, "y")
+    assert_bits(pool_g, pool_e, "pool")
+    assert sc.get_error() == 0
+
+
 def _ambiguous(exact, bound):
     """True where [exact - bound, exact + bound] holds a bf16 rounding boundary
     (rounding is monotone, so exactly where its two ends round apart)."""
