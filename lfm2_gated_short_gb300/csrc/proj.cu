@@ -96,6 +96,11 @@ constexpr int kInEpiWarps = SC_INPROJ_EPI_WARPS;
 constexpr int kInEpiThreads = 32 * kInEpiWarps;
 constexpr int kInThreads = 64 + kInEpiThreads;
 constexpr int kChPerWarp = kConvCh * 4 / kInEpiWarps;  // channels per epilogue warp
+constexpr uint32_t kInYBox = 32 * kPBK * 2;  // a y box: 32 rows x 64 channels, 4 KB
+#ifndef SC_INPROJ_YBOX
+#define SC_INPROJ_YBOX 1
+#endif
+constexpr bool kInYBoxed = SC_INPROJ_YBOX && kChPerWarp == kPBK;  // a warp's channels fill one y box
 constexpr int kChPass = 32;  // channels of one TMEM read pass (3 x 32 registers in flight)
 static_assert(kInEpiWarps == 4 || kInEpiWarps == 8, "4 or 8 epilogue warps");
 
@@ -136,6 +141,8 @@ constexpr size_t out_smem_bytes() {
 static_assert(conv_smem_bytes() <= 232448 && out_smem_bytes() <= 232448,
               "stage ring larger than a CTA's shared memory");
 static_assert(kInStages <= kMaxStages && kOutStages <= kMaxStages, "too many stages");
+static_assert(kInEpiWarps * kInYBox <= (uint32_t)kInStages * kConvStage,
+              "the stage ring holds every epilogue warp's y box");
 
 // ------------------------------------------------------------ persistent mainloop
 //
@@ -415,6 +422,7 @@ __device__ __forceinline__ void pipe_finish(uint32_t tmem) {
 template <int K, int CL>
 __global__ void __launch_bounds__(kInThreads, 1)
     k_in_proj_conv(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
+                   const __grid_constant__ CUtensorMap map_y,
                    int64_t T_rows, int D, int H, const bf16 *__restrict__ w,
                    const bf16 *__restrict__ bias, const int32_t *__restrict__ cu, int N,
                    const int32_t *__restrict__ slots, bf16 *__restrict__ pool, int n_slots,
@@ -480,6 +488,9 @@ __global__ void __launch_bounds__(kInThreads, 1)
         if (bad && blockIdx.x == 0 && et == 0) raise_error(SC_DEV_BAD_SEQLENS);
         auto CU = [&](int j) -> int64_t { return staged ? s_cu[j] : gld(cu + j); };
         unsigned char *urow = u_tile + r * kUStride;
+        // The last tile's y box of this warp (32 rows x 64 channels) in the stage ring.
+        unsigned char *ybox = base + (size_t)(warp - 2) * kInYBox;
+        if (et == 0) tma_prefetch_map(&map_y);
 
         int it = 0;
         bool all = true;
@@ -569,6 +580,14 @@ __global__ void __launch_bounds__(kInThreads, 1)
                     out_row = false;
                 }
             }
+            // The CTA's last tile: its MMAs have consumed every stage and no load
+            // follows, so the warp's 32 rows x 64 channels go out as one TMA box
+            // (128-byte swizzle) when each of its rows is an output row or past
+            // the end; a box with a history row (the previous tile's output) or a
+            // refused row takes the 16-byte stores.
+            const int64_t box_row = (int64_t)mt * OUT - (K - 1) + q * 32;
+            const bool boxed = kInYBoxed && grp + tw.step >= tw.n_groups && box_row >= 0 &&
+                               __all_sync(0xffffffffu, out_row || t >= T_rows);
             if (out_row) {
                 const bool fresh_hist = t - s0 >= K - 1;  // whole window inside the sequence
 #pragma unroll
@@ -624,8 +643,12 @@ __global__ void __launch_bounds__(kInThreads, 1)
                         }
                         pk[j / 2] = pack_bf16(o[0], o[1]);
                     }
-                    gst(reinterpret_cast<uint4 *>(y + t * (int64_t)H + h0 + c0),
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]));
+                    if (boxed)  // 16-byte chunk sc8 of row `lane`, at position sc8 ^ (lane % 8)
+                        *reinterpret_cast<uint4 *>(ybox + lane * 128 + ((sc8 ^ (lane & 7)) << 4)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    else
+                        gst(reinterpret_cast<uint4 *>(y + t * (int64_t)H + h0 + c0),
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]));
                     if (!single && t >= s1 - K) {  // one of the sequence's last K rows: its u to the tail
                         const int m = (int)(K - (s1 - t));
                         const uint16_t *ur = reinterpret_cast<const uint16_t *>(urow + c0 * 2);
@@ -636,8 +659,18 @@ __global__ void __launch_bounds__(kInThreads, 1)
                     }
                 }
             }
+            if (boxed) {  // rows past T and channels past H are not written
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&map_y, smem_addr(ybox), h0 + cw, (int)box_row);
+                    bulk_commit();
+                }
+            }
             named_sync(1, kInEpiThreads);  // u_tile, taps and bias free for the next tile
         }
+        if (lane == 0) bulk_wait_read<0>();  // the ring stays valid until the stores read it
+        __syncwarp();
         fin_ok = all && !bad;
     }
     pipe_finish<CL>(tmem);
@@ -1252,7 +1285,8 @@ static cudaError_t max_clusters(F kern, size_t smem, int threads, int sm_count,
 size_t in_proj_workspace_bytes(int H, int K, int N) { return (size_t)N * H * K * 2; }
 
 template <int K>
-static cudaError_t in_proj_inst(const CUtensorMap &mh, const CUtensorMap &mw, int64_t T, int D,
+static cudaError_t in_proj_inst(const CUtensorMap &mh, const CUtensorMap &mw, const CUtensorMap &my,
+                                int64_t T, int D,
                                 int H, const void *w, const void *bias, const int32_t *cu, int N,
                                 const int32_t *slots, void *pool, int n_slots, void *y,
                                 void *tail, int sm_count, cudaStream_t stream) {
@@ -1278,7 +1312,7 @@ static cudaError_t in_proj_inst(const CUtensorMap &mh, const CUtensorMap &mw, in
         single = N == 1 && n_ctiles <= clusters &&
                  (pairs == 1 || groups >= (int64_t)clusters + n_ctiles);
         e = launch_pdl_cluster(kern, dim3((unsigned)grid), dim3(kInThreads), conv_smem_bytes(),
-                               stream, kPCluster, mh, mw, T, D, H, (const bf16 *)w,
+                               stream, kPCluster, mh, mw, my, T, D, H, (const bf16 *)w,
                                (const bf16 *)bias, cu, N, slots, (bf16 *)pool, n_slots,
                                (bf16 *)y, (bf16 *)tail, n_ctiles, (int)n_mtiles, single ? 1 : 0);
         if (e != cudaSuccess) return e;
@@ -1296,18 +1330,20 @@ cudaError_t launch_in_proj_prefill(int D, int H, int K, const void *hidden, int6
                                    const int32_t *cu, int N, const int32_t *slots, void *pool,
                                    int n_slots, void *y, void *workspace, int sm_count,
                                    cudaStream_t stream) {
-    CUtensorMap mh, mw;
+    CUtensorMap mh, mw, my;
     if (T > 0) {
         cudaError_t e = map_2d(&mh, hidden, (uint64_t)D, (uint64_t)T, kPBM);
         if (e != cudaSuccess) return e;
         e = map_2d(&mw, w_in, (uint64_t)D, (uint64_t)3 * H, kConvBoxRows);
         if (e != cudaSuccess) return e;
+        e = map_2d(&my, y, (uint64_t)H, (uint64_t)T, 32);
+        if (e != cudaSuccess) return e;
     }
     switch (K) {
-        case 1: return in_proj_inst<1>(mh, mw, T, D, H, w, bias, cu, N, slots, pool, n_slots, y, workspace, sm_count, stream);
-        case 2: return in_proj_inst<2>(mh, mw, T, D, H, w, bias, cu, N, slots, pool, n_slots, y, workspace, sm_count, stream);
-        case 3: return in_proj_inst<3>(mh, mw, T, D, H, w, bias, cu, N, slots, pool, n_slots, y, workspace, sm_count, stream);
-        default: return in_proj_inst<4>(mh, mw, T, D, H, w, bias, cu, N, slots, pool, n_slots, y, workspace, sm_count, stream);
+        case 1: return in_proj_inst<1>(mh, mw, my, T, D, H, w, bias, cu, N, slots, pool, n_slots, y, workspace, sm_count, stream);
+        case 2: return in_proj_inst<2>(mh, mw, my, T, D, H, w, bias, cu, N, slots, pool, n_slots, y, workspace, sm_count, stream);
+        case 3: return in_proj_inst<3>(mh, mw, my, T, D, H, w, bias, cu, N, slots, pool, n_slots, y, workspace, sm_count, stream);
+        default: return in_proj_inst<4>(mh, mw, my, T, D, H, w, bias, cu, N, slots, pool, n_slots, y, workspace, sm_count, stream);
     }
 }
 
