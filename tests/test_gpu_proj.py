@@ -195,6 +195,25 @@ def test_single_sequence_continued_over_calls(H, splits):
     assert_close("bf16", np.concatenate(ys), y_ref, "y")
 
 
+@pytest.mark.parametrize("T", [50, 20000])
+def test_single_sequence_errors_write_nothing(T):
+    """One-sequence calls (with and without the reordered walk): lengths that
+    do not cover the rows, or a slot id out of range, report the error and
+    leave y and the whole pool as they were."""
+    rng = np.random.default_rng(880 + T)
+    D, H, K = 64, 128, 3
+    c = make_case(rng, [T], D, H, K, extra_slots=3)
+    for cu, slots, code in ((np.array([0, T - 1], np.int32), c["slots"], sc.DEV_BAD_SEQLENS),
+                            (c["cu"], np.array([10 ** 6], np.int32), sc.DEV_BAD_SLOT)):
+        pool = dev(c["pool"], "bf16")
+        y = torch.full((T, H), 3.0, dtype=torch.bfloat16, device="cuda")
+        sc.in_proj_prefill(dev(c["hidden"], "bf16"), dev(c["w_in"], "bf16"), dev(c["w"], "bf16"),
+                           dev(cu, "i32"), dev(slots, "i32"), pool, y=y)
+        assert sc.get_error() == code
+        assert np.all(host(y) == np.uint16(0x4040)), "y written"
+        assert_bits(host(pool), c["pool"], "pool")
+
+
 def test_single_sequence_calls_in_a_cuda_graph():
     """Two single-sequence fused prefills of one slot, captured in a CUDA
     graph and replayed twice, give the bits of the same calls made eagerly."""
