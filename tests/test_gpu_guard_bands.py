@@ -276,6 +276,36 @@ def test_in_proj_prefill_and_out_proj(D, H, K):
     assert sc.get_error() == 0
 
 
+@pytest.mark.parametrize("T,H", [(20000, 192), (200, 192)])
+def test_in_proj_prefill_one_sequence(T, H):
+    """One sequence: the fused call writes the new state itself, and its CTAs'
+    last tiles store y through TMA boxes (the upper half of the last
+    128-channel tile lies past H = 192 and must be clipped). Nothing outside
+    y and the slot's state changes."""
+    rng = np.random.default_rng(1870 + T)
+    D, K = 64, 3
+    hidden = _dyadic(rng, (T, D), 8, -3)
+    w_in = _dyadic(rng, (3 * H, D), 8, -6)
+    w = oracle.round_bf16(rng.standard_normal((H, K)) * np.sqrt(1 / 3))
+    n_slots = 4
+    slots = np.array([2], np.int32)
+    pool0 = np.full((n_slots, H, K), 0xDEAD, np.uint16)
+    pool0[2] = oracle.round_bf16(rng.standard_normal((H, K)))
+    pool = banded_from(pool0, "bf16")
+    y = banded_empty((T, H), "bf16")
+    cu = np.array([0, T], np.int32)
+    sc.in_proj_prefill(dev(hidden, "bf16"), dev(w_in, "bf16"), dev(w, "bf16"), dev(cu, "i32"),
+                       dev(slots, "i32"), pool.t, y=y.t)
+    for x, what in ((pool, "pool"), (y, "y")):
+        x.check(what)
+    ref = pool0.copy()
+    st, y_ref = layer.in_proj_prefill("bf16", hidden, w_in, w, cu, slots, ref)
+    assert st == oracle.OK
+    assert sc.get_error() == 0
+    assert_bits(host(pool.t), ref, "pool")
+    assert_close("bf16", host(y.t), y_ref, "y")
+
+
 @pytest.mark.parametrize("N,D,H,K", [(1, 64, 64, 3), (130, 64, 192, 4), (300, 128, 64, 1)])
 def test_in_proj_decode(N, D, H, K):
     rng = np.random.default_rng(1850 + N)
