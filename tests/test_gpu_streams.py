@@ -125,3 +125,69 @@ def test_host_threads_calling_at_once():
     for j in range(4):
         for got, want, what in zip(results[j], expect[j], ("y", "pool", "dbcx", "dw")):
             assert np.array_equal(got, want), f"thread {j}: {what}"
+
+
+def test_host_threads_calling_the_projections_at_once():
+    """Four host threads, each with its own stream and buffers, call the
+    tensor-core projections concurrently: a fused in_proj prefill (one
+    sequence in threads 0 and 2, so that the fused kernel writes the state
+    itself; three in threads 1 and 3, with the commit pass), out_proj on its
+    output, and a fused decode step continuing the same slots. Results must
+    match single-threaded calls bit for bit."""
+    import threading
+    D, H, K, n_iter = 64, 128, 3, 4
+    rng = np.random.default_rng(1300)
+
+    def dyadic(shape, lim, exp):
+        return oracle.round_bf16(rng.integers(-lim, lim, size=shape, endpoint=True) * 2.0 ** exp)
+
+    cases = []
+    for j in range(4):
+        lengths = [20000] if j % 2 == 0 else [700, 3, 5000]
+        cu = np.r_[0, np.cumsum(lengths)].astype(np.int32)
+        n = len(lengths)
+        pool = np.zeros((n + 2, H, K), np.uint16)
+        pool[:n] = oracle.round_bf16(rng.standard_normal((n, H, K)))
+        cases.append(dict(hidden=dev(dyadic((int(cu[-1]), D), 8, -3), "bf16"),
+                          w_in=dev(dyadic((3 * H, D), 8, -6), "bf16"),
+                          w=dev(oracle.round_bf16(rng.standard_normal((H, K)) * 0.5), "bf16"),
+                          cu=dev(cu, "i32"), slots=dev(np.arange(n, dtype=np.int32), "i32"),
+                          w_out=dev(dyadic((256, H), 8, -6), "bf16"),
+                          step=dev(dyadic((n, D), 8, -3), "bf16"), pool=pool))
+
+    def run(c):
+        pool = dev(c["pool"], "bf16")
+        y = sc.in_proj_prefill(c["hidden"], c["w_in"], c["w"], c["cu"], c["slots"], pool)
+        out = sc.out_proj(y, c["w_out"])
+        y1 = sc.in_proj_decode(c["step"], c["w_in"], c["w"], c["slots"], pool)
+        return y, pool, out, y1
+
+    expect = []
+    for c in cases:  # single-threaded results first
+        r = run(c)
+        torch.cuda.synchronize()
+        expect.append(tuple(host(v) for v in r))
+    results = [None] * 4
+    errors = []
+
+    def worker(j):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(n_iter):
+                    r = run(cases[j])
+            s.synchronize()
+            results[j] = tuple(host(v) for v in r)
+        except Exception as e:  # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(j,)) for j in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    assert sc.get_error() == 0
+    for j in range(4):
+        for got, want, what in zip(results[j], expect[j], ("y", "pool", "out", "decode y")):
+            assert np.array_equal(got, want), f"thread {j}: {what}"
